@@ -1,0 +1,178 @@
+"""fp64 CPU oracle for attention-score vision-token pruning.
+
+TEST INFRASTRUCTURE ONLY. This module is the plain, slow, obviously correct
+statement of what the CUDA library computes. Only the tests, the smoke check
+and the benchmark's CPU-baseline leg may import it; the library never calls it
+and never falls back to it. It shares no code with the CUDA path.
+
+What it follows (page titles and sections):
+
+* "LiteVLM: A Low-Latency Vision-Language Model Inference Pipeline for
+  Resource-Constrained Environments" (paper review), section 3.2 "Token
+  Selection Module" and the "core formulas" paragraph: visual tokens are
+  scored by attention, s_j = Attn(h, v_j), from the first decoder layer, and
+  the most important are kept with keep ratio r (r = 0.8 keeps 80 %).
+* The dynamic vision-token compression article, section 3.1 (VisionZip: a few
+  dominant tokens identified by attention score), section 3.2 (score = the
+  mean attention each visual token receives at a ViT layer; all images of a
+  request share one candidate pool under one global budget; probabilities are
+  rebuilt from the softmax LSE and reduced along columns, so only one score per
+  token leaves the kernel; after pruning the lengths, image boundaries,
+  original spatial indices and position ids are updated).
+
+Readings taken where the pages are silent (each is also listed in the design
+notes):
+
+* Mean over heads and over the query rows of the token's own segment:
+  score_j = (1 / (H * Nq_g)) * sum_h sum_i P[h, i, j].
+* The softmax of a query row runs over the keys of its own segment only
+  (block-diagonal varlen attention, no causal mask); scale 1/sqrt(d) unless
+  given.
+* GQA: query head h reads KV head floor(h / (H / Hkv)).
+* A segment with no query rows gives its keys score 0; a query row with no
+  keys has LSE = -inf.
+* Budget: B = floor(r * N) in integer per-mille arithmetic.
+* Top-B order: score descending, ties to the lowest token index; the kept
+  indices are returned in ascending order, requests concatenated.
+* Compaction copies rows and position ids of the kept tokens in ascending
+  order; the image id of a token is the segment holding it; the new per-image
+  boundaries are prefix sums of kept counts.
+
+Parity status: every function here is pinned by closed forms, invariants and
+brute force in tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# Input conversion
+# ---------------------------------------------------------------------------
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> fp64 values, exactly (bf16 is a truncated fp32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Importance (LiteVLM token selection; VisionZip-style mean attention received)
+# ---------------------------------------------------------------------------
+
+def attention_probabilities(q: np.ndarray, k: np.ndarray, scale: float):
+    """Full attention matrix of one segment and one head, materialised.
+
+    q: [Nq, d] fp64, k: [Nk, d] fp64. Returns (P [Nq, Nk], lse [Nq]) with
+    P = softmax(scale * q k^T) row by row and lse the natural-log normaliser
+    (the softmax LSE a FlashAttention-style kernel returns).
+    """
+    nq, nk = q.shape[0], k.shape[0]
+    if nk == 0:
+        return np.zeros((nq, 0)), np.full(nq, -np.inf)
+    s = scale * (q @ k.T)
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=1, keepdims=True)
+    p = e / l
+    lse = (m + np.log(l))[:, 0]
+    return p, lse
+
+
+def importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale=None):
+    """Mean attention probability received by every key token.
+
+    q_bits: uint16 [Tq, H, d] bf16 bits; k_bits: uint16 [Tk, Hkv, d].
+    cu_seqlens_q / cu_seqlens_k: int [G+1]; segment g attends queries
+    [cu_q[g], cu_q[g+1]) to keys [cu_k[g], cu_k[g+1]).
+    Returns (lse [H, Tq] fp64 natural log, scores [Tk] fp64).
+    """
+    q = bf16_bits_to_f64(q_bits)
+    k = bf16_bits_to_f64(k_bits)
+    tq, H, d = q.shape
+    tk, Hkv, _ = k.shape
+    group = H // Hkv
+    scale = (1.0 / np.sqrt(d)) if (softmax_scale is None or softmax_scale <= 0) else float(softmax_scale)
+    cu_q = np.asarray(cu_seqlens_q, dtype=np.int64)
+    cu_k = np.asarray(cu_seqlens_k, dtype=np.int64)
+    lse = np.full((H, tq), -np.inf)
+    scores = np.zeros(tk)
+    for g in range(cu_k.shape[0] - 1):
+        q0, q1 = cu_q[g], cu_q[g + 1]
+        k0, k1 = cu_k[g], cu_k[g + 1]
+        acc = np.zeros(k1 - k0)
+        for h in range(H):
+            p, lse_h = attention_probabilities(q[q0:q1, h, :], k[k0:k1, h // group, :], scale)
+            lse[h, q0:q1] = lse_h
+            acc += p.sum(axis=0)          # attention received = column sum
+        n_rows = H * (q1 - q0)
+        scores[k0:k1] = acc / n_rows if n_rows > 0 else 0.0
+    return lse, scores
+
+
+# ---------------------------------------------------------------------------
+# Budget and pooled global top-B
+# ---------------------------------------------------------------------------
+
+def keep_count(n_tokens: int, keep_permille: int) -> int:
+    """Tokens kept at keep ratio r = keep_permille / 1000: floor(r * n)."""
+    return (int(n_tokens) * int(keep_permille)) // 1000
+
+
+def select_topk(scores, req_tok_offsets, keep_per_req):
+    """Global top-B per request over the pooled tokens of all its images.
+
+    Order: score descending, then token index ascending. The comparison is
+    made in the dtype of ``scores`` (fp32 scores are compared as fp32).
+    Returns (keep_idx int32 [sum B], cu_keep int32 [R+1]); indices ascending
+    inside each request, requests in order.
+    """
+    scores = np.asarray(scores)
+    off = np.asarray(req_tok_offsets, dtype=np.int64)
+    keep = np.asarray(keep_per_req, dtype=np.int64)
+    out = []
+    cu = [0]
+    for r in range(off.shape[0] - 1):
+        lo, hi = off[r], off[r + 1]
+        idx = np.arange(lo, hi)
+        order = np.lexsort((idx, -scores[lo:hi]))   # primary: -score, then index
+        chosen = np.sort(idx[order[: keep[r]]])
+        out.append(chosen)
+        cu.append(cu[-1] + chosen.shape[0])
+    keep_idx = np.concatenate(out) if out else np.zeros(0, np.int64)
+    return keep_idx.astype(np.int32), np.asarray(cu, dtype=np.int32)
+
+
+# ---------------------------------------------------------------------------
+# Compaction with metadata
+# ---------------------------------------------------------------------------
+
+def gather_compact(hidden, pos, cu_seqlens_k, keep_idx):
+    """Copy kept rows in ascending order and rebuild per-image metadata.
+
+    hidden: [Tk, D] (any dtype, copied bit for bit); pos: int [Tk, P].
+    Returns (out_hidden [K, D], out_pos [K, P], img_id int32 [K],
+    cu_seqlens_kept int32 [G+1]).
+    """
+    keep_idx = np.asarray(keep_idx, dtype=np.int64)
+    cu = np.asarray(cu_seqlens_k, dtype=np.int64)
+    out_hidden = np.asarray(hidden)[keep_idx]
+    out_pos = np.asarray(pos)[keep_idx]
+    img_id = np.zeros(keep_idx.shape[0], dtype=np.int32)
+    counts = np.zeros(cu.shape[0] - 1, dtype=np.int64)
+    for n, t in enumerate(keep_idx):
+        g = int(np.searchsorted(cu, t, side="right") - 1)   # segment holding token t
+        img_id[n] = g
+        counts[g] += 1
+    cu_kept = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    return out_hidden, out_pos, img_id, cu_kept
+
+
+def prune(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, req_tok_offsets, keep_per_req,
+          hidden, pos, softmax_scale=None):
+    """The whole path: importance, pooled top-B, compaction."""
+    lse, scores = importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale)
+    keep_idx, cu_keep = select_topk(scores, req_tok_offsets, keep_per_req)
+    out_hidden, out_pos, img_id, cu_kept = gather_compact(hidden, pos, cu_seqlens_k, keep_idx)
+    return {"lse": lse, "scores": scores, "keep_idx": keep_idx, "cu_keep": cu_keep,
+            "hidden": out_hidden, "pos": out_pos, "img_id": img_id, "cu_seqlens_kept": cu_kept}
