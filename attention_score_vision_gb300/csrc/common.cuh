@@ -1,0 +1,82 @@
+// Shared definitions of libtsel: workspace layout, device status helpers and
+// the parameter blocks passed to the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/tsel.h"
+
+namespace tsel {
+
+constexpr int kTile = 128;          // rows per MMA tile (queries or keys)
+constexpr int kWsHeaderBytes = 1024;
+
+// First bytes of every workspace. Counters sit on separate 128-byte lines.
+struct WsHeader {
+  uint32_t status;        // TSEL_DEV_* bits
+  uint32_t pad0[31];
+  int32_t sched_ctr[2];   // dynamic unit counters of the two passes
+  uint32_t pad1[30];
+  int32_t num_units[2];   // units of the two passes (written by the prep kernel)
+  uint32_t pad2[30];
+};
+static_assert(sizeof(WsHeader) <= kWsHeaderBytes, "header too large");
+
+__host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Byte offsets of the importance workspace regions.
+struct ImpWsLayout {
+  int64_t qtile_off;   // int32 [G+1]: per-segment first 128-row tile of the padded LSE rows
+  int64_t scratch;     // int32 [8*G]: sort positions, inverses and unit starts (prep kernel)
+  int64_t units1;      // uint2 [U1]: pass-1 units (segment, head<<24 | q tile)
+  int64_t units2;      // uint2 [U2]: pass-2 units (segment, k tile)
+  int64_t nlse2;       // fp32 [H][lse_stride]: -LSE*log2(e), 128-row padded per segment
+  int64_t lse_stride;  // floats per head (multiple of 128)
+  int64_t u1_max, u2_max;
+  int64_t total;
+};
+
+__host__ __device__ inline ImpWsLayout imp_ws_layout(int G, int Tq, int Tk, int H) {
+  ImpWsLayout L{};
+  int64_t off = kWsHeaderBytes;
+  L.qtile_off = off;
+  off = align_up(off + 4 * (int64_t(G) + 1), 256);
+  L.scratch = off;
+  off = align_up(off + 32 * int64_t(G), 256);
+  L.u1_max = int64_t(H) * (ceil_div(Tq, kTile) + G);
+  L.u2_max = ceil_div(Tk, kTile) + G;
+  L.units1 = off;
+  off = align_up(off + 8 * L.u1_max, 256);
+  L.units2 = off;
+  off = align_up(off + 8 * L.u2_max, 1024);
+  L.lse_stride = int64_t(kTile) * (ceil_div(Tq, kTile) + G);
+  L.nlse2 = off;
+  off = align_up(off + 4 * int64_t(H) * L.lse_stride, 256);
+  L.total = off;
+  return L;
+}
+
+struct ImpPassParams {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const uint2* units;
+  const int32_t* num_units;
+  int32_t* sched_ctr;
+  const int32_t* qtile_off;
+  float* nlse2;          // pass 1 writes, pass 2 reads
+  int64_t lse_stride;
+  float* lse_out;        // natural log [H][Tq] (pass 1, may be null)
+  float* scores;         // [Tk] (pass 2)
+  uint32_t* status;
+  int H, Hkv, Tq;
+  float c;               // softmax_scale * log2(e)
+  uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
+  atomicOr(status, bits);
+}
+
+}  // namespace tsel

@@ -1,0 +1,693 @@
+// Importance scores: mean softmax attention received by every key token.
+//
+// Follows the LiteVLM review (section 3.2, s_j = Attn(h, v_j)) and the
+// dynamic vision-token compression article (section 3.2: mean attention
+// received; probabilities recovered block by block from the row LSE and
+// reduced along columns; the attention matrix never leaves the chip).
+//
+// Three launches on one stream:
+//   prep   one CTA: checks cu_seqlens, sorts segments by cost (longest first)
+//          and writes the unit lists of both passes into the workspace.
+//   pass 1 units (segment, head, 128-query tile): S = Q K^T tile by tile on
+//          the tensor cores (tcgen05, accumulators in TMEM), online max/sum
+//          per query row -> row LSE (kept as -LSE*log2 e, 128-row padded).
+//   pass 2 units (segment, 128-key tile), all heads: S^T = K Q^T with the
+//          keys on the MMA M dimension, so each epilogue thread owns one key
+//          and sums exp2(S*c - LSE2) over the query columns in registers:
+//          the column reduction needs no shuffles and no atomics, and the
+//          result is deterministic.
+//
+// CTA layout (384 threads, one CTA per SM, persistent, units fetched from a
+// global counter in longest-first order):
+//   warp 0      TMA producer (Q/K tiles, LSE slices)
+//   warp 1      TMEM allocator + MMA issuer (one thread)
+//   warps 2-3   idle
+//   warps 4-11  two epilogue warpgroups; warp w reads TMEM lanes 32*(w%4)..,
+//               warpgroup 0 takes columns 0-63 of each 128-column tile,
+//               warpgroup 1 columns 64-127; the halves are merged per unit.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace tsel {
+
+using namespace ptx;
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr int kAccBufs = 4;      // TMEM accumulators of 128 columns (512 columns)
+constexpr int kLseSlots = 8;     // LSE slices in flight (pass 2)
+constexpr int kSchedSlots = 4;   // scheduler ring depth
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 384;
+
+template <int D>
+struct TileCfg {
+  static_assert(D % 16 == 0 && D >= 64 && D <= 128, "head_dim");
+  static constexpr int N64 = D / 64;               // 64-column chunks (128-byte swizzle)
+  static constexpr int N16 = (D % 64) / 16;        // 16-column chunks (32-byte swizzle)
+  static constexpr int TILE_BYTES = kTile * D * 2; // one 128-row bf16 tile
+  static constexpr int STAGES_RAW = (196608 - 2 * TILE_BYTES) / TILE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = 2 * TILE_BYTES;
+  static constexpr int OFF_LSE = OFF_B + STAGES * TILE_BYTES;
+  static constexpr int OFF_COMB = OFF_LSE + kLseSlots * kTile * 4;
+  static constexpr int OFF_BAR = OFF_COMB + 2 * 2 * kTile * 4;
+  static constexpr int NUM_BARS = 2 + 2 + 2 * STAGES + 2 * kAccBufs + 2 * kLseSlots +
+                                  2 * kSchedSlots + 2 + 2 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  static_assert(TILE_BYTES % 1024 == 0, "tiles stay 1024-byte aligned");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
+};
+
+// ---------------------------------------------------------------------------
+// Prep kernel
+// ---------------------------------------------------------------------------
+
+// Exclusive scan of one value per thread over a 1024-thread block.
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  total = warp_sums[31];
+  __syncthreads();
+  return excl;
+}
+
+// In-place exclusive scan of a[0..n); returns the sum.
+__device__ int block_scan_array(int* a, int n, int* warp_sums) {
+  int carry = 0;
+  for (int base = 0; base < n; base += 1024) {
+    const int i = base + threadIdx.x;
+    const int v = i < n ? a[i] : 0;
+    int total;
+    const int e = block_excl_scan(v, warp_sums, total);
+    if (i < n) a[i] = carry + e;
+    carry += total;
+    __syncthreads();
+  }
+  return carry;
+}
+
+// Replaces key[g] (0..1023) by g's position in descending key order.
+__device__ void bucket_positions_desc(int* key, int G, int* hist, int* warp_sums) {
+  hist[threadIdx.x] = 0;
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += 1024) atomicAdd(&hist[key[g]], 1);
+  __syncthreads();
+  const int b = 1023 - threadIdx.x;  // bucket 1023 comes first
+  const int cnt = hist[b];
+  int total;
+  const int start = block_excl_scan(cnt, warp_sums, total);
+  hist[b] = start;
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += 1024) key[g] = atomicAdd(&hist[key[g]], 1);
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restrict__ cu_q,
+                                                        const int32_t* __restrict__ cu_k, int G,
+                                                        int Tq, int Tk, int max_q, int max_k,
+                                                        int H, uint8_t* ws, ImpWsLayout L) {
+  __shared__ int bad;
+  __shared__ int hist[1024];
+  __shared__ int warp_sums[32];
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  int32_t* qtile_off = reinterpret_cast<int32_t*>(ws + L.qtile_off);
+  int32_t* pos1 = reinterpret_cast<int32_t*>(ws + L.scratch);
+  int32_t* pos2 = pos1 + G;
+  int32_t* inv1 = pos2 + G;
+  int32_t* inv2 = inv1 + G;
+  int32_t* start1 = inv2 + G;
+  int32_t* start2 = start1 + G;
+  uint2* units1 = reinterpret_cast<uint2*>(ws + L.units1);
+  uint2* units2 = reinterpret_cast<uint2*>(ws + L.units2);
+
+  if (threadIdx.x == 0) {
+    bad = 0;
+    hdr->num_units[0] = 0;
+    hdr->num_units[1] = 0;
+    hdr->sched_ctr[0] = 0;
+    hdr->sched_ctr[1] = 0;
+    if (cu_q[0] != 0 || cu_k[0] != 0 || cu_q[G] != Tq || cu_k[G] != Tk) bad = 1;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += 1024) {
+    const int nq = cu_q[g + 1] - cu_q[g];
+    const int nk = cu_k[g + 1] - cu_k[g];
+    if (nq < 0 || nk < 0 || nq > max_q || nk > max_k) atomicOr(&bad, 1);
+  }
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) set_status(&hdr->status, TSEL_DEV_SEQLENS);
+    return;
+  }
+  // Cost keys: a pass-1 unit walks all key tiles of its segment, a pass-2
+  // unit all query tiles (times the heads).
+  for (int g = threadIdx.x; g < G; g += 1024) {
+    const int nqt = int(ceil_div(cu_q[g + 1] - cu_q[g], kTile));
+    const int nkt = int(ceil_div(cu_k[g + 1] - cu_k[g], kTile));
+    pos1[g] = min(nkt, 1023);
+    pos2[g] = min(nqt, 1023);
+    qtile_off[g] = nqt;
+  }
+  __syncthreads();
+  bucket_positions_desc(pos1, G, hist, warp_sums);
+  bucket_positions_desc(pos2, G, hist, warp_sums);
+  for (int g = threadIdx.x; g < G; g += 1024) {
+    const int nqt = int(ceil_div(cu_q[g + 1] - cu_q[g], kTile));
+    const int nkt = int(ceil_div(cu_k[g + 1] - cu_k[g], kTile));
+    inv1[pos1[g]] = g;
+    inv2[pos2[g]] = g;
+    start1[pos1[g]] = H * nqt;
+    start2[pos2[g]] = nkt;
+  }
+  __syncthreads();
+  const int total1 = block_scan_array(start1, G, warp_sums);
+  const int total2 = block_scan_array(start2, G, warp_sums);
+  const int total_qt = block_scan_array(qtile_off, G, warp_sums);
+  if (threadIdx.x == 0) qtile_off[G] = total_qt;
+  // Unit lists in descending-cost segment order.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < G; i += 32) {
+    const int g = inv1[i];
+    const int nqt = int(ceil_div(cu_q[g + 1] - cu_q[g], kTile));
+    const int n = H * nqt;
+    const int s = start1[i];
+    for (int j = lane; j < n; j += 32) {
+      const int h = j / nqt, qt = j - h * nqt;
+      units1[s + j] = make_uint2(uint32_t(g), (uint32_t(h) << 24) | uint32_t(qt));
+    }
+    const int g2 = inv2[i];
+    const int nkt = int(ceil_div(cu_k[g2 + 1] - cu_k[g2], kTile));
+    const int s2 = start2[i];
+    for (int j = lane; j < nkt; j += 32) units2[s2 + j] = make_uint2(uint32_t(g2), uint32_t(j));
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    hdr->num_units[0] = total1;
+    hdr->num_units[1] = total2;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Pass kernel
+// ---------------------------------------------------------------------------
+
+struct Unit {
+  int g, h, tile, q0, nq, k0, nk;
+};
+
+template <int PASS>
+__device__ __forceinline__ Unit decode_unit(const ImpPassParams& p, uint2 u) {
+  Unit r;
+  r.g = int(u.x);
+  if (PASS == 1) {
+    r.h = int(u.y >> 24);
+    r.tile = int(u.y & 0xFFFFFFu);
+  } else {
+    r.h = 0;
+    r.tile = int(u.y);
+  }
+  r.q0 = __ldg(p.cu_q + r.g);
+  r.nq = __ldg(p.cu_q + r.g + 1) - r.q0;
+  r.k0 = __ldg(p.cu_k + r.g);
+  r.nk = __ldg(p.cu_k + r.g + 1) - r.k0;
+  return r;
+}
+
+// Loads one 128-row tile of head columns [x0, x0 + D) starting at row y.
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* m64,
+                                          const CUtensorMap* m16, uint64_t* bar, int x0, int y) {
+  using C = TileCfg<D>;
+#pragma unroll
+  for (int c = 0; c < C::N64; ++c) tma_load_2d(dst + c * 16384, m64, bar, x0 + 64 * c, y);
+#pragma unroll
+  for (int j = 0; j < C::N16; ++j)
+    tma_load_2d(dst + C::N64 * 16384 + j * 4096, m16, bar, x0 + 64 * C::N64 + 16 * j, y);
+}
+
+// Issues the MMAs of one 128x128 tile: D = A * B^T over the head dimension.
+template <int D>
+__device__ __forceinline__ void issue_tile_mmas(uint32_t d_tmem, const uint8_t* a,
+                                                const uint8_t* b) {
+  using C = TileCfg<D>;
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
+  const uint32_t a0 = smem_u32(a), b0 = smem_u32(b);
+  uint32_t acc = 0;
+#pragma unroll
+  for (int c = 0; c < C::N64; ++c) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t off = c * 16384 + k * 32;
+      mma_bf16(d_tmem, smem_desc(a0 + off, 2, 1024), smem_desc(b0 + off, 2, 1024), kIdesc, acc);
+      acc = 1;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < C::N16; ++j) {
+    const uint32_t off = C::N64 * 16384 + j * 4096;
+    mma_bf16(d_tmem, smem_desc(a0 + off, 6, 256), smem_desc(b0 + off, 6, 256), kIdesc, acc);
+    acc = 1;
+  }
+}
+
+// Waits with the time limit only (used to drain copies before exit).
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  const int zero = 0;
+  return wait_bounded(bar, parity, &zero, timeout_ns);
+}
+
+// Epilogue waits: all lanes wait, and the outcome is made warp-uniform so a
+// timeout never leaves part of a warp in front of a .sync.aligned TMEM load.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          const volatile int* abort_flag, uint64_t timeout_ns) {
+  return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag, timeout_ns));
+}
+
+template <int PASS, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    imp_pass_kernel(const __grid_constant__ CUtensorMap mapA64,
+                    const __grid_constant__ CUtensorMap mapA16,
+                    const __grid_constant__ CUtensorMap mapB64,
+                    const __grid_constant__ CUtensorMap mapB16, const ImpPassParams p) {
+  using C = TileCfg<D>;
+  constexpr int S = C::STAGES;
+  extern __shared__ uint8_t smem_dyn[];
+  // 128-byte swizzle atoms key off shared-address bits: align the carve-out
+  // on the shared-window address itself.
+  uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  float* sLse = reinterpret_cast<float*>(smem + C::OFF_LSE);
+  float* sComb = reinterpret_cast<float*>(smem + C::OFF_COMB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* a_full = bars;
+  uint64_t* a_empty = a_full + 2;
+  uint64_t* b_full = a_empty + 2;
+  uint64_t* b_empty = b_full + S;
+  uint64_t* acc_full = b_empty + S;
+  uint64_t* acc_empty = acc_full + kAccBufs;
+  uint64_t* lse_full = acc_empty + kAccBufs;
+  uint64_t* lse_empty = lse_full + kLseSlots;
+  uint64_t* sch_full = lse_empty + kLseSlots;
+  uint64_t* sch_empty = sch_full + kSchedSlots;
+  uint64_t* comb_full = sch_empty + kSchedSlots;
+  uint64_t* comb_empty = comb_full + 2;
+  uint64_t* mma_done = comb_empty + 2;
+  int* sched = reinterpret_cast<int*>(smem + C::OFF_MISC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched + kSchedSlots);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sched + kSchedSlots + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t T = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+      mbar_init(&comb_full[i], 4);
+      mbar_init(&comb_empty[i], 4);
+    }
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < kAccBufs; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps);
+    }
+    for (int i = 0; i < kLseSlots; ++i) {
+      mbar_init(&lse_full[i], 1);
+      mbar_init(&lse_empty[i], kEpiWarps);
+    }
+    for (int i = 0; i < kSchedSlots; ++i) {
+      mbar_init(&sch_full[i], 1);
+      mbar_init(&sch_empty[i], 1 + kEpiWarps);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&mapA64);
+    prefetch_tensormap(&mapA16);
+    prefetch_tensormap(&mapB64);
+    prefetch_tensormap(&mapB16);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_units = *reinterpret_cast<const volatile int*>(p.num_units);
+  const int group = p.H / p.Hkv;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s_it = 0, a_it = 0, b_it = 0, l_it = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = s_it % kSchedSlots;
+        if (!wait_bounded(&sch_empty[slot], ((s_it / kSchedSlots) & 1) ^ 1, abort_flag, T)) {
+          ok = false;
+          break;
+        }
+        int u = atomicAdd(p.sched_ctr, 1);
+        if (u >= total_units) u = -1;
+        sched[slot] = u;
+        mbar_arrive(&sch_full[slot]);
+        ++s_it;
+        if (u < 0) break;
+        const Unit w = decode_unit<PASS>(p, p.units[u]);
+        if (PASS == 1) {
+          const int nkt = int(ceil_div(w.nk, kTile));
+          if (nkt == 0) continue;
+          const int as = a_it & 1;
+          if (!wait_bounded(&a_empty[as], ((a_it >> 1) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
+          mbar_arrive_expect_tx(&a_full[as], C::TILE_BYTES);
+          load_tile<D>(sA + as * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as], w.h * D,
+                       w.q0 + w.tile * kTile);
+          ++a_it;
+          const int kvh = w.h / group;
+          for (int kt = 0; kt < nkt; ++kt) {
+            const int bs = b_it % S;
+            if (!wait_bounded(&b_empty[bs], ((b_it / S) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
+            mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES);
+            load_tile<D>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], kvh * D,
+                         w.k0 + kt * kTile);
+            ++b_it;
+          }
+        } else {
+          const int nqt = int(ceil_div(w.nq, kTile));
+          if (nqt == 0) continue;
+          const int qtile_base = __ldg(p.qtile_off + w.g);
+          for (int hk = 0; hk < p.Hkv && ok; ++hk) {
+            const int as = a_it & 1;
+            if (!wait_bounded(&a_empty[as], ((a_it >> 1) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
+            mbar_arrive_expect_tx(&a_full[as], C::TILE_BYTES);
+            load_tile<D>(sA + as * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as], hk * D,
+                         w.k0 + w.tile * kTile);
+            ++a_it;
+            for (int hh = 0; hh < group && ok; ++hh) {
+              const int h = hk * group + hh;
+              for (int qt = 0; qt < nqt; ++qt) {
+                const int bs = b_it % S;
+                if (!wait_bounded(&b_empty[bs], ((b_it / S) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
+                mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES);
+                load_tile<D>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], h * D,
+                             w.q0 + qt * kTile);
+                ++b_it;
+                const int ls = l_it % kLseSlots;
+                if (!wait_bounded(&lse_empty[ls], ((l_it / kLseSlots) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
+                mbar_arrive_expect_tx(&lse_full[ls], kTile * 4);
+                bulk_load(sLse + ls * kTile,
+                          p.nlse2 + int64_t(h) * p.lse_stride + int64_t(qtile_base + qt) * kTile,
+                          kTile * 4, &lse_full[ls]);
+                ++l_it;
+              }
+            }
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, TSEL_DEV_TIMEOUT);
+      }
+      // Drain: every copy this thread issued has landed before the CTA exits.
+      for (int i = 0; i < S && i < b_it; ++i) {
+        const int n = b_it - 1 - i;
+        wait_drain(&b_full[n % S], (n / S) & 1, T);
+      }
+      for (int i = 0; i < 2 && i < a_it; ++i) {
+        const int n = a_it - 1 - i;
+        wait_drain(&a_full[n & 1], (n >> 1) & 1, T);
+      }
+      for (int i = 0; i < kLseSlots && i < l_it; ++i) {
+        const int n = l_it - 1 - i;
+        wait_drain(&lse_full[n % kLseSlots], (n / kLseSlots) & 1, T);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int s_it = 0, a_it = 0, b_it = 0, c_it = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = s_it % kSchedSlots;
+        if (!wait_bounded(&sch_full[slot], (s_it / kSchedSlots) & 1, abort_flag, T)) { ok = false; break; }
+        const int u = sched[slot];
+        mbar_arrive(&sch_empty[slot]);
+        ++s_it;
+        if (u < 0) break;
+        const Unit w = decode_unit<PASS>(p, p.units[u]);
+        const int n_a = PASS == 1 ? (w.nk > 0 ? 1 : 0) : (w.nq > 0 ? p.Hkv : 0);
+        const int n_b = PASS == 1 ? int(ceil_div(w.nk, kTile)) : group * int(ceil_div(w.nq, kTile));
+        for (int ai = 0; ai < n_a && ok; ++ai) {
+          const int as = a_it & 1;
+          if (!wait_bounded(&a_full[as], (a_it >> 1) & 1, abort_flag, T)) { ok = false; break; }
+          tc_fence_after();
+          for (int bi = 0; bi < n_b; ++bi) {
+            const int bs = b_it % S;
+            if (!wait_bounded(&b_full[bs], (b_it / S) & 1, abort_flag, T)) { ok = false; break; }
+            const int ab = c_it % kAccBufs;
+            if (!wait_bounded(&acc_empty[ab], ((c_it / kAccBufs) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
+            tc_fence_after();
+            issue_tile_mmas<D>(tmem_base + uint32_t(ab * kTile), sA + as * C::TILE_BYTES,
+                               sB + bs * C::TILE_BYTES);
+            mma_commit(&b_empty[bs]);
+            mma_commit(&acc_full[ab]);
+            ++b_it;
+            ++c_it;
+          }
+          mma_commit(&a_empty[as]);
+          ++a_it;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        set_status(p.status, TSEL_DEV_TIMEOUT);
+      }
+      // All MMAs issued by this thread have completed before TMEM is freed.
+      mma_commit(mma_done);
+      wait_drain(mma_done, 0, T);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int wg = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(wg * 64);
+    const float c = p.c;
+    int s_it = 0, c_it = 0, l_it = 0, unit_it = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = s_it % kSchedSlots;
+      if (!warp_wait(&sch_full[slot], (s_it / kSchedSlots) & 1, abort_flag, T)) { ok = false; break; }
+      const int u = sched[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sch_empty[slot]);
+      ++s_it;
+      if (u < 0) break;
+      const Unit w = decode_unit<PASS>(p, p.units[u]);
+      const int cb = unit_it & 1;
+      const uint32_t cpar = (unit_it >> 1) & 1;
+      float* comb = sComb + cb * 2 * kTile;
+
+      if (PASS == 1) {
+        float m = kNegInf, l = 0.f;
+        const int nkt = int(ceil_div(w.nk, kTile));
+        for (int kt = 0; kt < nkt; ++kt) {
+          const int ab = c_it % kAccBufs;
+          if (!warp_wait(&acc_full[ab], (c_it / kAccBufs) & 1, abort_flag, T)) { ok = false; break; }
+          tc_fence_after();
+          float v[64];
+          tmem_ld64(lane_base + uint32_t(ab * kTile), v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[ab]);
+          ++c_it;
+          const int valid = w.nk - kt * kTile - wg * 64;
+          if (valid < 64) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) v[j] = j < valid ? v[j] : kNegInf;
+          }
+          float t0 = v[0], t1 = v[1], t2 = v[2], t3 = v[3];
+#pragma unroll
+          for (int j = 4; j < 64; j += 4) {
+            t0 = fmaxf(t0, v[j]);
+            t1 = fmaxf(t1, v[j + 1]);
+            t2 = fmaxf(t2, v[j + 2]);
+            t3 = fmaxf(t3, v[j + 3]);
+          }
+          const float tmax = fmaxf(fmaxf(t0, t1), fmaxf(t2, t3));
+          if (tmax > kNegInf) {
+            const float mn = fmaxf(m, tmax * c);
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              s0 += ex2(fmaf(v[j], c, -mn));
+              s1 += ex2(fmaf(v[j + 1], c, -mn));
+              s2 += ex2(fmaf(v[j + 2], c, -mn));
+              s3 += ex2(fmaf(v[j + 3], c, -mn));
+            }
+            l = l * ex2(m - mn) + ((s0 + s1) + (s2 + s3));
+            m = mn;
+          }
+        }
+        if (!ok) break;
+        if (wg == 1) {
+          if (!warp_wait(&comb_empty[cb], cpar ^ 1, abort_flag, T)) { ok = false; break; }
+          comb[row] = m;
+          comb[kTile + row] = l;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_full[cb]);
+        } else {
+          if (!warp_wait(&comb_full[cb], cpar, abort_flag, T)) { ok = false; break; }
+          const float m1 = comb[row], l1 = comb[kTile + row];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_empty[cb]);
+          const float M = fmaxf(m, m1);
+          float Lsum = 0.f;
+          if (M > kNegInf) Lsum = l * ex2(m - M) + l1 * ex2(m1 - M);
+          const int qrow = w.tile * kTile + row;
+          const bool valid = qrow < w.nq;
+          const float lse2 = Lsum > 0.f ? M + log2f(Lsum) : kNegInf;
+          const int qtile_base = __ldg(p.qtile_off + w.g);
+          p.nlse2[int64_t(w.h) * p.lse_stride + int64_t(qtile_base + w.tile) * kTile + row] =
+              (valid && Lsum > 0.f) ? -lse2 : kNegInf;
+          if (valid && p.lse_out != nullptr)
+            p.lse_out[int64_t(w.h) * p.Tq + w.q0 + qrow] = lse2 * 0.69314718055994531f;
+        }
+      } else {
+        float acc = 0.f;
+        const int nqt = int(ceil_div(w.nq, kTile));
+        const int n_iter = nqt > 0 ? p.H * nqt : 0;
+        for (int it = 0; it < n_iter; ++it) {
+          const int ab = c_it % kAccBufs;
+          if (!warp_wait(&acc_full[ab], (c_it / kAccBufs) & 1, abort_flag, T)) { ok = false; break; }
+          tc_fence_after();
+          float v[64];
+          tmem_ld64(lane_base + uint32_t(ab * kTile), v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[ab]);
+          ++c_it;
+          const int ls = l_it % kLseSlots;
+          if (!warp_wait(&lse_full[ls], (l_it / kLseSlots) & 1, abort_flag, T)) { ok = false; break; }
+          const float4* nl = reinterpret_cast<const float4*>(sLse + ls * kTile + wg * 64);
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float4 t = nl[j];
+            s0 += ex2(fmaf(v[4 * j], c, t.x));
+            s1 += ex2(fmaf(v[4 * j + 1], c, t.y));
+            s2 += ex2(fmaf(v[4 * j + 2], c, t.z));
+            s3 += ex2(fmaf(v[4 * j + 3], c, t.w));
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&lse_empty[ls]);
+          ++l_it;
+          acc += (s0 + s1) + (s2 + s3);
+        }
+        if (!ok) break;
+        if (wg == 1) {
+          if (!warp_wait(&comb_empty[cb], cpar ^ 1, abort_flag, T)) { ok = false; break; }
+          comb[row] = acc;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_full[cb]);
+        } else {
+          if (!warp_wait(&comb_full[cb], cpar, abort_flag, T)) { ok = false; break; }
+          const float acc1 = comb[row];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_empty[cb]);
+          const int krow = w.tile * kTile + row;
+          if (krow < w.nk) {
+            const float total = acc + acc1;
+            p.scores[w.k0 + krow] = w.nq > 0 ? total / float(p.H * w.nq) : 0.f;
+          }
+        }
+      }
+      ++unit_it;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      set_status(p.status, TSEL_DEV_TIMEOUT);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launch helpers (called from tsel_api.cu)
+// ---------------------------------------------------------------------------
+
+cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
+                            int max_q, int max_k, int H, uint8_t* ws, const ImpWsLayout& L,
+                            cudaStream_t stream) {
+  imp_prep_kernel<<<1, 1024, 0, stream>>>(cu_q, cu_k, G, Tq, Tk, max_q, max_k, H, ws, L);
+  return cudaPeekAtLastError();
+}
+
+template <int PASS, int D>
+static cudaError_t launch_pass_t(const CUtensorMap* maps, const ImpPassParams& p, int grid,
+                                 cudaStream_t stream) {
+  using C = TileCfg<D>;
+  auto kern = imp_pass_kernel<PASS, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  return cudaPeekAtLastError();
+}
+
+// maps: A64, A16, B64, B16 (pass 1: A = Q, B = K; pass 2: A = K, B = Q).
+cudaError_t launch_imp_pass(int pass, int head_dim, const CUtensorMap* maps,
+                            const ImpPassParams& p, int grid, cudaStream_t stream) {
+#define TSEL_PASS_CASE(DD)                                                              \
+  case DD:                                                                              \
+    return pass == 1 ? launch_pass_t<1, DD>(maps, p, grid, stream)                      \
+                     : launch_pass_t<2, DD>(maps, p, grid, stream);
+  switch (head_dim) {
+    TSEL_PASS_CASE(64)
+    TSEL_PASS_CASE(80)
+    TSEL_PASS_CASE(96)
+    TSEL_PASS_CASE(112)
+    TSEL_PASS_CASE(128)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef TSEL_PASS_CASE
+}
+
+}  // namespace tsel

@@ -1,0 +1,349 @@
+// Host side of the C ABI declared in include/tsel.h: argument checks, TMA
+// descriptor encoding, workspace carving and kernel launches. Nothing here
+// allocates device memory or synchronises, except tsel_read_device_status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace tsel {
+cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
+                            int max_q, int max_k, int H, uint8_t* ws, const ImpWsLayout& L,
+                            cudaStream_t stream);
+cudaError_t launch_imp_pass(int pass, int head_dim, const CUtensorMap* maps,
+                            const ImpPassParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
+                        int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
+                        int32_t* cu_keep, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_bytes,
+                          const int32_t* pos, int pos_dim, const int32_t* cu_k, int G, int Tk,
+                          const int32_t* keep_idx, int K, void* out_hidden, int32_t* out_pos,
+                          int32_t* out_img, int32_t* out_cu, uint32_t* status, int num_sms,
+                          cudaStream_t stream);
+cudaError_t launch_probe_ex2(int blocks, int iters, float* sink, cudaStream_t stream);
+}  // namespace tsel
+
+using namespace tsel;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+tsel_status fail(tsel_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+tsel_status fail(tsel_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+tsel_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(TSEL_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return -1;
+  static int cache[128] = {0};
+  if (dev >= 0 && dev < 128 && cache[dev] > 0) {
+    *out = cache[dev];
+    return 0;
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess || n <= 0) return -1;
+  if (dev >= 0 && dev < 128) cache[dev] = n;
+  *out = n;
+  return 0;
+}
+
+// 2-D bf16 tensor map over `rows` rows of `width` elements (row stride in
+// bytes), box of `box_w` x 128 elements.
+bool make_map(CUtensorMap* map, const void* base, int64_t width, int64_t rows,
+              int64_t row_stride_bytes, int box_w, CUtensorMapSwizzle sw) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(width), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(row_stride_bytes)};
+  cuuint32_t box[2] = {cuuint32_t(box_w), cuuint32_t(kTile)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t t = [] {
+    const char* s = std::getenv("TSEL_WAIT_TIMEOUT_MS");
+    long v = s ? std::strtol(s, nullptr, 10) : 0;
+    if (v <= 0) v = 1000;
+    return uint64_t(v) * 1000000ull;
+  }();
+  return t;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tsel_status_string(tsel_status s) {
+  switch (s) {
+    case TSEL_OK: return "TSEL_OK";
+    case TSEL_ERR_INVALID_VALUE: return "TSEL_ERR_INVALID_VALUE";
+    case TSEL_ERR_UNSUPPORTED: return "TSEL_ERR_UNSUPPORTED";
+    case TSEL_ERR_WORKSPACE: return "TSEL_ERR_WORKSPACE";
+    case TSEL_ERR_CUDA: return "TSEL_ERR_CUDA";
+    case TSEL_ERR_DEVICE_CHECK: return "TSEL_ERR_DEVICE_CHECK";
+  }
+  return "TSEL_ERR_UNKNOWN";
+}
+
+const char* tsel_last_error(void) { return g_last_error.c_str(); }
+
+int tsel_keep_count(int n_tokens, int keep_permille) {
+  if (n_tokens < 0 || keep_permille < 0) return -1;
+  return int((int64_t(n_tokens) * int64_t(keep_permille)) / 1000);
+}
+
+size_t tsel_importance_workspace_size(int num_seg, int total_q, int total_k, int num_heads) {
+  if (num_seg < 0 || total_q < 0 || total_k < 0 || num_heads < 1) return 0;
+  return size_t(imp_ws_layout(num_seg, total_q, total_k, num_heads).total);
+}
+
+size_t tsel_select_topk_workspace_size(int num_req) {
+  (void)num_req;
+  return kWsHeaderBytes;
+}
+
+size_t tsel_gather_compact_workspace_size(void) { return kWsHeaderBytes; }
+
+tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
+                            int64_t k_row_stride, const int32_t* cu_seqlens_q,
+                            const int32_t* cu_seqlens_k, int num_seg, int total_q, int total_k,
+                            int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                            int head_dim, float softmax_scale, unsigned flags, float* lse,
+                            float* scores, void* workspace, size_t workspace_bytes,
+                            void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (num_seg < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return fail(TSEL_ERR_INVALID_VALUE, "negative size");
+  if (num_heads < 1 || num_heads > 256 || num_kv_heads < 1 || num_heads % num_kv_heads != 0)
+    return fail(TSEL_ERR_INVALID_VALUE, "num_heads=%d num_kv_heads=%d", num_heads, num_kv_heads);
+  if (!(head_dim == 64 || head_dim == 80 || head_dim == 96 || head_dim == 112 || head_dim == 128))
+    return fail(TSEL_ERR_UNSUPPORTED, "head_dim=%d (supported: 64, 80, 96, 112, 128)", head_dim);
+  if ((flags & ~(TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2)) != 0)
+    return fail(TSEL_ERR_UNSUPPORTED, "flags=0x%x", flags);
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || workspace == nullptr)
+    return fail(TSEL_ERR_INVALID_VALUE, "null cu_seqlens or workspace");
+  if ((total_k > 0 && (scores == nullptr || k == nullptr)) || (total_q > 0 && q == nullptr))
+    return fail(TSEL_ERR_INVALID_VALUE, "null q/k/scores");
+  const int64_t hd = int64_t(num_heads) * head_dim, kvd = int64_t(num_kv_heads) * head_dim;
+  if (q_row_stride == 0) q_row_stride = hd;
+  if (k_row_stride == 0) k_row_stride = kvd;
+  if (q_row_stride < hd || k_row_stride < kvd || (q_row_stride * 2) % 16 != 0 ||
+      (k_row_stride * 2) % 16 != 0)
+    return fail(TSEL_ERR_INVALID_VALUE, "row strides %lld/%lld", (long long)q_row_stride,
+                (long long)k_row_stride);
+  if ((q && !aligned16(q)) || (k && !aligned16(k)))
+    return fail(TSEL_ERR_INVALID_VALUE, "q/k must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(TSEL_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  const ImpWsLayout L = imp_ws_layout(num_seg, total_q, total_k, num_heads);
+  if (workspace_bytes < size_t(L.total))
+    return fail(TSEL_ERR_WORKSPACE, "workspace %zu < %lld bytes", workspace_bytes,
+                (long long)L.total);
+  const unsigned stages = (flags & (TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 |
+                                    TSEL_IMP_STAGE_PASS2))
+                              ? flags
+                              : (TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  cudaError_t e;
+
+  if (stages & TSEL_IMP_STAGE_PREP) {
+    e = launch_imp_prep(cu_seqlens_q, cu_seqlens_k, num_seg, total_q, total_k, max_seqlen_q,
+                        max_seqlen_k, num_heads, ws, L, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prep launch");
+  }
+  if (total_k == 0 || num_seg == 0) return TSEL_OK;
+  if (total_q == 0) {
+    // No query rows anywhere: every score is 0 (mean over zero rows).
+    if (stages & TSEL_IMP_STAGE_PASS2) {
+      e = cudaMemsetAsync(scores, 0, sizeof(float) * size_t(total_k), stream);
+      if (e != cudaSuccess) return cuda_fail(e, "memset scores");
+    }
+    return TSEL_OK;
+  }
+  if (!(stages & (TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2))) return TSEL_OK;
+
+  CUtensorMap qm64, qm16, km64, km16;
+  const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw32 = CU_TENSOR_MAP_SWIZZLE_32B;
+  const bool tail = (head_dim % 64) != 0;
+  if (!make_map(&qm64, q, hd, total_q, q_row_stride * 2, 64, sw128) ||
+      !make_map(&km64, k, kvd, total_k, k_row_stride * 2, 64, sw128))
+    return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (64-wide box)");
+  if (tail) {
+    if (!make_map(&qm16, q, hd, total_q, q_row_stride * 2, 16, sw32) ||
+        !make_map(&km16, k, kvd, total_k, k_row_stride * 2, 16, sw32))
+      return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (16-wide box)");
+  } else {
+    qm16 = qm64;
+    km16 = km64;
+  }
+  int sms = 0;
+  if (sm_count(&sms) != 0) return fail(TSEL_ERR_CUDA, "cannot query the SM count");
+
+  ImpPassParams p{};
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.qtile_off = reinterpret_cast<const int32_t*>(ws + L.qtile_off);
+  p.nlse2 = reinterpret_cast<float*>(ws + L.nlse2);
+  p.lse_stride = L.lse_stride;
+  p.lse_out = lse;
+  p.scores = scores;
+  p.status = &hdr->status;
+  p.H = num_heads;
+  p.Hkv = num_kv_heads;
+  p.Tq = total_q;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(float(head_dim));
+  p.c = scale * 1.4426950408889634f;
+  p.timeout_ns = wait_timeout_ns();
+
+  if (stages & TSEL_IMP_STAGE_PASS1) {
+    const CUtensorMap maps[4] = {qm64, qm16, km64, km16};
+    ImpPassParams p1 = p;
+    p1.units = reinterpret_cast<const uint2*>(ws + L.units1);
+    p1.num_units = &hdr->num_units[0];
+    p1.sched_ctr = &hdr->sched_ctr[0];
+    const int grid = int(L.u1_max < sms ? L.u1_max : sms);
+    e = launch_imp_pass(1, head_dim, maps, p1, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pass-1 launch");
+  }
+  if (stages & TSEL_IMP_STAGE_PASS2) {
+    const CUtensorMap maps[4] = {km64, km16, qm64, qm16};
+    ImpPassParams p2 = p;
+    p2.units = reinterpret_cast<const uint2*>(ws + L.units2);
+    p2.num_units = &hdr->num_units[1];
+    p2.sched_ctr = &hdr->sched_ctr[1];
+    const int grid = int(L.u2_max < sms ? L.u2_max : sms);
+    e = launch_imp_pass(2, head_dim, maps, p2, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pass-2 launch");
+  }
+  return TSEL_OK;
+}
+
+tsel_status tsel_select_topk(const float* scores, int total_tokens,
+                             const int32_t* req_tok_offsets, int num_req,
+                             const int32_t* keep_per_req, int total_keep, int32_t* keep_idx,
+                             int32_t* cu_keep, void* workspace, size_t workspace_bytes,
+                             void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (num_req < 0 || total_tokens < 0 || total_keep < 0)
+    return fail(TSEL_ERR_INVALID_VALUE, "negative size");
+  if (req_tok_offsets == nullptr || keep_per_req == nullptr || cu_keep == nullptr ||
+      workspace == nullptr || (total_tokens > 0 && scores == nullptr) ||
+      (total_keep > 0 && keep_idx == nullptr))
+    return fail(TSEL_ERR_INVALID_VALUE, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < kWsHeaderBytes)
+    return fail(TSEL_ERR_WORKSPACE, "workspace must be >= %d bytes, 256-byte aligned",
+                kWsHeaderBytes);
+  if (num_req == 0) {
+    cudaError_t e = cudaMemsetAsync(cu_keep, 0, sizeof(int32_t), stream);
+    return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "memset cu_keep");
+  }
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  cudaError_t e = launch_topk(scores, total_tokens, req_tok_offsets, num_req, keep_per_req,
+                              total_keep, keep_idx, cu_keep, &hdr->status, stream);
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "top-k launch");
+}
+
+tsel_status tsel_gather_compact(const void* hidden, int64_t hidden_row_stride, int hidden_dim,
+                                int elem_bytes, const int32_t* pos, int pos_dim,
+                                const int32_t* cu_seqlens_k, int num_seg, int total_k,
+                                const int32_t* keep_idx, int total_keep, void* out_hidden,
+                                int32_t* out_pos, int32_t* out_img_id, int32_t* out_cu_seqlens,
+                                void* workspace, size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (num_seg < 0 || total_k < 0 || total_keep < 0 || hidden_dim < 0 || pos_dim < 0 ||
+      pos_dim > 8 || !(elem_bytes == 1 || elem_bytes == 2 || elem_bytes == 4 || elem_bytes == 8))
+    return fail(TSEL_ERR_INVALID_VALUE, "bad size argument");
+  if (hidden_row_stride == 0) hidden_row_stride = hidden_dim;
+  const int64_t row_bytes = int64_t(hidden_dim) * elem_bytes;
+  const int64_t stride_bytes = hidden_row_stride * elem_bytes;
+  if (row_bytes % 16 != 0 || stride_bytes % 16 != 0 || hidden_row_stride < hidden_dim ||
+      row_bytes > (int64_t(1) << 30))
+    return fail(TSEL_ERR_INVALID_VALUE, "row bytes %lld / stride %lld not multiples of 16",
+                (long long)row_bytes, (long long)stride_bytes);
+  if (cu_seqlens_k == nullptr || out_cu_seqlens == nullptr || workspace == nullptr)
+    return fail(TSEL_ERR_INVALID_VALUE, "null pointer");
+  if (total_keep > 0 && (keep_idx == nullptr || out_img_id == nullptr ||
+                         (row_bytes > 0 && (hidden == nullptr || out_hidden == nullptr)) ||
+                         (pos_dim > 0 && (pos == nullptr || out_pos == nullptr))))
+    return fail(TSEL_ERR_INVALID_VALUE, "null pointer");
+  if ((hidden && !aligned16(hidden)) || (out_hidden && !aligned16(out_hidden)))
+    return fail(TSEL_ERR_INVALID_VALUE, "hidden buffers must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < kWsHeaderBytes)
+    return fail(TSEL_ERR_WORKSPACE, "workspace must be >= %d bytes, 256-byte aligned",
+                kWsHeaderBytes);
+  int sms = 0;
+  if (sm_count(&sms) != 0) return fail(TSEL_ERR_CUDA, "cannot query the SM count");
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  cudaError_t e = launch_gather(hidden, stride_bytes, int(row_bytes), pos, pos_dim, cu_seqlens_k,
+                                num_seg, total_k, keep_idx, total_keep, out_hidden, out_pos,
+                                out_img_id, out_cu_seqlens, &hdr->status, sms, stream);
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "gather launch");
+}
+
+tsel_status tsel_read_device_status(const void* workspace, uint32_t* bits, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (workspace == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "null workspace");
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "read status");
+  if (bits) *bits = word;
+  return word == 0 ? TSEL_OK : fail(TSEL_ERR_DEVICE_CHECK, "device status 0x%x", word);
+}
+
+tsel_status tsel_clear_device_status(void* workspace, void* stream_) {
+  if (workspace == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "null workspace");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream_));
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "clear status");
+}
+
+tsel_status tsel_probe_ex2(int blocks, int iters, float* sink, void* stream_) {
+  if (blocks < 1 || iters < 1 || sink == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "bad probe args");
+  cudaError_t e = launch_probe_ex2(blocks, iters, sink, static_cast<cudaStream_t>(stream_));
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "probe launch");
+}
+
+}  // extern "C"

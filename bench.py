@@ -1,0 +1,551 @@
+#!/usr/bin/env python3
+"""Benchmark: vision tokens scored + selected per second on one GB300.
+
+One step = the whole hot path over one batch: importance scores (schedule,
+row-LSE pass, column pass), pooled top-B, compaction of hidden rows and
+position ids. Inputs are resident in HBM before the timed region; L2 is
+flushed (a 512 MiB write) between steps and the flush is not timed.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead (the reference arm).
+Replicas only: under torchrun every rank runs its own copy of the workload on
+its own GPU with no data exchange; value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "vision tokens scored+selected/sec at 1 GB300; importance % of roofline"
+DEFAULT_WORKLOAD = "thirty_images"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["attention_score_vision_gb300/csrc/importance.cu",
+                  "attention_score_vision_gb300/csrc/topk.cu",
+                  "attention_score_vision_gb300/csrc/gather.cu",
+                  "attention_score_vision_gb300/csrc/ptx.cuh",
+                  "attention_score_vision_gb300/csrc/common.cuh"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["tsel", "reference"], default="tsel")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-child", nargs=2, metavar=("WORKLOAD", "PAIRS"), help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+def src_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs (run in a child process with single-threaded BLAS)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, pair_budget: float):
+    """Images of the workload, in order, that fit in ~pair_budget attended pairs
+    (at least one image). Returns the list of image indices and their pairs."""
+    import numpy as np
+    nq = np.diff(w.cu_seqlens_q).astype(np.int64)
+    nk = np.diff(w.cu_seqlens_k).astype(np.int64)
+    cost = w.num_heads * nq * nk
+    chosen, pairs = [], 0
+    for g in range(w.num_seg):
+        if pairs + cost[g] <= pair_budget:
+            chosen.append(g)
+            pairs += int(cost[g])
+    if not chosen:
+        g = int(np.argmin(cost))
+        chosen, pairs = [g], int(cost[g])
+    return chosen, pairs
+
+
+def sample_inputs(w, chosen):
+    """Packed inputs of the chosen images as one request (60% keep)."""
+    import numpy as np
+    import workloads as W
+    qs = [w.q_bits[w.cu_seqlens_q[g]:w.cu_seqlens_q[g + 1]] for g in chosen]
+    ks = [w.k_bits[w.cu_seqlens_k[g]:w.cu_seqlens_k[g + 1]] for g in chosen]
+    hs = [w.hidden_bits[w.cu_seqlens_k[g]:w.cu_seqlens_k[g + 1]] for g in chosen]
+    ps = [w.pos[w.cu_seqlens_k[g]:w.cu_seqlens_k[g + 1]] for g in chosen]
+    cu_q = np.concatenate([[0], np.cumsum([len(x) for x in qs])]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum([len(x) for x in ks])]).astype(np.int32)
+    n = int(cu_k[-1])
+    return (np.concatenate(qs), np.concatenate(ks), cu_q, cu_k, np.array([0, n], np.int32),
+            np.array([W.keep_floor(n, 600)], np.int32), np.concatenate(hs), np.concatenate(ps))
+
+
+def time_oracle_sample(w, chosen, pairs) -> dict:
+    import oracle
+    args = sample_inputs(w, chosen)
+    t0 = time.perf_counter()
+    oracle.prune(*args)
+    dt = time.perf_counter() - t0
+    return {"seconds": dt, "images": len(chosen), "tokens": int(args[3][-1]), "pairs": pairs,
+            "full_pairs": w.attended_pairs(), "full_tokens": w.total_k}
+
+
+def cpu_child(workload: str, pair_budget: float) -> dict:
+    import workloads as W
+    w = W.make(workload)
+    chosen, pairs = oracle_sample(w, pair_budget)
+    return time_oracle_sample(w, chosen, pairs)
+
+
+def run_cpu_child(workload: str, pair_budget: float) -> dict:
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = "1"
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", workload,
+                        str(pair_budget)], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_rate(res: dict) -> float:
+    """Tokens/s of the full workload, extrapolated from the sample by attended pairs."""
+    t_full = res["seconds"] * res["full_pairs"] / max(res["pairs"], 1)
+    return res["full_tokens"] / t_full
+
+
+def reference_arm(args) -> None:
+    """The fp64 oracle, as it stands, on a bounded sample per step (1 core)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import workloads as W
+    w = W.make(args.workload)
+    # ~90 s of oracle work in total, spread over warm-up + timed steps
+    budget = max(2e6, REFERENCE_PAIRS_PER_S * 90.0 / max(1, args.steps + args.warmup))
+    chosen, pairs = oracle_sample(w, budget)
+    res = []
+    for i in range(args.warmup + args.steps):
+        r = time_oracle_sample(w, chosen, pairs)
+        if i >= args.warmup:
+            res.append(r)
+    r0 = res[0]
+    rate = statistics.median(cpu_rate(r) for r in res)
+    sample = (f"images {chosen} ({r0['tokens']} tokens, {r0['pairs']:.3g} attended "
+              f"head-query-key pairs) of the {args.workload} workload per step; fp64 numpy, "
+              f"1 BLAS thread; tokens/s extrapolated to the full workload by attended pairs")
+    line = {"metric": METRIC, "value": rate, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(r["seconds"] for r in res),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "l2": "n/a (CPU)", "parallelism": "replicas"},
+            "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh)
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("src_hash") != src_hash(KERNEL_SOURCES):
+        return None
+    return e.get("bytes_per_launch")
+
+
+def gpu_arm(args) -> None:
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    # CPU baseline first (a child process, before this process touches the GPU).
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            cpu = run_cpu_child(args.workload, REFERENCE_PAIRS_PER_S * 15.0)
+        except Exception as exc:  # reported, never fatal
+            cpu = {"error": str(exc)[-300:]}
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import attention_score_vision_gb300 as tsel
+    import workloads as W
+    tsel.build()
+    tsel.load_library()
+
+    w = W.make(args.workload)
+    dev = torch.device("cuda", local)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+
+    host = {"q": bf16(w.q_bits), "k": bf16(w.k_bits), "cu_q": i32(w.cu_seqlens_q),
+            "cu_k": i32(w.cu_seqlens_k), "req_off": i32(w.req_tok_offsets),
+            "keep": i32(w.keep_per_req), "hidden": bf16(w.hidden_bits), "pos": i32(w.pos)}
+    d = {k: v.to(dev) for k, v in host.items()}
+    G, Tq, Tk, H, Hkv, hd = w.num_seg, w.total_q, w.total_k, w.num_heads, w.num_kv_heads, w.head_dim
+    K = w.total_keep
+    D = w.hidden_bits.shape[1]
+    P = w.pos.shape[1]
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(G, Tq, Tk, H), dtype=torch.uint8, device=dev)
+    scores = torch.empty(Tk, dtype=torch.float32, device=dev)
+    lse = torch.empty((H, Tq), dtype=torch.float32, device=dev)
+    keep_idx = torch.empty(K, dtype=torch.int32, device=dev)
+    cu_keep = torch.empty(w.keep_per_req.size + 1, dtype=torch.int32, device=dev)
+    out_h = torch.empty((K, D), dtype=torch.bfloat16, device=dev)
+    out_p = torch.empty((K, P), dtype=torch.int32, device=dev)
+    out_i = torch.empty(K, dtype=torch.int32, device=dev)
+    out_c = torch.empty(G + 1, dtype=torch.int32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    S1, S2, S3 = tsel.TSEL_IMP_STAGE_PREP, tsel.TSEL_IMP_STAGE_PASS1, tsel.TSEL_IMP_STAGE_PASS2
+
+    def importance(flags, q=None, k=None, cu_q=None, cu_k=None):
+        tsel.tsel_importance(q if q is not None else d["q"], k if k is not None else d["k"],
+                             cu_q if cu_q is not None else d["cu_q"],
+                             cu_k if cu_k is not None else d["cu_k"],
+                             w.max_seqlen_q, w.max_seqlen_k, flags=flags, lse=lse, scores=scores,
+                             workspace=ws, stream=stream)
+
+    def topk(req_off=None, keep=None):
+        tsel.tsel_select_topk(scores, req_off if req_off is not None else d["req_off"],
+                              keep if keep is not None else d["keep"], K, keep_idx=keep_idx,
+                              cu_keep=cu_keep, workspace=ws, stream=stream)
+
+    def gather(hidden=None, pos=None, cu_k=None):
+        tsel.tsel_gather_compact(hidden if hidden is not None else d["hidden"],
+                                 pos if pos is not None else d["pos"],
+                                 cu_k if cu_k is not None else d["cu_k"], keep_idx, out_hidden=out_h,
+                                 out_pos=out_p, out_img_id=out_i, out_cu_seqlens=out_c,
+                                 workspace=ws, stream=stream)
+
+    # --- MUFU ex2 peak (probe kernel, best of 3) --------------------------
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    pblocks, piters = sms * 4, 2048
+    sink = torch.empty(pblocks * 512, dtype=torch.float32, device=dev)
+    tsel.tsel_probe_ex2(pblocks, piters, sink)
+    best = None
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        tsel.tsel_probe_ex2(pblocks, piters, sink)
+        b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b) * 1e-3
+        best = t if best is None else min(best, t)
+    ex2_peak = pblocks * 512 * piters * 8 / best        # exp2 / s
+
+    # --- warm-up -----------------------------------------------------------
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        importance(0)
+        topk()
+        gather()
+    torch.cuda.synchronize()
+    if tsel.tsel_read_device_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    # --- timed (device-resident inputs) -------------------------------------
+    names = ["prep", "pass1", "pass2", "topk", "gather"]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e = evs[i]
+        e[0].record(stream)
+        importance(S1)
+        e[1].record(stream)
+        importance(S2)
+        e[2].record(stream)
+        importance(S3)
+        e[3].record(stream)
+        topk()
+        e[4].record(stream)
+        gather()
+        e[5].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    per = {n: [] for n in names}
+    step_ms = []
+    for e in evs:
+        for j, n in enumerate(names):
+            per[n].append(e[j].elapsed_time(e[j + 1]))
+        step_ms.append(e[0].elapsed_time(e[5]))
+    status = tsel.tsel_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status 0x{status:x} after the timed loop")
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * Tk / (ms * 1e-3)
+
+    # --- end to end through the API with host buffers ------------------------
+    e2e = None
+    if not args.no_e2e:
+        pin = {k: v.pin_memory() for k, v in host.items()}
+        dbuf = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        h_keep = torch.empty(K, dtype=torch.int32).pin_memory()
+        h_cu = torch.empty(cu_keep.numel(), dtype=torch.int32).pin_memory()
+        h_img = torch.empty(K, dtype=torch.int32).pin_memory()
+        h_pos = torch.empty((K, P), dtype=torch.int32).pin_memory()
+        h_cuk = torch.empty(G + 1, dtype=torch.int32).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in (h_keep, h_cu, h_img, h_pos, h_cuk))
+
+        def e2e_step():
+            for k2, v in pin.items():
+                dbuf[k2].copy_(v, non_blocking=True)
+            importance(0, dbuf["q"], dbuf["k"], dbuf["cu_q"], dbuf["cu_k"])
+            topk(dbuf["req_off"], dbuf["keep"])
+            gather(dbuf["hidden"], dbuf["pos"], dbuf["cu_k"])
+            h_keep.copy_(keep_idx, non_blocking=True)
+            h_cu.copy_(cu_keep, non_blocking=True)
+            h_img.copy_(out_i, non_blocking=True)
+            h_pos.copy_(out_p, non_blocking=True)
+            h_cuk.copy_(out_c, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(5, min(args.steps, 50))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * Tk / (e2e_ms * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms,
+               "note": "pinned host inputs copied in, importance+top-B+compaction, selection "
+                       "metadata copied out; compacted hidden rows stay on the device"}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # --- roofline ------------------------------------------------------------
+    peaks, peak_src = load_peaks()
+    bf16_peak = peaks["bf16_tflops"] * 1e12
+    hbm_peak = peaks["hbm_gbs"] * 1e9
+    E = w.attended_pairs()
+    med = {n: statistics.median(v) for n, v in per.items()}
+    mean = {n: sum(v) / len(v) for n, v in per.items()}
+
+    def pass_roof(t_ms):
+        t_tensor = 2 * hd * E / bf16_peak
+        t_exp = E / ex2_peak
+        return {"t_tensor_ms": 1e3 * t_tensor, "t_exp_ms": 1e3 * t_exp,
+                "bound": "alu" if t_exp >= t_tensor else "tensor",
+                "frac": max(t_tensor, t_exp) / (t_ms * 1e-3)}
+
+    roof1, roof2 = pass_roof(mean["pass1"]), pass_roof(mean["pass2"])
+    dom = "pass2" if mean["pass2"] >= mean["pass1"] else "pass1"
+    t_dom = mean[dom] * 1e-3
+    if (roof2 if dom == "pass2" else roof1)["bound"] == "alu":
+        roofline = {"kernel": f"imp_pass_kernel<{dom[-1]},{hd}>", "bound": "alu",
+                    "achieved": E / t_dom / 1e9, "peak": ex2_peak / 1e9, "unit": "Gex2/s",
+                    "frac": (E / t_dom) / ex2_peak}
+    else:
+        roofline = {"kernel": f"imp_pass_kernel<{dom[-1]},{hd}>", "bound": "tensor",
+                    "achieved": 2 * hd * E / t_dom / 1e12, "peak": bf16_peak / 1e12,
+                    "unit": "TFLOP/s", "frac": (2 * hd * E / t_dom) / bf16_peak}
+    roofline["traffic"] = load_traffic(roofline["kernel"], args.workload)
+    roofline["peak_source"] = f"{peak_src}; ex2 peak measured by the probe kernel in this run"
+    t_imp = (mean["prep"] + mean["pass1"] + mean["pass2"]) * 1e-3
+    imp_roof = max(4 * hd * E / bf16_peak, 2 * E / ex2_peak)
+    R = w.keep_per_req.size
+    topk_bytes = 4 * Tk + 4 * K + 4 * (R + 1) + 4 * R
+    gather_bytes = K * (2 * 2 * D + 2 * 4 * P + 4 + 4) + 4 * 2 * (G + 1)
+    kernels = {
+        "prep": {"ms": mean["prep"]},
+        "pass1": {"ms": mean["pass1"], **roof1},
+        "pass2": {"ms": mean["pass2"], **roof2},
+        "topk": {"ms": mean["topk"], "GB/s": topk_bytes / (mean["topk"] * 1e-3) / 1e9,
+                 "hbm_frac": topk_bytes / (mean["topk"] * 1e-3) / hbm_peak},
+        "gather": {"ms": mean["gather"], "GB/s": gather_bytes / (mean["gather"] * 1e-3) / 1e9,
+                   "hbm_frac": gather_bytes / (mean["gather"] * 1e-3) / hbm_peak},
+    }
+
+    cpu_baseline = None
+    if cpu is not None and "error" not in cpu:
+        cpu_baseline = {"value": cpu_rate(cpu), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                        "sample": (f"first {cpu['images']} images ({cpu['tokens']} tokens, "
+                                   f"{cpu['pairs']:.3g} attended pairs, {cpu['seconds']:.1f} s) "
+                                   f"of {args.workload}; fp64 numpy, 1 BLAS thread; tokens/s "
+                                   f"extrapolated to the full workload by attended pairs")}
+    elif cpu is not None:
+        cpu_baseline = {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                        "sample": "failed: " + cpu["error"]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "images": G, "visual_tokens": Tk,
+                   "query_tokens": Tq, "heads": H, "kv_heads": Hkv, "head_dim": hd,
+                   "hidden": D, "pos_dim": P, "keep_total": K, "requests": R,
+                   "attended_pairs": E, "l2": "flushed (512 MiB write) between steps, untimed",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "importance_roofline_frac": imp_roof / t_imp,
+        "roofline": roofline,
+        "kernels": kernels,
+        "cpu_baseline": cpu_baseline,
+        "e2e": e2e,
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks,
+        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+                  "ex2_per_s": ex2_peak, "ex2_per_clk_per_sm_at_max":
+                      ex2_peak / sms / (clocks["sm_max_mhz"] * 1e6) if clocks.get("sm_max_mhz") else None,
+                  "source": peak_src},
+        "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+REFERENCE_PAIRS_PER_S = 2.5e7   # rough single-core oracle speed; only sizes the samples
+
+
+def _single_thread_blas():
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        os.environ[v] = "1"
+
+
+def main():
+    args = parse_args()
+    if args.cpu_child or args.impl == "reference":
+        _single_thread_blas()   # before numpy is imported
+    if args.cpu_child:
+        print(json.dumps(cpu_child(args.cpu_child[0], float(args.cpu_child[1]))))
+        return
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+    gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

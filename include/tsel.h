@@ -1,0 +1,234 @@
+/*
+ * tsel.h — C ABI of libtsel: attention-score vision-token pruning on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The library scores every visual token by the mean softmax attention it
+ * receives, keeps the global top-B tokens of each request's pooled candidate
+ * set, and compacts the kept rows with their original indices. It follows:
+ *
+ *   [LiteVLM]  "LiteVLM: A Low-Latency Vision-Language Model Inference
+ *              Pipeline for Resource-Constrained Environments" (paper
+ *              review), section 3.2 "Token Selection Module" and the core
+ *              formula s_j = Attn(h_dec, v_j); keep ratio r.
+ *   [VTC]      The dynamic vision-token compression / SERE article (REDtech),
+ *              section 3.1 (VisionZip: dominant tokens found by attention
+ *              score), section 3.2 (mean attention received per visual token
+ *              at a ViT layer; one candidate pool and one global budget per
+ *              request; blockwise probability recovery from the softmax LSE
+ *              with a column reduction, only per-token scores leave the
+ *              kernel; lengths, image boundaries, original indices and
+ *              positions updated after pruning), section 3.3 (unified top-k).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor arguments are DEVICE pointers owned by the caller; the library
+ *   allocates no device memory and keeps no pointer after a call returns.
+ *   Scratch space is the caller's `workspace` (size from the matching
+ *   *_workspace_size function, 256-byte aligned). One workspace serves one
+ *   call in flight at a time.
+ * - Every call enqueues its kernels on `stream` (a cudaStream_t; NULL is the
+ *   legacy default stream) and returns without synchronising.
+ * - Host-side checks (null pointers, sizes, alignment, supported shapes) fail
+ *   synchronously with TSEL_ERR_INVALID_VALUE or TSEL_ERR_UNSUPPORTED before
+ *   anything is enqueued. A failed launch returns TSEL_ERR_CUDA.
+ * - Checks that need device data (cu_seqlens, offsets, keep counts, keep
+ *   indices) run inside the kernels: a violation sets a bit of the device
+ *   status word held in the first bytes of the workspace (TSEL_DEV_* below),
+ *   and the affected work is skipped without touching memory out of range.
+ *   tsel_read_device_status() returns that word; a fresh workspace must have
+ *   it cleared first (tsel_clear_device_status, or zero-filled memory), since
+ *   calls only ever set bits. Device waits are bounded:
+ *   a wait that runs out sets TSEL_DEV_TIMEOUT and the kernel returns.
+ * - No C++ exception crosses this ABI. There is no CPU fallback.
+ * - Token index arrays are int32; bf16 tensors are row-major with the
+ *   head dimension innermost.
+ */
+#ifndef TSEL_H_
+#define TSEL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TSEL_API __attribute__((visibility("default")))
+#else
+#define TSEL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tsel_status {
+  TSEL_OK = 0,
+  TSEL_ERR_INVALID_VALUE = 1, /* bad pointer, size, stride or alignment */
+  TSEL_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle */
+  TSEL_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned */
+  TSEL_ERR_CUDA = 4,          /* CUDA runtime/driver error (launch, device) */
+  TSEL_ERR_DEVICE_CHECK = 5   /* a device-side check fired (see status word) */
+} tsel_status;
+
+/* Bits of the device status word (tsel_read_device_status). */
+#define TSEL_DEV_SEQLENS   0x1u  /* cu_seqlens not monotone / wrong ends / > max_seqlen */
+#define TSEL_DEV_REQUESTS  0x2u  /* request offsets or keep counts out of range */
+#define TSEL_DEV_KEEP_IDX  0x4u  /* keep_idx out of range or not strictly ascending */
+#define TSEL_DEV_TIMEOUT   0x8u  /* a bounded device wait gave up */
+#define TSEL_DEV_NAN       0x10u /* NaN score given to the top-B selection */
+
+/* tsel_importance flags */
+#define TSEL_IMP_STAGE_PREP   0x100u /* run only the listed stages (none listed = all): */
+#define TSEL_IMP_STAGE_PASS1  0x200u /*   schedule/validation, row-LSE pass, column pass. */
+#define TSEL_IMP_STAGE_PASS2  0x400u /*   Stages must run in order on one stream/workspace. */
+
+/* ------------------------------------------------------------------------ */
+/* Importance scores                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of workspace tsel_importance needs for these sizes. */
+TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int total_k, int num_heads);
+
+/*
+ * Mean attention probability each key token receives ([LiteVLM] section 3.2,
+ * s_j = Attn(h, v_j); [VTC] section 3.2, mean attention received, computed
+ * blockwise from the softmax LSE with a column reduction so the attention
+ * matrix never reaches memory).
+ *
+ * For segment g, queries Q[cu_seqlens_q[g] : cu_seqlens_q[g+1]] attend to
+ * keys K[cu_seqlens_k[g] : cu_seqlens_k[g+1]] (block-diagonal varlen
+ * attention, no causal mask). With s = softmax_scale and kvh(h) = h / (H/Hkv):
+ *   P[h,i,j] = exp(s * q_{i,h} . k_{j,kvh(h)} - lse[h,i]),
+ *   lse[h,i] = log sum_j exp(s * q_{i,h} . k_{j,kvh(h)})     (natural log)
+ *   scores[j] = (1 / (H * Nq_g)) * sum_h sum_i P[h,i,j]
+ * so each segment's scores sum to 1. Keys of a segment with no queries get 0;
+ * query rows of a segment with no keys get lse = -inf.
+ *
+ * q            bf16 [total_q, num_heads, head_dim]; row r starts at
+ *              q + r*q_row_stride elements (0 = dense, num_heads*head_dim).
+ *              16-byte aligned; q_row_stride*2 a multiple of 16.
+ * k            bf16 [total_k, num_kv_heads, head_dim]; same rules.
+ * cu_seqlens_q int32 [num_seg+1] device; cu_seqlens_k int32 [num_seg+1].
+ *              Checked on the device: start 0, monotone, end at total_q /
+ *              total_k, lengths <= max_seqlen_q / max_seqlen_k.
+ * num_heads    H in [1, 256]; num_kv_heads divides it.
+ * head_dim     64, 80, 96, 112 or 128 (else TSEL_ERR_UNSUPPORTED).
+ * softmax_scale  <= 0 selects 1/sqrt(head_dim).
+ * flags        0, or TSEL_IMP_STAGE_* bits.
+ * lse          out fp32 [num_heads, total_q], natural log; may be NULL.
+ * scores       out fp32 [total_k].
+ * workspace    >= tsel_importance_workspace_size(num_seg, total_q, total_k,
+ *              num_heads) bytes; holds the status word and the schedule.
+ */
+TSEL_API tsel_status tsel_importance(const void* q, int64_t q_row_stride,
+                            const void* k, int64_t k_row_stride,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            int num_seg, int total_q, int total_k,
+                            int max_seqlen_q, int max_seqlen_k,
+                            int num_heads, int num_kv_heads, int head_dim,
+                            float softmax_scale, unsigned flags,
+                            float* lse, float* scores,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Pooled global top-B                                                      */
+/* ------------------------------------------------------------------------ */
+
+TSEL_API size_t tsel_select_topk_workspace_size(int num_req);
+
+/*
+ * Per request r, keep the keep_per_req[r] tokens with the largest scores
+ * among tokens [req_tok_offsets[r], req_tok_offsets[r+1]) — every image of
+ * the request in one candidate pool under one budget ([VTC] sections 3.2 and
+ * 3.3; keep ratio r of [LiteVLM] section 3.2 gives B = floor(r*N), see
+ * tsel_keep_count). Order: score descending, ties to the lowest token index
+ * (-0 is treated as +0). Kept token indices are written in ascending order,
+ * requests concatenated; cu_keep[r] is the first output slot of request r.
+ *
+ * scores          fp32 [total_tokens] device (NaN sets TSEL_DEV_NAN; its
+ *                 rank is then unspecified).
+ * req_tok_offsets int32 [num_req+1] device: 0 <= o[r] <= o[r+1] <= total_tokens.
+ * keep_per_req    int32 [num_req] device: 0 <= B_r <= o[r+1]-o[r];
+ *                 sum must equal total_keep (host value, sizes keep_idx).
+ * keep_idx        out int32 [total_keep]; cu_keep out int32 [num_req+1].
+ * A request that fails its checks sets TSEL_DEV_REQUESTS and writes nothing.
+ */
+TSEL_API tsel_status tsel_select_topk(const float* scores, int total_tokens,
+                             const int32_t* req_tok_offsets, int num_req,
+                             const int32_t* keep_per_req, int total_keep,
+                             int32_t* keep_idx, int32_t* cu_keep,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Order-preserving compaction with metadata                                */
+/* ------------------------------------------------------------------------ */
+
+TSEL_API size_t tsel_gather_compact_workspace_size(void);
+
+/*
+ * Compact the kept tokens and rebuild their metadata ([VTC] section 3.2:
+ * after pruning, input lengths, image boundaries, original spatial indices
+ * and position ids must stay consistent for prefill and the KV cache).
+ *
+ * For k in [0, total_keep), t = keep_idx[k]:
+ *   out_hidden[k, :] = hidden[t, :]          (bytes copied unchanged)
+ *   out_pos[k, :]    = pos[t, :]
+ *   out_img_id[k]    = g with cu_seqlens_k[g] <= t < cu_seqlens_k[g+1]
+ * and out_cu_seqlens[g] = number of kept tokens below cu_seqlens_k[g]
+ * (the kept per-image lengths, prefix-summed). keep_idx itself is the
+ * original-index output.
+ *
+ * hidden         [total_k rows], row t at hidden + t*hidden_row_stride
+ *                elements of elem_bytes each; hidden_dim*elem_bytes and
+ *                hidden_row_stride*elem_bytes multiples of 16; 16-byte aligned.
+ * pos            int32 [total_k, pos_dim] dense (pos_dim in [0, 8]; NULL
+ *                allowed when pos_dim == 0).
+ * cu_seqlens_k   int32 [num_seg+1] device.
+ * keep_idx       int32 [total_keep] device, strictly ascending, in
+ *                [0, total_k) (else TSEL_DEV_KEEP_IDX and the row is skipped).
+ * out_hidden     [total_keep, hidden_dim] dense, 16-byte aligned.
+ * out_pos        int32 [total_keep, pos_dim] (NULL when pos_dim == 0).
+ * out_img_id     int32 [total_keep]; out_cu_seqlens int32 [num_seg+1].
+ */
+TSEL_API tsel_status tsel_gather_compact(const void* hidden, int64_t hidden_row_stride,
+                                int hidden_dim, int elem_bytes,
+                                const int32_t* pos, int pos_dim,
+                                const int32_t* cu_seqlens_k, int num_seg, int total_k,
+                                const int32_t* keep_idx, int total_keep,
+                                void* out_hidden, int32_t* out_pos,
+                                int32_t* out_img_id, int32_t* out_cu_seqlens,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Host helpers                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Budget at keep ratio keep_permille/1000: floor(n_tokens*keep_permille/1000)
+ * in 64-bit integer arithmetic ([LiteVLM] section 3.2 and its results table:
+ * r = 0.8 of 896 visual tokens keeps 716, so 716 + 142 text = 858 tokens).
+ * Returns -1 for negative arguments. */
+TSEL_API int tsel_keep_count(int n_tokens, int keep_permille);
+
+/* Reads the device status word of `workspace` after synchronising `stream`.
+ * *bits receives the TSEL_DEV_* bits (may be NULL). Returns TSEL_OK when the
+ * word is zero, TSEL_ERR_DEVICE_CHECK when any bit is set, TSEL_ERR_CUDA on a
+ * CUDA error. */
+TSEL_API tsel_status tsel_read_device_status(const void* workspace, uint32_t* bits, void* stream);
+
+/* Enqueues a reset of the device status word to zero. */
+TSEL_API tsel_status tsel_clear_device_status(void* workspace, void* stream);
+
+TSEL_API const char* tsel_status_string(tsel_status s);
+
+/* Detail of the last non-OK status returned on this host thread. */
+TSEL_API const char* tsel_last_error(void);
+
+/* Measurement probe: enqueues a kernel of `blocks` x 512 threads, each thread
+ * issuing `iters` x 8 dependent-chain ex2.approx.f32 operations (a MUFU
+ * throughput probe; the count of exp2 per launch is blocks*512*iters*8).
+ * `sink` receives one float per thread so nothing is optimised away. */
+TSEL_API tsel_status tsel_probe_ex2(int blocks, int iters, float* sink, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSEL_H_ */

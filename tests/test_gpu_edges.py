@@ -1,0 +1,202 @@
+"""GPU edge cases: ragged and empty segments, one-key segments, segments
+without queries, every supported head_dim, GQA ratios, strided (packed QKV)
+inputs, closed forms, top-B ties and budgets at the extremes, and the device
+status word for malformed metadata (checked on the device, no fault)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_util import REL_TOL, bits_to_bf16, check_selection_exact, i32, max_rel_err, run_path
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tsel():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_score_vision_gb300 as t
+    t.build()
+    t.load_library()
+    return t
+
+
+def _importance(tsel, w, **kw):
+    q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
+                     dtype=torch.uint8, device="cuda")
+    s, lse = tsel.tsel_importance(q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k),
+                                  max(w.max_seqlen_q, 1), max(w.max_seqlen_k, 1), workspace=ws, **kw)
+    st = tsel.tsel_read_device_status(ws)
+    return s.cpu().numpy(), lse.cpu().numpy(), st
+
+
+@pytest.mark.parametrize("d", [64, 80, 96, 112, 128])
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (8, 2)])
+def test_head_dims_and_gqa(tsel, d, H, Hkv):
+    L = [1, 127, 128, 129, 257]
+    w = W.make_segments(L, L, H, Hkv, d, seed=200 + d + H, sink_counts=[0, 1, 2, 3, 4], hidden_dim=64)
+    s, lse, st = _importance(tsel, w)
+    assert st == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
+
+
+def test_long_segment_4096_and_cross_lengths(tsel):
+    w = W.make_segments([4096, 5, 300], [4096, 777, 3], 2, 1, 64, seed=301, sink_counts=[40, 7, 0],
+                        hidden_dim=64)
+    s, lse, st = _importance(tsel, w)
+    assert st == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
+
+
+def test_empty_segments_and_missing_queries(tsel):
+    # segment 1 is empty, segment 2 has keys but no queries (scores 0),
+    # segment 3 has queries but no keys (lse -inf)
+    w = W.make_segments([50, 0, 0, 9, 130], [60, 0, 33, 0, 1], 4, 4, 64, seed=302, hidden_dim=64)
+    s, lse, st = _importance(tsel, w)
+    assert st == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    assert np.all(s[60:93] == 0)
+    assert s[93] == pytest.approx(1.0, rel=1e-6)      # one-key segment
+    assert np.all(np.isneginf(lse[:, 50:59]))
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=1e-5, atol=1e-4)
+
+
+def test_zero_queries_uniform_and_one_hot_closed_form(tsel):
+    nq, nk, d, H = 130, 300, 64, 2
+    q = np.zeros((nq, H, d), np.float32)
+    q[:, :, 0] = 2.0
+    k = np.zeros((nk, H, d), np.float32)
+    k[123, :, 0] = 2.0
+    w = W.Workload("onehot", W.f32_to_bf16_bits(q), W.f32_to_bf16_bits(k), np.array([0, nq], np.int32),
+                   np.array([0, nk], np.int32), np.array([0, nk], np.int32), np.array([10], np.int32),
+                   np.zeros((nk, 8), np.uint16), np.zeros((nk, 1), np.int32), 1 / 8)
+    s, lse, st = _importance(tsel, w)
+    c = math.exp(4.0 / 8.0)
+    expect = np.full(nk, 1 / (c + nk - 1))
+    expect[123] = c / (c + nk - 1)
+    assert np.max(np.abs(s - expect) / expect) <= REL_TOL
+    np.testing.assert_allclose(lse, math.log(c + nk - 1), rtol=1e-5)
+    w.q_bits[:] = 0
+    s0, _, _ = _importance(tsel, w)
+    np.testing.assert_allclose(s0, 1 / nk, rtol=REL_TOL)
+
+
+def test_strided_packed_qkv_rows(tsel):
+    """q and k as views into one packed [T, 3, H, d] buffer (row stride 3*H*d)."""
+    L = [200, 90]
+    w = W.make_segments(L, L, 4, 4, 80, seed=303, sink_counts=[2, 1], hidden_dim=64)
+    T, H, d = w.total_q, 4, 80
+    packed = torch.zeros((T, 3, H, d), dtype=torch.bfloat16, device="cuda")
+    packed[:, 0] = bits_to_bf16(w.q_bits)
+    packed[:, 1] = bits_to_bf16(w.k_bits)
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(2, T, T, H), dtype=torch.uint8, device="cuda")
+    s, _ = tsel.tsel_importance(packed[:, 0], packed[:, 1], i32(w.cu_seqlens_q), i32(w.cu_seqlens_k),
+                                200, 200, workspace=ws)
+    _, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s.cpu().numpy(), s_ref) <= REL_TOL
+    assert tsel.tsel_read_device_status(ws) == 0
+
+
+def test_explicit_softmax_scale(tsel):
+    w = W.make_segments([100], [140], 4, 4, 64, seed=304, hidden_dim=64)
+    s, lse, st = _importance(tsel, w, softmax_scale=0.05)
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k, 0.05)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
+
+
+# ---------------------------------------------------------------- top-B / gather
+
+def _topk(tsel, scores, off, keep):
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    k_idx, cu = tsel.tsel_select_topk(torch.from_numpy(np.asarray(scores, np.float32)).cuda(), i32(off),
+                                      i32(keep), int(np.sum(keep)), workspace=ws)
+    return k_idx.cpu().numpy(), cu.cpu().numpy(), tsel.tsel_read_device_status(ws)
+
+
+def test_topk_ties_and_extreme_budgets(tsel):
+    rng = np.random.default_rng(5)
+    for n, vals in [(1, 3), (9, 2), (1000, 3), (5000, 1), (70000, 40)]:
+        s = rng.integers(0, vals, n).astype(np.float32) * 0.125
+        for B in sorted({0, 1, n // 3, n - 1, n}):
+            if B < 0:
+                continue
+            got, cu, st = _topk(tsel, s, [0, n], [B])
+            ref, cref = oracle.select_topk(s, [0, n], [B])
+            assert st == 0
+            assert np.array_equal(got, ref), (n, B)
+            assert np.array_equal(cu, cref)
+
+
+def test_topk_many_requests_and_negative_zero(tsel):
+    rng = np.random.default_rng(6)
+    s = rng.random(3000).astype(np.float32)
+    s[::7] = -0.0
+    s[1::7] = 0.0
+    off = [0, 0, 10, 1000, 1001, 3000]
+    keep = [0, 10, 300, 0, 1500]
+    got, cu, st = _topk(tsel, s, off, keep)
+    ref, cref = oracle.select_topk(np.where(s == 0, 0.0, s).astype(np.float32), off, keep)
+    assert st == 0 and np.array_equal(got, ref) and np.array_equal(cu, cref)
+
+
+def test_gather_fp32_rows_and_no_pos(tsel):
+    hidden = torch.randn(500, 12, device="cuda", dtype=torch.float32)
+    cu = i32([0, 100, 100, 500])
+    keep = torch.tensor([0, 5, 99, 100, 499], dtype=torch.int32, device="cuda")
+    oh, op, oi, oc = tsel.tsel_gather_compact(hidden, None, cu, keep)
+    assert op is None
+    assert torch.equal(oh, hidden[keep.long()])
+    assert oi.tolist() == [0, 0, 0, 2, 2]
+    assert oc.tolist() == [0, 3, 3, 5]
+
+
+def test_full_selection_bit_exact_on_mid_size(tsel):
+    w = W.make_segments([333, 1200, 17], [333, 1200, 17], 4, 4, 64, seed=305, hidden_dim=1280,
+                        pos_dim=3, requests=[2, 1], keep_per_req=[900, 5])
+    out = run_path(tsel, w)
+    assert out["status"] == 0
+    check_selection_exact(w, out)
+
+
+# ---------------------------------------------------------------- device checks
+
+def test_malformed_cu_seqlens_sets_status(tsel):
+    q = torch.zeros((10, 2, 64), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(2, 10, 10, 2), dtype=torch.uint8, device="cuda")
+    for cu in ([0, 7, 5], [0, 5, 9], [1, 5, 10], [0, 9, 10]):
+        tsel.tsel_clear_device_status(ws)
+        # [0, 9, 10] violates max_seqlen = 8
+        tsel.tsel_importance(q, q, i32(cu), i32([0, 5, 10]), 8, 8, workspace=ws)
+        assert tsel.tsel_read_device_status(ws) & tsel.TSEL_DEV_SEQLENS, cu
+
+
+def test_bad_requests_and_keep_idx_set_status(tsel):
+    s = torch.rand(100, device="cuda")
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    tsel.tsel_select_topk(s, i32([0, 50, 100]), i32([10, 60]), 70, workspace=ws)   # 60 > 50 tokens
+    assert tsel.tsel_read_device_status(ws) & tsel.TSEL_DEV_REQUESTS
+    tsel.tsel_clear_device_status(ws)
+    tsel.tsel_select_topk(s, i32([0, 50, 100]), i32([10, 20]), 31, workspace=ws)   # sum != total
+    assert tsel.tsel_read_device_status(ws) & tsel.TSEL_DEV_REQUESTS
+    tsel.tsel_clear_device_status(ws)
+    s[3] = float("nan")
+    tsel.tsel_select_topk(s, i32([0, 100]), i32([10]), 10, workspace=ws)
+    assert tsel.tsel_read_device_status(ws) & tsel.TSEL_DEV_NAN
+    tsel.tsel_clear_device_status(ws)
+    hidden = torch.zeros((20, 8), dtype=torch.bfloat16, device="cuda")
+    for bad in ([3, 2], [1, 20], [-1, 4]):
+        tsel.tsel_clear_device_status(ws)
+        tsel.tsel_gather_compact(hidden, None, i32([0, 20]), i32(bad), workspace=ws)
+        assert tsel.tsel_read_device_status(ws) & tsel.TSEL_DEV_KEEP_IDX, bad
