@@ -18,7 +18,7 @@ from ._build import LIB_PATH, build
 
 __all__ = [
     "TselError", "load_library", "build",
-    "tsel_importance_workspace_size", "tsel_importance",
+    "tsel_importance_workspace_size", "tsel_importance", "tsel_importance_noalloc",
     "tsel_select_topk_workspace_size", "tsel_select_topk",
     "tsel_gather_compact_workspace_size", "tsel_gather_compact",
     "tsel_keep_count", "tsel_read_device_status", "tsel_clear_device_status",
@@ -63,6 +63,9 @@ _SIGNATURES = {
     "tsel_status_string": (ctypes.c_char_p, [_c_int]),
     "tsel_last_error": (ctypes.c_char_p, []),
     "tsel_probe_ex2": (_c_int, [_c_int, _c_int, _p, _p]),
+    "tsel_importance_noalloc": (_c_int, [_p, _c_i64, _p, _c_i64, _p, _p, _c_int, _c_int, _c_int,
+                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _p, _p,
+                                         _p, _p]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -162,6 +165,34 @@ def tsel_importance(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torch.Tensor
                              _ptr(cu_seqlens_k), G, tq, tk, int(max_seqlen_q), int(max_seqlen_k),
                              H, Hkv, d, float(softmax_scale), int(flags), _ptr(lse), _ptr(scores),
                              _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(st)
+    return scores, lse
+
+
+def tsel_importance_noalloc(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                            cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int, *,
+                            softmax_scale: float = 0.0, lse: Optional[torch.Tensor] = None,
+                            scores: Optional[torch.Tensor] = None,
+                            device_status: Optional[torch.Tensor] = None, want_lse: bool = True,
+                            stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """tsel_importance with the library's static scratch array instead of a
+    workspace (for callers that cannot allocate device memory). Output
+    tensors passed in are used as they are; calls on one device must not
+    overlap on the GPU."""
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.bfloat16, "k")
+    tq, H, d = q.shape
+    tk, Hkv, _ = k.shape
+    G = cu_seqlens_k.numel() - 1
+    dev = q.device
+    if scores is None:
+        scores = torch.empty(tk, dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((H, tq), dtype=torch.float32, device=dev)
+    st = load_library().tsel_importance_noalloc(
+        _ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), G, tq,
+        tk, int(max_seqlen_q), int(max_seqlen_k), H, Hkv, d, float(softmax_scale), _ptr(lse),
+        _ptr(scores), _ptr(device_status), _stream(stream, dev))
     _check(st)
     return scores, lse
 

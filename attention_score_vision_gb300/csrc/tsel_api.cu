@@ -113,6 +113,11 @@ uint64_t wait_timeout_ns() {
 
 }  // namespace
 
+namespace tsel {
+// Lets other translation units of the library report a detailed error.
+void record_error(const char* msg) { g_last_error = msg; }
+}  // namespace tsel
+
 extern "C" {
 
 const char* tsel_status_string(tsel_status s) {

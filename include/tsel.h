@@ -128,6 +128,35 @@ TSEL_API tsel_status tsel_importance(const void* q, int64_t q_row_stride,
                             float* lse, float* scores,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Same scores as tsel_importance, for callers that cannot allocate device
+ * memory and have no workspace to pass: plugins of an inference engine whose
+ * memory pool already owns all of HBM, or embedded/automotive stacks that
+ * forbid allocation after start-up. None of the pages has a counterpart of
+ * this entry point; it is a deployment convenience.
+ *
+ * Scratch comes from one static device array of 16 MiB inside the library
+ * (held by every GPU that loads the library until the process exits). A
+ * problem whose tsel_importance_workspace_size() exceeds 16 MiB is rejected
+ * with TSEL_ERR_WORKSPACE. The call allocates nothing (no cudaMalloc, no
+ * library allocator). The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture. Every call on a device shares the
+ * array: its status word is cleared at the start of each call, and calls that
+ * overlap on the GPU race on the array, so serialise them.
+ *
+ * Arguments are those of tsel_importance (flags fixed to 0). device_status,
+ * if not NULL, is a device uint32 that receives this call's TSEL_DEV_* bits.
+ */
+TSEL_API tsel_status tsel_importance_noalloc(const void* q, int64_t q_row_stride,
+                                             const void* k, int64_t k_row_stride,
+                                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                             int num_seg, int total_q, int total_k,
+                                             int max_seqlen_q, int max_seqlen_k,
+                                             int num_heads, int num_kv_heads, int head_dim,
+                                             float softmax_scale, float* lse, float* scores,
+                                             uint32_t* device_status, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Pooled global top-B                                                      */
 /* ------------------------------------------------------------------------ */
