@@ -246,6 +246,22 @@ def load_traffic(kernel: str, workload: str):
     return e.get("bytes_per_launch")
 
 
+def reduce_max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank value over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_replica: int, world: int, ms_max: float) -> float:
+    """Whole-job tokens/s: every rank processed its own replica of the workload."""
+    return world * tokens_per_replica / (ms_max * 1e-3)
+
+
 def gpu_arm(args) -> None:
     import numpy as np
     import torch
@@ -386,12 +402,8 @@ def gpu_arm(args) -> None:
     if status != 0:
         raise RuntimeError(f"device status 0x{status:x} after the timed loop")
     ms_local = sum(step_ms) / len(step_ms)
-    ms = ms_local
-    if world > 1:
-        t = torch.tensor([ms_local], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * Tk / (ms * 1e-3)
+    ms = reduce_max_over_ranks(ms_local, dev)
+    value = replica_throughput(Tk, world, ms)
 
     # --- end to end through the API with host buffers ------------------------
     e2e = None
@@ -428,12 +440,8 @@ def gpu_arm(args) -> None:
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / n_e2e
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * Tk / (e2e_ms * 1e-3), "unit": "tokens/s",
+        e2e_ms = reduce_max_over_ranks(a.elapsed_time(b) / n_e2e, dev)
+        e2e = {"value": replica_throughput(Tk, world, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms,
                "note": "pinned host inputs copied in, importance+top-B+compaction, selection "
