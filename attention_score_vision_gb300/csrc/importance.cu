@@ -8,23 +8,31 @@
 // Three launches on one stream:
 //   prep   one CTA: checks cu_seqlens, sorts segments by cost (longest first)
 //          and writes the unit lists of both passes into the workspace.
-//   pass 1 units (segment, head, 128-query tile): S = Q K^T tile by tile on
-//          the tensor cores (tcgen05, accumulators in TMEM), online max/sum
-//          per query row -> row LSE (kept as -LSE*log2 e, 128-row padded).
-//   pass 2 units (segment, 128-key tile), all heads: S^T = K Q^T with the
-//          keys on the MMA M dimension, so each epilogue thread owns one key
-//          and sums exp2(S*c - LSE2) over the query columns in registers:
-//          the column reduction needs no shuffles and no atomics, and the
-//          result is deterministic.
+//   pass 1 units (segment, head, 256 query rows = two 128-row A tiles):
+//          S = Q K^T tile by tile on the tensor cores (tcgen05, accumulators
+//          in TMEM), each 128-key B tile multiplied by both A tiles, online
+//          max/sum per query row -> row LSE (kept as -LSE*log2 e, padded to
+//          128-row tiles per segment).
+//   pass 2 units (segment, 256 keys), all heads: S^T = K Q^T with the keys
+//          on the MMA M dimension, so each epilogue thread owns one key and
+//          sums exp2(S*c - LSE2) over the query columns in registers: the
+//          column reduction needs no shuffles and no atomics, and the result
+//          is deterministic.
+// Two A tiles per unit halve the operand bytes each B tile costs per element
+// (the shared-memory feed, not the tensor cores, limited 128-row units).
 //
-// CTA layout (384 threads, one CTA per SM, persistent, units fetched from a
+// CTA layout (576 threads, one CTA per SM, persistent, units fetched from a
 // global counter in longest-first order):
-//   warp 0      TMA producer (Q/K tiles, LSE slices)
-//   warp 1      TMEM allocator + MMA issuer (one thread)
-//   warps 2-3   idle
-//   warps 4-11  two epilogue warpgroups; warp w reads TMEM lanes 32*(w%4)..,
-//               warpgroup 0 takes columns 0-63 of each 128-column tile,
-//               warpgroup 1 columns 64-127; the halves are merged per unit.
+//   warp 0      TMA producer (A tile pairs, B tiles, LSE slices)
+//   warp 1      TMEM allocator + MMA issuer (one thread): per B tile, one
+//               128x128 accumulator for each A tile
+//   warps 2-17  four epilogue warpgroups; warpgroup 2*par + a owns TMEM
+//               accumulator 2*par + a (A tile a, B tiles of parity par);
+//               warp w reads TMEM lanes 32*(w%4).. . Each warp loads its
+//               128 columns in 32-column pieces, the next piece in flight
+//               while the current one is computed. The math is packed (f32x2
+//               FMA/ADD, 3-input max), one MUFU exp2 per element. The two
+//               warpgroups of an A tile merge their partials once per unit.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -35,11 +43,13 @@ namespace tsel {
 using namespace ptx;
 
 constexpr float kNegInf = -__builtin_huge_valf();
-constexpr int kAccBufs = 4;      // TMEM accumulators of 128 columns (512 columns)
-constexpr int kLseSlots = 8;     // LSE slices in flight (pass 2)
-constexpr int kSchedSlots = 4;   // scheduler ring depth
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 384;
+constexpr int kPair = 2 * kTile;    // A rows per unit: two 128-row A tiles
+constexpr int kAccBufs = 4;         // TMEM accumulators of 128 columns (512 columns)
+constexpr int kLseSlots = 8;        // LSE slices in flight (pass 2)
+constexpr int kSchedSlots = 4;      // scheduler ring depth
+constexpr int kEpiWarps = 16;       // four warpgroups
+constexpr int kEpiFirstWarp = 2;
+constexpr int kThreads = 32 * (kEpiFirstWarp + kEpiWarps);  // 576
 
 template <int D>
 struct TileCfg {
@@ -47,17 +57,19 @@ struct TileCfg {
   static constexpr int N64 = D / 64;               // 64-column chunks (128-byte swizzle)
   static constexpr int N16 = (D % 64) / 16;        // 16-column chunks (32-byte swizzle)
   static constexpr int TILE_BYTES = kTile * D * 2; // one 128-row bf16 tile
-  static constexpr int STAGES_RAW = (196608 - 2 * TILE_BYTES) / TILE_BYTES;
+  static constexpr int A_BYTES = 4 * TILE_BYTES;   // 2 slots x 2 A tiles
+  static constexpr int STAGES_RAW = (200 * 1024 - A_BYTES - 8192) / TILE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = 2 * TILE_BYTES;
+  static constexpr int OFF_B = A_BYTES;
   static constexpr int OFF_LSE = OFF_B + STAGES * TILE_BYTES;
   static constexpr int OFF_COMB = OFF_LSE + kLseSlots * kTile * 4;
-  static constexpr int OFF_BAR = OFF_COMB + 2 * 2 * kTile * 4;
+  static constexpr int OFF_BAR = OFF_COMB + 2 * 2 * 2 * kTile * 4;
   static constexpr int NUM_BARS = 2 + 2 + 2 * STAGES + 2 * kAccBufs + 2 * kLseSlots +
-                                  2 * kSchedSlots + 2 + 2 + 1;
+                                  2 * kSchedSlots + 4 + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  static_assert(STAGES >= 2, "at least double-buffered B tiles");
   static_assert(TILE_BYTES % 1024 == 0, "tiles stay 1024-byte aligned");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
@@ -175,12 +187,12 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
   bucket_positions_desc(pos1, G, hist, warp_sums);
   bucket_positions_desc(pos2, G, hist, warp_sums);
   for (int g = threadIdx.x; g < G; g += 1024) {
-    const int nqt = int(ceil_div(cu_q[g + 1] - cu_q[g], kTile));
-    const int nkt = int(ceil_div(cu_k[g + 1] - cu_k[g], kTile));
+    const int nqp = int(ceil_div(cu_q[g + 1] - cu_q[g], kPair));
+    const int nkp = int(ceil_div(cu_k[g + 1] - cu_k[g], kPair));
     inv1[pos1[g]] = g;
     inv2[pos2[g]] = g;
-    start1[pos1[g]] = H * nqt;
-    start2[pos2[g]] = nkt;
+    start1[pos1[g]] = H * nqp;
+    start2[pos2[g]] = nkp;
   }
   __syncthreads();
   const int total1 = block_scan_array(start1, G, warp_sums);
@@ -191,17 +203,17 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = warp; i < G; i += 32) {
     const int g = inv1[i];
-    const int nqt = int(ceil_div(cu_q[g + 1] - cu_q[g], kTile));
-    const int n = H * nqt;
+    const int nqp = int(ceil_div(cu_q[g + 1] - cu_q[g], kPair));
+    const int n = H * nqp;
     const int s = start1[i];
     for (int j = lane; j < n; j += 32) {
-      const int h = j / nqt, qt = j - h * nqt;
-      units1[s + j] = make_uint2(uint32_t(g), (uint32_t(h) << 24) | uint32_t(qt));
+      const int h = j / nqp, qp = j - h * nqp;
+      units1[s + j] = make_uint2(uint32_t(g), (uint32_t(h) << 24) | uint32_t(qp));
     }
     const int g2 = inv2[i];
-    const int nkt = int(ceil_div(cu_k[g2 + 1] - cu_k[g2], kTile));
+    const int nkp = int(ceil_div(cu_k[g2 + 1] - cu_k[g2], kPair));
     const int s2 = start2[i];
-    for (int j = lane; j < nkt; j += 32) units2[s2 + j] = make_uint2(uint32_t(g2), uint32_t(j));
+    for (int j = lane; j < nkp; j += 32) units2[s2 + j] = make_uint2(uint32_t(g2), uint32_t(j));
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -215,7 +227,8 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
 // ---------------------------------------------------------------------------
 
 struct Unit {
-  int g, h, tile, q0, nq, k0, nk;
+  int g, h, pair, q0, nq, k0, nk;
+  int nA;  // valid 128-row A tiles in this unit's 256-row pair (1 or 2)
 };
 
 template <int PASS>
@@ -224,15 +237,17 @@ __device__ __forceinline__ Unit decode_unit(const ImpPassParams& p, uint2 u) {
   r.g = int(u.x);
   if (PASS == 1) {
     r.h = int(u.y >> 24);
-    r.tile = int(u.y & 0xFFFFFFu);
+    r.pair = int(u.y & 0xFFFFFFu);
   } else {
     r.h = 0;
-    r.tile = int(u.y);
+    r.pair = int(u.y);
   }
   r.q0 = __ldg(p.cu_q + r.g);
   r.nq = __ldg(p.cu_q + r.g + 1) - r.q0;
   r.k0 = __ldg(p.cu_k + r.g);
   r.nk = __ldg(p.cu_k + r.g + 1) - r.k0;
+  const int rows_left = (PASS == 1 ? r.nq : r.nk) - r.pair * kPair;
+  r.nA = rows_left > kTile ? 2 : 1;
   return r;
 }
 
@@ -286,6 +301,68 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag, timeout_ns));
 }
 
+// Online softmax of one query row over 32 columns of S (pass 1). Columns at
+// or beyond `valid` lie outside the segment. m is a reference max of S*c and l
+// the sum of exp2(S*c - m); m only moves when the chunk max exceeds it by
+// more than 8 (terms stay below 2^8), so rescaling is rare.
+__device__ __forceinline__ void row_softmax_chunk(const uint32_t (&r)[32], int valid, float c,
+                                                  uint64_t c2, float& m, float& l,
+                                                  uint64_t (&a)[2]) {
+  if (valid <= 0) return;
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  if (valid < 32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < valid ? v[j] : kNegInf;
+  }
+  float t0 = fmax3(v[0], v[1], v[2]), t1 = fmax3(v[3], v[4], v[5]);
+#pragma unroll
+  for (int j = 6; j < 30; j += 4) {
+    t0 = fmax3(t0, v[j], v[j + 1]);
+    t1 = fmax3(t1, v[j + 2], v[j + 3]);
+  }
+  const float tmax = fmax3(t0, t1, fmaxf(v[30], v[31])) * c;
+  if (tmax > m + 8.f) {
+    // also covers the first chunk of a row (m = -inf, l = 0)
+    const float s = ex2(m - tmax);
+    float x0, x1;
+    unpack2(fadd2(a[0], a[1]), x0, x1);
+    l = (l + x0 + x1) * s;
+    a[0] = 0ull;
+    a[1] = 0ull;
+    m = tmax;
+  }
+  if (m > kNegInf) {
+    const uint64_t nm2 = pack2(-m, -m);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float x0, x1;
+      unpack2(ffma2(pack2(v[2 * j], v[2 * j + 1]), c2, nm2), x0, x1);
+      a[j & 1] = fadd2(a[j & 1], pack2(ex2(x0), ex2(x1)));
+    }
+  }
+}
+
+// Adds exp2(S*c - LSE2) of 32 query columns into the packed per-key
+// accumulators (pass 2). nl holds -LSE2 of those columns (-inf for padding).
+__device__ __forceinline__ void column_sum_chunk(const uint32_t (&r)[32], const float4* nl,
+                                                 uint64_t c2, uint64_t (&acc)[2]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 t = nl[j];
+    float x0, x1, x2, x3;
+    unpack2(ffma2(pack2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), c2,
+                  pack2(t.x, t.y)),
+            x0, x1);
+    unpack2(ffma2(pack2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), c2,
+                  pack2(t.z, t.w)),
+            x2, x3);
+    acc[0] = fadd2(acc[0], pack2(ex2(x0), ex2(x1)));
+    acc[1] = fadd2(acc[1], pack2(ex2(x2), ex2(x3)));
+  }
+}
+
 template <int PASS, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     imp_pass_kernel(const __grid_constant__ CUtensorMap mapA64,
@@ -298,10 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 128-byte swizzle atoms key off shared-address bits: align the carve-out
   // on the shared-window address itself.
   uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
-  uint8_t* sA = smem + C::OFF_A;
-  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* sA = smem + C::OFF_A;   // [2 slots][2 tiles]
+  uint8_t* sB = smem + C::OFF_B;   // [S stages]
   float* sLse = reinterpret_cast<float*>(smem + C::OFF_LSE);
-  float* sComb = reinterpret_cast<float*>(smem + C::OFF_COMB);
+  float* sComb = reinterpret_cast<float*>(smem + C::OFF_COMB);  // [A half][buf][m|l][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* a_full = bars;
   uint64_t* a_empty = a_full + 2;
@@ -313,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* lse_empty = lse_full + kLseSlots;
   uint64_t* sch_full = lse_empty + kLseSlots;
   uint64_t* sch_empty = sch_full + kSchedSlots;
-  uint64_t* comb_full = sch_empty + kSchedSlots;
-  uint64_t* comb_empty = comb_full + 2;
-  uint64_t* mma_done = comb_empty + 2;
+  uint64_t* comb_full = sch_empty + kSchedSlots;  // [A half][buf]
+  uint64_t* comb_empty = comb_full + 4;
+  uint64_t* mma_done = comb_empty + 4;
   int* sched = reinterpret_cast<int*>(smem + C::OFF_MISC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched + kSchedSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sched + kSchedSlots + 1);
@@ -327,6 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&a_full[i], 1);
       mbar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&comb_full[i], 4);
       mbar_init(&comb_empty[i], 4);
     }
@@ -336,11 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kAccBufs; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kEpiWarps);
+      mbar_init(&acc_empty[i], 4);           // the owning warpgroup
     }
     for (int i = 0; i < kLseSlots; ++i) {
       mbar_init(&lse_full[i], 1);
-      mbar_init(&lse_empty[i], kEpiWarps);
+      mbar_init(&lse_empty[i], 8);           // both warpgroups of the B-tile parity
     }
     for (int i = 0; i < kSchedSlots; ++i) {
       mbar_init(&sch_full[i], 1);
@@ -370,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int s_it = 0, a_it = 0, b_it = 0, l_it = 0;
+      int s_it = 0, a_it = 0, b_it = 0;
       bool ok = true;
       while (ok) {
         const int slot = s_it % kSchedSlots;
@@ -385,52 +464,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++s_it;
         if (u < 0) break;
         const Unit w = decode_unit<PASS>(p, p.units[u]);
-        if (PASS == 1) {
-          const int nkt = int(ceil_div(w.nk, kTile));
-          if (nkt == 0) continue;
+        const int n_b = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
+        if (n_b == 0) continue;
+        const int n_agroups = PASS == 1 ? 1 : p.Hkv;
+        const int qtile_base = PASS == 2 ? __ldg(p.qtile_off + w.g) : 0;
+        for (int ag = 0; ag < n_agroups && ok; ++ag) {
           const int as = a_it & 1;
           if (!wait_bounded(&a_empty[as], ((a_it >> 1) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
-          mbar_arrive_expect_tx(&a_full[as], C::TILE_BYTES);
-          load_tile<D>(sA + as * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as], w.h * D,
-                       w.q0 + w.tile * kTile);
+          mbar_arrive_expect_tx(&a_full[as], uint32_t(w.nA * C::TILE_BYTES));
+          const int ax = PASS == 1 ? w.h * D : ag * D;
+          const int ay = (PASS == 1 ? w.q0 : w.k0) + w.pair * kPair;
+          for (int a = 0; a < w.nA; ++a)
+            load_tile<D>(sA + (as * 2 + a) * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as], ax,
+                         ay + a * kTile);
           ++a_it;
-          const int kvh = w.h / group;
-          for (int kt = 0; kt < nkt; ++kt) {
-            const int bs = b_it % S;
-            if (!wait_bounded(&b_empty[bs], ((b_it / S) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
-            mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES);
-            load_tile<D>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], kvh * D,
-                         w.k0 + kt * kTile);
-            ++b_it;
-          }
-        } else {
-          const int nqt = int(ceil_div(w.nq, kTile));
-          if (nqt == 0) continue;
-          const int qtile_base = __ldg(p.qtile_off + w.g);
-          for (int hk = 0; hk < p.Hkv && ok; ++hk) {
-            const int as = a_it & 1;
-            if (!wait_bounded(&a_empty[as], ((a_it >> 1) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
-            mbar_arrive_expect_tx(&a_full[as], C::TILE_BYTES);
-            load_tile<D>(sA + as * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as], hk * D,
-                         w.k0 + w.tile * kTile);
-            ++a_it;
-            for (int hh = 0; hh < group && ok; ++hh) {
-              const int h = hk * group + hh;
-              for (int qt = 0; qt < nqt; ++qt) {
-                const int bs = b_it % S;
-                if (!wait_bounded(&b_empty[bs], ((b_it / S) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
-                mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES);
-                load_tile<D>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], h * D,
-                             w.q0 + qt * kTile);
-                ++b_it;
-                const int ls = l_it % kLseSlots;
-                if (!wait_bounded(&lse_empty[ls], ((l_it / kLseSlots) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
+          const int n_heads = PASS == 1 ? 1 : group;
+          for (int hh = 0; hh < n_heads && ok; ++hh) {
+            const int h = PASS == 1 ? w.h : ag * group + hh;
+            const int bx = PASS == 1 ? (w.h / group) * D : h * D;
+            const int nbt = PASS == 1 ? n_b : int(ceil_div(w.nq, kTile));
+            for (int bt = 0; bt < nbt; ++bt) {
+              const int bs = b_it % S;
+              if (!wait_bounded(&b_empty[bs], ((b_it / S) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
+              mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES);
+              load_tile<D>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], bx,
+                           (PASS == 1 ? w.k0 : w.q0) + bt * kTile);
+              if (PASS == 2) {
+                const int ls = b_it % kLseSlots;
+                if (!wait_bounded(&lse_empty[ls], ((b_it / kLseSlots) & 1) ^ 1, abort_flag, T)) {
+                  ++b_it;
+                  ok = false;
+                  break;
+                }
                 mbar_arrive_expect_tx(&lse_full[ls], kTile * 4);
                 bulk_load(sLse + ls * kTile,
-                          p.nlse2 + int64_t(h) * p.lse_stride + int64_t(qtile_base + qt) * kTile,
+                          p.nlse2 + int64_t(h) * p.lse_stride + int64_t(qtile_base + bt) * kTile,
                           kTile * 4, &lse_full[ls]);
-                ++l_it;
               }
+              ++b_it;
             }
           }
         }
@@ -448,15 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = a_it - 1 - i;
         wait_drain(&a_full[n & 1], (n >> 1) & 1, T);
       }
-      for (int i = 0; i < kLseSlots && i < l_it; ++i) {
-        const int n = l_it - 1 - i;
-        wait_drain(&lse_full[n % kLseSlots], (n / kLseSlots) & 1, T);
+      if (PASS == 2) {
+        for (int i = 0; i < kLseSlots && i < b_it; ++i) {
+          const int n = b_it - 1 - i;
+          wait_drain(&lse_full[n % kLseSlots], (n / kLseSlots) & 1, T);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int s_it = 0, a_it = 0, b_it = 0, c_it = 0;
+      int s_it = 0, a_it = 0, b_it = 0;
       bool ok = true;
       while (ok) {
         const int slot = s_it % kSchedSlots;
@@ -466,24 +539,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++s_it;
         if (u < 0) break;
         const Unit w = decode_unit<PASS>(p, p.units[u]);
-        const int n_a = PASS == 1 ? (w.nk > 0 ? 1 : 0) : (w.nq > 0 ? p.Hkv : 0);
-        const int n_b = PASS == 1 ? int(ceil_div(w.nk, kTile)) : group * int(ceil_div(w.nq, kTile));
-        for (int ai = 0; ai < n_a && ok; ++ai) {
+        const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
+        if (nbt == 0) continue;
+        const int n_agroups = PASS == 1 ? 1 : p.Hkv;
+        const int n_b = PASS == 1 ? nbt : group * nbt;
+        for (int ag = 0; ag < n_agroups && ok; ++ag) {
           const int as = a_it & 1;
           if (!wait_bounded(&a_full[as], (a_it >> 1) & 1, abort_flag, T)) { ok = false; break; }
           tc_fence_after();
           for (int bi = 0; bi < n_b; ++bi) {
             const int bs = b_it % S;
             if (!wait_bounded(&b_full[bs], (b_it / S) & 1, abort_flag, T)) { ok = false; break; }
-            const int ab = c_it % kAccBufs;
-            if (!wait_bounded(&acc_empty[ab], ((c_it / kAccBufs) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
-            tc_fence_after();
-            issue_tile_mmas<D>(tmem_base + uint32_t(ab * kTile), sA + as * C::TILE_BYTES,
-                               sB + bs * C::TILE_BYTES);
+            const uint32_t use = uint32_t(b_it >> 1) & 1u;
+            for (int a = 0; a < 2; ++a) {
+              const int k = 2 * (b_it & 1) + a;
+              if (!wait_bounded(&acc_empty[k], use ^ 1u, abort_flag, T)) { ok = false; break; }
+              tc_fence_after();
+              if (a < w.nA)
+                issue_tile_mmas<D>(tmem_base + uint32_t(k * kTile),
+                                   sA + (as * 2 + a) * C::TILE_BYTES, sB + bs * C::TILE_BYTES);
+              mma_commit(&acc_full[k]);
+            }
+            if (!ok) break;
             mma_commit(&b_empty[bs]);
-            mma_commit(&acc_full[ab]);
             ++b_it;
-            ++c_it;
           }
           mma_commit(&a_empty[as]);
           ++a_it;
@@ -497,14 +576,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(mma_done);
       wait_drain(mma_done, 0, T);
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------ epilogue
-    const int wg = (warp - 4) >> 2;
+    // Warpgroup wg = 2*par + a owns TMEM accumulator k = 2*par + a: rows of
+    // A tile `a` against the B tiles of parity `par`.
+    const int wg = (warp - kEpiFirstWarp) >> 2;
+    const int a_half = wg & 1, par = wg >> 1;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const uint32_t lane_base = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(wg * 64);
+    const int kbuf = 2 * par + a_half;
+    const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(kbuf * kTile);
     const float c = p.c;
-    int s_it = 0, c_it = 0, l_it = 0, unit_it = 0;
+    const uint64_t c2 = pack2(c, c);
+    int s_it = 0, b_it = 0, unit_it = 0;
     bool ok = true;
     while (ok) {
       const int slot = s_it % kSchedSlots;
@@ -515,121 +599,96 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++s_it;
       if (u < 0) break;
       const Unit w = decode_unit<PASS>(p, p.units[u]);
-      const int cb = unit_it & 1;
-      const uint32_t cpar = (unit_it >> 1) & 1;
-      float* comb = sComb + cb * 2 * kTile;
-
-      if (PASS == 1) {
-        float m = kNegInf, l = 0.f;
-        const int nkt = int(ceil_div(w.nk, kTile));
-        for (int kt = 0; kt < nkt; ++kt) {
-          const int ab = c_it % kAccBufs;
-          if (!warp_wait(&acc_full[ab], (c_it / kAccBufs) & 1, abort_flag, T)) { ok = false; break; }
-          tc_fence_after();
-          float v[64];
-          tmem_ld64(lane_base + uint32_t(ab * kTile), v);
+      const bool mine = a_half < w.nA;   // this warpgroup's A tile holds rows of the unit
+      const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
+      const int n_b = PASS == 1 ? nbt : (nbt > 0 ? p.H * nbt : 0);
+      float m = kNegInf, l = 0.f;           // pass 1
+      uint64_t acc[2] = {0ull, 0ull};      // pass 1: sum of exp2 since m; pass 2: per-key sum
+      for (int bi = 0; bi < n_b; ++bi, ++b_it) {
+        if ((b_it & 1) != par) continue;
+        const uint32_t use = uint32_t(b_it >> 1) & 1u;
+        if (!warp_wait(&acc_full[kbuf], use, abort_flag, T)) { ok = false; break; }
+        const int ls = b_it % kLseSlots;
+        if (PASS == 2 && !warp_wait(&lse_full[ls], (b_it / kLseSlots) & 1, abort_flag, T)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (mine) {
+          const int col0 = (PASS == 1 ? (bi % nbt) : (bi % nbt)) * kTile;
+          const int valid = (PASS == 1 ? w.nk : w.nq) - col0;
+          const float4* nl = reinterpret_cast<const float4*>(sLse + ls * kTile);
+          uint32_t r0[32], r1[32];
+          tmem_ld32_async(taddr, r0);
+          tmem_wait_ld(r0);
+          tmem_ld32_async(taddr + 32, r1);
+          if (PASS == 1) row_softmax_chunk(r0, valid, c, c2, m, l, acc);
+          else if (valid > 0) column_sum_chunk(r0, nl, c2, acc);
+          tmem_wait_ld(r1);
+          tmem_ld32_async(taddr + 64, r0);
+          if (PASS == 1) row_softmax_chunk(r1, valid - 32, c, c2, m, l, acc);
+          else if (valid > 32) column_sum_chunk(r1, nl + 8, c2, acc);
+          tmem_wait_ld(r0);
+          tmem_ld32_async(taddr + 96, r1);
+          if (PASS == 1) row_softmax_chunk(r0, valid - 64, c, c2, m, l, acc);
+          else if (valid > 64) column_sum_chunk(r0, nl + 16, c2, acc);
+          tmem_wait_ld(r1);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[ab]);
-          ++c_it;
-          const int valid = w.nk - kt * kTile - wg * 64;
-          if (valid < 64) {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] = j < valid ? v[j] : kNegInf;
-          }
-          float t0 = v[0], t1 = v[1], t2 = v[2], t3 = v[3];
-#pragma unroll
-          for (int j = 4; j < 64; j += 4) {
-            t0 = fmaxf(t0, v[j]);
-            t1 = fmaxf(t1, v[j + 1]);
-            t2 = fmaxf(t2, v[j + 2]);
-            t3 = fmaxf(t3, v[j + 3]);
-          }
-          const float tmax = fmaxf(fmaxf(t0, t1), fmaxf(t2, t3));
-          if (tmax > kNegInf) {
-            const float mn = fmaxf(m, tmax * c);
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              s0 += ex2(fmaf(v[j], c, -mn));
-              s1 += ex2(fmaf(v[j + 1], c, -mn));
-              s2 += ex2(fmaf(v[j + 2], c, -mn));
-              s3 += ex2(fmaf(v[j + 3], c, -mn));
-            }
-            l = l * ex2(m - mn) + ((s0 + s1) + (s2 + s3));
-            m = mn;
-          }
-        }
-        if (!ok) break;
-        if (wg == 1) {
-          if (!warp_wait(&comb_empty[cb], cpar ^ 1, abort_flag, T)) { ok = false; break; }
-          comb[row] = m;
-          comb[kTile + row] = l;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&comb_full[cb]);
+          if (lane == 0) mbar_arrive(&acc_empty[kbuf]);
+          if (PASS == 1) row_softmax_chunk(r1, valid - 96, c, c2, m, l, acc);
+          else if (valid > 96) column_sum_chunk(r1, nl + 24, c2, acc);
         } else {
-          if (!warp_wait(&comb_full[cb], cpar, abort_flag, T)) { ok = false; break; }
-          const float m1 = comb[row], l1 = comb[kTile + row];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&comb_empty[cb]);
-          const float M = fmaxf(m, m1);
-          float Lsum = 0.f;
-          if (M > kNegInf) Lsum = l * ex2(m - M) + l1 * ex2(m1 - M);
-          const int qrow = w.tile * kTile + row;
-          const bool valid = qrow < w.nq;
-          const float lse2 = Lsum > 0.f ? M + log2f(Lsum) : kNegInf;
-          const int qtile_base = __ldg(p.qtile_off + w.g);
-          p.nlse2[int64_t(w.h) * p.lse_stride + int64_t(qtile_base + w.tile) * kTile + row] =
-              (valid && Lsum > 0.f) ? -lse2 : kNegInf;
-          if (valid && p.lse_out != nullptr)
-            p.lse_out[int64_t(w.h) * p.Tq + w.q0 + qrow] = lse2 * 0.69314718055994531f;
-        }
-      } else {
-        float acc = 0.f;
-        const int nqt = int(ceil_div(w.nq, kTile));
-        const int n_iter = nqt > 0 ? p.H * nqt : 0;
-        for (int it = 0; it < n_iter; ++it) {
-          const int ab = c_it % kAccBufs;
-          if (!warp_wait(&acc_full[ab], (c_it / kAccBufs) & 1, abort_flag, T)) { ok = false; break; }
-          tc_fence_after();
-          float v[64];
-          tmem_ld64(lane_base + uint32_t(ab * kTile), v);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[ab]);
-          ++c_it;
-          const int ls = l_it % kLseSlots;
-          if (!warp_wait(&lse_full[ls], (l_it / kLseSlots) & 1, abort_flag, T)) { ok = false; break; }
-          const float4* nl = reinterpret_cast<const float4*>(sLse + ls * kTile + wg * 64);
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float4 t = nl[j];
-            s0 += ex2(fmaf(v[4 * j], c, t.x));
-            s1 += ex2(fmaf(v[4 * j + 1], c, t.y));
-            s2 += ex2(fmaf(v[4 * j + 2], c, t.z));
-            s3 += ex2(fmaf(v[4 * j + 3], c, t.w));
-          }
+          if (lane == 0) mbar_arrive(&acc_empty[kbuf]);
+        }
+        if (PASS == 2) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&lse_empty[ls]);
-          ++l_it;
-          acc += (s0 + s1) + (s2 + s3);
         }
-        if (!ok) break;
-        if (wg == 1) {
-          if (!warp_wait(&comb_empty[cb], cpar ^ 1, abort_flag, T)) { ok = false; break; }
-          comb[row] = acc;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&comb_full[cb]);
-        } else {
-          if (!warp_wait(&comb_full[cb], cpar, abort_flag, T)) { ok = false; break; }
-          const float acc1 = comb[row];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&comb_empty[cb]);
-          const int krow = w.tile * kTile + row;
-          if (krow < w.nk) {
-            const float total = acc + acc1;
-            p.scores[w.k0 + krow] = w.nq > 0 ? total / float(p.H * w.nq) : 0.f;
+      }
+      if (!ok) break;
+      // Merge the two warpgroups of the same A half (B-tile parities 0 and 1).
+      const int cb = unit_it & 1;
+      const uint32_t cpar = (unit_it >> 1) & 1;
+      float* comb = sComb + (a_half * 2 + cb) * 2 * kTile;
+      uint64_t* cfull = &comb_full[a_half * 2 + cb];
+      uint64_t* cempty = &comb_empty[a_half * 2 + cb];
+      float x0, x1;
+      unpack2(fadd2(acc[0], acc[1]), x0, x1);
+      const float part = x0 + x1;   // pass 1: sum since m; pass 2: per-key sum
+      if (par == 1) {
+        if (!warp_wait(cempty, cpar ^ 1, abort_flag, T)) { ok = false; break; }
+        comb[row] = PASS == 1 ? m : part;
+        comb[kTile + row] = PASS == 1 ? l + part : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cfull);
+      } else {
+        if (!warp_wait(cfull, cpar, abort_flag, T)) { ok = false; break; }
+        const float o0 = comb[row], o1 = comb[kTile + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cempty);
+        if (mine) {
+          if (PASS == 1) {
+            const float l0 = l + part;
+            const float M = fmaxf(m, o0);
+            float Lsum = 0.f;
+            if (M > kNegInf) Lsum = l0 * ex2(m - M) + o1 * ex2(o0 - M);
+            const int qrow = w.pair * kPair + a_half * kTile + row;
+            const bool valid = qrow < w.nq;
+            const float lse2 = Lsum > 0.f ? M + log2f(Lsum) : kNegInf;
+            const int qtile = __ldg(p.qtile_off + w.g) + w.pair * 2 + a_half;
+            p.nlse2[int64_t(w.h) * p.lse_stride + int64_t(qtile) * kTile + row] =
+                (valid && Lsum > 0.f) ? -lse2 : kNegInf;
+            if (valid && p.lse_out != nullptr)
+              p.lse_out[int64_t(w.h) * p.Tq + w.q0 + qrow] = lse2 * 0.69314718055994531f;
+          } else {
+            const int krow = w.pair * kPair + a_half * kTile + row;
+            if (krow < w.nk) {
+              const float total = part + o0;
+              p.scores[w.k0 + krow] = w.nq > 0 ? total / float(p.H * w.nq) : 0.f;
+            }
           }
         }
       }
