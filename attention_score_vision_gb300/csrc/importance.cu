@@ -68,7 +68,7 @@ struct TileCfg {
   static constexpr int NUM_BARS = 2 + 2 + 2 * STAGES + 2 * kAccBufs + 2 * kLseSlots +
                                   2 * kSchedSlots + 4 + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + alignment slack
+  static constexpr int SMEM_BYTES = OFF_MISC + 256 + 64 + 1024;  // + alignment slack
   static_assert(STAGES >= 2, "at least double-buffered B tiles");
   static_assert(TILE_BYTES % 1024 == 0, "tiles stay 1024-byte aligned");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -228,8 +228,12 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
 
 struct Unit {
   int g, h, pair, q0, nq, k0, nk;
-  int nA;  // valid 128-row A tiles in this unit's 256-row pair (1 or 2)
+  int nA;          // valid 128-row A tiles in this unit's 256-row pair (1 or 2)
+  int qtile_base;  // first 128-row tile of the segment in the padded LSE rows
+  int valid;       // 1 for a unit, 0 for the end-of-work marker
 };
+
+static_assert(kSchedSlots * sizeof(Unit) <= 256, "scheduler ring fits its shared-memory slot");
 
 template <int PASS>
 __device__ __forceinline__ Unit decode_unit(const ImpPassParams& p, uint2 u) {
@@ -248,6 +252,8 @@ __device__ __forceinline__ Unit decode_unit(const ImpPassParams& p, uint2 u) {
   r.nk = __ldg(p.cu_k + r.g + 1) - r.k0;
   const int rows_left = (PASS == 1 ? r.nq : r.nk) - r.pair * kPair;
   r.nA = rows_left > kTile ? 2 : 1;
+  r.qtile_base = __ldg(p.qtile_off + r.g);
+  r.valid = 1;
   return r;
 }
 
@@ -393,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* comb_full = sch_empty + kSchedSlots;  // [A half][buf]
   uint64_t* comb_empty = comb_full + 4;
   uint64_t* mma_done = comb_empty + 4;
-  int* sched = reinterpret_cast<int*>(smem + C::OFF_MISC);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sched + kSchedSlots);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sched + kSchedSlots + 1);
+  Unit* sched = reinterpret_cast<Unit*>(smem + C::OFF_MISC);   // decoded units in flight
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t T = p.timeout_ns;
@@ -457,17 +463,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        int u = atomicAdd(p.sched_ctr, 1);
-        if (u >= total_units) u = -1;
-        sched[slot] = u;
+        const int u = atomicAdd(p.sched_ctr, 1);
+        Unit w;
+        if (u < total_units) {
+          w = decode_unit<PASS>(p, p.units[u]);
+        } else {
+          w = Unit{};
+          w.valid = 0;
+        }
+        sched[slot] = w;   // consumers read the decoded unit from shared memory
         mbar_arrive(&sch_full[slot]);
         ++s_it;
-        if (u < 0) break;
-        const Unit w = decode_unit<PASS>(p, p.units[u]);
+        if (!w.valid) break;
         const int n_b = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
         if (n_b == 0) continue;
         const int n_agroups = PASS == 1 ? 1 : p.Hkv;
-        const int qtile_base = PASS == 2 ? __ldg(p.qtile_off + w.g) : 0;
+        const int qtile_base = w.qtile_base;
         for (int ag = 0; ag < n_agroups && ok; ++ag) {
           const int as = a_it & 1;
           if (!wait_bounded(&a_empty[as], ((a_it >> 1) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
@@ -534,11 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok) {
         const int slot = s_it % kSchedSlots;
         if (!wait_bounded(&sch_full[slot], (s_it / kSchedSlots) & 1, abort_flag, T)) { ok = false; break; }
-        const int u = sched[slot];
+        const Unit w = sched[slot];
         mbar_arrive(&sch_empty[slot]);
         ++s_it;
-        if (u < 0) break;
-        const Unit w = decode_unit<PASS>(p, p.units[u]);
+        if (!w.valid) break;
         const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
         if (nbt == 0) continue;
         const int n_agroups = PASS == 1 ? 1 : p.Hkv;
@@ -593,12 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok) {
       const int slot = s_it % kSchedSlots;
       if (!warp_wait(&sch_full[slot], (s_it / kSchedSlots) & 1, abort_flag, T)) { ok = false; break; }
-      const int u = sched[slot];
+      const Unit w = sched[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sch_empty[slot]);
       ++s_it;
-      if (u < 0) break;
-      const Unit w = decode_unit<PASS>(p, p.units[u]);
+      if (!w.valid) break;
       const bool mine = a_half < w.nA;   // this warpgroup's A tile holds rows of the unit
       const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
       const int n_b = PASS == 1 ? nbt : (nbt > 0 ? p.H * nbt : 0);
@@ -615,27 +624,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         if (mine) {
-          const int col0 = (PASS == 1 ? (bi % nbt) : (bi % nbt)) * kTile;
+          const int col0 = (bi % nbt) * kTile;
           const int valid = (PASS == 1 ? w.nk : w.nq) - col0;
           const float4* nl = reinterpret_cast<const float4*>(sLse + ls * kTile);
+          // Two 32-column pieces in flight: the accumulator is fully read,
+          // and handed back to the MMA, once half of the tile is computed.
           uint32_t r0[32], r1[32];
           tmem_ld32_async(taddr, r0);
-          tmem_wait_ld(r0);
           tmem_ld32_async(taddr + 32, r1);
+          tmem_wait_ld(r0);
+          tmem_wait_ld(r1);
           if (PASS == 1) row_softmax_chunk(r0, valid, c, c2, m, l, acc);
           else if (valid > 0) column_sum_chunk(r0, nl, c2, acc);
-          tmem_wait_ld(r1);
           tmem_ld32_async(taddr + 64, r0);
           if (PASS == 1) row_softmax_chunk(r1, valid - 32, c, c2, m, l, acc);
           else if (valid > 32) column_sum_chunk(r1, nl + 8, c2, acc);
-          tmem_wait_ld(r0);
           tmem_ld32_async(taddr + 96, r1);
-          if (PASS == 1) row_softmax_chunk(r0, valid - 64, c, c2, m, l, acc);
-          else if (valid > 64) column_sum_chunk(r0, nl + 16, c2, acc);
+          tmem_wait_ld(r0);
           tmem_wait_ld(r1);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[kbuf]);
+          if (PASS == 1) row_softmax_chunk(r0, valid - 64, c, c2, m, l, acc);
+          else if (valid > 64) column_sum_chunk(r0, nl + 16, c2, acc);
           if (PASS == 1) row_softmax_chunk(r1, valid - 96, c, c2, m, l, acc);
           else if (valid > 96) column_sum_chunk(r1, nl + 24, c2, acc);
         } else {
@@ -678,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qrow = w.pair * kPair + a_half * kTile + row;
             const bool valid = qrow < w.nq;
             const float lse2 = Lsum > 0.f ? M + log2f(Lsum) : kNegInf;
-            const int qtile = __ldg(p.qtile_off + w.g) + w.pair * 2 + a_half;
+            const int qtile = w.qtile_base + w.pair * 2 + a_half;
             p.nlse2[int64_t(w.h) * p.lse_stride + int64_t(qtile) * kTile + row] =
                 (valid && Lsum > 0.f) ? -lse2 : kNegInf;
             if (valid && p.lse_out != nullptr)
