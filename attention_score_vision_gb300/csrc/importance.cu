@@ -734,9 +734,15 @@ static cudaError_t launch_pass_t(const CUtensorMap* maps, const ImpPassParams& p
                                  cudaStream_t stream) {
   using C = TileCfg<D>;
   auto kern = imp_pass_kernel<PASS, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  static bool attr_set[128] = {};  // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) attr_set[dev] = true;
+  }
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
   return cudaPeekAtLastError();
 }

@@ -5,20 +5,32 @@
 // under one global budget; LiteVLM (section 3.2) fixes the budget through the
 // keep ratio r.
 //
-// One CTA per request:
-//   1. radix select, 8 bits per pass from the top, finds the key of the B-th
-//      largest score (keys are fp32 bits mapped to an order-preserving uint32);
-//   2. one pass in index order keeps every token above that key and the
-//      lowest-index tokens equal to it, writing indices in ascending order
-//      through block-wide prefix sums (deterministic, bit-exact).
+// One thread-block cluster per request (up to 16 CTAs, one slice of the
+// request's tokens each, cached in shared memory):
+//   1. radix select, 8 bits per round from the top: every CTA builds
+//      warp-private histograms of its slice, adds them into CTA 0's histogram
+//      through distributed shared memory, and after one cluster barrier every
+//      CTA reads the merged histogram and picks the same digit. After four
+//      rounds the key of the B-th largest score is known (keys are fp32 bits
+//      mapped to an order-preserving uint32);
+//   2. each CTA counts its keys above / equal to that key, the counts are
+//      exchanged the same way, and each CTA writes its kept indices in index
+//      order through block-wide prefix sums: tokens above the key, and the
+//      lowest-index tokens equal to it. The output is deterministic.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace tsel {
 
-constexpr int kTopkThreads = 1024;
-constexpr int kTopkItems = 4;  // consecutive tokens per thread in the compaction pass
+constexpr int kTopkThreads = 256;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkItems = 4;               // consecutive tokens per thread when compacting
+constexpr int kTopkMaxCluster = 16;
+constexpr int kTopkCacheKeys = 16384;       // keys cached in shared memory per CTA
 
 // fp32 bits -> uint32 with the same order; -0 maps to +0.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -43,86 +55,140 @@ __device__ __forceinline__ int topk_block_scan(int v, int* warp_sums, int& total
   const int x = warp_incl_scan(v);
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
-  if (warp == 0) warp_sums[lane] = warp_incl_scan(warp_sums[lane]);
+  if (warp == 0) {
+    const int w = lane < kTopkWarps ? warp_sums[lane] : 0;
+    const int s = warp_incl_scan(w);
+    if (lane < kTopkWarps) warp_sums[lane] = s;
+  }
   __syncthreads();
   const int excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
-  total = warp_sums[31];
+  total = warp_sums[kTopkWarps - 1];
   __syncthreads();
   return excl;
 }
 
+struct TopkShared {
+  int whist[kTopkWarps][256];      // warp-private histograms
+  int hist[4][256];                // merged histograms (rank 0's copy is the one used)
+  int cnt_gt[kTopkMaxCluster];     // per-CTA counts above / equal to the threshold (rank 0)
+  int cnt_eq[kTopkMaxCluster];
+  int warp_sums[32];
+  int digit, above, bad, nan_seen;
+};
+
 __global__ void __launch_bounds__(kTopkThreads)
-    topk_kernel(const float* __restrict__ scores, int total_tokens,
-                const int32_t* __restrict__ req_off, int num_req,
-                const int32_t* __restrict__ keep, int total_keep, int32_t* __restrict__ keep_idx,
-                int32_t* __restrict__ cu_keep, uint32_t* status) {
-  __shared__ int hist[256];
-  __shared__ int warp_sums[32];
-  __shared__ int s_base, s_bad, s_digit, s_above;
-  const int r = blockIdx.x;
+    topk_cluster_kernel(const float* __restrict__ scores, int total_tokens,
+                        const int32_t* __restrict__ req_off, int num_req,
+                        const int32_t* __restrict__ keep, int total_keep,
+                        int32_t* __restrict__ keep_idx, int32_t* __restrict__ cu_keep,
+                        uint32_t* status) {
+  __shared__ TopkShared sh;
+  extern __shared__ uint32_t skeys[];  // kTopkCacheKeys
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = int(cluster.block_rank());
+  const int csize = int(cluster.num_blocks());
+  const int r = int(blockIdx.x) / csize;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  // Output offset of this request = sum of the budgets before it.
-  int part = 0;
-  int neg = 0;
+  // ---- request checks and output offset (identical in every CTA) --------
+  int part = 0, neg = 0;
   for (int i = tid; i < r; i += kTopkThreads) {
     const int b = keep[i];
     part += b;
     neg |= b < 0;
   }
-  int total;
-  (void)topk_block_scan(part, warp_sums, total);
+  int before;
+  (void)topk_block_scan(part, sh.warp_sums, before);
+  const int lo = req_off[r], hi = req_off[r + 1];
+  const int B = keep[r];
   if (tid == 0) {
-    const int lo = req_off[r], hi = req_off[r + 1];
-    const int B = keep[r];
-    int bad = 0;
+    int bad = neg;
     if (lo < 0 || hi < lo || hi > total_tokens || B < 0 || B > hi - lo) bad = 1;
-    if (total < 0 || int64_t(total) + B > total_keep) bad = 1;
-    if (r == num_req - 1 && int64_t(total) + B != total_keep) bad = 1;
-    s_base = total;
-    s_bad = bad;
+    if (before < 0 || int64_t(before) + B > total_keep) bad = 1;
+    if (r == num_req - 1 && int64_t(before) + B != total_keep) bad = 1;
+    sh.bad = bad;
+    sh.nan_seen = 0;
+  }
+  for (int i = tid; i < 4 * 256; i += kTopkThreads) (&sh.hist[0][0])[i] = 0;
+  if (tid < kTopkMaxCluster) {
+    sh.cnt_gt[tid] = 0;
+    sh.cnt_eq[tid] = 0;
   }
   __syncthreads();
-  if (neg) atomicOr(&s_bad, 1);
-  __syncthreads();
-  if (s_bad) {
-    if (tid == 0) set_status(status, TSEL_DEV_REQUESTS);
+  if (sh.bad) {
+    // every CTA of the cluster takes this branch together (same request)
+    if (tid == 0 && crank == 0) set_status(status, TSEL_DEV_REQUESTS);
     return;
   }
-  const int lo = req_off[r], hi = req_off[r + 1];
-  const int n = hi - lo;
-  const int B = keep[r];
-  const int base = s_base;
-  if (tid == 0) {
+  if (tid == 0 && crank == 0) {
     if (r == 0) cu_keep[0] = 0;
-    cu_keep[r + 1] = base + B;
+    cu_keep[r + 1] = before + B;
   }
-  const float* s = scores + lo;
-  int32_t* out = keep_idx + base;
+  const int n = hi - lo;
   if (B == 0) return;
 
-  // ---- radix select: key of the B-th largest element --------------------
+  // This CTA's slice of the request.
+  const int chunk = (n + csize - 1) / csize;
+  const int c0 = min(n, crank * chunk), c1 = min(n, c0 + chunk);
+  const int len = c1 - c0;
+  const float* s = scores + lo + c0;
+  const bool cached = len <= kTopkCacheKeys;
+  // Histograms are zeroed everywhere before any remote add: arrive now, wait
+  // after the slice is loaded.
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  int nan_local = 0;
+  for (int i0 = 0; i0 < len; i0 += kTopkThreads * 8) {
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {   // eight independent loads in flight per thread
+      const int i = i0 + j * kTopkThreads + tid;
+      f[j] = i < len ? __ldcg(s + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * kTopkThreads + tid;
+      nan_local |= (f[j] != f[j]);
+      if (cached && i < len) skeys[i] = order_key(f[j]);
+    }
+  }
+  if (nan_local) atomicOr(&sh.nan_seen, 1);
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  __syncthreads();
+
+  // ---- radix select -------------------------------------------------------
+  int* hist0 = cluster.map_shared_rank(&sh.hist[0][0], 0);
   uint32_t prefix = 0, mask = 0;
   int remaining = B;  // how many still to take among keys matching `prefix`
-  int nan_seen = 0;
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    if (tid < 256) hist[tid] = 0;
+  for (int round = 0; round < 4; ++round) {
+    const int shift = 24 - 8 * round;
+    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&sh.whist[0][0])[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kTopkThreads) {
-      const float f = s[i];
-      if (shift == 24) nan_seen |= (f != f);
-      const uint32_t k = order_key(f);
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    for (int i0 = 0; i0 < len; i0 += kTopkThreads) {
+      const int i = i0 + tid;
+      const bool in = i < len;
+      const uint32_t k = in ? (cached ? skeys[i] : order_key(s[i])) : 0u;
+      const bool match = in && (k & mask) == prefix;
+      const uint32_t d = (k >> shift) & 255u;
+      // aggregate equal digits within the warp: one shared atomic per value
+      const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0x100u);
+      if (match && (__ffs(peers) - 1) == lane) atomicAdd(&sh.whist[warp][d], __popc(peers));
     }
     __syncthreads();
+    {
+      int v = 0;
+#pragma unroll
+      for (int w = 0; w < kTopkWarps; ++w) v += sh.whist[w][tid];
+      if (v) atomicAdd(hist0 + round * 256 + tid, v);   // into CTA 0's shared memory
+    }
+    cluster.sync();
     if (warp == 0) {
       // lane l owns bins 255-8l ... 248-8l (descending)
       int c[8];
       int sum = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = hist[255 - 8 * lane - j];
+        c[j] = hist0[round * 256 + 255 - 8 * lane - j];
         sum += c[j];
       }
       const int incl = warp_incl_scan(sum);
@@ -137,38 +203,70 @@ __global__ void __launch_bounds__(kTopkThreads)
         above += c[j];
       }
       if (found >= 0) {
-        s_digit = found;
-        s_above = found_above;
+        sh.digit = found;
+        sh.above = found_above;
       }
     }
     __syncthreads();
-    prefix |= uint32_t(s_digit) << shift;
+    prefix |= uint32_t(sh.digit) << shift;
     mask |= 255u << shift;
-    remaining -= s_above;
+    remaining -= sh.above;
     __syncthreads();
   }
-  if (nan_seen) set_status(status, TSEL_DEV_NAN);
+  if (tid == 0 && sh.nan_seen) set_status(status, TSEL_DEV_NAN);   // this CTA's slice
   const uint32_t thr = prefix;
-  const int need_eq = remaining;  // tokens equal to the threshold to keep
+  const int need_eq = remaining;  // tokens equal to the threshold to keep (request-wide)
 
-  // ---- compaction in index order ------------------------------------------
-  int written = 0, eq_seen = 0;
-  for (int c0 = 0; c0 < n; c0 += kTopkThreads * kTopkItems) {
-    const int i0 = c0 + tid * kTopkItems;
+  // ---- per-CTA counts, exchanged through CTA 0 -----------------------------
+  int gt = 0, eq = 0;
+  for (int i = tid; i < len; i += kTopkThreads) {
+    const uint32_t k = cached ? skeys[i] : order_key(s[i]);
+    gt += k > thr;
+    eq += k == thr;
+  }
+  int gt_total, eq_total;
+  (void)topk_block_scan(gt, sh.warp_sums, gt_total);
+  (void)topk_block_scan(eq, sh.warp_sums, eq_total);
+  if (tid == 0) {
+    int* rg = cluster.map_shared_rank(&sh.cnt_gt[0], 0);
+    int* re = cluster.map_shared_rank(&sh.cnt_eq[0], 0);
+    rg[crank] = gt_total;
+    re[crank] = eq_total;
+  }
+  cluster.sync();
+  int out_base = 0, eq_before = 0;
+  {
+    const int* rg = cluster.map_shared_rank(&sh.cnt_gt[0], 0);
+    const int* re = cluster.map_shared_rank(&sh.cnt_eq[0], 0);
+    for (int c = 0; c < crank; ++c) {
+      const int e = re[c];
+      const int take = max(0, min(e, need_eq - eq_before));
+      out_base += rg[c] + take;
+      eq_before += e;
+    }
+  }
+  cluster.sync();   // CTA 0's shared memory is no longer read after this point
+
+  // ---- compaction in index order --------------------------------------------
+  int32_t* out = keep_idx + before + out_base;
+  int written = 0, eq_seen = eq_before;
+  for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkItems) {
+    const int ib = i0 + tid * kTopkItems;
     uint32_t k[kTopkItems];
     int n_eq = 0;
 #pragma unroll
     for (int j = 0; j < kTopkItems; ++j) {
-      k[j] = (i0 + j < n) ? order_key(s[i0 + j]) : 0u;
-      n_eq += (i0 + j < n) && k[j] == thr;
+      const int i = ib + j;
+      k[j] = i < len ? (cached ? skeys[i] : order_key(s[i])) : 0u;
+      n_eq += (i < len) && k[j] == thr;
     }
-    int eq_total;
-    int eq_rank = eq_seen + topk_block_scan(n_eq, warp_sums, eq_total);
+    int eqt;
+    int eq_rank = eq_seen + topk_block_scan(n_eq, sh.warp_sums, eqt);
     bool take[kTopkItems];
     int n_take = 0;
 #pragma unroll
     for (int j = 0; j < kTopkItems; ++j) {
-      const bool valid = i0 + j < n;
+      const bool valid = ib + j < len;
       bool t = valid && k[j] > thr;
       if (valid && k[j] == thr) {
         t = eq_rank < need_eq;
@@ -178,21 +276,87 @@ __global__ void __launch_bounds__(kTopkThreads)
       n_take += t;
     }
     int take_total;
-    int pos = written + topk_block_scan(n_take, warp_sums, take_total);
+    int pos = written + topk_block_scan(n_take, sh.warp_sums, take_total);
 #pragma unroll
     for (int j = 0; j < kTopkItems; ++j) {
-      if (take[j]) out[pos++] = lo + i0 + j;
+      if (take[j]) out[pos++] = lo + c0 + ib + j;
     }
     written += take_total;
-    eq_seen += eq_total;
+    eq_seen += eqt;
   }
+}
+
+// Cluster size from the average request size (the host does not see the
+// per-request offsets): small requests need no cluster.
+static int topk_cluster_size(int total_tokens, int num_req) {
+  const int64_t avg = num_req > 0 ? (int64_t(total_tokens) + num_req - 1) / num_req : 0;
+  if (avg >= 16384) return 16;
+  if (avg >= 4096) return 8;
+  if (avg >= 1024) return 4;
+  return 1;
+}
+
+// Largest cluster size <= `want` this device can co-schedule, cached per
+// device (the attributes are set once per device as well).
+static int topk_usable_cluster(int want, size_t dyn, cudaError_t* err) {
+  static int cache[128][5] = {};  // [device][log2 size] -> 1 + usable size, 0 = unknown
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return 1;
+  int lw = 0;
+  while ((1 << (lw + 1)) <= want && lw < 4) ++lw;
+  if (dev >= 0 && dev < 128 && cache[dev][lw] > 0) return cache[dev][lw] - 1;
+  *err = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              int(dyn));
+  if (*err != cudaSuccess) return 1;
+  *err = cudaFuncSetAttribute(topk_cluster_kernel,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (*err != cudaSuccess) return 1;
+  int csize = 1 << lw;
+  for (; csize > 1; csize /= 2) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(csize);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(csize));
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, topk_cluster_kernel, &cfg) == cudaSuccess &&
+        active > 0)
+      break;
+    (void)cudaGetLastError();
+  }
+  if (dev >= 0 && dev < 128) cache[dev][lw] = csize + 1;
+  return csize;
 }
 
 cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
                         int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
                         int32_t* cu_keep, uint32_t* status, cudaStream_t stream) {
-  topk_kernel<<<num_req, kTopkThreads, 0, stream>>>(scores, total_tokens, req_off, num_req, keep,
-                                                    total_keep, keep_idx, cu_keep, status);
+  const size_t dyn = size_t(kTopkCacheKeys) * sizeof(uint32_t);
+  cudaError_t e = cudaSuccess;
+  const int csize = topk_usable_cluster(topk_cluster_size(total_tokens, num_req), dyn, &e);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(num_req) * unsigned(csize));
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, total_tokens, req_off, num_req, keep,
+                         total_keep, keep_idx, cu_keep, status);
+  if (e != cudaSuccess) return e;
   return cudaPeekAtLastError();
 }
 
