@@ -719,6 +719,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// LSE import (LSE-provided mode)
+// ---------------------------------------------------------------------------
+
+// Writes -LSE*log2(e) of a caller-provided natural-log LSE [H, Tq] into the
+// padded per-segment layout the column pass reads (pad rows and rows without
+// keys get -inf, so they add nothing). One CTA per (128-row tile, head).
+__global__ void __launch_bounds__(kTile) imp_lse_import_kernel(
+    const float* __restrict__ lse_in, int Tq, const int32_t* __restrict__ cu_q, int G,
+    const int32_t* __restrict__ qtile_off, float* __restrict__ nlse2, int64_t lse_stride,
+    const uint32_t* status) {
+  if (*reinterpret_cast<const volatile uint32_t*>(status) & TSEL_DEV_SEQLENS) return;
+  const int t = blockIdx.x, h = blockIdx.y;
+  const int total = qtile_off[G];
+  if (t >= total) return;
+  int lo = 0, hi = G;  // last g with qtile_off[g] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (qtile_off[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int g = lo;
+  const int r = (t - qtile_off[g]) * kTile + int(threadIdx.x);
+  const int q0 = cu_q[g], nq = cu_q[g + 1] - q0;
+  float v = kNegInf;
+  if (r < nq) {
+    v = -lse_in[int64_t(h) * Tq + q0 + r] * 1.4426950408889634f;
+    if (!(v < __builtin_huge_valf() && v > kNegInf)) v = kNegInf;  // no keys (lse -inf) or NaN
+  }
+  nlse2[int64_t(h) * lse_stride + int64_t(t) * kTile + threadIdx.x] = v;
+}
+
+// ---------------------------------------------------------------------------
 // Host-side launch helpers (called from tsel_api.cu)
 // ---------------------------------------------------------------------------
 
@@ -744,6 +776,15 @@ static cudaError_t launch_pass_t(const CUtensorMap* maps, const ImpPassParams& p
     if (dev >= 0 && dev < 128) attr_set[dev] = true;
   }
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
+                              const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
+                              int max_qtiles, int H, const uint32_t* status, cudaStream_t stream) {
+  if (max_qtiles <= 0) return cudaSuccess;
+  imp_lse_import_kernel<<<dim3(unsigned(max_qtiles), unsigned(H)), kTile, 0, stream>>>(
+      lse_in, Tq, cu_q, G, qtile_off, nlse2, lse_stride, status);
   return cudaPeekAtLastError();
 }
 

@@ -20,6 +20,9 @@ cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int
                             cudaStream_t stream);
 cudaError_t launch_imp_pass(int pass, int head_dim, const CUtensorMap* maps,
                             const ImpPassParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
+                              const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
+                              int max_qtiles, int H, const uint32_t* status, cudaStream_t stream);
 cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
                         int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
                         int32_t* cu_keep, uint32_t* status, cudaStream_t stream);
@@ -165,8 +168,12 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     return fail(TSEL_ERR_INVALID_VALUE, "num_heads=%d num_kv_heads=%d", num_heads, num_kv_heads);
   if (!(head_dim == 64 || head_dim == 80 || head_dim == 96 || head_dim == 112 || head_dim == 128))
     return fail(TSEL_ERR_UNSUPPORTED, "head_dim=%d (supported: 64, 80, 96, 112, 128)", head_dim);
-  if ((flags & ~(TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2)) != 0)
+  if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 |
+                 TSEL_IMP_STAGE_PASS2)) != 0)
     return fail(TSEL_ERR_UNSUPPORTED, "flags=0x%x", flags);
+  const bool lse_provided = (flags & TSEL_IMP_LSE_PROVIDED) != 0;
+  if (lse_provided && total_q > 0 && lse == nullptr)
+    return fail(TSEL_ERR_INVALID_VALUE, "TSEL_IMP_LSE_PROVIDED needs the lse input");
   if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr || workspace == nullptr)
     return fail(TSEL_ERR_INVALID_VALUE, "null cu_seqlens or workspace");
   if ((total_k > 0 && (scores == nullptr || k == nullptr)) || (total_q > 0 && q == nullptr))
@@ -186,10 +193,8 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   if (workspace_bytes < size_t(L.total))
     return fail(TSEL_ERR_WORKSPACE, "workspace %zu < %lld bytes", workspace_bytes,
                 (long long)L.total);
-  const unsigned stages = (flags & (TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 |
-                                    TSEL_IMP_STAGE_PASS2))
-                              ? flags
-                              : (TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2);
+  const unsigned stage_bits = TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2;
+  const unsigned stages = (flags & stage_bits) ? (flags & stage_bits) : stage_bits;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   cudaError_t e;
@@ -243,7 +248,13 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   p.c = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
 
-  if (stages & TSEL_IMP_STAGE_PASS1) {
+  if ((stages & TSEL_IMP_STAGE_PASS1) && lse_provided) {
+    // The caller's LSE replaces the row-LSE pass.
+    e = launch_lse_import(lse, total_q, cu_seqlens_q, num_seg, p.qtile_off, p.nlse2, L.lse_stride,
+                          int(ceil_div(total_q, kTile) + num_seg), num_heads, &hdr->status,
+                          stream);
+    if (e != cudaSuccess) return cuda_fail(e, "LSE import launch");
+  } else if (stages & TSEL_IMP_STAGE_PASS1) {
     const CUtensorMap maps[4] = {qm64, qm16, km64, km16};
     ImpPassParams p1 = p;
     p1.units = reinterpret_cast<const uint2*>(ws + L.units1);

@@ -405,6 +405,27 @@ def gpu_arm(args) -> None:
     ms = reduce_max_over_ranks(ms_local, dev)
     value = replica_throughput(Tk, world, ms)
 
+    # --- LSE-provided mode: the attention kernel's LSE reused, column pass only ---
+    lse_given = lse.clone()
+    lp_ms = []
+    LP = tsel.TSEL_IMP_LSE_PROVIDED
+    for i in range(args.warmup + args.steps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        tsel.tsel_importance(d["q"], d["k"], d["cu_q"], d["cu_k"], w.max_seqlen_q, w.max_seqlen_k,
+                             flags=LP, lse=lse_given, scores=scores, workspace=ws, stream=stream)
+        topk()
+        gather()
+        b.record(stream)
+        if i >= args.warmup:
+            lp_ms.append((a, b))
+    torch.cuda.synchronize()
+    lp = reduce_max_over_ranks(sum(x.elapsed_time(y) for x, y in lp_ms) / len(lp_ms), dev)
+    lse_provided = {"ms_per_step": lp, "value": replica_throughput(Tk, world, lp), "unit": "tokens/s",
+                    "note": "LSE supplied by the caller (as the attention kernel's LSE would be); "
+                            "prep + LSE import + column pass + top-B + compaction"}
+
     # --- end to end through the API with host buffers ------------------------
     e2e = None
     if not args.no_e2e:
@@ -521,6 +542,7 @@ def gpu_arm(args) -> None:
         "kernels": kernels,
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
+        "lse_provided": lse_provided,
         "gpu_launches": 5 * args.steps,
         "clocks": clocks,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],

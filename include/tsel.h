@@ -76,6 +76,9 @@ typedef enum tsel_status {
 #define TSEL_DEV_NAN       0x10u /* NaN score given to the top-B selection */
 
 /* tsel_importance flags */
+#define TSEL_IMP_LSE_PROVIDED 0x1u   /* lse is an INPUT (natural log [H, Tq], e.g. the softmax
+                                        LSE FlashAttention returned): the row-LSE pass is
+                                        replaced by importing it */
 #define TSEL_IMP_STAGE_PREP   0x100u /* run only the listed stages (none listed = all): */
 #define TSEL_IMP_STAGE_PASS1  0x200u /*   schedule/validation, row-LSE pass, column pass. */
 #define TSEL_IMP_STAGE_PASS2  0x400u /*   Stages must run in order on one stream/workspace. */
@@ -112,8 +115,11 @@ TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int tot
  * num_heads    H in [1, 256]; num_kv_heads divides it.
  * head_dim     64, 80, 96, 112 or 128 (else TSEL_ERR_UNSUPPORTED).
  * softmax_scale  <= 0 selects 1/sqrt(head_dim).
- * flags        0, or TSEL_IMP_STAGE_* bits.
- * lse          out fp32 [num_heads, total_q], natural log; may be NULL.
+ * flags        0, TSEL_IMP_LSE_PROVIDED, and/or TSEL_IMP_STAGE_* bits.
+ * lse          fp32 [num_heads, total_q], natural log: an output (may be NULL), or
+ *              with TSEL_IMP_LSE_PROVIDED an input that must not be NULL — the
+ *              [VTC] section 3.2 design, which reuses the LSE the attention kernel
+ *              already produced and runs only the column pass.
  * scores       out fp32 [total_k].
  * workspace    >= tsel_importance_workspace_size(num_seg, total_q, total_k,
  *              num_heads) bytes; holds the status word and the schedule.

@@ -200,3 +200,46 @@ def test_bad_requests_and_keep_idx_set_status(tsel):
         tsel.tsel_clear_device_status(ws)
         tsel.tsel_gather_compact(hidden, None, i32([0, 20]), i32(bad), workspace=ws)
         assert tsel.tsel_read_device_status(ws) & tsel.TSEL_DEV_KEEP_IDX, bad
+
+
+# ---------------------------------------------------------------- LSE-provided mode
+
+@pytest.mark.parametrize("name", ["six_views_1536", "text_query_3072"])
+def test_lse_provided_matches_oracle(tsel, name):
+    """Column pass only, fed the oracle's own LSE (the attention kernel's LSE in a
+    serving stack): the scores match the oracle without running the row pass."""
+    w = W.make(name)
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    lse_in = torch.from_numpy(lse_ref.astype(np.float32)).cuda()
+    q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
+                     dtype=torch.uint8, device="cuda")
+    s, lse_out = tsel.tsel_importance(q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), w.max_seqlen_q,
+                                      w.max_seqlen_k, flags=tsel.TSEL_IMP_LSE_PROVIDED, lse=lse_in,
+                                      workspace=ws)
+    assert tsel.tsel_read_device_status(ws) == 0
+    assert max_rel_err(s.cpu().numpy(), s_ref) <= REL_TOL
+    assert lse_out.data_ptr() == lse_in.data_ptr()
+    assert torch.equal(lse_in.cpu(), torch.from_numpy(lse_ref.astype(np.float32)))  # input untouched
+
+
+def test_lse_provided_with_empty_and_keyless_segments(tsel):
+    w = W.make_segments([50, 0, 0, 9, 300], [60, 0, 33, 0, 129], 4, 2, 80, seed=306, hidden_dim=64)
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    lse_in = torch.from_numpy(lse_ref.astype(np.float32)).cuda()    # -inf rows included
+    s, _ = tsel.tsel_importance(bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits), i32(w.cu_seqlens_q),
+                                i32(w.cu_seqlens_k), 300, 129, flags=tsel.TSEL_IMP_LSE_PROVIDED,
+                                lse=lse_in)
+    assert max_rel_err(s.cpu().numpy(), s_ref) <= REL_TOL
+
+
+def test_lse_provided_agrees_with_full_path(tsel):
+    w = W.make_segments([1000, 257, 3000], [1000, 257, 3000], 16, 16, 80, seed=307,
+                        sink_counts=[20, 5, 60], hidden_dim=64)
+    q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
+    cq, ck = i32(w.cu_seqlens_q), i32(w.cu_seqlens_k)
+    s_full, lse = tsel.tsel_importance(q, k, cq, ck, 3000, 3000)
+    s_imp, _ = tsel.tsel_importance(q, k, cq, ck, 3000, 3000, flags=tsel.TSEL_IMP_LSE_PROVIDED,
+                                    lse=lse.clone())
+    a, b = s_full.cpu().numpy().astype(np.float64), s_imp.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(a - b) / a) <= 1e-4
