@@ -24,7 +24,7 @@ __all__ = [
     "tsel_keep_count", "tsel_read_device_status", "tsel_clear_device_status",
     "tsel_status_string", "tsel_last_error", "tsel_probe_ex2",
     "TSEL_DEV_SEQLENS", "TSEL_DEV_REQUESTS", "TSEL_DEV_KEEP_IDX", "TSEL_DEV_TIMEOUT", "TSEL_DEV_NAN",
-    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
+    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
 ]
 
 TSEL_OK = 0
@@ -41,6 +41,7 @@ TSEL_DEV_TIMEOUT = 0x8
 TSEL_DEV_NAN = 0x10
 
 TSEL_IMP_LSE_PROVIDED = 0x1
+TSEL_IMP_TEST_STALL = 0x10000
 TSEL_IMP_STAGE_PREP = 0x100
 TSEL_IMP_STAGE_PASS1 = 0x200
 TSEL_IMP_STAGE_PASS2 = 0x400

@@ -73,6 +73,7 @@ struct ImpPassParams {
   int H, Hkv, Tq;
   float c;               // softmax_scale * log2(e)
   uint64_t timeout_ns;
+  int stall;             // test hook: publish no work so every wait runs out
 };
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {

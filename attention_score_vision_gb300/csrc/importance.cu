@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int s_it = 0, a_it = 0, b_it = 0;
-      bool ok = true;
+      bool ok = p.stall == 0;   // the test hook leaves the consumers waiting for work
       while (ok) {
         const int slot = s_it % kSchedSlots;
         if (!wait_bounded(&sch_empty[slot], ((s_it / kSchedSlots) & 1) ^ 1, abort_flag, T)) {
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && p.stall == 0) {
         *abort_flag = 1;
         set_status(p.status, TSEL_DEV_TIMEOUT);
       }

@@ -168,8 +168,8 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     return fail(TSEL_ERR_INVALID_VALUE, "num_heads=%d num_kv_heads=%d", num_heads, num_kv_heads);
   if (!(head_dim == 64 || head_dim == 80 || head_dim == 96 || head_dim == 112 || head_dim == 128))
     return fail(TSEL_ERR_UNSUPPORTED, "head_dim=%d (supported: 64, 80, 96, 112, 128)", head_dim);
-  if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 |
-                 TSEL_IMP_STAGE_PASS2)) != 0)
+  if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_TEST_STALL | TSEL_IMP_STAGE_PREP |
+                 TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2)) != 0)
     return fail(TSEL_ERR_UNSUPPORTED, "flags=0x%x", flags);
   const bool lse_provided = (flags & TSEL_IMP_LSE_PROVIDED) != 0;
   if (lse_provided && total_q > 0 && lse == nullptr)
@@ -247,6 +247,8 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(float(head_dim));
   p.c = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
+  p.stall = (flags & TSEL_IMP_TEST_STALL) ? 1 : 0;
+  if (p.stall) p.timeout_ns = 50ull * 1000000ull;
 
   if ((stages & TSEL_IMP_STAGE_PASS1) && lse_provided) {
     // The caller's LSE replaces the row-LSE pass.

@@ -79,6 +79,11 @@ typedef enum tsel_status {
 #define TSEL_IMP_LSE_PROVIDED 0x1u   /* lse is an INPUT (natural log [H, Tq], e.g. the softmax
                                         LSE FlashAttention returned): the row-LSE pass is
                                         replaced by importing it */
+#define TSEL_IMP_TEST_STALL   0x10000u /* test hook for failure detection: the pass kernels'
+                                          scheduler publishes no work, every bounded wait
+                                          runs out after ~50 ms and TSEL_DEV_TIMEOUT is set;
+                                          no copy or MMA is in flight, the context stays
+                                          usable. Scores are not written. */
 #define TSEL_IMP_STAGE_PREP   0x100u /* run only the listed stages (none listed = all): */
 #define TSEL_IMP_STAGE_PASS1  0x200u /*   schedule/validation, row-LSE pass, column pass. */
 #define TSEL_IMP_STAGE_PASS2  0x400u /*   Stages must run in order on one stream/workspace. */

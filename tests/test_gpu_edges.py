@@ -243,3 +243,74 @@ def test_lse_provided_agrees_with_full_path(tsel):
                                     lse=lse.clone())
     a, b = s_full.cpu().numpy().astype(np.float64), s_imp.cpu().numpy().astype(np.float64)
     assert np.max(np.abs(a - b) / a) <= 1e-4
+
+
+# ---------------------------------------------------------------- failure detection
+
+def test_bounded_waits_report_timeout_and_context_survives(tsel):
+    """The test hook makes the pass kernels' scheduler publish nothing: every
+    waiting role gives up after its ~50 ms limit, sets TSEL_DEV_TIMEOUT and
+    exits with no copy or MMA in flight. The next call on the same context
+    works and matches the oracle."""
+    w = W.make("six_views_1536")
+    q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
+    cq, ck = i32(w.cu_seqlens_q), i32(w.cu_seqlens_k)
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
+                     dtype=torch.uint8, device="cuda")
+    tsel.tsel_importance(q, k, cq, ck, 256, 256, flags=tsel.TSEL_IMP_TEST_STALL, workspace=ws)
+    bits = tsel.tsel_read_device_status(ws)
+    assert bits & tsel.TSEL_DEV_TIMEOUT
+    tsel.tsel_clear_device_status(ws)
+    s, _ = tsel.tsel_importance(q, k, cq, ck, 256, 256, workspace=ws)
+    assert tsel.tsel_read_device_status(ws) == 0
+    _, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s.cpu().numpy(), s_ref) <= REL_TOL
+
+
+# ---------------------------------------------------------------- CUDA graph capture
+
+def test_whole_path_captures_into_a_cuda_graph(tsel):
+    """The three entry points enqueue kernels only (no allocation, no host
+    synchronisation), so the whole path can be captured once and replayed —
+    the launch-latency path for small requests. Replays match the eager run
+    bit for bit (the kernels are deterministic)."""
+    from gpu_util import to_device
+    w = W.make("six_views_1536")
+    d = to_device(w)
+    G, Tq, Tk, H, K = w.num_seg, w.total_q, w.total_k, w.num_heads, w.total_keep
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(G, Tq, Tk, H), dtype=torch.uint8, device="cuda")
+    scores = torch.empty(Tk, device="cuda")
+    lse = torch.empty((H, Tq), device="cuda")
+    keep_idx = torch.empty(K, dtype=torch.int32, device="cuda")
+    cu_keep = torch.empty(2, dtype=torch.int32, device="cuda")
+    oh = torch.empty((K, d["hidden"].shape[1]), dtype=torch.bfloat16, device="cuda")
+    op = torch.empty((K, 1), dtype=torch.int32, device="cuda")
+    oi = torch.empty(K, dtype=torch.int32, device="cuda")
+    oc = torch.empty(G + 1, dtype=torch.int32, device="cuda")
+
+    def path():
+        tsel.tsel_importance(d["q"], d["k"], d["cu_q"], d["cu_k"], 256, 256, lse=lse, scores=scores,
+                             workspace=ws)
+        tsel.tsel_select_topk(scores, d["req_off"], d["keep"], K, keep_idx=keep_idx, cu_keep=cu_keep,
+                              workspace=ws)
+        tsel.tsel_gather_compact(d["hidden"], d["pos"], d["cu_k"], keep_idx, out_hidden=oh, out_pos=op,
+                                 out_img_id=oi, out_cu_seqlens=oc, workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        path()                       # eager warm-up (sets per-device launch attributes)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (scores, keep_idx, oh, oi, oc)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        path()
+    for _ in range(3):
+        for t in (scores, keep_idx, oh, oi, oc):
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(ref, (scores, keep_idx, oh, oi, oc)):
+            assert torch.equal(a, b)
+    assert tsel.tsel_read_device_status(ws) == 0
