@@ -45,6 +45,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-small", action="store_true")
     ap.add_argument("--cpu-child", nargs=2, metavar=("WORKLOAD", "PAIRS"), help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -262,6 +263,68 @@ def replica_throughput(tokens_per_replica: int, world: int, ms_max: float) -> fl
     return world * tokens_per_replica / (ms_max * 1e-3)
 
 
+def small_request_latency(tsel, w, dev, flush, stream, reps: int = 20) -> dict:
+    """Device time of the whole path (importance, top-B, compaction) for one small
+    request, launched eagerly and replayed from a CUDA graph; L2 flushed (untimed)
+    before every timed run."""
+    import numpy as np
+    import torch
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    q, k, hidden = bf16(w.q_bits), bf16(w.k_bits), bf16(w.hidden_bits)
+    cq, ck, ro, kp, pos = (i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.req_tok_offsets),
+                           i32(w.keep_per_req), i32(w.pos))
+    G, Tq, Tk, H, K = w.num_seg, w.total_q, w.total_k, w.num_heads, w.total_keep
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(G, Tq, Tk, H), dtype=torch.uint8, device=dev)
+    scores = torch.empty(Tk, device=dev)
+    lse = torch.empty((H, Tq), device=dev)
+    keep_idx = torch.empty(K, dtype=torch.int32, device=dev)
+    cu_keep = torch.empty(w.keep_per_req.size + 1, dtype=torch.int32, device=dev)
+    oh = torch.empty((K, hidden.shape[1]), dtype=torch.bfloat16, device=dev)
+    op = torch.empty((K, w.pos.shape[1]), dtype=torch.int32, device=dev)
+    oi = torch.empty(K, dtype=torch.int32, device=dev)
+    oc = torch.empty(G + 1, dtype=torch.int32, device=dev)
+
+    def path(st):
+        tsel.tsel_importance(q, k, cq, ck, w.max_seqlen_q, w.max_seqlen_k, lse=lse, scores=scores,
+                             workspace=ws, stream=st)
+        tsel.tsel_select_topk(scores, ro, kp, K, keep_idx=keep_idx, cu_keep=cu_keep, workspace=ws,
+                              stream=st)
+        tsel.tsel_gather_compact(hidden, pos, ck, keep_idx, out_hidden=oh, out_pos=op, out_img_id=oi,
+                                 out_cu_seqlens=oc, workspace=ws, stream=st)
+
+    def timed(fn):
+        out = []
+        for i in range(reps + 3):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            if i >= 3:
+                out.append(a.elapsed_time(b) * 1e3)
+        return float(np.median(out))
+
+    eager_us = timed(lambda: path(stream))
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        path(side)
+    stream.wait_stream(side)
+    graph_us = timed(g.replay)
+    if tsel.tsel_read_device_status(ws) != 0:
+        raise RuntimeError(f"device status set for {w.name}")
+    return {"tokens": Tk, "keep": K, "eager_us": eager_us, "graph_us": graph_us,
+            "note": "median of 20 runs, L2 flushed before each (untimed)"}
+
+
 def gpu_arm(args) -> None:
     import numpy as np
     import torch
@@ -468,6 +531,12 @@ def gpu_arm(args) -> None:
                "note": "pinned host inputs copied in, importance+top-B+compaction, selection "
                        "metadata copied out; compacted hidden rows stay on the device"}
 
+    # --- small requests: whole path replayed from one CUDA graph -------------
+    small = {}
+    if not args.no_small:
+        for name in ("single_image_256", "six_views_1536", "text_query_3072"):
+            small[name] = small_request_latency(tsel, W.make(name), dev, flush, stream)
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -543,6 +612,7 @@ def gpu_arm(args) -> None:
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "lse_provided": lse_provided,
+        "small_requests": small,
         "gpu_launches": 5 * args.steps,
         "clocks": clocks,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
