@@ -310,10 +310,12 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
 // Online softmax of one query row over 32 columns of S (pass 1). Columns at
 // or beyond `valid` lie outside the segment. m is a reference max of S*c and l
 // the sum of exp2(S*c - m); m only moves when the chunk max exceeds it by
-// more than 8 (terms stay below 2^8), so rescaling is rare.
+// more than 8 (terms stay below 2^8), so rescaling is rare. Packed float2
+// arithmetic (one f32x2 FMA / ADD per two columns) around one MUFU exp2 per
+// column.
 __device__ __forceinline__ void row_softmax_chunk(const uint32_t (&r)[32], int valid, float c,
-                                                  uint64_t c2, float& m, float& l,
-                                                  uint64_t (&a)[2]) {
+                                                  float2 c2, float& m, float& l,
+                                                  float2 (&a)[2]) {
   if (valid <= 0) return;
   float v[32];
 #pragma unroll
@@ -332,20 +334,17 @@ __device__ __forceinline__ void row_softmax_chunk(const uint32_t (&r)[32], int v
   if (tmax > m + 8.f) {
     // also covers the first chunk of a row (m = -inf, l = 0)
     const float s = ex2(m - tmax);
-    float x0, x1;
-    unpack2(fadd2(a[0], a[1]), x0, x1);
-    l = (l + x0 + x1) * s;
-    a[0] = 0ull;
-    a[1] = 0ull;
+    l = (l + a[0].x + a[0].y + a[1].x + a[1].y) * s;
+    a[0] = make_float2(0.f, 0.f);
+    a[1] = make_float2(0.f, 0.f);
     m = tmax;
   }
   if (m > kNegInf) {
-    const uint64_t nm2 = pack2(-m, -m);
+    const float2 nm2 = make_float2(-m, -m);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      float x0, x1;
-      unpack2(ffma2(pack2(v[2 * j], v[2 * j + 1]), c2, nm2), x0, x1);
-      a[j & 1] = fadd2(a[j & 1], pack2(ex2(x0), ex2(x1)));
+      const float2 x = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), c2, nm2);
+      a[j & 1] = __fadd2_rn(a[j & 1], make_float2(ex2(x.x), ex2(x.y)));
     }
   }
 }
@@ -353,19 +352,18 @@ __device__ __forceinline__ void row_softmax_chunk(const uint32_t (&r)[32], int v
 // Adds exp2(S*c - LSE2) of 32 query columns into the packed per-key
 // accumulators (pass 2). nl holds -LSE2 of those columns (-inf for padding).
 __device__ __forceinline__ void column_sum_chunk(const uint32_t (&r)[32], const float4* nl,
-                                                 uint64_t c2, uint64_t (&acc)[2]) {
+                                                 float2 c2, float2 (&acc)[2]) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float4 t = nl[j];
-    float x0, x1, x2, x3;
-    unpack2(ffma2(pack2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), c2,
-                  pack2(t.x, t.y)),
-            x0, x1);
-    unpack2(ffma2(pack2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), c2,
-                  pack2(t.z, t.w)),
-            x2, x3);
-    acc[0] = fadd2(acc[0], pack2(ex2(x0), ex2(x1)));
-    acc[1] = fadd2(acc[1], pack2(ex2(x2), ex2(x3)));
+    const float2 x01 = __ffma2_rn(
+        make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), c2,
+        make_float2(t.x, t.y));
+    const float2 x23 = __ffma2_rn(
+        make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), c2,
+        make_float2(t.z, t.w));
+    acc[0] = __fadd2_rn(acc[0], make_float2(ex2(x01.x), ex2(x01.y)));
+    acc[1] = __fadd2_rn(acc[1], make_float2(ex2(x23.x), ex2(x23.y)));
   }
 }
 
@@ -597,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kbuf = 2 * par + a_half;
     const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(kbuf * kTile);
     const float c = p.c;
-    const uint64_t c2 = pack2(c, c);
+    const float2 c2 = make_float2(c, c);
     int s_it = 0, b_it = 0, unit_it = 0;
     bool ok = true;
     while (ok) {
@@ -612,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
       const int n_b = PASS == 1 ? nbt : (nbt > 0 ? p.H * nbt : 0);
       float m = kNegInf, l = 0.f;           // pass 1
-      uint64_t acc[2] = {0ull, 0ull};      // pass 1: sum of exp2 since m; pass 2: per-key sum
+      float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // pass 1: sum since m; pass 2: per-key sum
       for (int bi = 0; bi < n_b; ++bi, ++b_it) {
         if ((b_it & 1) != par) continue;
         const uint32_t use = uint32_t(b_it >> 1) & 1u;
@@ -666,9 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* comb = sComb + (a_half * 2 + cb) * 2 * kTile;
       uint64_t* cfull = &comb_full[a_half * 2 + cb];
       uint64_t* cempty = &comb_empty[a_half * 2 + cb];
-      float x0, x1;
-      unpack2(fadd2(acc[0], acc[1]), x0, x1);
-      const float part = x0 + x1;   // pass 1: sum since m; pass 2: per-key sum
+      const float2 accs = __fadd2_rn(acc[0], acc[1]);
+      const float part = accs.x + accs.y;   // pass 1: sum since m; pass 2: per-key sum
       if (par == 1) {
         if (!warp_wait(cempty, cpar ^ 1, abort_flag, T)) { ok = false; break; }
         comb[row] = PASS == 1 ? m : part;
