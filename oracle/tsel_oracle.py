@@ -56,6 +56,32 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return b.view(np.float32).astype(np.float64)
 
 
+def e4m3_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 (OCP 8-bit floating point, "FN" variant) -> fp64, exactly.
+
+    1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
+    subnormal (2^-6 * m/8); no infinities; S.1111.111 is NaN; largest finite
+    magnitude 448. (LiteVLM's FP8 deployment quantises to this format.)
+    """
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    normal = np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    sub = np.ldexp(m / 8.0, -6)
+    val = np.where(e == 0, sub, normal)
+    val = np.where((e == 15) & ((b & 0x7) == 7), np.nan, val)
+    return sign * val
+
+
+def decode_inputs(bits, fmt: str) -> np.ndarray:
+    if fmt == "bf16":
+        return bf16_bits_to_f64(bits)
+    if fmt == "e4m3":
+        return e4m3_bits_to_f64(bits)
+    raise ValueError(f"unknown input format {fmt}")
+
+
 # ---------------------------------------------------------------------------
 # Importance (LiteVLM token selection; VisionZip-style mean attention received)
 # ---------------------------------------------------------------------------
@@ -79,16 +105,18 @@ def attention_probabilities(q: np.ndarray, k: np.ndarray, scale: float):
     return p, lse
 
 
-def importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale=None):
+def importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale=None, fmt="bf16"):
     """Mean attention probability received by every key token.
 
-    q_bits: uint16 [Tq, H, d] bf16 bits; k_bits: uint16 [Tk, Hkv, d].
-    cu_seqlens_q / cu_seqlens_k: int [G+1]; segment g attends queries
-    [cu_q[g], cu_q[g+1]) to keys [cu_k[g], cu_k[g+1]).
+    q_bits: [Tq, H, d] and k_bits: [Tk, Hkv, d] as bit patterns of `fmt`
+    ("bf16": uint16, "e4m3": uint8). cu_seqlens_q / cu_seqlens_k: int [G+1];
+    segment g attends queries [cu_q[g], cu_q[g+1]) to keys [cu_k[g], cu_k[g+1]).
+    softmax_scale multiplies q.k (defaults to 1/sqrt(d)); for quantised inputs
+    it carries the dequantisation scales too.
     Returns (lse [H, Tq] fp64 natural log, scores [Tk] fp64).
     """
-    q = bf16_bits_to_f64(q_bits)
-    k = bf16_bits_to_f64(k_bits)
+    q = decode_inputs(q_bits, fmt)
+    k = decode_inputs(k_bits, fmt)
     tq, H, d = q.shape
     tk, Hkv, _ = k.shape
     group = H // Hkv
@@ -169,9 +197,9 @@ def gather_compact(hidden, pos, cu_seqlens_k, keep_idx):
 
 
 def prune(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, req_tok_offsets, keep_per_req,
-          hidden, pos, softmax_scale=None):
+          hidden, pos, softmax_scale=None, fmt="bf16"):
     """The whole path: importance, pooled top-B, compaction."""
-    lse, scores = importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale)
+    lse, scores = importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale, fmt)
     keep_idx, cu_keep = select_topk(scores, req_tok_offsets, keep_per_req)
     out_hidden, out_pos, img_id, cu_kept = gather_compact(hidden, pos, cu_seqlens_k, keep_idx)
     return {"lse": lse, "scores": scores, "keep_idx": keep_idx, "cu_keep": cu_keep,

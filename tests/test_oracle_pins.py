@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
-from workloads import f32_to_bf16_bits, make_segments
+from workloads import f32_to_bf16_bits, f32_to_e4m3_bits, make_segments
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -304,3 +304,55 @@ def test_end_to_end_invariants():
     s = out["scores"]
     dropped = np.setdiff1d(np.arange(128), k)
     assert s[k].min() >= s[dropped].max()
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 inputs (LiteVLM's FP8 deployment)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decode_known_codes():
+    """Values fixed by the OCP FP8 E4M3 definition (bias 7, 3 mantissa bits,
+    subnormals below 2^-6, max 448, S.1111.111 = NaN)."""
+    codes = np.array([0x00, 0x38, 0x40, 0x7E, 0x01, 0x07, 0x08, 0x37, 0x80, 0xB8, 0xFE], np.uint8)
+    expect = [0.0, 1.0, 2.0, 448.0, 2.0 ** -9, 7 * 2.0 ** -9, 2.0 ** -6, 0.9375, -0.0, -1.0, -448.0]
+    got = oracle.e4m3_bits_to_f64(codes)
+    assert list(got) == expect
+    assert np.isnan(oracle.e4m3_bits_to_f64(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_decode_is_monotone_with_one_ulp_steps():
+    v = oracle.e4m3_bits_to_f64(np.arange(0, 0x7F, dtype=np.uint8))
+    assert np.all(np.diff(v) > 0)
+    # within each binade of normals the spacing is 2^(e-10); subnormals step 2^-9
+    steps = np.diff(v)
+    for code in range(1, 0x7E):
+        e = max(code >> 3, 1)
+        assert steps[code] == 2.0 ** (e - 10) or (code & 7) == 7
+
+
+def test_e4m3_quantiser_is_nearest_ties_even_and_saturating():
+    rng = np.random.default_rng(20)
+    x = np.concatenate([rng.normal(0, 50, 2000), [0.0, -0.0, 500.0, -1e9, 2.0 ** -10, 3 * 2.0 ** -11]])
+    bits = f32_to_e4m3_bits(x)
+    table = oracle.e4m3_bits_to_f64(np.arange(0, 0x7F, dtype=np.uint8))
+    dec = oracle.e4m3_bits_to_f64(bits)
+    for xi, di, bi in zip(x, dec, bits):
+        a = min(abs(xi), 448.0)
+        best = np.min(np.abs(table - a))
+        assert abs(abs(di) - a) == best
+        if best > 0 and np.sum(np.abs(table - a) == best) == 2:
+            assert (int(bi) & 1) == 0          # tie -> even code
+    assert dec[-4] == 448.0 and dec[-3] == -448.0
+
+
+def test_importance_with_e4m3_inputs_one_hot_closed_form():
+    nq, nk, d, H = 5, 40, 64, 2
+    q = np.zeros((nq, H, d), np.uint8)
+    q[:, :, 0] = 0x40            # 2.0
+    k = np.zeros((nk, H, d), np.uint8)
+    k[7, :, 0] = 0x40
+    lse, scores = oracle.importance(q, k, [0, nq], [0, nk], fmt="e4m3")
+    c = math.exp(4.0 / 8.0)
+    assert abs(scores[7] - c / (c + nk - 1)) < 1e-13
+    assert abs(scores[0] - 1 / (c + nk - 1)) < 1e-13
+    np.testing.assert_allclose(lse, math.log(c + nk - 1), rtol=1e-13)

@@ -45,6 +45,33 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def _e4m3_table() -> np.ndarray:
+    """Non-negative finite E4M3 values indexed by their code 0x00..0x7E."""
+    vals = np.empty(127, dtype=np.float64)
+    for code in range(127):
+        e, m = code >> 3, code & 7
+        vals[code] = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+_E4M3 = _e4m3_table()
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Quantise to FP8 E4M3: nearest value, ties to the even code, magnitudes
+    above 448 saturate to 448 (no NaN is produced)."""
+    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), 448.0)
+    hi = np.searchsorted(_E4M3, a, side="left")          # first value >= a
+    hi = np.minimum(hi, 126)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E4M3[lo]
+    d_hi = _E4M3[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    neg = np.signbit(np.asarray(x, dtype=np.float64)) & (code != 0)
+    return (code | np.where(neg, 0x80, 0).astype(np.uint8)).astype(np.uint8)
+
+
 @dataclass
 class Workload:
     """One seeded problem: packed varlen Q/K, metadata, hidden rows and positions."""
@@ -190,6 +217,22 @@ def make_segments(lengths_q, lengths_k, num_heads, num_kv_heads, head_dim, *,
 def keep_floor(n: int, permille: int) -> int:
     """floor(n * permille / 1000) in integer arithmetic (budget rounding)."""
     return (int(n) * int(permille)) // 1000
+
+
+def to_e4m3(w: "Workload") -> "Workload":
+    """The same problem with Q and K quantised to FP8 E4M3 with one scale per
+    tensor (amax maps to 448); the scales are folded into softmax_scale."""
+    q = bf16_bits_to_f32(w.q_bits).astype(np.float64)
+    k = bf16_bits_to_f32(w.k_bits).astype(np.float64)
+    sq = max(float(np.abs(q).max(initial=0.0)), 1e-30) / 448.0
+    sk = max(float(np.abs(k).max(initial=0.0)), 1e-30) / 448.0
+    meta = dict(w.meta)
+    meta.update(fmt="e4m3", q_scale=sq, k_scale=sk)
+    return Workload(name=w.name + "_e4m3", q_bits=f32_to_e4m3_bits(q / sq),
+                    k_bits=f32_to_e4m3_bits(k / sk), cu_seqlens_q=w.cu_seqlens_q,
+                    cu_seqlens_k=w.cu_seqlens_k, req_tok_offsets=w.req_tok_offsets,
+                    keep_per_req=w.keep_per_req, hidden_bits=w.hidden_bits, pos=w.pos,
+                    softmax_scale=w.softmax_scale * sq * sk, meta=meta)
 
 
 # ---------------------------------------------------------------------------
