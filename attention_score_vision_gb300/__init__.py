@@ -24,7 +24,7 @@ __all__ = [
     "tsel_keep_count", "tsel_read_device_status", "tsel_clear_device_status",
     "tsel_status_string", "tsel_last_error", "tsel_probe_ex2",
     "TSEL_DEV_SEQLENS", "TSEL_DEV_REQUESTS", "TSEL_DEV_KEEP_IDX", "TSEL_DEV_TIMEOUT", "TSEL_DEV_NAN",
-    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
+    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
 ]
 
 TSEL_OK = 0
@@ -41,6 +41,7 @@ TSEL_DEV_TIMEOUT = 0x8
 TSEL_DEV_NAN = 0x10
 
 TSEL_IMP_LSE_PROVIDED = 0x1
+TSEL_IMP_FP8_E4M3 = 0x2
 TSEL_IMP_TEST_STALL = 0x10000
 TSEL_IMP_STAGE_PREP = 0x100
 TSEL_IMP_STAGE_PASS1 = 0x200
@@ -142,10 +143,17 @@ def tsel_importance(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torch.Tensor
     q: bf16 [Tq, H, d] (rows may be strided, head dim contiguous);
     k: bf16 [Tk, Hkv, d]; cu_seqlens_*: int32 [G+1] on the same device.
     With flags containing TSEL_IMP_LSE_PROVIDED, `lse` (fp32 [H, Tq], natural
-    log) is an input and only the column pass runs.
+    log) is an input and only the column pass runs. uint8 / float8_e4m3fn q and
+    k are E4M3 inputs; softmax_scale then includes their dequantisation scales.
     """
-    _need(q, torch.bfloat16, "q")
-    _need(k, torch.bfloat16, "k")
+    fp8_types = (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+    if q.dtype in fp8_types and k.dtype in fp8_types:
+        flags |= TSEL_IMP_FP8_E4M3   # E4M3 bytes; softmax_scale must carry the dequant scales
+        if not (q.is_cuda and k.is_cuda):
+            raise TypeError("q and k must be CUDA tensors")
+    else:
+        _need(q, torch.bfloat16, "q")
+        _need(k, torch.bfloat16, "k")
     _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
     _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
     tq, H, d = q.shape

@@ -51,13 +51,19 @@ constexpr int kEpiWarps = 16;       // four warpgroups
 constexpr int kEpiFirstWarp = 2;
 constexpr int kThreads = 32 * (kEpiFirstWarp + kEpiWarps);  // 576
 
-template <int D>
+// Shared-memory tile geometry. bf16 rows are D*2 bytes, split into 64-column
+// chunks (128-byte swizzle) and 16-column chunks (32-byte swizzle). E4M3 rows
+// are padded to one 128-byte chunk (128 columns; the padding reads as zeros)
+// and the MMA runs ceil(D/32) K-steps of 32 over it.
+template <int D, bool FP8>
 struct TileCfg {
   static_assert(D % 16 == 0 && D >= 64 && D <= 128, "head_dim");
-  static constexpr int N64 = D / 64;               // 64-column chunks (128-byte swizzle)
-  static constexpr int N16 = (D % 64) / 16;        // 16-column chunks (32-byte swizzle)
-  static constexpr int TILE_BYTES = kTile * D * 2; // one 128-row bf16 tile
-  static constexpr int A_BYTES = 4 * TILE_BYTES;   // 2 slots x 2 A tiles
+  static constexpr int N64 = FP8 ? 1 : D / 64;           // 128-byte swizzle chunks
+  static constexpr int N16 = FP8 ? 0 : (D % 64) / 16;    // 32-byte swizzle chunks
+  static constexpr int KSTEPS128 = FP8 ? (D + 31) / 32 : 4;  // MMA K-steps per 128-byte chunk
+  static constexpr int ROW_BYTES = FP8 ? 128 : D * 2;
+  static constexpr int TILE_BYTES = kTile * ROW_BYTES;   // one 128-row tile
+  static constexpr int A_BYTES = 4 * TILE_BYTES;         // 2 slots x 2 A tiles
   static constexpr int STAGES_RAW = (200 * 1024 - A_BYTES - 8192) / TILE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int OFF_A = 0;
@@ -257,26 +263,43 @@ __device__ __forceinline__ Unit decode_unit(const ImpPassParams& p, uint2 u) {
   return r;
 }
 
-// Loads one 128-row tile of head columns [x0, x0 + D) starting at row y.
-template <int D>
+// Loads one 128-row tile of head `head` (columns [0, D)) starting at row y.
+// bf16: 2-D maps over [rows, heads*D] (x = head*D + column); E4M3: a 3-D map
+// over [rows, heads, D] whose 128-column box pads past D with zeros.
+template <int D, bool FP8>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* m64,
-                                          const CUtensorMap* m16, uint64_t* bar, int x0, int y) {
-  using C = TileCfg<D>;
+                                          const CUtensorMap* m16, uint64_t* bar, int head, int y) {
+  using C = TileCfg<D, FP8>;
+  if (FP8) {
+    tma_load_3d(dst, m64, bar, 0, head, y);
+  } else {
+    const int x0 = head * D;
 #pragma unroll
-  for (int c = 0; c < C::N64; ++c) tma_load_2d(dst + c * 16384, m64, bar, x0 + 64 * c, y);
+    for (int c = 0; c < C::N64; ++c) tma_load_2d(dst + c * 16384, m64, bar, x0 + 64 * c, y);
 #pragma unroll
-  for (int j = 0; j < C::N16; ++j)
-    tma_load_2d(dst + C::N64 * 16384 + j * 4096, m16, bar, x0 + 64 * C::N64 + 16 * j, y);
+    for (int j = 0; j < C::N16; ++j)
+      tma_load_2d(dst + C::N64 * 16384 + j * 4096, m16, bar, x0 + 64 * C::N64 + 16 * j, y);
+  }
 }
 
 // Issues the MMAs of one 128x128 tile: D = A * B^T over the head dimension.
-template <int D>
+template <int D, bool FP8>
 __device__ __forceinline__ void issue_tile_mmas(uint32_t d_tmem, const uint8_t* a,
                                                 const uint8_t* b) {
-  using C = TileCfg<D>;
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
+  using C = TileCfg<D, FP8>;
   const uint32_t a0 = smem_u32(a), b0 = smem_u32(b);
   uint32_t acc = 0;
+  if (FP8) {
+    constexpr uint32_t kIdesc = idesc_e4m3_f32(kTile, kTile);
+#pragma unroll
+    for (int k = 0; k < C::KSTEPS128; ++k) {
+      mma_f8(d_tmem, smem_desc(a0 + k * 32, 2, 1024), smem_desc(b0 + k * 32, 2, 1024), kIdesc,
+             acc);
+      acc = 1;
+    }
+    return;
+  }
+  constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
 #pragma unroll
   for (int c = 0; c < C::N64; ++c) {
 #pragma unroll
@@ -367,13 +390,13 @@ __device__ __forceinline__ void column_sum_chunk(const uint32_t (&r)[32], const 
   }
 }
 
-template <int PASS, int D>
+template <int PASS, int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     imp_pass_kernel(const __grid_constant__ CUtensorMap mapA64,
                     const __grid_constant__ CUtensorMap mapA16,
                     const __grid_constant__ CUtensorMap mapB64,
                     const __grid_constant__ CUtensorMap mapB16, const ImpPassParams p) {
-  using C = TileCfg<D>;
+  using C = TileCfg<D, FP8>;
   constexpr int S = C::STAGES;
   extern __shared__ uint8_t smem_dyn[];
   // 128-byte swizzle atoms key off shared-address bits: align the carve-out
@@ -481,23 +504,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int as = a_it & 1;
           if (!wait_bounded(&a_empty[as], ((a_it >> 1) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
           mbar_arrive_expect_tx(&a_full[as], uint32_t(w.nA * C::TILE_BYTES));
-          const int ax = PASS == 1 ? w.h * D : ag * D;
+          const int ahead = PASS == 1 ? w.h : ag;
           const int ay = (PASS == 1 ? w.q0 : w.k0) + w.pair * kPair;
           for (int a = 0; a < w.nA; ++a)
-            load_tile<D>(sA + (as * 2 + a) * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as], ax,
-                         ay + a * kTile);
+            load_tile<D, FP8>(sA + (as * 2 + a) * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as],
+                              ahead, ay + a * kTile);
           ++a_it;
           const int n_heads = PASS == 1 ? 1 : group;
           for (int hh = 0; hh < n_heads && ok; ++hh) {
             const int h = PASS == 1 ? w.h : ag * group + hh;
-            const int bx = PASS == 1 ? (w.h / group) * D : h * D;
+            const int bhead = PASS == 1 ? w.h / group : h;
             const int nbt = PASS == 1 ? n_b : int(ceil_div(w.nq, kTile));
             for (int bt = 0; bt < nbt; ++bt) {
               const int bs = b_it % S;
               if (!wait_bounded(&b_empty[bs], ((b_it / S) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
               mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES);
-              load_tile<D>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], bx,
-                           (PASS == 1 ? w.k0 : w.q0) + bt * kTile);
+              load_tile<D, FP8>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], bhead,
+                                (PASS == 1 ? w.k0 : w.q0) + bt * kTile);
               if (PASS == 2) {
                 const int ls = b_it % kLseSlots;
                 if (!wait_bounded(&lse_empty[ls], ((b_it / kLseSlots) & 1) ^ 1, abort_flag, T)) {
@@ -564,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!wait_bounded(&acc_empty[k], use ^ 1u, abort_flag, T)) { ok = false; break; }
               tc_fence_after();
               if (a < w.nA)
-                issue_tile_mmas<D>(tmem_base + uint32_t(k * kTile),
+                issue_tile_mmas<D, FP8>(tmem_base + uint32_t(k * kTile),
                                    sA + (as * 2 + a) * C::TILE_BYTES, sB + bs * C::TILE_BYTES);
               mma_commit(&acc_full[k]);
             }
@@ -758,11 +781,11 @@ cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int
   return cudaPeekAtLastError();
 }
 
-template <int PASS, int D>
+template <int PASS, int D, bool FP8>
 static cudaError_t launch_pass_t(const CUtensorMap* maps, const ImpPassParams& p, int grid,
                                  cudaStream_t stream) {
-  using C = TileCfg<D>;
-  auto kern = imp_pass_kernel<PASS, D>;
+  using C = TileCfg<D, FP8>;
+  auto kern = imp_pass_kernel<PASS, D, FP8>;
   static bool attr_set[128] = {};  // per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -785,13 +808,17 @@ cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, 
   return cudaPeekAtLastError();
 }
 
-// maps: A64, A16, B64, B16 (pass 1: A = Q, B = K; pass 2: A = K, B = Q).
-cudaError_t launch_imp_pass(int pass, int head_dim, const CUtensorMap* maps,
+// maps: A64, A16, B64, B16 (pass 1: A = Q, B = K; pass 2: A = K, B = Q). For
+// E4M3 inputs A64 / B64 are the 3-D maps and A16 / B16 are unused.
+cudaError_t launch_imp_pass(int pass, int head_dim, bool fp8, const CUtensorMap* maps,
                             const ImpPassParams& p, int grid, cudaStream_t stream) {
-#define TSEL_PASS_CASE(DD)                                                              \
-  case DD:                                                                              \
-    return pass == 1 ? launch_pass_t<1, DD>(maps, p, grid, stream)                      \
-                     : launch_pass_t<2, DD>(maps, p, grid, stream);
+#define TSEL_PASS_CASE(DD)                                                                    \
+  case DD:                                                                                    \
+    if (fp8)                                                                                  \
+      return pass == 1 ? launch_pass_t<1, DD, true>(maps, p, grid, stream)                    \
+                       : launch_pass_t<2, DD, true>(maps, p, grid, stream);                   \
+    return pass == 1 ? launch_pass_t<1, DD, false>(maps, p, grid, stream)                     \
+                     : launch_pass_t<2, DD, false>(maps, p, grid, stream);
   switch (head_dim) {
     TSEL_PASS_CASE(64)
     TSEL_PASS_CASE(80)

@@ -18,7 +18,7 @@ namespace tsel {
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
                             int max_q, int max_k, int H, uint8_t* ws, const ImpWsLayout& L,
                             cudaStream_t stream);
-cudaError_t launch_imp_pass(int pass, int head_dim, const CUtensorMap* maps,
+cudaError_t launch_imp_pass(int pass, int head_dim, bool fp8, const CUtensorMap* maps,
                             const ImpPassParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
                               const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
@@ -104,6 +104,22 @@ bool make_map(CUtensorMap* map, const void* base, int64_t width, int64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+// 3-D uint8 tensor map over [rows, heads, head_dim] bytes, box of 128 columns
+// (past head_dim the box reads zeros) x 1 head x 128 rows, 128-byte swizzle.
+bool make_map_fp8(CUtensorMap* map, const void* base, int64_t head_dim, int64_t heads, int64_t rows,
+                  int64_t row_stride_bytes) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(heads), cuuint64_t(rows)};
+  cuuint64_t strides[2] = {cuuint64_t(head_dim), cuuint64_t(row_stride_bytes)};
+  cuuint32_t box[3] = {128u, 1u, cuuint32_t(kTile)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 uint64_t wait_timeout_ns() {
   static uint64_t t = [] {
     const char* s = std::getenv("TSEL_WAIT_TIMEOUT_MS");
@@ -168,8 +184,8 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     return fail(TSEL_ERR_INVALID_VALUE, "num_heads=%d num_kv_heads=%d", num_heads, num_kv_heads);
   if (!(head_dim == 64 || head_dim == 80 || head_dim == 96 || head_dim == 112 || head_dim == 128))
     return fail(TSEL_ERR_UNSUPPORTED, "head_dim=%d (supported: 64, 80, 96, 112, 128)", head_dim);
-  if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_TEST_STALL | TSEL_IMP_STAGE_PREP |
-                 TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2)) != 0)
+  if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_FP8_E4M3 | TSEL_IMP_TEST_STALL |
+                 TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2)) != 0)
     return fail(TSEL_ERR_UNSUPPORTED, "flags=0x%x", flags);
   const bool lse_provided = (flags & TSEL_IMP_LSE_PROVIDED) != 0;
   if (lse_provided && total_q > 0 && lse == nullptr)
@@ -178,11 +194,15 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     return fail(TSEL_ERR_INVALID_VALUE, "null cu_seqlens or workspace");
   if ((total_k > 0 && (scores == nullptr || k == nullptr)) || (total_q > 0 && q == nullptr))
     return fail(TSEL_ERR_INVALID_VALUE, "null q/k/scores");
+  const bool fp8 = (flags & TSEL_IMP_FP8_E4M3) != 0;
+  const int elem = fp8 ? 1 : 2;
+  if (fp8 && !(softmax_scale > 0.f))
+    return fail(TSEL_ERR_INVALID_VALUE, "TSEL_IMP_FP8_E4M3 needs softmax_scale > 0");
   const int64_t hd = int64_t(num_heads) * head_dim, kvd = int64_t(num_kv_heads) * head_dim;
   if (q_row_stride == 0) q_row_stride = hd;
   if (k_row_stride == 0) k_row_stride = kvd;
-  if (q_row_stride < hd || k_row_stride < kvd || (q_row_stride * 2) % 16 != 0 ||
-      (k_row_stride * 2) % 16 != 0)
+  if (q_row_stride < hd || k_row_stride < kvd || (q_row_stride * elem) % 16 != 0 ||
+      (k_row_stride * elem) % 16 != 0)
     return fail(TSEL_ERR_INVALID_VALUE, "row strides %lld/%lld", (long long)q_row_stride,
                 (long long)k_row_stride);
   if ((q && !aligned16(q)) || (k && !aligned16(k)))
@@ -217,10 +237,15 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
 
   CUtensorMap qm64, qm16, km64, km16;
   const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw32 = CU_TENSOR_MAP_SWIZZLE_32B;
-  const bool tail = (head_dim % 64) != 0;
-  if (!make_map(&qm64, q, hd, total_q, q_row_stride * 2, 64, sw128) ||
-      !make_map(&km64, k, kvd, total_k, k_row_stride * 2, 64, sw128))
+  const bool tail = !fp8 && (head_dim % 64) != 0;
+  if (fp8) {
+    if (!make_map_fp8(&qm64, q, head_dim, num_heads, total_q, q_row_stride) ||
+        !make_map_fp8(&km64, k, head_dim, num_kv_heads, total_k, k_row_stride))
+      return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E4M3 maps)");
+  } else if (!make_map(&qm64, q, hd, total_q, q_row_stride * 2, 64, sw128) ||
+             !make_map(&km64, k, kvd, total_k, k_row_stride * 2, 64, sw128)) {
     return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (64-wide box)");
+  }
   if (tail) {
     if (!make_map(&qm16, q, hd, total_q, q_row_stride * 2, 16, sw32) ||
         !make_map(&km16, k, kvd, total_k, k_row_stride * 2, 16, sw32))
@@ -263,7 +288,7 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     p1.num_units = &hdr->num_units[0];
     p1.sched_ctr = &hdr->sched_ctr[0];
     const int grid = int(L.u1_max < sms ? L.u1_max : sms);
-    e = launch_imp_pass(1, head_dim, maps, p1, grid, stream);
+    e = launch_imp_pass(1, head_dim, fp8, maps, p1, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pass-1 launch");
   }
   if (stages & TSEL_IMP_STAGE_PASS2) {
@@ -273,7 +298,7 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     p2.num_units = &hdr->num_units[1];
     p2.sched_ctr = &hdr->sched_ctr[1];
     const int grid = int(L.u2_max < sms ? L.u2_max : sms);
-    e = launch_imp_pass(2, head_dim, maps, p2, grid, stream);
+    e = launch_imp_pass(2, head_dim, fp8, maps, p2, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pass-2 launch");
   }
   return TSEL_OK;

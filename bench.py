@@ -46,6 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--cpu-child", nargs=2, metavar=("WORKLOAD", "PAIRS"), help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
@@ -489,6 +490,36 @@ def gpu_arm(args) -> None:
                     "note": "LSE supplied by the caller (as the attention kernel's LSE would be); "
                             "prep + LSE import + column pass + top-B + compaction"}
 
+    # --- FP8 E4M3 Q/K (one scale per tensor folded into the softmax scale) ----
+    fp8 = None
+    if not args.no_fp8:
+        w8 = W.to_e4m3(w)
+        q8 = torch.from_numpy(w8.q_bits).to(dev)
+        k8 = torch.from_numpy(w8.k_bits).to(dev)
+        f_ms, f_imp = [], []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i & 0xFF)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            ev[0].record(stream)
+            tsel.tsel_importance(q8, k8, d["cu_q"], d["cu_k"], w.max_seqlen_q, w.max_seqlen_k,
+                                 softmax_scale=w8.softmax_scale, lse=lse, scores=scores,
+                                 workspace=ws, stream=stream)
+            ev[1].record(stream)
+            topk()
+            gather()
+            ev[2].record(stream)
+            if i >= args.warmup:
+                f_ms.append(ev)
+        torch.cuda.synchronize()
+        if tsel.tsel_read_device_status(ws) != 0:
+            raise RuntimeError("device status set in the FP8 run")
+        step = reduce_max_over_ranks(sum(e[0].elapsed_time(e[2]) for e in f_ms) / len(f_ms), dev)
+        imp = sum(e[0].elapsed_time(e[1]) for e in f_ms) / len(f_ms)
+        fp8 = {"ms_per_step": step, "value": replica_throughput(Tk, world, step),
+               "unit": "tokens/s", "importance_ms": imp,
+               "note": "Q and K in FP8 E4M3 (kind::f8f6f4 MMAs, K padded to a multiple of "
+                       "32), everything else as the bf16 line"}
+
     # --- end to end through the API with host buffers ------------------------
     e2e = None
     if not args.no_e2e:
@@ -585,6 +616,12 @@ def gpu_arm(args) -> None:
                    "hbm_frac": gather_bytes / (mean["gather"] * 1e-3) / hbm_peak},
     }
 
+    if fp8 is not None:
+        kd = (hd + 31) // 32 * 32          # K padded to the f8f6f4 K-step
+        t_tensor8 = 2 * 2 * kd * E / (2 * bf16_peak)   # two passes; FP8 peak = 2 x bf16 (nominal ratio)
+        t_exp8 = 2 * E / ex2_peak
+        fp8["importance_roofline_frac"] = max(t_tensor8, t_exp8) / (fp8["importance_ms"] * 1e-3)
+
     cpu_baseline = None
     if cpu is not None and "error" not in cpu:
         cpu_baseline = {"value": cpu_rate(cpu), "unit": "tokens/s", "cores": 1, "kind": "oracle",
@@ -612,6 +649,7 @@ def gpu_arm(args) -> None:
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "lse_provided": lse_provided,
+        "fp8": fp8,
         "small_requests": small,
         "gpu_launches": 5 * args.steps,
         "clocks": clocks,

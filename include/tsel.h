@@ -79,6 +79,9 @@ typedef enum tsel_status {
 #define TSEL_IMP_LSE_PROVIDED 0x1u   /* lse is an INPUT (natural log [H, Tq], e.g. the softmax
                                         LSE FlashAttention returned): the row-LSE pass is
                                         replaced by importing it */
+#define TSEL_IMP_FP8_E4M3     0x2u   /* q and k hold FP8 E4M3 bytes (row strides in bytes);
+                                        fold their dequantisation scales into
+                                        softmax_scale ([LiteVLM] FP8 deployment) */
 #define TSEL_IMP_TEST_STALL   0x10000u /* test hook for failure detection: the pass kernels'
                                           scheduler publishes no work, every bounded wait
                                           runs out after ~50 ms and TSEL_DEV_TIMEOUT is set;
@@ -120,7 +123,11 @@ TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int tot
  * num_heads    H in [1, 256]; num_kv_heads divides it.
  * head_dim     64, 80, 96, 112 or 128 (else TSEL_ERR_UNSUPPORTED).
  * softmax_scale  <= 0 selects 1/sqrt(head_dim).
- * flags        0, TSEL_IMP_LSE_PROVIDED, and/or TSEL_IMP_STAGE_* bits.
+ * flags        0, TSEL_IMP_LSE_PROVIDED, TSEL_IMP_FP8_E4M3, and/or TSEL_IMP_STAGE_* bits.
+ *              With TSEL_IMP_FP8_E4M3, q and k are E4M3 [rows, heads, head_dim] (one byte
+ *              per element, row strides in bytes, multiples of 16) and softmax_scale is
+ *              the full factor applied to the fp8 dot products (scale x q_scale x
+ *              k_scale; must be > 0).
  * lse          fp32 [num_heads, total_q], natural log: an output (may be NULL), or
  *              with TSEL_IMP_LSE_PROVIDED an input that must not be NULL — the
  *              [VTC] section 3.2 design, which reuses the LSE the attention kernel

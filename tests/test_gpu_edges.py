@@ -314,3 +314,57 @@ def test_whole_path_captures_into_a_cuda_graph(tsel):
         for a, b in zip(ref, (scores, keep_idx, oh, oi, oc)):
             assert torch.equal(a, b)
     assert tsel.tsel_read_device_status(ws) == 0
+
+
+# ---------------------------------------------------------------- FP8 E4M3 inputs
+
+def _fp8_importance(tsel, w, **kw):
+    q = torch.from_numpy(w.q_bits).cuda()
+    k = torch.from_numpy(w.k_bits).cuda()
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
+                     dtype=torch.uint8, device="cuda")
+    s, lse = tsel.tsel_importance(q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), max(w.max_seqlen_q, 1),
+                                  max(w.max_seqlen_k, 1), softmax_scale=w.softmax_scale, workspace=ws,
+                                  **kw)
+    return s.cpu().numpy(), lse.cpu().numpy(), tsel.tsel_read_device_status(ws)
+
+
+@pytest.mark.parametrize("d", [64, 80, 96, 112, 128])
+def test_fp8_e4m3_head_dims(tsel, d):
+    L = [1, 127, 128, 129, 300]
+    w = W.to_e4m3(W.make_segments(L, L, 4, 2, d, seed=400 + d, sink_counts=[0, 1, 2, 3, 6],
+                                  hidden_dim=16))
+    s, lse, st = _fp8_importance(tsel, w)
+    assert st == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k,
+                                       w.softmax_scale, fmt="e4m3")
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("name", ["six_views_1536", "text_query_3072"])
+def test_fp8_e4m3_workloads(tsel, name):
+    w = W.to_e4m3(W.make(name))
+    s, lse, st = _fp8_importance(tsel, w)
+    assert st == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k,
+                                       w.softmax_scale, fmt="e4m3")
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
+    # LSE-provided works on FP8 inputs too
+    s2, _, st2 = _fp8_importance(tsel, w, flags=tsel.TSEL_IMP_LSE_PROVIDED,
+                                 lse=torch.from_numpy(lse_ref.astype(np.float32)).cuda())
+    assert st2 == 0 and max_rel_err(s2, s_ref) <= REL_TOL
+
+
+def test_fp8_thirty_images_sampled(tsel):
+    from gpu_util import segment_slice
+    w = W.to_e4m3(W.make("thirty_images"))
+    s, lse, st = _fp8_importance(tsel, w)
+    assert st == 0
+    lens = np.diff(w.cu_seqlens_k)
+    for g in sorted({int(np.argmin(lens)), int(np.argmax(lens)), 3}):
+        qb, kb, cq, ck, (q0, q1, k0, k1) = segment_slice(w, g)
+        lse_ref, s_ref = oracle.importance(qb, kb, cq, ck, w.softmax_scale, fmt="e4m3")
+        assert max_rel_err(s[k0:k1], s_ref) <= REL_TOL
+        np.testing.assert_allclose(lse[:, q0:q1], lse_ref, rtol=1e-5, atol=1e-4)

@@ -45,31 +45,26 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _e4m3_table() -> np.ndarray:
-    """Non-negative finite E4M3 values indexed by their code 0x00..0x7E."""
-    vals = np.empty(127, dtype=np.float64)
-    for code in range(127):
-        e, m = code >> 3, code & 7
-        vals[code] = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
-    return vals
-
-
-_E4M3 = _e4m3_table()
-
-
 def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
-    """Quantise to FP8 E4M3: nearest value, ties to the even code, magnitudes
-    above 448 saturate to 448 (no NaN is produced)."""
-    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), 448.0)
-    hi = np.searchsorted(_E4M3, a, side="left")          # first value >= a
-    hi = np.minimum(hi, 126)
-    lo = np.maximum(hi - 1, 0)
-    d_lo = a - _E4M3[lo]
-    d_hi = _E4M3[hi] - a
-    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
-    code = np.where(pick_hi, hi, lo).astype(np.uint8)
-    neg = np.signbit(np.asarray(x, dtype=np.float64)) & (code != 0)
-    return (code | np.where(neg, 0x80, 0).astype(np.uint8)).astype(np.uint8)
+    """Quantise to FP8 E4M3 (bias 7, 3 mantissa bits, subnormals below 2^-6):
+    nearest value, ties to the even code, magnitudes above 448 saturate to 448
+    (no NaN is produced)."""
+    f = np.asarray(x, dtype=np.float32)
+    a = np.minimum(np.abs(f), np.float32(448.0))
+    bits = a.view(np.int32)
+    exp = (bits >> 23) - 127 + 7                       # E4M3 exponent field if normal
+    mant = bits & 0x7FFFFF
+    # normal range: round the 23-bit mantissa to 3 bits, ties to even
+    m = (mant + 0x7FFFF + ((mant >> 20) & 1)) >> 20
+    exp = exp + (m >> 3)                               # mantissa overflow carries
+    m = m & 7
+    code_n = (exp << 3) | m
+    # subnormal range |x| < 2^-6: multiples of 2^-9, round half to even
+    code_s = np.rint(a * np.float32(512.0)).astype(np.int32)   # exact scaling by 2^9
+    code = np.where(exp >= 1, code_n, code_s)
+    code = np.minimum(code, 0x7E)
+    neg = np.signbit(f) & (code != 0)
+    return (code | np.where(neg, 0x80, 0)).astype(np.uint8)
 
 
 @dataclass
@@ -219,17 +214,28 @@ def keep_floor(n: int, permille: int) -> int:
     return (int(n) * int(permille)) // 1000
 
 
+def _quantise_tensor_e4m3(bits: np.ndarray, chunk: int = 1 << 23):
+    """bf16 tensor -> (E4M3 bits, scale) with amax mapped to 448, in chunks."""
+    flat = bits.reshape(-1)
+    amax = 0.0
+    for i in range(0, flat.size, chunk):
+        amax = max(amax, float(np.abs(bf16_bits_to_f32(flat[i:i + chunk])).max(initial=0.0)))
+    scale = max(amax, 1e-30) / 448.0
+    inv = np.float32(1.0 / scale)
+    out = np.empty(flat.size, dtype=np.uint8)
+    for i in range(0, flat.size, chunk):
+        out[i:i + chunk] = f32_to_e4m3_bits(bf16_bits_to_f32(flat[i:i + chunk]) * inv)
+    return out.reshape(bits.shape), scale
+
+
 def to_e4m3(w: "Workload") -> "Workload":
     """The same problem with Q and K quantised to FP8 E4M3 with one scale per
     tensor (amax maps to 448); the scales are folded into softmax_scale."""
-    q = bf16_bits_to_f32(w.q_bits).astype(np.float64)
-    k = bf16_bits_to_f32(w.k_bits).astype(np.float64)
-    sq = max(float(np.abs(q).max(initial=0.0)), 1e-30) / 448.0
-    sk = max(float(np.abs(k).max(initial=0.0)), 1e-30) / 448.0
+    qb, sq = _quantise_tensor_e4m3(w.q_bits)
+    kb, sk = _quantise_tensor_e4m3(w.k_bits)
     meta = dict(w.meta)
     meta.update(fmt="e4m3", q_scale=sq, k_scale=sk)
-    return Workload(name=w.name + "_e4m3", q_bits=f32_to_e4m3_bits(q / sq),
-                    k_bits=f32_to_e4m3_bits(k / sk), cu_seqlens_q=w.cu_seqlens_q,
+    return Workload(name=w.name + "_e4m3", q_bits=qb, k_bits=kb, cu_seqlens_q=w.cu_seqlens_q,
                     cu_seqlens_k=w.cu_seqlens_k, req_tok_offsets=w.req_tok_offsets,
                     keep_per_req=w.keep_per_req, hidden_bits=w.hidden_bits, pos=w.pos,
                     softmax_scale=w.softmax_scale * sq * sk, meta=meta)
