@@ -13,11 +13,14 @@
 //          in TMEM), each 128-key B tile multiplied by both A tiles, online
 //          max/sum per query row -> row LSE (kept as -LSE*log2 e, padded to
 //          128-row tiles per segment).
-//   pass 2 units (segment, 256 keys), all heads: S^T = K Q^T with the keys
-//          on the MMA M dimension, so each epilogue thread owns one key and
-//          sums exp2(S*c - LSE2) over the query columns in registers: the
-//          column reduction needs no shuffles and no atomics, and the result
-//          is deterministic.
+//   pass 2 units (segment, 256 keys, group of query heads): S^T = K Q^T with
+//          the keys on the MMA M dimension, so each epilogue thread owns one
+//          key and sums exp2(S*c - LSE2) over the query columns in registers:
+//          the column reduction needs no shuffles. When the heads are split
+//          into groups (so that small requests still fill every SM), each
+//          group stores its partial sums and the last group to finish a
+//          32-key slice adds them up in group order: the result stays
+//          deterministic.
 // Two A tiles per unit halve the operand bytes each B tile costs per element
 // (the shared-memory feed, not the tensor cores, limited 128-row units).
 //
@@ -146,12 +149,15 @@ __device__ void bucket_positions_desc(int* key, int G, int* hist, int* warp_sums
 __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restrict__ cu_q,
                                                         const int32_t* __restrict__ cu_k, int G,
                                                         int Tq, int Tk, int max_q, int max_k,
-                                                        int H, uint8_t* ws, ImpWsLayout L) {
+                                                        int H, int HG, uint8_t* ws,
+                                                        ImpWsLayout L) {
   __shared__ int bad;
   __shared__ int hist[1024];
   __shared__ int warp_sums[32];
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   int32_t* qtile_off = reinterpret_cast<int32_t*>(ws + L.qtile_off);
+  int32_t* kpair_off = reinterpret_cast<int32_t*>(ws + L.kpair_off);
+  int32_t* grp_ctr = reinterpret_cast<int32_t*>(ws + L.grp_ctr);
   int32_t* pos1 = reinterpret_cast<int32_t*>(ws + L.scratch);
   int32_t* pos2 = pos1 + G;
   int32_t* inv1 = pos2 + G;
@@ -188,7 +194,9 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
     pos1[g] = min(nkt, 1023);
     pos2[g] = min(nqt, 1023);
     qtile_off[g] = nqt;
+    kpair_off[g] = int(ceil_div(cu_k[g + 1] - cu_k[g], kPair));
   }
+  for (int64_t i = threadIdx.x; i < L.n_grp; i += 1024) grp_ctr[i] = 0;
   __syncthreads();
   bucket_positions_desc(pos1, G, hist, warp_sums);
   bucket_positions_desc(pos2, G, hist, warp_sums);
@@ -198,13 +206,17 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
     inv1[pos1[g]] = g;
     inv2[pos2[g]] = g;
     start1[pos1[g]] = H * nqp;
-    start2[pos2[g]] = nkp;
+    start2[pos2[g]] = HG * nkp;
   }
   __syncthreads();
   const int total1 = block_scan_array(start1, G, warp_sums);
   const int total2 = block_scan_array(start2, G, warp_sums);
   const int total_qt = block_scan_array(qtile_off, G, warp_sums);
-  if (threadIdx.x == 0) qtile_off[G] = total_qt;
+  const int total_kp = block_scan_array(kpair_off, G, warp_sums);
+  if (threadIdx.x == 0) {
+    qtile_off[G] = total_qt;
+    kpair_off[G] = total_kp;
+  }
   // Unit lists in descending-cost segment order.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = warp; i < G; i += 32) {
@@ -219,7 +231,12 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
     const int g2 = inv2[i];
     const int nkp = int(ceil_div(cu_k[g2 + 1] - cu_k[g2], kPair));
     const int s2 = start2[i];
-    for (int j = lane; j < nkp; j += 32) units2[s2 + j] = make_uint2(uint32_t(g2), uint32_t(j));
+    // The head groups of one key pair are adjacent, so the last one to finish
+    // (which adds up the partial sums) follows the others closely.
+    for (int j = lane; j < HG * nkp; j += 32) {
+      const int kp = j / HG, hg = j - kp * HG;
+      units2[s2 + j] = make_uint2(uint32_t(g2), (uint32_t(hg) << 24) | uint32_t(kp));
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -236,6 +253,8 @@ struct Unit {
   int g, h, pair, q0, nq, k0, nk;
   int nA;          // valid 128-row A tiles in this unit's 256-row pair (1 or 2)
   int qtile_base;  // first 128-row tile of the segment in the padded LSE rows
+  int h1;          // pass 2: query heads [h, h1) (pass 1: h + 1)
+  int hg;          // pass 2: head group of the unit
   int valid;       // 1 for a unit, 0 for the end-of-work marker
 };
 
@@ -245,12 +264,16 @@ template <int PASS>
 __device__ __forceinline__ Unit decode_unit(const ImpPassParams& p, uint2 u) {
   Unit r;
   r.g = int(u.x);
+  r.pair = int(u.y & 0xFFFFFFu);
   if (PASS == 1) {
     r.h = int(u.y >> 24);
-    r.pair = int(u.y & 0xFFFFFFu);
+    r.h1 = r.h + 1;
+    r.hg = 0;
   } else {
-    r.h = 0;
-    r.pair = int(u.y);
+    r.hg = int(u.y >> 24);
+    const int per = p.H / p.hgroups;
+    r.h = r.hg * per;
+    r.h1 = r.h + per;
   }
   r.q0 = __ldg(p.cu_q + r.g);
   r.nq = __ldg(p.cu_q + r.g + 1) - r.q0;
@@ -498,9 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!w.valid) break;
         const int n_b = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
         if (n_b == 0) continue;
-        const int n_agroups = PASS == 1 ? 1 : p.Hkv;
+        // pass 2: one A tile pair per kv head the unit's query heads read
+        const int ag0 = PASS == 1 ? 0 : w.h / group;
+        const int ag1 = PASS == 1 ? 1 : (w.h1 - 1) / group + 1;
         const int qtile_base = w.qtile_base;
-        for (int ag = 0; ag < n_agroups && ok; ++ag) {
+        for (int ag = ag0; ag < ag1 && ok; ++ag) {
           const int as = a_it & 1;
           if (!wait_bounded(&a_empty[as], ((a_it >> 1) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
           mbar_arrive_expect_tx(&a_full[as], uint32_t(w.nA * C::TILE_BYTES));
@@ -510,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_tile<D, FP8>(sA + (as * 2 + a) * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as],
                               ahead, ay + a * kTile);
           ++a_it;
-          const int n_heads = PASS == 1 ? 1 : group;
-          for (int hh = 0; hh < n_heads && ok; ++hh) {
-            const int h = PASS == 1 ? w.h : ag * group + hh;
+          const int hb0 = PASS == 1 ? w.h : max(w.h, ag * group);
+          const int hb1 = PASS == 1 ? w.h + 1 : min(w.h1, (ag + 1) * group);
+          for (int h = hb0; h < hb1 && ok; ++h) {
             const int bhead = PASS == 1 ? w.h / group : h;
             const int nbt = PASS == 1 ? n_b : int(ceil_div(w.nq, kTile));
             for (int bt = 0; bt < nbt; ++bt) {
@@ -572,12 +597,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!w.valid) break;
         const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
         if (nbt == 0) continue;
-        const int n_agroups = PASS == 1 ? 1 : p.Hkv;
-        const int n_b = PASS == 1 ? nbt : group * nbt;
-        for (int ag = 0; ag < n_agroups && ok; ++ag) {
+        const int ag0 = PASS == 1 ? 0 : w.h / group;
+        const int ag1 = PASS == 1 ? 1 : (w.h1 - 1) / group + 1;
+        for (int ag = ag0; ag < ag1 && ok; ++ag) {
           const int as = a_it & 1;
           if (!wait_bounded(&a_full[as], (a_it >> 1) & 1, abort_flag, T)) { ok = false; break; }
           tc_fence_after();
+          const int n_b = PASS == 1
+                              ? nbt
+                              : (min(w.h1, (ag + 1) * group) - max(w.h, ag * group)) * nbt;
           for (int bi = 0; bi < n_b; ++bi) {
             const int bs = b_it % S;
             if (!wait_bounded(&b_full[bs], (b_it / S) & 1, abort_flag, T)) { ok = false; break; }
@@ -631,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!w.valid) break;
       const bool mine = a_half < w.nA;   // this warpgroup's A tile holds rows of the unit
       const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
-      const int n_b = PASS == 1 ? nbt : (nbt > 0 ? p.H * nbt : 0);
+      const int n_b = PASS == 1 ? nbt : (nbt > 0 ? (w.h1 - w.h) * nbt : 0);
       float m = kNegInf, l = 0.f;           // pass 1
       float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // pass 1: sum since m; pass 2: per-key sum
       for (int bi = 0; bi < n_b; ++bi, ++b_it) {
@@ -716,9 +744,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               p.lse_out[int64_t(w.h) * p.Tq + w.q0 + qrow] = lse2 * 0.69314718055994531f;
           } else {
             const int krow = w.pair * kPair + a_half * kTile + row;
-            if (krow < w.nk) {
-              const float total = part + o0;
-              p.scores[w.k0 + krow] = w.nq > 0 ? total / float(p.H * w.nq) : 0.f;
+            const float total = part + o0;
+            const float rows = float(p.H * w.nq);
+            if (p.hgroups == 1) {
+              if (krow < w.nk) p.scores[w.k0 + krow] = w.nq > 0 ? total / rows : 0.f;
+            } else {
+              // Partial sums of this head group; the last group of the 32-key
+              // slice adds all groups' partials in group order.
+              if (krow < w.nk) p.part[int64_t(w.hg) * p.Tk + w.k0 + krow] = total;
+              __threadfence();
+              __syncwarp();
+              int old = 0;
+              if (lane == 0) {
+                const int slice = (__ldg(p.kpair_off + w.g) + w.pair) * 8 + a_half * 4 + quad;
+                old = atomicAdd(p.grp_ctr + slice, 1);
+                if (old == p.hgroups - 1) p.grp_ctr[slice] = 0;   // no other arrival follows
+              }
+              old = __shfl_sync(0xffffffffu, old, 0);
+              if (old == p.hgroups - 1) {
+                __threadfence();
+                if (krow < w.nk) {
+                  float sum = 0.f;
+                  for (int gi = 0; gi < p.hgroups; ++gi)
+                    sum += __ldcg(p.part + int64_t(gi) * p.Tk + w.k0 + krow);
+                  p.scores[w.k0 + krow] = w.nq > 0 ? sum / rows : 0.f;
+                }
+              }
             }
           }
         }
@@ -775,9 +826,9 @@ __global__ void __launch_bounds__(kTile) imp_lse_import_kernel(
 // ---------------------------------------------------------------------------
 
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
-                            int max_q, int max_k, int H, uint8_t* ws, const ImpWsLayout& L,
-                            cudaStream_t stream) {
-  imp_prep_kernel<<<1, 1024, 0, stream>>>(cu_q, cu_k, G, Tq, Tk, max_q, max_k, H, ws, L);
+                            int max_q, int max_k, int H, int HG, uint8_t* ws,
+                            const ImpWsLayout& L, cudaStream_t stream) {
+  imp_prep_kernel<<<1, 1024, 0, stream>>>(cu_q, cu_k, G, Tq, Tk, max_q, max_k, H, HG, ws, L);
   return cudaPeekAtLastError();
 }
 

@@ -16,8 +16,8 @@
 
 namespace tsel {
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
-                            int max_q, int max_k, int H, uint8_t* ws, const ImpWsLayout& L,
-                            cudaStream_t stream);
+                            int max_q, int max_k, int H, int HG, uint8_t* ws,
+                            const ImpWsLayout& L, cudaStream_t stream);
 cudaError_t launch_imp_pass(int pass, int head_dim, bool fp8, const CUtensorMap* maps,
                             const ImpPassParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
@@ -86,6 +86,17 @@ int sm_count(int* out) {
   if (dev >= 0 && dev < 128) cache[dev] = n;
   *out = n;
   return 0;
+}
+
+// Query-head groups per pass-2 key pair: the smallest power of two (dividing
+// the head count, at most kMaxHeadGroups) that gives every SM about four
+// units, so the last units of the pass do not leave most SMs idle. A pure
+// function of the sizes: the stages of one call agree on it.
+int pass2_head_groups(int H, int G, int Tk, int sms) {
+  const int64_t pairs = ceil_div(Tk, kPairRows) + (G > 0 ? G / 2 : 0);
+  int hg = 1;
+  while (2 * hg <= kMaxHeadGroups && H % (2 * hg) == 0 && pairs * hg < 4 * int64_t(sms)) hg *= 2;
+  return hg;
 }
 
 // 2-D bf16 tensor map over `rows` rows of `width` elements (row stride in
@@ -218,10 +229,13 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   cudaError_t e;
+  int sms = 0;
+  if (sm_count(&sms) != 0) return fail(TSEL_ERR_CUDA, "cannot query the SM count");
+  const int hgroups = pass2_head_groups(num_heads, num_seg, total_k, sms);
 
   if (stages & TSEL_IMP_STAGE_PREP) {
     e = launch_imp_prep(cu_seqlens_q, cu_seqlens_k, num_seg, total_q, total_k, max_seqlen_q,
-                        max_seqlen_k, num_heads, ws, L, stream);
+                        max_seqlen_k, num_heads, hgroups, ws, L, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prep launch");
   }
   if (total_k == 0 || num_seg == 0) return TSEL_OK;
@@ -254,9 +268,6 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     qm16 = qm64;
     km16 = km64;
   }
-  int sms = 0;
-  if (sm_count(&sms) != 0) return fail(TSEL_ERR_CUDA, "cannot query the SM count");
-
   ImpPassParams p{};
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
@@ -297,6 +308,11 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     p2.units = reinterpret_cast<const uint2*>(ws + L.units2);
     p2.num_units = &hdr->num_units[1];
     p2.sched_ctr = &hdr->sched_ctr[1];
+    p2.hgroups = hgroups;
+    p2.Tk = total_k;
+    p2.kpair_off = reinterpret_cast<const int32_t*>(ws + L.kpair_off);
+    p2.grp_ctr = reinterpret_cast<int32_t*>(ws + L.grp_ctr);
+    p2.part = reinterpret_cast<float*>(ws + L.part);
     const int grid = int(L.u2_max < sms ? L.u2_max : sms);
     e = launch_imp_pass(2, head_dim, fp8, maps, p2, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pass-2 launch");

@@ -89,7 +89,9 @@ typedef enum tsel_status {
                                           usable. Scores are not written. */
 #define TSEL_IMP_STAGE_PREP   0x100u /* run only the listed stages (none listed = all): */
 #define TSEL_IMP_STAGE_PASS1  0x200u /*   schedule/validation, row-LSE pass, column pass. */
-#define TSEL_IMP_STAGE_PASS2  0x400u /*   Stages must run in order on one stream/workspace. */
+#define TSEL_IMP_STAGE_PASS2  0x400u /*   Stages run in order on one stream/workspace; each
+                                          pass needs a schedule stage after the previous
+                                          run of that pass (it resets the pass's counters). */
 
 /* ------------------------------------------------------------------------ */
 /* Importance scores                                                        */

@@ -36,7 +36,7 @@ def _importance(tsel, w, **kw):
 
 
 @pytest.mark.parametrize("d", [64, 80, 96, 112, 128])
-@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (8, 2)])
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (4, 2), (8, 2), (3, 1), (6, 3), (12, 4)])
 def test_head_dims_and_gqa(tsel, d, H, Hkv):
     L = [1, 127, 128, 129, 257]
     w = W.make_segments(L, L, H, Hkv, d, seed=200 + d + H, sink_counts=[0, 1, 2, 3, 4], hidden_dim=64)
@@ -45,6 +45,30 @@ def test_head_dims_and_gqa(tsel, d, H, Hkv):
     lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
     assert max_rel_err(s, s_ref) <= REL_TOL
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
+
+
+def test_column_pass_rerun_is_bit_for_bit(tsel):
+    # The column pass splits the query heads into groups whose partial sums
+    # the last group of each 32-key slice adds up in group order: reruns of
+    # the schedule + column pass on the stored LSE give the same bits.
+    w = W.make_segments([700, 40, 300], [513, 1, 260], 8, 2, 64, seed=303, sink_counts=[5, 0, 2],
+                        hidden_dim=64)
+    q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
+                     dtype=torch.uint8, device="cuda")
+    args = (q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), w.max_seqlen_q, w.max_seqlen_k)
+    s_all, _ = tsel.tsel_importance(*args, workspace=ws)
+    s_all = s_all.clone()
+    runs = []
+    for _ in range(3):
+        s, _ = tsel.tsel_importance(*args, workspace=ws, want_lse=False,
+                                    flags=tsel.TSEL_IMP_STAGE_PREP | tsel.TSEL_IMP_STAGE_PASS2)
+        runs.append(s.clone())
+    assert tsel.tsel_read_device_status(ws) == 0
+    for s in runs:
+        assert torch.equal(s, s_all)
+    _, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s_all.cpu().numpy(), s_ref) <= REL_TOL
 
 
 def test_long_segment_4096_and_cross_lengths(tsel):
