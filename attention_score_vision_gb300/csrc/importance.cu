@@ -36,6 +36,9 @@
 //               while the current one is computed. The math is packed (f32x2
 //               FMA/ADD, 3-input max), one MUFU exp2 per element. The two
 //               warpgroups of an A tile merge their partials once per unit.
+// The issue slots, not only the MUFU, bound the epilogue: each warp walks its
+// own parity's tiles directly, full tiles run without column masks, waits
+// sleep on the barrier instead of spinning, and arrivals are predicated.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -359,14 +362,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
 // more than 8 (terms stay below 2^8), so rescaling is rare. Packed float2
 // arithmetic (one f32x2 FMA / ADD per two columns) around one MUFU exp2 per
 // column.
+template <bool FULL>
 __device__ __forceinline__ void row_softmax_chunk(const uint32_t (&r)[32], int valid, float c,
                                                   float2 c2, float& m, float& l,
                                                   float2 (&a)[2]) {
-  if (valid <= 0) return;
+  if (!FULL && valid <= 0) return;
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  if (valid < 32) {
+  if (!FULL && valid < 32) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = j < valid ? v[j] : kNegInf;
   }
@@ -411,6 +415,36 @@ __device__ __forceinline__ void column_sum_chunk(const uint32_t (&r)[32], const 
     acc[0] = __fadd2_rn(acc[0], make_float2(ex2(x01.x), ex2(x01.y)));
     acc[1] = __fadd2_rn(acc[1], make_float2(ex2(x23.x), ex2(x23.y)));
   }
+}
+
+
+// One 128-column accumulator: two 32-column pieces in flight; the
+// accumulator is handed back to the MMA once all of it is in registers.
+// FULL: all 128 columns lie inside the segment (no masking).
+template <int PASS, bool FULL>
+__device__ __forceinline__ void epilogue_tile(uint32_t taddr, int valid, const float4* nl,
+                                              float c, float2 c2, float& m, float& l,
+                                              float2 (&acc)[2], uint64_t* acc_empty, int lane) {
+  uint32_t r0[32], r1[32];
+  tmem_ld32_async(taddr, r0);
+  tmem_ld32_async(taddr + 32, r1);
+  tmem_wait_ld(r0);
+  tmem_wait_ld(r1);
+  if (PASS == 1) row_softmax_chunk<FULL>(r0, valid, c, c2, m, l, acc);
+  else if (FULL || valid > 0) column_sum_chunk(r0, nl, c2, acc);
+  tmem_ld32_async(taddr + 64, r0);
+  if (PASS == 1) row_softmax_chunk<FULL>(r1, valid - 32, c, c2, m, l, acc);
+  else if (FULL || valid > 32) column_sum_chunk(r1, nl + 8, c2, acc);
+  tmem_ld32_async(taddr + 96, r1);
+  tmem_wait_ld(r0);
+  tmem_wait_ld(r1);
+  tc_fence_before();
+  __syncwarp();
+  mbar_arrive_lane0(acc_empty, lane);
+  if (PASS == 1) row_softmax_chunk<FULL>(r0, valid - 64, c, c2, m, l, acc);
+  else if (FULL || valid > 64) column_sum_chunk(r0, nl + 16, c2, acc);
+  if (PASS == 1) row_softmax_chunk<FULL>(r1, valid - 96, c, c2, m, l, acc);
+  else if (FULL || valid > 96) column_sum_chunk(r1, nl + 24, c2, acc);
 }
 
 template <int PASS, int D, bool FP8>
@@ -662,53 +696,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_b = PASS == 1 ? nbt : (nbt > 0 ? (w.h1 - w.h) * nbt : 0);
       float m = kNegInf, l = 0.f;           // pass 1
       float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // pass 1: sum since m; pass 2: per-key sum
-      for (int bi = 0; bi < n_b; ++bi, ++b_it) {
-        if ((b_it & 1) != par) continue;
-        const uint32_t use = uint32_t(b_it >> 1) & 1u;
+      // This warpgroup's tiles: global B-tile indices of parity `par`; bt is
+      // the tile's column block within its head.
+      const int b_end = b_it + n_b;
+      int g = b_it + ((par ^ b_it) & 1);
+      int bt = g - b_it;
+      if (bt >= nbt) bt -= nbt;
+      for (; g < b_end; g += 2) {
+        const uint32_t use = uint32_t(g >> 1) & 1u;
         if (!warp_wait(&acc_full[kbuf], use, abort_flag, T)) { ok = false; break; }
-        const int ls = b_it % kLseSlots;
-        if (PASS == 2 && !warp_wait(&lse_full[ls], (b_it / kLseSlots) & 1, abort_flag, T)) {
+        const int ls = g & (kLseSlots - 1);
+        if (PASS == 2 && !warp_wait(&lse_full[ls], (g / kLseSlots) & 1, abort_flag, T)) {
           ok = false;
           break;
         }
         tc_fence_after();
         if (mine) {
-          const int col0 = (bi % nbt) * kTile;
-          const int valid = (PASS == 1 ? w.nk : w.nq) - col0;
+          const int valid = (PASS == 1 ? w.nk : w.nq) - bt * kTile;
           const float4* nl = reinterpret_cast<const float4*>(sLse + ls * kTile);
-          // Two 32-column pieces in flight: the accumulator is fully read,
-          // and handed back to the MMA, once half of the tile is computed.
-          uint32_t r0[32], r1[32];
-          tmem_ld32_async(taddr, r0);
-          tmem_ld32_async(taddr + 32, r1);
-          tmem_wait_ld(r0);
-          tmem_wait_ld(r1);
-          if (PASS == 1) row_softmax_chunk(r0, valid, c, c2, m, l, acc);
-          else if (valid > 0) column_sum_chunk(r0, nl, c2, acc);
-          tmem_ld32_async(taddr + 64, r0);
-          if (PASS == 1) row_softmax_chunk(r1, valid - 32, c, c2, m, l, acc);
-          else if (valid > 32) column_sum_chunk(r1, nl + 8, c2, acc);
-          tmem_ld32_async(taddr + 96, r1);
-          tmem_wait_ld(r0);
-          tmem_wait_ld(r1);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[kbuf]);
-          if (PASS == 1) row_softmax_chunk(r0, valid - 64, c, c2, m, l, acc);
-          else if (valid > 64) column_sum_chunk(r0, nl + 16, c2, acc);
-          if (PASS == 1) row_softmax_chunk(r1, valid - 96, c, c2, m, l, acc);
-          else if (valid > 96) column_sum_chunk(r1, nl + 24, c2, acc);
+          if (valid >= kTile)
+            epilogue_tile<PASS, true>(taddr, valid, nl, c, c2, m, l, acc, &acc_empty[kbuf], lane);
+          else
+            epilogue_tile<PASS, false>(taddr, valid, nl, c, c2, m, l, acc, &acc_empty[kbuf], lane);
         } else {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[kbuf]);
+          mbar_arrive_lane0(&acc_empty[kbuf], lane);
         }
         if (PASS == 2) {
           __syncwarp();
-          if (lane == 0) mbar_arrive(&lse_empty[ls]);
+          mbar_arrive_lane0(&lse_empty[ls], lane);
         }
+        bt += 2;
+        if (bt >= nbt) bt -= nbt;
+        if (bt >= nbt) bt -= nbt;
       }
       if (!ok) break;
+      b_it = b_end;
       // Merge the two warpgroups of the same A half (B-tile parities 0 and 1).
       const int cb = unit_it & 1;
       const uint32_t cpar = (unit_it >> 1) & 1;

@@ -34,6 +34,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
+// Arrives on `bar` from lane 0 of the warp (predicated, no branch).
+__device__ __forceinline__ void mbar_arrive_lane0(uint64_t* bar, int lane) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 st;\n\t"
+      "setp.eq.s32 p, %1, 0;\n\t"
+      "@p mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar)), "r"(lane)
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"
@@ -42,16 +51,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
-// One bounded test of the phase (the hardware may suspend the thread for a
-// short, system-defined time while it waits).
+// Suspend-time hint of one try_wait: the thread sleeps until the phase
+// completes or this many nanoseconds pass, instead of spinning (a spinning
+// waiter takes issue slots from the warps that compute on the same SMSP).
+constexpr uint32_t kTryWaitSuspendNs = 20000;
+
+// One bounded test of the phase.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -69,12 +82,10 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
                                              uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > timeout_ns) return false;
-    }
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 
