@@ -37,11 +37,21 @@ notes):
 * Compaction copies rows and position ids of the kept tokens in ascending
   order; the image id of a token is the segment holding it; the new per-image
   boundaries are prefix sums of kept counts.
+* Score normalisation: "mean" (the default above) or "sum" (the same total
+  attention received, not divided by H * Nq_g).
+* Dynamic keep ratio (the article's section 6.2 leaves the rule open): per
+  request, the fewest top tokens whose scores hold a fraction tau of the
+  request's total score, bounded by a floor and a ceiling ratio. Scores enter
+  as integers q_j = floor(s_j * 2^(24 - E)), E the binary exponent with
+  max_j s_j in [2^(E-1), 2^E), so the sums are exact and independent of the
+  summation order.
 
 Parity status: every function here is pinned by closed forms, invariants and
 brute force in tests/test_oracle_pins.py.
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -105,16 +115,20 @@ def attention_probabilities(q: np.ndarray, k: np.ndarray, scale: float):
     return p, lse
 
 
-def importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale=None, fmt="bf16"):
+def importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale=None, fmt="bf16",
+               norm="mean"):
     """Mean attention probability received by every key token.
 
     q_bits: [Tq, H, d] and k_bits: [Tk, Hkv, d] as bit patterns of `fmt`
     ("bf16": uint16, "e4m3": uint8). cu_seqlens_q / cu_seqlens_k: int [G+1];
     segment g attends queries [cu_q[g], cu_q[g+1]) to keys [cu_k[g], cu_k[g+1]).
     softmax_scale multiplies q.k (defaults to 1/sqrt(d)); for quantised inputs
-    it carries the dequantisation scales too.
+    it carries the dequantisation scales too. norm="sum" returns the total
+    attention received (sum over heads and query rows) instead of the mean.
     Returns (lse [H, Tq] fp64 natural log, scores [Tk] fp64).
     """
+    if norm not in ("mean", "sum"):
+        raise ValueError(f"unknown normalisation {norm}")
     q = decode_inputs(q_bits, fmt)
     k = decode_inputs(k_bits, fmt)
     tq, H, d = q.shape
@@ -134,7 +148,10 @@ def importance(q_bits, k_bits, cu_seqlens_q, cu_seqlens_k, softmax_scale=None, f
             lse[h, q0:q1] = lse_h
             acc += p.sum(axis=0)          # attention received = column sum
         n_rows = H * (q1 - q0)
-        scores[k0:k1] = acc / n_rows if n_rows > 0 else 0.0
+        if norm == "sum":
+            scores[k0:k1] = acc
+        else:
+            scores[k0:k1] = acc / n_rows if n_rows > 0 else 0.0
     return lse, scores
 
 
@@ -169,6 +186,51 @@ def select_topk(scores, req_tok_offsets, keep_per_req):
         cu.append(cu[-1] + chosen.shape[0])
     keep_idx = np.concatenate(out) if out else np.zeros(0, np.int64)
     return keep_idx.astype(np.int32), np.asarray(cu, dtype=np.int32)
+
+
+def score_quanta(scores) -> list:
+    """Integer score quanta of one request: q_j = floor(s_j * 2^(24 - E)) with
+    max_j s_j in [2^(E-1), 2^E); all zero when every score is 0. Exact: the
+    scaling is by a power of two and the floor is taken in fp64 on fp32 inputs.
+    Scores must be finite and >= 0."""
+    s = np.asarray(scores, dtype=np.float64)
+    if s.size == 0:
+        return []
+    smax = float(s.max())
+    if smax <= 0.0:
+        return [0] * s.size
+    _, e = math.frexp(smax)          # smax = m * 2^e, m in [0.5, 1)
+    return [int(math.floor(math.ldexp(float(v), 24 - e))) for v in s]
+
+
+def dynamic_budget(scores, req_tok_offsets, mass_permille, min_permille, max_permille):
+    """Per request: the fewest tokens, taken in top-B order (score descending,
+    index ascending), whose quanta sum to at least T = ceil(tau * M) with
+    tau = mass_permille / 1000 and M the request's total quanta; then bounded
+    to [floor(n * min_permille / 1000), floor(n * max_permille / 1000)].
+    Returns int32 [R]."""
+    scores = np.asarray(scores)
+    off = np.asarray(req_tok_offsets, dtype=np.int64)
+    out = []
+    for r in range(off.shape[0] - 1):
+        lo, hi = int(off[r]), int(off[r + 1])
+        n = hi - lo
+        q = score_quanta(scores[lo:hi])
+        M = sum(q)
+        T = (M * int(mass_permille) + 999) // 1000
+        b = 0
+        if T > 0:
+            idx = np.arange(lo, hi)
+            order = np.lexsort((idx, -scores[lo:hi].astype(np.float64)))
+            acc = 0
+            for b, j in enumerate(order, start=1):
+                acc += q[j]
+                if acc >= T:
+                    break
+        floor_b = (n * int(min_permille)) // 1000
+        ceil_b = (n * int(max_permille)) // 1000
+        out.append(min(max(b, floor_b), ceil_b))
+    return np.asarray(out, dtype=np.int32)
 
 
 # ---------------------------------------------------------------------------

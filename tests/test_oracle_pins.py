@@ -356,3 +356,102 @@ def test_importance_with_e4m3_inputs_one_hot_closed_form():
     assert abs(scores[7] - c / (c + nk - 1)) < 1e-13
     assert abs(scores[0] - 1 / (c + nk - 1)) < 1e-13
     np.testing.assert_allclose(lse, math.log(c + nk - 1), rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# SUM normalisation
+# ---------------------------------------------------------------------------
+
+def test_sum_normalisation_totals_heads_times_query_rows():
+    """Total attention received: a segment's sums add up to H * Nq_g (each of
+    its H * Nq_g query rows spreads probability 1), and a segment without
+    query rows gets 0."""
+    rng = np.random.default_rng(41)
+    lq, lk, H, Hkv = [20, 0, 7], [33, 5, 64], 4, 2
+    qb, kb, cu_q, cu_k = _rand_case(rng, lq, lk, H, Hkv, 32, std=2.0)
+    _, s_sum = oracle.importance(qb, kb, cu_q, cu_k, norm="sum")
+    for g in range(3):
+        seg = s_sum[cu_k[g]:cu_k[g + 1]]
+        assert abs(seg.sum() - H * lq[g]) < 1e-9 * max(1, H * lq[g])
+    assert np.all(s_sum[cu_k[1]:cu_k[2]] == 0)
+    # one-hot closed form in sum mode: the hot key collects c/(c+Nk-1) per row
+    nq, nk, d, alpha = 6, 9, 16, 3.0
+    q = np.zeros((nq, 1, d), np.float32)
+    q[:, 0, 0] = alpha
+    k = np.zeros((nk, 1, d), np.float32)
+    k[4, 0, 0] = alpha
+    _, s = oracle.importance(_bits(q), _bits(k), [0, nq], [0, nk], norm="sum")
+    c = math.exp(alpha * alpha / math.sqrt(d))
+    assert s[4] == pytest.approx(nq * c / (c + nk - 1), rel=1e-12)
+    assert s[0] == pytest.approx(nq / (c + nk - 1), rel=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Dynamic keep ratio (mass budget)
+# ---------------------------------------------------------------------------
+
+def test_score_quanta_closed_forms():
+    # max 1.0 lies in [2^0, 2^1): E = 1, quanta = s * 2^23
+    assert oracle.score_quanta([1.0, 0.5, 0.25, 0.0]) == [1 << 23, 1 << 22, 1 << 21, 0]
+    # max 0.75 lies in [2^-1, 2^0): E = 0, quanta = floor(s * 2^24)
+    assert oracle.score_quanta([0.75, 1e-9, 0.3]) == [12582912, 0, int(math.floor(0.3 * 2 ** 24))]
+    assert oracle.score_quanta([0.0, 0.0]) == [0, 0]
+    assert oracle.score_quanta([]) == []
+    # quanta never reach 2^24 and the largest is at least 2^23
+    q = oracle.score_quanta(np.random.default_rng(5).random(1000).astype(np.float32))
+    assert max(q) < 1 << 24 and max(q) >= 1 << 23
+
+
+def _budget_brute(s, tau):
+    """Smallest B whose top-B quanta reach ceil(tau * M / 1000), by trying every B."""
+    q = oracle.score_quanta(s)
+    M = sum(q)
+    T = -(-M * tau // 1000)
+    order = sorted(range(len(s)), key=lambda j: (-float(s[j]), j))
+    for b in range(len(s) + 1):
+        if sum(q[j] for j in order[:b]) >= T:
+            return b
+    raise AssertionError("unreachable")
+
+
+def test_dynamic_budget_brute_force_small_inputs():
+    vals = [0.0, 0.25, 0.5, 1.0]
+    for n in range(0, 5):
+        for combo in itertools.product(vals, repeat=n):
+            s = np.asarray(combo, dtype=np.float32)
+            for tau in (0, 1, 333, 500, 900, 1000):
+                got = oracle.dynamic_budget(s, [0, n], tau, 0, 1000)
+                assert got.tolist() == [_budget_brute(s, tau)], (combo, tau)
+
+
+def test_dynamic_budget_closed_forms_and_bounds():
+    # uniform scores: B = ceil(n * tau / 1000)
+    for n, tau in [(7, 500), (1000, 900), (13, 1), (64, 1000)]:
+        s = np.full(n, 0.01, np.float32)
+        assert oracle.dynamic_budget(s, [0, n], tau, 0, 1000)[0] == -(-n * tau // 1000)
+    # one token holding all the mass: B = 1 for any tau > 0
+    s = np.zeros(50, np.float32)
+    s[17] = 0.9
+    assert oracle.dynamic_budget(s, [0, 50], 999, 0, 1000)[0] == 1
+    # tau = 1000 keeps every token with a nonzero quantum
+    s = np.asarray([0.5, 1e-12, 0.25, 0.0, 0.125], np.float32)
+    assert oracle.dynamic_budget(s, [0, 5], 1000, 0, 1000)[0] == 3
+    # floor and ceiling ratios
+    assert oracle.dynamic_budget(np.full(100, 0.1, np.float32), [0, 100], 0, 200, 1000)[0] == 20
+    assert oracle.dynamic_budget(np.full(100, 0.1, np.float32), [0, 100], 1000, 0, 750)[0] == 75
+    # requests are independent; an empty request keeps 0
+    s = np.concatenate([np.full(10, 0.2, np.float32), np.zeros(0, np.float32),
+                        np.asarray([1.0, 0.0, 0.0], np.float32)])
+    assert oracle.dynamic_budget(s, [0, 10, 10, 13], 500, 0, 1000).tolist() == [5, 0, 1]
+
+
+def test_dynamic_budget_invariances():
+    rng = np.random.default_rng(6)
+    s = (rng.random(300) ** 4).astype(np.float32)
+    b = oracle.dynamic_budget(s, [0, 300], 800, 0, 1000)[0]
+    # scaling by a power of two leaves the quanta, hence B, unchanged
+    assert oracle.dynamic_budget(s * np.float32(8.0), [0, 300], 800, 0, 1000)[0] == b
+    # permuting the tokens leaves B unchanged
+    assert oracle.dynamic_budget(s[rng.permutation(300)], [0, 300], 800, 0, 1000)[0] == b
+    # concentrating the same ranking raises the top tokens' share: B cannot grow
+    assert oracle.dynamic_budget(s ** 2, [0, 300], 800, 0, 1000)[0] <= b
