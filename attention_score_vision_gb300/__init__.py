@@ -20,11 +20,12 @@ __all__ = [
     "TselError", "load_library", "build",
     "tsel_importance_workspace_size", "tsel_importance", "tsel_importance_noalloc",
     "tsel_select_topk_workspace_size", "tsel_select_topk",
-    "tsel_gather_compact_workspace_size", "tsel_gather_compact",
+    "tsel_gather_compact_workspace_size", "tsel_gather_compact", "tsel_gather_compact_counted",
+    "tsel_dynamic_budget", "TSEL_KEEP_FROM_DEVICE",
     "tsel_keep_count", "tsel_read_device_status", "tsel_clear_device_status",
     "tsel_status_string", "tsel_last_error", "tsel_probe_ex2",
     "TSEL_DEV_SEQLENS", "TSEL_DEV_REQUESTS", "TSEL_DEV_KEEP_IDX", "TSEL_DEV_TIMEOUT", "TSEL_DEV_NAN",
-    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
+    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_SCORE_SUM", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
 ]
 
 TSEL_OK = 0
@@ -40,8 +41,11 @@ TSEL_DEV_KEEP_IDX = 0x4
 TSEL_DEV_TIMEOUT = 0x8
 TSEL_DEV_NAN = 0x10
 
+TSEL_KEEP_FROM_DEVICE = -1
+
 TSEL_IMP_LSE_PROVIDED = 0x1
 TSEL_IMP_FP8_E4M3 = 0x2
+TSEL_IMP_SCORE_SUM = 0x4
 TSEL_IMP_TEST_STALL = 0x10000
 TSEL_IMP_STAGE_PREP = 0x100
 TSEL_IMP_STAGE_PASS1 = 0x200
@@ -60,6 +64,11 @@ _SIGNATURES = {
     "tsel_gather_compact_workspace_size": (_c_size, []),
     "tsel_gather_compact": (_c_int, [_p, _c_i64, _c_int, _c_int, _p, _c_int, _p, _c_int, _c_int,
                                      _p, _c_int, _p, _p, _p, _p, _p, _c_size, _p]),
+    "tsel_gather_compact_counted": (_c_int, [_p, _c_i64, _c_int, _c_int, _p, _c_int, _p, _c_int,
+                                             _c_int, _p, _p, _c_int, _p, _p, _p, _p, _p, _c_size,
+                                             _p]),
+    "tsel_dynamic_budget": (_c_int, [_p, _c_int, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p,
+                                     _c_size, _p]),
     "tsel_keep_count": (_c_int, [_c_int, _c_int]),
     "tsel_read_device_status": (_c_int, [_p, ctypes.POINTER(ctypes.c_uint32), _p]),
     "tsel_clear_device_status": (_c_int, [_p, _p]),
@@ -222,14 +231,19 @@ def tsel_select_topk(scores: torch.Tensor, req_tok_offsets: torch.Tensor,
                      keep_idx: Optional[torch.Tensor] = None, cu_keep: Optional[torch.Tensor] = None,
                      workspace: Optional[torch.Tensor] = None,
                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Pooled top-B per request; returns (keep_idx int32 [total_keep], cu_keep int32 [R+1])."""
+    """Pooled top-B per request; returns (keep_idx int32 [total_keep], cu_keep int32 [R+1]).
+
+    total_keep = TSEL_KEEP_FROM_DEVICE takes budgets computed on the device
+    (tsel_dynamic_budget): keep_idx then has room for every token and
+    cu_keep[R] holds the kept count."""
     _need(scores, torch.float32, "scores")
     _need(req_tok_offsets, torch.int32, "req_tok_offsets")
     _need(keep_per_req, torch.int32, "keep_per_req")
     R = keep_per_req.numel()
     dev = scores.device
     if keep_idx is None:
-        keep_idx = torch.empty(int(total_keep), dtype=torch.int32, device=dev)
+        cap = scores.numel() if int(total_keep) == TSEL_KEEP_FROM_DEVICE else int(total_keep)
+        keep_idx = torch.empty(cap, dtype=torch.int32, device=dev)
     if cu_keep is None:
         cu_keep = torch.empty(R + 1, dtype=torch.int32, device=dev)
     if workspace is None:
@@ -240,6 +254,32 @@ def tsel_select_topk(scores: torch.Tensor, req_tok_offsets: torch.Tensor,
                                          _stream(stream, dev))
     _check(st)
     return keep_idx, cu_keep
+
+
+def tsel_dynamic_budget(scores: torch.Tensor, req_tok_offsets: torch.Tensor, mass_permille: int,
+                        min_permille: int = 0, max_permille: int = 1000, *,
+                        keep_per_req: Optional[torch.Tensor] = None,
+                        total_keep: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-request budgets from the scores (fewest top tokens holding mass_permille of
+    the request's score quanta, bounded); returns (keep_per_req int32 [R], total int32 [1])."""
+    _need(scores, torch.float32, "scores")
+    _need(req_tok_offsets, torch.int32, "req_tok_offsets")
+    R = req_tok_offsets.numel() - 1
+    dev = scores.device
+    if keep_per_req is None:
+        keep_per_req = torch.empty(max(R, 0), dtype=torch.int32, device=dev)
+    if total_keep is None:
+        total_keep = torch.empty(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _new_workspace(tsel_select_topk_workspace_size(R), dev)
+    st = load_library().tsel_dynamic_budget(_ptr(scores), scores.numel(), _ptr(req_tok_offsets), R,
+                                            int(mass_permille), int(min_permille), int(max_permille),
+                                            _ptr(keep_per_req), _ptr(total_keep), _ptr(workspace),
+                                            workspace.numel(), _stream(stream, dev))
+    _check(st)
+    return keep_per_req, total_keep
 
 
 # ---------------------------------------------------------------------------
@@ -282,6 +322,51 @@ def tsel_gather_compact(hidden: torch.Tensor, pos: Optional[torch.Tensor], cu_se
     st = load_library().tsel_gather_compact(
         _ptr(hidden), hidden.stride(0), D, hidden.element_size(), _ptr(pos), P, _ptr(cu_seqlens_k),
         G, tk, _ptr(keep_idx), K, _ptr(out_hidden), _ptr(out_pos), _ptr(out_img_id),
+        _ptr(out_cu_seqlens), _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(st)
+    return out_hidden, out_pos, out_img_id, out_cu_seqlens
+
+
+def tsel_gather_compact_counted(hidden: torch.Tensor, pos: Optional[torch.Tensor],
+                                cu_seqlens_k: torch.Tensor, keep_idx: torch.Tensor,
+                                num_kept: torch.Tensor, max_kept: int, *,
+                                out_hidden: Optional[torch.Tensor] = None,
+                                out_pos: Optional[torch.Tensor] = None,
+                                out_img_id: Optional[torch.Tensor] = None,
+                                out_cu_seqlens: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None, stream=None):
+    """tsel_gather_compact with the kept count read on the device (num_kept: int32
+    device scalar, e.g. cu_keep[R:]); outputs have room for max_kept rows, of which
+    the first *num_kept are written."""
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    _need(keep_idx, torch.int32, "keep_idx")
+    _need(num_kept, torch.int32, "num_kept")
+    if hidden.dim() != 2 or hidden.stride(1) != 1 or not hidden.is_cuda:
+        raise ValueError("hidden must be a CUDA [T, D] tensor with contiguous rows")
+    tk, D = hidden.shape
+    K = int(max_kept)
+    if keep_idx.numel() < K:
+        raise ValueError("keep_idx has fewer than max_kept entries")
+    G = cu_seqlens_k.numel() - 1
+    dev = hidden.device
+    P = 0 if pos is None else pos.shape[1]
+    if pos is not None:
+        _need(pos, torch.int32, "pos")
+        if not pos.is_contiguous() or pos.shape[0] != tk:
+            raise ValueError("pos must be a contiguous int32 [T, P] tensor")
+    if out_hidden is None:
+        out_hidden = torch.empty((K, D), dtype=hidden.dtype, device=dev)
+    if out_pos is None and P > 0:
+        out_pos = torch.empty((K, P), dtype=torch.int32, device=dev)
+    if out_img_id is None:
+        out_img_id = torch.empty(K, dtype=torch.int32, device=dev)
+    if out_cu_seqlens is None:
+        out_cu_seqlens = torch.empty(G + 1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _new_workspace(tsel_gather_compact_workspace_size(), dev)
+    st = load_library().tsel_gather_compact_counted(
+        _ptr(hidden), hidden.stride(0), D, hidden.element_size(), _ptr(pos), P, _ptr(cu_seqlens_k),
+        G, tk, _ptr(keep_idx), _ptr(num_kept), K, _ptr(out_hidden), _ptr(out_pos), _ptr(out_img_id),
         _ptr(out_cu_seqlens), _ptr(workspace), workspace.numel(), _stream(stream, dev))
     _check(st)
     return out_hidden, out_pos, out_img_id, out_cu_seqlens

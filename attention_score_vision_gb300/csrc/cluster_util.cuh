@@ -1,0 +1,83 @@
+// Cluster-size helpers shared by the per-request cluster kernels (top-B and
+// dynamic budget): one thread-block cluster per request, sized from the
+// average request length, capped by what the device can co-schedule.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace tsel {
+
+constexpr int kMaxClusterCtas = 16;
+
+// Cluster size from the average request size (the host does not see the
+// per-request offsets): small requests need no cluster.
+inline int cluster_size_for(int total_tokens, int num_req) {
+  const int64_t avg = num_req > 0 ? (int64_t(total_tokens) + num_req - 1) / num_req : 0;
+  if (avg >= 16384) return 16;
+  if (avg >= 4096) return 8;
+  if (avg >= 1024) return 4;
+  return 1;
+}
+
+// Largest power-of-two cluster size <= want that `kernel` (threads per CTA,
+// dyn bytes of dynamic shared memory) can co-schedule on the current device.
+// cache[dev][log2 size] keeps 1 + the answer (0 = unknown); the kernel's
+// attributes are set on the first query per device.
+template <typename Kernel>
+int usable_cluster_size(Kernel kernel, int want, int threads, size_t dyn, int (*cache)[5],
+                        cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return 1;
+  int lw = 0;
+  while ((1 << (lw + 1)) <= want && lw < 4) ++lw;
+  if (dev >= 0 && dev < 128 && cache[dev][lw] > 0) return cache[dev][lw] - 1;
+  *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
+  if (*err != cudaSuccess) return 1;
+  *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (*err != cudaSuccess) return 1;
+  int csize = 1 << lw;
+  for (; csize > 1; csize /= 2) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(csize);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(csize));
+    cfg.blockDim = dim3(unsigned(threads));
+    cfg.dynamicSmemBytes = dyn;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) == cudaSuccess && active > 0) break;
+    (void)cudaGetLastError();
+  }
+  if (dev >= 0 && dev < 128) cache[dev][lw] = csize + 1;
+  return csize;
+}
+
+// Launches `kernel` with one cluster of `csize` CTAs per request.
+template <typename Kernel, typename... Args>
+cudaError_t launch_clusters(Kernel kernel, int num_req, int csize, int threads, size_t dyn,
+                            cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(num_req) * unsigned(csize));
+  cfg.blockDim = dim3(unsigned(threads));
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(csize);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaPeekAtLastError();
+}
+
+}  // namespace tsel

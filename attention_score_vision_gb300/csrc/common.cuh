@@ -26,8 +26,8 @@ static_assert(sizeof(WsHeader) <= kWsHeaderBytes, "header too large");
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr int64_t align_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
-// Pass-2 units may split the kv heads into up to this many groups; each group
-// writes partial column sums that the last group of a 32-key slice adds up.
+// Pass-2 units may split the query heads into up to this many groups; each
+// group writes partial column sums that the last group of a 32-key slice adds up.
 constexpr int kMaxHeadGroups = 8;
 constexpr int kPairRows = 256;   // A rows per unit (two 128-row tiles)
 
@@ -95,10 +95,23 @@ struct ImpPassParams {
   const int32_t* kpair_off;
   int32_t* grp_ctr;
   float* part;
+  int sum_norm;          // 1: scores are total attention received (no division by H*Nq)
 };
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   atomicOr(status, bits);
+}
+
+// fp32 bits -> uint32 with the same order; -0 maps to +0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Inverse of order_key (for keys of non-negative scores).
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 }  // namespace tsel

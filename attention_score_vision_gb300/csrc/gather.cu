@@ -43,10 +43,19 @@ __global__ void __launch_bounds__(kGatherThreads)
     gather_kernel(const uint8_t* __restrict__ hidden, int64_t row_stride_bytes, int row_vecs,
                   const int32_t* __restrict__ pos, int pos_dim,
                   const int32_t* __restrict__ cu_k, int G, int Tk,
-                  const int32_t* __restrict__ keep_idx, int K, uint8_t* __restrict__ out_hidden,
-                  int32_t* __restrict__ out_pos, int32_t* __restrict__ out_img,
-                  int32_t* __restrict__ out_cu, uint32_t* status) {
+                  const int32_t* __restrict__ keep_idx, int K, const int32_t* K_dev,
+                  uint8_t* __restrict__ out_hidden, int32_t* __restrict__ out_pos,
+                  int32_t* __restrict__ out_img, int32_t* __restrict__ out_cu,
+                  uint32_t* status) {
   const int lane = threadIdx.x & 31;
+  if (K_dev != nullptr) {
+    // kept count produced on the device; K is the capacity the launch was sized for
+    const int kd = __ldg(K_dev);
+    if (kd < 0 || kd > K) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, TSEL_DEV_KEEP_IDX);
+    }
+    K = kd < 0 ? 0 : (kd > K ? K : kd);
+  }
   const int gwarp = (blockIdx.x * kGatherThreads + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * kGatherThreads) >> 5;
   const int gtid = blockIdx.x * kGatherThreads + threadIdx.x;
@@ -80,9 +89,9 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_bytes,
                           const int32_t* pos, int pos_dim, const int32_t* cu_k, int G, int Tk,
-                          const int32_t* keep_idx, int K, void* out_hidden, int32_t* out_pos,
-                          int32_t* out_img, int32_t* out_cu, uint32_t* status, int num_sms,
-                          cudaStream_t stream) {
+                          const int32_t* keep_idx, int K, const int32_t* K_dev,
+                          void* out_hidden, int32_t* out_pos, int32_t* out_img, int32_t* out_cu,
+                          uint32_t* status, int num_sms, cudaStream_t stream) {
   const int64_t warps_needed = K > G + 1 ? K : G + 1;
   int64_t blocks = (warps_needed * 32 + kGatherThreads - 1) / kGatherThreads;
   const int64_t max_blocks = int64_t(num_sms) * (2048 / kGatherThreads);
@@ -90,7 +99,8 @@ cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_
   if (blocks < 1) blocks = 1;
   gather_kernel<<<int(blocks), kGatherThreads, 0, stream>>>(
       static_cast<const uint8_t*>(hidden), row_stride_bytes, row_bytes / 16, pos, pos_dim, cu_k,
-      G, Tk, keep_idx, K, static_cast<uint8_t*>(out_hidden), out_pos, out_img, out_cu, status);
+      G, Tk, keep_idx, K, K_dev, static_cast<uint8_t*>(out_hidden), out_pos, out_img, out_cu,
+      status);
   return cudaPeekAtLastError();
 }
 

@@ -769,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             const int krow = w.pair * kPair + a_half * kTile + row;
             const float total = part + o0;
-            const float rows = float(p.H * w.nq);
+            const float rows = p.sum_norm ? 1.f : float(p.H * w.nq);
             if (p.hgroups == 1) {
               if (krow < w.nk) p.scores[w.k0 + krow] = w.nq > 0 ? total / rows : 0.f;
             } else {

@@ -20,6 +20,7 @@
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
+#include "cluster_util.cuh"
 #include "common.cuh"
 
 namespace cg = cooperative_groups;
@@ -29,15 +30,8 @@ namespace tsel {
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkItems = 4;               // consecutive tokens per thread when compacting
-constexpr int kTopkMaxCluster = 16;
+constexpr int kTopkMaxCluster = kMaxClusterCtas;
 constexpr int kTopkCacheKeys = 16384;       // keys cached in shared memory per CTA
-
-// fp32 bits -> uint32 with the same order; -0 maps to +0.
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 __device__ __forceinline__ int warp_incl_scan(int x) {
   const int lane = threadIdx.x & 31;
@@ -104,8 +98,13 @@ __global__ void __launch_bounds__(kTopkThreads)
   if (tid == 0) {
     int bad = neg;
     if (lo < 0 || hi < lo || hi > total_tokens || B < 0 || B > hi - lo) bad = 1;
-    if (before < 0 || int64_t(before) + B > total_keep) bad = 1;
-    if (r == num_req - 1 && int64_t(before) + B != total_keep) bad = 1;
+    if (before < 0) bad = 1;
+    if (total_keep >= 0) {
+      if (int64_t(before) + B > total_keep) bad = 1;
+      if (r == num_req - 1 && int64_t(before) + B != total_keep) bad = 1;
+    } else if (int64_t(before) + B > total_tokens) {
+      bad = 1;   // budgets from the device: keep_idx has room for total_tokens entries
+    }
     sh.bad = bad;
     sh.nan_seen = 0;
   }
@@ -286,78 +285,19 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
 }
 
-// Cluster size from the average request size (the host does not see the
-// per-request offsets): small requests need no cluster.
-static int topk_cluster_size(int total_tokens, int num_req) {
-  const int64_t avg = num_req > 0 ? (int64_t(total_tokens) + num_req - 1) / num_req : 0;
-  if (avg >= 16384) return 16;
-  if (avg >= 4096) return 8;
-  if (avg >= 1024) return 4;
-  return 1;
-}
-
-// Largest cluster size <= `want` this device can co-schedule, cached per
-// device (the attributes are set once per device as well).
-static int topk_usable_cluster(int want, size_t dyn, cudaError_t* err) {
-  static int cache[128][5] = {};  // [device][log2 size] -> 1 + usable size, 0 = unknown
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return 1;
-  int lw = 0;
-  while ((1 << (lw + 1)) <= want && lw < 4) ++lw;
-  if (dev >= 0 && dev < 128 && cache[dev][lw] > 0) return cache[dev][lw] - 1;
-  *err = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(dyn));
-  if (*err != cudaSuccess) return 1;
-  *err = cudaFuncSetAttribute(topk_cluster_kernel,
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (*err != cudaSuccess) return 1;
-  int csize = 1 << lw;
-  for (; csize > 1; csize /= 2) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(csize);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(unsigned(csize));
-    cfg.blockDim = dim3(kTopkThreads);
-    cfg.dynamicSmemBytes = dyn;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, topk_cluster_kernel, &cfg) == cudaSuccess &&
-        active > 0)
-      break;
-    (void)cudaGetLastError();
-  }
-  if (dev >= 0 && dev < 128) cache[dev][lw] = csize + 1;
-  return csize;
-}
-
 cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
                         int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
                         int32_t* cu_keep, uint32_t* status, cudaStream_t stream) {
+  static int cache[128][5] = {};
   const size_t dyn = size_t(kTopkCacheKeys) * sizeof(uint32_t);
   cudaError_t e = cudaSuccess;
-  const int csize = topk_usable_cluster(topk_cluster_size(total_tokens, num_req), dyn, &e);
+  const int csize = usable_cluster_size(topk_cluster_kernel,
+                                        cluster_size_for(total_tokens, num_req), kTopkThreads,
+                                        dyn, cache, &e);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(num_req) * unsigned(csize));
-  cfg.blockDim = dim3(kTopkThreads);
-  cfg.dynamicSmemBytes = dyn;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(csize);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, total_tokens, req_off, num_req, keep,
-                         total_keep, keep_idx, cu_keep, status);
-  if (e != cudaSuccess) return e;
-  return cudaPeekAtLastError();
+  return launch_clusters(topk_cluster_kernel, num_req, csize, kTopkThreads, dyn, stream, scores,
+                         total_tokens, req_off, num_req, keep, total_keep, keep_idx, cu_keep,
+                         status);
 }
 
 }  // namespace tsel

@@ -28,9 +28,12 @@ cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* re
                         int32_t* cu_keep, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_bytes,
                           const int32_t* pos, int pos_dim, const int32_t* cu_k, int G, int Tk,
-                          const int32_t* keep_idx, int K, void* out_hidden, int32_t* out_pos,
-                          int32_t* out_img, int32_t* out_cu, uint32_t* status, int num_sms,
-                          cudaStream_t stream);
+                          const int32_t* keep_idx, int K, const int32_t* K_dev,
+                          void* out_hidden, int32_t* out_pos, int32_t* out_img, int32_t* out_cu,
+                          uint32_t* status, int num_sms, cudaStream_t stream);
+cudaError_t launch_budget(const float* scores, int total_tokens, const int32_t* req_off,
+                          int num_req, int mass_pm, int min_pm, int max_pm, int32_t* keep_out,
+                          int32_t* total_out, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_probe_ex2(int blocks, int iters, float* sink, cudaStream_t stream);
 }  // namespace tsel
 
@@ -195,8 +198,9 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     return fail(TSEL_ERR_INVALID_VALUE, "num_heads=%d num_kv_heads=%d", num_heads, num_kv_heads);
   if (!(head_dim == 64 || head_dim == 80 || head_dim == 96 || head_dim == 112 || head_dim == 128))
     return fail(TSEL_ERR_UNSUPPORTED, "head_dim=%d (supported: 64, 80, 96, 112, 128)", head_dim);
-  if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_FP8_E4M3 | TSEL_IMP_TEST_STALL |
-                 TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2)) != 0)
+  if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_FP8_E4M3 | TSEL_IMP_SCORE_SUM |
+                 TSEL_IMP_TEST_STALL | TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 |
+                 TSEL_IMP_STAGE_PASS2)) != 0)
     return fail(TSEL_ERR_UNSUPPORTED, "flags=0x%x", flags);
   const bool lse_provided = (flags & TSEL_IMP_LSE_PROVIDED) != 0;
   if (lse_provided && total_q > 0 && lse == nullptr)
@@ -284,6 +288,7 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   p.c = scale * 1.4426950408889634f;
   p.timeout_ns = wait_timeout_ns();
   p.stall = (flags & TSEL_IMP_TEST_STALL) ? 1 : 0;
+  p.sum_norm = (flags & TSEL_IMP_SCORE_SUM) ? 1 : 0;
   if (p.stall) p.timeout_ns = 50ull * 1000000ull;
 
   if ((stages & TSEL_IMP_STAGE_PASS1) && lse_provided) {
@@ -326,11 +331,12 @@ tsel_status tsel_select_topk(const float* scores, int total_tokens,
                              int32_t* cu_keep, void* workspace, size_t workspace_bytes,
                              void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (num_req < 0 || total_tokens < 0 || total_keep < 0)
+  if (num_req < 0 || total_tokens < 0 || (total_keep < 0 && total_keep != TSEL_KEEP_FROM_DEVICE))
     return fail(TSEL_ERR_INVALID_VALUE, "negative size");
+  const int capacity = total_keep == TSEL_KEEP_FROM_DEVICE ? total_tokens : total_keep;
   if (req_tok_offsets == nullptr || keep_per_req == nullptr || cu_keep == nullptr ||
       workspace == nullptr || (total_tokens > 0 && scores == nullptr) ||
-      (total_keep > 0 && keep_idx == nullptr))
+      (capacity > 0 && keep_idx == nullptr))
     return fail(TSEL_ERR_INVALID_VALUE, "null pointer");
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < kWsHeaderBytes)
     return fail(TSEL_ERR_WORKSPACE, "workspace must be >= %d bytes, 256-byte aligned",
@@ -345,13 +351,15 @@ tsel_status tsel_select_topk(const float* scores, int total_tokens,
   return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "top-k launch");
 }
 
-tsel_status tsel_gather_compact(const void* hidden, int64_t hidden_row_stride, int hidden_dim,
-                                int elem_bytes, const int32_t* pos, int pos_dim,
-                                const int32_t* cu_seqlens_k, int num_seg, int total_k,
-                                const int32_t* keep_idx, int total_keep, void* out_hidden,
-                                int32_t* out_pos, int32_t* out_img_id, int32_t* out_cu_seqlens,
-                                void* workspace, size_t workspace_bytes, void* stream_) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+namespace {
+
+tsel_status gather_impl(const void* hidden, int64_t hidden_row_stride, int hidden_dim,
+                        int elem_bytes, const int32_t* pos, int pos_dim,
+                        const int32_t* cu_seqlens_k, int num_seg, int total_k,
+                        const int32_t* keep_idx, int total_keep, const int32_t* num_kept,
+                        void* out_hidden, int32_t* out_pos, int32_t* out_img_id,
+                        int32_t* out_cu_seqlens, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
   if (num_seg < 0 || total_k < 0 || total_keep < 0 || hidden_dim < 0 || pos_dim < 0 ||
       pos_dim > 8 || !(elem_bytes == 1 || elem_bytes == 2 || elem_bytes == 4 || elem_bytes == 8))
     return fail(TSEL_ERR_INVALID_VALUE, "bad size argument");
@@ -377,9 +385,67 @@ tsel_status tsel_gather_compact(const void* hidden, int64_t hidden_row_stride, i
   if (sm_count(&sms) != 0) return fail(TSEL_ERR_CUDA, "cannot query the SM count");
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   cudaError_t e = launch_gather(hidden, stride_bytes, int(row_bytes), pos, pos_dim, cu_seqlens_k,
-                                num_seg, total_k, keep_idx, total_keep, out_hidden, out_pos,
-                                out_img_id, out_cu_seqlens, &hdr->status, sms, stream);
+                                num_seg, total_k, keep_idx, total_keep, num_kept, out_hidden,
+                                out_pos, out_img_id, out_cu_seqlens, &hdr->status, sms, stream);
   return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "gather launch");
+}
+
+}  // namespace
+
+tsel_status tsel_gather_compact(const void* hidden, int64_t hidden_row_stride, int hidden_dim,
+                                int elem_bytes, const int32_t* pos, int pos_dim,
+                                const int32_t* cu_seqlens_k, int num_seg, int total_k,
+                                const int32_t* keep_idx, int total_keep, void* out_hidden,
+                                int32_t* out_pos, int32_t* out_img_id, int32_t* out_cu_seqlens,
+                                void* workspace, size_t workspace_bytes, void* stream_) {
+  return gather_impl(hidden, hidden_row_stride, hidden_dim, elem_bytes, pos, pos_dim,
+                     cu_seqlens_k, num_seg, total_k, keep_idx, total_keep, nullptr, out_hidden,
+                     out_pos, out_img_id, out_cu_seqlens, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream_));
+}
+
+tsel_status tsel_gather_compact_counted(const void* hidden, int64_t hidden_row_stride,
+                                        int hidden_dim, int elem_bytes, const int32_t* pos,
+                                        int pos_dim, const int32_t* cu_seqlens_k, int num_seg,
+                                        int total_k, const int32_t* keep_idx,
+                                        const int32_t* num_kept, int max_kept, void* out_hidden,
+                                        int32_t* out_pos, int32_t* out_img_id,
+                                        int32_t* out_cu_seqlens, void* workspace,
+                                        size_t workspace_bytes, void* stream_) {
+  if (num_kept == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "null num_kept");
+  return gather_impl(hidden, hidden_row_stride, hidden_dim, elem_bytes, pos, pos_dim,
+                     cu_seqlens_k, num_seg, total_k, keep_idx, max_kept, num_kept, out_hidden,
+                     out_pos, out_img_id, out_cu_seqlens, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream_));
+}
+
+tsel_status tsel_dynamic_budget(const float* scores, int total_tokens,
+                                const int32_t* req_tok_offsets, int num_req, int mass_permille,
+                                int min_permille, int max_permille, int32_t* keep_per_req,
+                                int32_t* total_keep, void* workspace, size_t workspace_bytes,
+                                void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (num_req < 0 || total_tokens < 0) return fail(TSEL_ERR_INVALID_VALUE, "negative size");
+  if (mass_permille < 0 || mass_permille > 1000 || min_permille < 0 ||
+      max_permille > 1000 || min_permille > max_permille)
+    return fail(TSEL_ERR_INVALID_VALUE, "permille arguments %d/%d/%d", mass_permille,
+                min_permille, max_permille);
+  if (req_tok_offsets == nullptr || workspace == nullptr ||
+      (num_req > 0 && keep_per_req == nullptr) || (total_tokens > 0 && scores == nullptr))
+    return fail(TSEL_ERR_INVALID_VALUE, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < kWsHeaderBytes)
+    return fail(TSEL_ERR_WORKSPACE, "workspace must be >= %d bytes, 256-byte aligned",
+                kWsHeaderBytes);
+  if (num_req == 0) {
+    if (total_keep == nullptr) return TSEL_OK;
+    cudaError_t e = cudaMemsetAsync(total_keep, 0, sizeof(int32_t), stream);
+    return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "memset total_keep");
+  }
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  cudaError_t e = launch_budget(scores, total_tokens, req_tok_offsets, num_req, mass_permille,
+                                min_permille, max_permille, keep_per_req, total_keep,
+                                &hdr->status, stream);
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "budget launch");
 }
 
 tsel_status tsel_read_device_status(const void* workspace, uint32_t* bits, void* stream_) {

@@ -490,6 +490,46 @@ def gpu_arm(args) -> None:
                     "note": "LSE supplied by the caller (as the attention kernel's LSE would be); "
                             "prep + LSE import + column pass + top-B + compaction"}
 
+    # --- dynamic keep budget: importance -> budget -> top-B -> compaction, with
+    # the kept count staying on the device (no host round trip) ----------------
+    R = w.keep_per_req.size
+    dyn_keep = torch.empty(R, dtype=torch.int32, device=dev)
+    dyn_total = torch.empty(1, dtype=torch.int32, device=dev)
+    dyn_idx = torch.empty(Tk, dtype=torch.int32, device=dev)
+    dyn_cu = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    dyn_h = torch.empty((Tk, D), dtype=torch.bfloat16, device=dev)
+    dyn_p = torch.empty((Tk, P), dtype=torch.int32, device=dev)
+    dyn_i = torch.empty(Tk, dtype=torch.int32, device=dev)
+    DYN = (900, 100, 900)   # tau: 90% of the score mass; keep between 10% and 90%
+    dy_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(i & 0xFF)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        importance(0)
+        ev[1].record(stream)
+        tsel.tsel_dynamic_budget(scores, d["req_off"], *DYN, keep_per_req=dyn_keep,
+                                 total_keep=dyn_total, workspace=ws, stream=stream)
+        tsel.tsel_select_topk(scores, d["req_off"], dyn_keep, tsel.TSEL_KEEP_FROM_DEVICE,
+                              keep_idx=dyn_idx, cu_keep=dyn_cu, workspace=ws, stream=stream)
+        tsel.tsel_gather_compact_counted(d["hidden"], d["pos"], d["cu_k"], dyn_idx, dyn_cu[R:], Tk,
+                                         out_hidden=dyn_h, out_pos=dyn_p, out_img_id=dyn_i,
+                                         out_cu_seqlens=out_c, workspace=ws, stream=stream)
+        ev[2].record(stream)
+        if i >= args.warmup:
+            dy_ms.append(ev)
+    torch.cuda.synchronize()
+    if tsel.tsel_read_device_status(ws) != 0:
+        raise RuntimeError("device status set in the dynamic-budget run")
+    dy = reduce_max_over_ranks(sum(e[0].elapsed_time(e[2]) for e in dy_ms) / len(dy_ms), dev)
+    dy_sel = sum(e[1].elapsed_time(e[2]) for e in dy_ms) / len(dy_ms)
+    dynamic = {"ms_per_step": dy, "value": replica_throughput(Tk, world, dy), "unit": "tokens/s",
+               "selection_ms": dy_sel, "kept": int(dyn_total.item()), "tokens": Tk,
+               "mass_permille": DYN[0], "min_permille": DYN[1], "max_permille": DYN[2],
+               "note": "per-request budget from the scores (fewest top tokens holding 90% of the "
+                       "score quanta, kept between 10% and 90%); budget + top-B + compaction "
+                       "read the kept count on the device"}
+
     # --- FP8 E4M3 Q/K (one scale per tensor folded into the softmax scale) ----
     fp8 = None
     if not args.no_fp8:
@@ -649,6 +689,7 @@ def gpu_arm(args) -> None:
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "lse_provided": lse_provided,
+        "dynamic_budget": dynamic,
         "fp8": fp8,
         "small_requests": small,
         "gpu_launches": 5 * args.steps,

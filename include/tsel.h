@@ -73,7 +73,11 @@ typedef enum tsel_status {
 #define TSEL_DEV_REQUESTS  0x2u  /* request offsets or keep counts out of range */
 #define TSEL_DEV_KEEP_IDX  0x4u  /* keep_idx out of range or not strictly ascending */
 #define TSEL_DEV_TIMEOUT   0x8u  /* a bounded device wait gave up */
-#define TSEL_DEV_NAN       0x10u /* NaN score given to the top-B selection */
+#define TSEL_DEV_NAN       0x10u /* NaN score given to the top-B selection or budget */
+
+/* total_keep value of tsel_select_topk when the budgets were computed on the
+ * device (tsel_dynamic_budget): keep_idx then has room for total_tokens. */
+#define TSEL_KEEP_FROM_DEVICE (-1)
 
 /* tsel_importance flags */
 #define TSEL_IMP_LSE_PROVIDED 0x1u   /* lse is an INPUT (natural log [H, Tq], e.g. the softmax
@@ -82,6 +86,8 @@ typedef enum tsel_status {
 #define TSEL_IMP_FP8_E4M3     0x2u   /* q and k hold FP8 E4M3 bytes (row strides in bytes);
                                         fold their dequantisation scales into
                                         softmax_scale ([LiteVLM] FP8 deployment) */
+#define TSEL_IMP_SCORE_SUM    0x4u   /* scores are the total attention received,
+                                        sum_h sum_i P, not divided by H * Nq_g */
 #define TSEL_IMP_TEST_STALL   0x10000u /* test hook for failure detection: the pass kernels'
                                           scheduler publishes no work, every bounded wait
                                           runs out after ~50 ms and TSEL_DEV_TIMEOUT is set;
@@ -125,7 +131,8 @@ TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int tot
  * num_heads    H in [1, 256]; num_kv_heads divides it.
  * head_dim     64, 80, 96, 112 or 128 (else TSEL_ERR_UNSUPPORTED).
  * softmax_scale  <= 0 selects 1/sqrt(head_dim).
- * flags        0, TSEL_IMP_LSE_PROVIDED, TSEL_IMP_FP8_E4M3, and/or TSEL_IMP_STAGE_* bits.
+ * flags        0, TSEL_IMP_LSE_PROVIDED, TSEL_IMP_FP8_E4M3, TSEL_IMP_SCORE_SUM and/or
+ *              TSEL_IMP_STAGE_* bits.
  *              With TSEL_IMP_FP8_E4M3, q and k are E4M3 [rows, heads, head_dim] (one byte
  *              per element, row strides in bytes, multiples of 16) and softmax_scale is
  *              the full factor applied to the fp8 dot products (scale x q_scale x
@@ -197,6 +204,10 @@ TSEL_API size_t tsel_select_topk_workspace_size(int num_req);
  * req_tok_offsets int32 [num_req+1] device: 0 <= o[r] <= o[r+1] <= total_tokens.
  * keep_per_req    int32 [num_req] device: 0 <= B_r <= o[r+1]-o[r];
  *                 sum must equal total_keep (host value, sizes keep_idx).
+ *                 total_keep = TSEL_KEEP_FROM_DEVICE drops that check (budgets
+ *                 written by tsel_dynamic_budget, not known on the host):
+ *                 keep_idx then needs room for total_tokens entries and
+ *                 cu_keep[num_req] holds the kept count.
  * keep_idx        out int32 [total_keep]; cu_keep out int32 [num_req+1].
  * A request that fails its checks sets TSEL_DEV_REQUESTS and writes nothing.
  */
@@ -205,6 +216,36 @@ TSEL_API tsel_status tsel_select_topk(const float* scores, int total_tokens,
                              const int32_t* keep_per_req, int total_keep,
                              int32_t* keep_idx, int32_t* cu_keep,
                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Dynamic keep budget per request from its scores ([VTC] section 6.2 leaves a
+ * content-dependent compression ratio as future work and gives no rule; this
+ * is the rule the library uses). For request r with tokens
+ * [req_tok_offsets[r], req_tok_offsets[r+1]) (n_r of them):
+ *   q_j  = floor(s_j * 2^(24 - E)), E the binary exponent with the request's
+ *          largest score in [2^(E-1), 2^E) (integer quanta; NaN, negative
+ *          and zero scores count 0);
+ *   M    = sum_j q_j, T = ceil(mass_permille * M / 1000);
+ *   B_r  = the fewest tokens, taken in top-B order (score descending, lowest
+ *          index first), whose quanta reach T (0 when T = 0), then bounded to
+ *          [floor(n_r*min_permille/1000), floor(n_r*max_permille/1000)].
+ * Integer sums make B_r exact and deterministic. Feed keep_per_req to
+ * tsel_select_topk with total_keep = TSEL_KEEP_FROM_DEVICE.
+ *
+ * scores          fp32 [total_tokens] device (NaN sets TSEL_DEV_NAN).
+ * req_tok_offsets int32 [num_req+1] device (bad ranges set TSEL_DEV_REQUESTS
+ *                 and give B_r = 0).
+ * mass_permille   in [0, 1000]; 0 <= min_permille <= max_permille <= 1000.
+ * keep_per_req    out int32 [num_req] device.
+ * total_keep      out int32 device scalar = sum_r B_r (may be NULL).
+ * workspace       >= tsel_select_topk_workspace_size(num_req) bytes (status).
+ * Requests of up to 2^31 tokens; one CTA per request.
+ */
+TSEL_API tsel_status tsel_dynamic_budget(const float* scores, int total_tokens,
+                                         const int32_t* req_tok_offsets, int num_req,
+                                         int mass_permille, int min_permille, int max_permille,
+                                         int32_t* keep_per_req, int32_t* total_keep,
+                                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Order-preserving compaction with metadata                                */
@@ -242,6 +283,23 @@ TSEL_API tsel_status tsel_gather_compact(const void* hidden, int64_t hidden_row_
                                 const int32_t* pos, int pos_dim,
                                 const int32_t* cu_seqlens_k, int num_seg, int total_k,
                                 const int32_t* keep_idx, int total_keep,
+                                void* out_hidden, int32_t* out_pos,
+                                int32_t* out_img_id, int32_t* out_cu_seqlens,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * tsel_gather_compact with the kept count read on the device (e.g.
+ * cu_keep + num_req from tsel_select_topk with device budgets), so no host
+ * round trip is needed between the calls. K = *num_kept rows are compacted;
+ * max_kept (host) sizes the launch and bounds K: outputs need room for
+ * max_kept rows, and *num_kept outside [0, max_kept] sets TSEL_DEV_KEEP_IDX
+ * (K is then clamped). Other arguments as in tsel_gather_compact.
+ */
+TSEL_API tsel_status tsel_gather_compact_counted(const void* hidden, int64_t hidden_row_stride,
+                                int hidden_dim, int elem_bytes,
+                                const int32_t* pos, int pos_dim,
+                                const int32_t* cu_seqlens_k, int num_seg, int total_k,
+                                const int32_t* keep_idx, const int32_t* num_kept, int max_kept,
                                 void* out_hidden, int32_t* out_pos,
                                 int32_t* out_img_id, int32_t* out_cu_seqlens,
                                 void* workspace, size_t workspace_bytes, void* stream);

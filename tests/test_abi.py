@@ -101,12 +101,27 @@ def test_importance_host_checks_fail_before_any_cuda_call(lib):
     assert _call_importance(lib, ws=128) == 3               # workspace misaligned
     assert _call_importance(lib, wsb=64) == 3               # workspace too small
     assert _call_importance(lib, cuq=0) == 1                # null cu_seqlens
-    assert _call_importance(lib, flags=0x4) == 2            # unknown flag
+    assert _call_importance(lib, flags=0x8) == 2            # unknown flag
     assert _call_importance(lib, flags=0x2) == 1            # E4M3 inputs need softmax_scale
     assert _call_importance(lib, flags=0x2, scale=0.5, qs=4 * 64 + 4) == 1   # E4M3 row stride, 16-byte rule
     assert _call_importance(lib, flags=0x1, lse=0) == 1     # LSE-provided needs the lse input
     assert _call_importance(lib, tq=-1) == 1
     assert "head_dim=72" in (_call_importance(lib, d=72) and lib.tsel_last_error().decode())
+
+
+def test_dynamic_budget_and_counted_gather_host_checks(lib):
+    # permille arguments out of range, min > max, null pointers, workspace
+    assert lib.tsel_dynamic_budget(16, 10, 16, 1, 1001, 0, 1000, 16, 16, 256, 1024, None) == 1
+    assert lib.tsel_dynamic_budget(16, 10, 16, 1, 500, 600, 500, 16, 16, 256, 1024, None) == 1
+    assert lib.tsel_dynamic_budget(16, 10, 16, 1, -1, 0, 1000, 16, 16, 256, 1024, None) == 1
+    assert lib.tsel_dynamic_budget(16, 10, None, 1, 500, 0, 1000, 16, 16, 256, 1024, None) == 1
+    assert lib.tsel_dynamic_budget(16, 10, 16, 1, 500, 0, 1000, None, 16, 256, 1024, None) == 1
+    assert lib.tsel_dynamic_budget(16, 10, 16, 1, 500, 0, 1000, 16, 16, 128, 1024, None) == 3
+    # counted gather needs the device count pointer
+    assert lib.tsel_gather_compact_counted(16, 0, 8, 2, 16, 1, 16, 1, 4, 16, None, 2, 16, 16, 16,
+                                           16, 256, 1024, None) == 1
+    # top-B: only TSEL_KEEP_FROM_DEVICE (-1) is a valid negative total
+    assert lib.tsel_select_topk(16, 10, 16, 1, 16, -2, 16, 16, 256, 1024, None) == 1
 
 
 def test_topk_and_gather_host_checks(lib):
