@@ -77,7 +77,7 @@ struct TileCfg {
   static constexpr int OFF_LSE = OFF_B + STAGES * TILE_BYTES;
   static constexpr int OFF_COMB = OFF_LSE + kLseSlots * kTile * 4;
   static constexpr int OFF_BAR = OFF_COMB + 2 * 2 * 2 * kTile * 4;
-  static constexpr int NUM_BARS = 2 + 2 + 2 * STAGES + 2 * kAccBufs + 2 * kLseSlots +
+  static constexpr int NUM_BARS = 2 + 2 + 2 * STAGES + 2 * kAccBufs + kLseSlots +
                                   2 * kSchedSlots + 4 + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 256 + 64 + 1024;  // + alignment slack
@@ -375,12 +375,15 @@ __device__ __forceinline__ void row_softmax_chunk(const uint32_t (&r)[32], int v
     for (int j = 0; j < 32; ++j) v[j] = j < valid ? v[j] : kNegInf;
   }
   float t0 = fmax3(v[0], v[1], v[2]), t1 = fmax3(v[3], v[4], v[5]);
+  float t2 = fmax3(v[6], v[7], v[8]), t3 = fmax3(v[9], v[10], v[11]);
 #pragma unroll
-  for (int j = 6; j < 30; j += 4) {
+  for (int j = 12; j < 28; j += 8) {
     t0 = fmax3(t0, v[j], v[j + 1]);
     t1 = fmax3(t1, v[j + 2], v[j + 3]);
+    t2 = fmax3(t2, v[j + 4], v[j + 5]);
+    t3 = fmax3(t3, v[j + 6], v[j + 7]);
   }
-  const float tmax = fmax3(t0, t1, fmaxf(v[30], v[31])) * c;
+  const float tmax = fmax3(fmax3(t0, t1, v[28]), fmax3(t2, t3, v[29]), fmaxf(v[30], v[31])) * c;
   if (tmax > m + 8.f) {
     // also covers the first chunk of a row (m = -inf, l = 0)
     const float s = ex2(m - tmax);
@@ -470,8 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* b_empty = b_full + S;
   uint64_t* acc_full = b_empty + S;
   uint64_t* acc_empty = acc_full + kAccBufs;
-  uint64_t* lse_full = acc_empty + kAccBufs;
-  uint64_t* lse_empty = lse_full + kLseSlots;
+  // The LSE slice of a B tile lands on that tile's b_full barrier; the
+  // epilogue reads it after acc_full, which the MMA thread commits only after
+  // it has seen b_full complete. lse_empty returns the slot to the producer.
+  uint64_t* lse_empty = acc_empty + kAccBufs;
   uint64_t* sch_full = lse_empty + kLseSlots;
   uint64_t* sch_empty = sch_full + kSchedSlots;
   uint64_t* comb_full = sch_empty + kSchedSlots;  // [A half][buf]
@@ -502,7 +507,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[i], 4);           // the owning warpgroup
     }
     for (int i = 0; i < kLseSlots; ++i) {
-      mbar_init(&lse_full[i], 1);
       mbar_init(&lse_empty[i], 8);           // both warpgroups of the B-tile parity
     }
     for (int i = 0; i < kSchedSlots; ++i) {
@@ -577,21 +581,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int bt = 0; bt < nbt; ++bt) {
               const int bs = b_it % S;
               if (!wait_bounded(&b_empty[bs], ((b_it / S) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
-              mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES);
+              const int ls = b_it % kLseSlots;
+              if (PASS == 2 &&
+                  !wait_bounded(&lse_empty[ls], ((b_it / kLseSlots) & 1) ^ 1, abort_flag, T)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES + (PASS == 2 ? kTile * 4 : 0));
               load_tile<D, FP8>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], bhead,
                                 (PASS == 1 ? w.k0 : w.q0) + bt * kTile);
-              if (PASS == 2) {
-                const int ls = b_it % kLseSlots;
-                if (!wait_bounded(&lse_empty[ls], ((b_it / kLseSlots) & 1) ^ 1, abort_flag, T)) {
-                  ++b_it;
-                  ok = false;
-                  break;
-                }
-                mbar_arrive_expect_tx(&lse_full[ls], kTile * 4);
+              if (PASS == 2)
                 bulk_load(sLse + ls * kTile,
                           p.nlse2 + int64_t(h) * p.lse_stride + int64_t(qtile_base + bt) * kTile,
-                          kTile * 4, &lse_full[ls]);
-              }
+                          kTile * 4, &b_full[bs]);
               ++b_it;
             }
           }
@@ -610,12 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = a_it - 1 - i;
         wait_drain(&a_full[n & 1], (n >> 1) & 1, T);
       }
-      if (PASS == 2) {
-        for (int i = 0; i < kLseSlots && i < b_it; ++i) {
-          const int n = b_it - 1 - i;
-          wait_drain(&lse_full[n % kLseSlots], (n / kLseSlots) & 1, T);
-        }
-      }
+
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -706,10 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t use = uint32_t(g >> 1) & 1u;
         if (!warp_wait(&acc_full[kbuf], use, abort_flag, T)) { ok = false; break; }
         const int ls = g & (kLseSlots - 1);
-        if (PASS == 2 && !warp_wait(&lse_full[ls], (g / kLseSlots) & 1, abort_flag, T)) {
-          ok = false;
-          break;
-        }
+
         tc_fence_after();
         if (mine) {
           const int valid = (PASS == 1 ? w.nk : w.nq) - bt * kTile;
