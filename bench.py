@@ -573,11 +573,23 @@ def gpu_arm(args) -> None:
         h2d = sum(v.numel() * v.element_size() for v in pin.values())
         d2h = sum(t.numel() * t.element_size() for t in (h_keep, h_cu, h_img, h_pos, h_cuk))
 
+        copy_stream = torch.cuda.Stream(dev)
+        late = ("hidden", "pos")     # needed only by the compaction
+
         def e2e_step():
+            # Q, K and metadata first; the hidden rows and positions cross the
+            # host link while the importance passes run (one link: copies in
+            # parallel would only share its bandwidth).
             for k2, v in pin.items():
-                dbuf[k2].copy_(v, non_blocking=True)
+                if k2 not in late:
+                    dbuf[k2].copy_(v, non_blocking=True)
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                for k2 in late:
+                    dbuf[k2].copy_(pin[k2], non_blocking=True)
             importance(0, dbuf["q"], dbuf["k"], dbuf["cu_q"], dbuf["cu_k"])
             topk(dbuf["req_off"], dbuf["keep"])
+            stream.wait_stream(copy_stream)
             gather(dbuf["hidden"], dbuf["pos"], dbuf["cu_k"])
             h_keep.copy_(keep_idx, non_blocking=True)
             h_cu.copy_(cu_keep, non_blocking=True)
@@ -599,8 +611,9 @@ def gpu_arm(args) -> None:
         e2e = {"value": replica_throughput(Tk, world, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms,
-               "note": "pinned host inputs copied in, importance+top-B+compaction, selection "
-                       "metadata copied out; compacted hidden rows stay on the device"}
+               "note": "pinned host inputs copied in (hidden rows and positions on a second "
+                       "stream, overlapping the importance passes), importance+top-B+compaction, "
+                       "selection metadata copied out; compacted hidden rows stay on the device"}
 
     # --- small requests: whole path replayed from one CUDA graph -------------
     small = {}
