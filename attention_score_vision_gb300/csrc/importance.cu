@@ -149,12 +149,26 @@ __device__ void bucket_positions_desc(int* key, int G, int* hist, int* warp_sums
   __syncthreads();
 }
 
+// Exclusive scan over the 32 lanes of a warp; `total` gets the sum.
+__device__ __forceinline__ int warp_excl_scan(int v, int& total) {
+  const int lane = threadIdx.x & 31;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  total = __shfl_sync(0xffffffffu, x, 31);
+  return x - v;
+}
+
 __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restrict__ cu_q,
                                                         const int32_t* __restrict__ cu_k, int G,
                                                         int Tq, int Tk, int max_q, int max_k,
                                                         int H, int HG, uint8_t* ws,
                                                         ImpWsLayout L) {
   __shared__ int bad;
+  __shared__ int totals[2];
   __shared__ int hist[1024];
   __shared__ int warp_sums[32];
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
@@ -169,6 +183,7 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
   int32_t* start2 = start1 + G;
   uint2* units1 = reinterpret_cast<uint2*>(ws + L.units1);
   uint2* units2 = reinterpret_cast<uint2*>(ws + L.units2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     bad = 0;
@@ -176,52 +191,118 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
     hdr->num_units[1] = 0;
     hdr->sched_ctr[0] = 0;
     hdr->sched_ctr[1] = 0;
-    if (cu_q[0] != 0 || cu_k[0] != 0 || cu_q[G] != Tq || cu_k[G] != Tk) bad = 1;
-  }
-  __syncthreads();
-  for (int g = threadIdx.x; g < G; g += 1024) {
-    const int nq = cu_q[g + 1] - cu_q[g];
-    const int nk = cu_k[g + 1] - cu_k[g];
-    if (nq < 0 || nk < 0 || nq > max_q || nk > max_k) atomicOr(&bad, 1);
-  }
-  __syncthreads();
-  if (bad) {
-    if (threadIdx.x == 0) set_status(&hdr->status, TSEL_DEV_SEQLENS);
-    return;
-  }
-  // Cost keys: a pass-1 unit walks all key tiles of its segment, a pass-2
-  // unit all query tiles (times the heads).
-  for (int g = threadIdx.x; g < G; g += 1024) {
-    const int nqt = int(ceil_div(cu_q[g + 1] - cu_q[g], kTile));
-    const int nkt = int(ceil_div(cu_k[g + 1] - cu_k[g], kTile));
-    pos1[g] = min(nkt, 1023);
-    pos2[g] = min(nqt, 1023);
-    qtile_off[g] = nqt;
-    kpair_off[g] = int(ceil_div(cu_k[g + 1] - cu_k[g], kPair));
   }
   for (int64_t i = threadIdx.x; i < L.n_grp; i += 1024) grp_ctr[i] = 0;
-  __syncthreads();
-  bucket_positions_desc(pos1, G, hist, warp_sums);
-  bucket_positions_desc(pos2, G, hist, warp_sums);
-  for (int g = threadIdx.x; g < G; g += 1024) {
-    const int nqp = int(ceil_div(cu_q[g + 1] - cu_q[g], kPair));
-    const int nkp = int(ceil_div(cu_k[g + 1] - cu_k[g], kPair));
-    inv1[pos1[g]] = g;
-    inv2[pos2[g]] = g;
-    start1[pos1[g]] = H * nqp;
-    start2[pos2[g]] = HG * nkp;
-  }
-  __syncthreads();
-  const int total1 = block_scan_array(start1, G, warp_sums);
-  const int total2 = block_scan_array(start2, G, warp_sums);
-  const int total_qt = block_scan_array(qtile_off, G, warp_sums);
-  const int total_kp = block_scan_array(kpair_off, G, warp_sums);
-  if (threadIdx.x == 0) {
-    qtile_off[G] = total_qt;
-    kpair_off[G] = total_kp;
+  if (G <= 32) {
+    // Few segments: one warp checks, orders and scans them with shuffles.
+    if (warp == 0) {
+      const bool act = lane < G;
+      const int nq = act ? cu_q[lane + 1] - cu_q[lane] : 0;
+      const int nk = act ? cu_k[lane + 1] - cu_k[lane] : 0;
+      bool b = act && (nq < 0 || nk < 0 || nq > max_q || nk > max_k);
+      if (lane == 0) b = b || cu_q[0] != 0 || cu_k[0] != 0 || cu_q[G] != Tq || cu_k[G] != Tk;
+      const bool any_bad = __any_sync(0xffffffffu, b);
+      if (lane == 0) bad = any_bad ? 1 : 0;
+      if (!any_bad) {
+        const int nqt = int(ceil_div(nq, kTile)), nkt = int(ceil_div(nk, kTile));
+        const int nqp = int(ceil_div(nq, kPair)), nkp = int(ceil_div(nk, kPair));
+        // rank in descending cost (pass 1: key tiles, pass 2: query tiles),
+        // ties by segment index; idle lanes rank last
+        const int key1 = act ? nkt : -1, key2 = act ? nqt : -1;
+        int r1 = 0, r2 = 0;
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+          const int k1 = __shfl_sync(0xffffffffu, key1, j);
+          const int k2 = __shfl_sync(0xffffffffu, key2, j);
+          r1 += (k1 > key1) || (k1 == key1 && j < lane);
+          r2 += (k2 > key2) || (k2 == key2 && j < lane);
+        }
+        hist[r1] = lane;            // hist[0..31]: segment at pass-1 rank
+        hist[32 + r2] = lane;       // hist[32..63]: segment at pass-2 rank
+        __syncwarp();
+        const int g1 = hist[lane], g2 = hist[32 + lane];
+        // every lane takes part in the shuffles (a shuffle inside the
+        // conditional would leave the idle lanes out of a full-mask exchange)
+        const int nqp_g1 = __shfl_sync(0xffffffffu, nqp, g1);
+        const int nkp_g2 = __shfl_sync(0xffffffffu, nkp, g2);
+        const int v1 = act ? H * nqp_g1 : 0;
+        const int v2 = act ? HG * nkp_g2 : 0;
+        int t1, t2, tq, tk;
+        const int s1 = warp_excl_scan(v1, t1);
+        const int s2 = warp_excl_scan(v2, t2);
+        const int oq = warp_excl_scan(nqt, tq);
+        const int ok = warp_excl_scan(nkp, tk);
+        if (act) {
+          inv1[lane] = g1;
+          inv2[lane] = g2;
+          start1[lane] = s1;
+          start2[lane] = s2;
+          qtile_off[lane] = oq;
+          kpair_off[lane] = ok;
+        }
+        if (lane == 0) {
+          qtile_off[G] = tq;
+          kpair_off[G] = tk;
+          totals[0] = t1;
+          totals[1] = t2;
+        }
+      }
+    }
+    __syncthreads();
+    if (bad) {
+      if (threadIdx.x == 0) set_status(&hdr->status, TSEL_DEV_SEQLENS);
+      return;
+    }
+  } else {
+    if (threadIdx.x == 0 &&
+        (cu_q[0] != 0 || cu_k[0] != 0 || cu_q[G] != Tq || cu_k[G] != Tk))
+      bad = 1;
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += 1024) {
+      const int nq = cu_q[g + 1] - cu_q[g];
+      const int nk = cu_k[g + 1] - cu_k[g];
+      if (nq < 0 || nk < 0 || nq > max_q || nk > max_k) atomicOr(&bad, 1);
+    }
+    __syncthreads();
+    if (bad) {
+      if (threadIdx.x == 0) set_status(&hdr->status, TSEL_DEV_SEQLENS);
+      return;
+    }
+    // Cost keys: a pass-1 unit walks all key tiles of its segment, a pass-2
+    // unit all query tiles (times the heads).
+    for (int g = threadIdx.x; g < G; g += 1024) {
+      const int nqt = int(ceil_div(cu_q[g + 1] - cu_q[g], kTile));
+      const int nkt = int(ceil_div(cu_k[g + 1] - cu_k[g], kTile));
+      pos1[g] = min(nkt, 1023);
+      pos2[g] = min(nqt, 1023);
+      qtile_off[g] = nqt;
+      kpair_off[g] = int(ceil_div(cu_k[g + 1] - cu_k[g], kPair));
+    }
+    __syncthreads();
+    bucket_positions_desc(pos1, G, hist, warp_sums);
+    bucket_positions_desc(pos2, G, hist, warp_sums);
+    for (int g = threadIdx.x; g < G; g += 1024) {
+      const int nqp = int(ceil_div(cu_q[g + 1] - cu_q[g], kPair));
+      const int nkp = int(ceil_div(cu_k[g + 1] - cu_k[g], kPair));
+      inv1[pos1[g]] = g;
+      inv2[pos2[g]] = g;
+      start1[pos1[g]] = H * nqp;
+      start2[pos2[g]] = HG * nkp;
+    }
+    __syncthreads();
+    const int total1 = block_scan_array(start1, G, warp_sums);
+    const int total2 = block_scan_array(start2, G, warp_sums);
+    const int total_qt = block_scan_array(qtile_off, G, warp_sums);
+    const int total_kp = block_scan_array(kpair_off, G, warp_sums);
+    if (threadIdx.x == 0) {
+      qtile_off[G] = total_qt;
+      kpair_off[G] = total_kp;
+      totals[0] = total1;
+      totals[1] = total2;
+    }
+    __syncthreads();
   }
   // Unit lists in descending-cost segment order.
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = warp; i < G; i += 32) {
     const int g = inv1[i];
     const int nqp = int(ceil_div(cu_q[g + 1] - cu_q[g], kPair));
@@ -243,8 +324,8 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    hdr->num_units[0] = total1;
-    hdr->num_units[1] = total2;
+    hdr->num_units[0] = totals[0];
+    hdr->num_units[1] = totals[1];
   }
 }
 
