@@ -437,51 +437,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag, timeout_ns));
 }
 
-// Online softmax of one query row over 32 columns of S (pass 1). Columns at
-// or beyond `valid` lie outside the segment. m is a reference max of S*c and l
-// the sum of exp2(S*c - m); m only moves when the chunk max exceeds it by
-// more than 8 (terms stay below 2^8), so rescaling is rare. Packed float2
-// arithmetic (one f32x2 FMA / ADD per two columns) around one MUFU exp2 per
-// column.
-template <bool FULL>
-__device__ __forceinline__ void row_softmax_chunk(const uint32_t (&r)[32], int valid, float c,
-                                                  float2 c2, float& m, float& l,
-                                                  float2 (&a)[2]) {
-  if (!FULL && valid <= 0) return;
-  float v[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-  if (!FULL && valid < 32) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = j < valid ? v[j] : kNegInf;
-  }
-  float t0 = fmax3(v[0], v[1], v[2]), t1 = fmax3(v[3], v[4], v[5]);
-  float t2 = fmax3(v[6], v[7], v[8]), t3 = fmax3(v[9], v[10], v[11]);
-#pragma unroll
-  for (int j = 12; j < 28; j += 8) {
-    t0 = fmax3(t0, v[j], v[j + 1]);
-    t1 = fmax3(t1, v[j + 2], v[j + 3]);
-    t2 = fmax3(t2, v[j + 4], v[j + 5]);
-    t3 = fmax3(t3, v[j + 6], v[j + 7]);
-  }
-  const float tmax = fmax3(fmax3(t0, t1, v[28]), fmax3(t2, t3, v[29]), fmaxf(v[30], v[31])) * c;
-  if (tmax > m + 8.f) {
-    // also covers the first chunk of a row (m = -inf, l = 0)
-    const float s = ex2(m - tmax);
-    l = (l + a[0].x + a[0].y + a[1].x + a[1].y) * s;
-    a[0] = make_float2(0.f, 0.f);
-    a[1] = make_float2(0.f, 0.f);
-    m = tmax;
-  }
-  if (m > kNegInf) {
-    const float2 nm2 = make_float2(-m, -m);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float2 x = __ffma2_rn(make_float2(v[2 * j], v[2 * j + 1]), c2, nm2);
-      a[j & 1] = __fadd2_rn(a[j & 1], make_float2(ex2(x.x), ex2(x.y)));
-    }
-  }
-}
 
 // Adds exp2(S*c - LSE2) of 32 query columns into the packed per-key
 // accumulators (pass 2). nl holds -LSE2 of those columns (-inf for padding).
@@ -502,6 +457,53 @@ __device__ __forceinline__ void column_sum_chunk(const uint32_t (&r)[32], const 
 }
 
 
+
+// Pass 1 (row LSE), on 32 columns held as raw TMEM words. Per query row, m
+// is a reference max of S*c and l the sum of exp2(S*c - m) before the
+// current accumulators a; m only moves when the max of the next 64 columns
+// exceeds it by more than 8 (terms stay below 2^8), so rescaling is rare.
+// Columns at or beyond `valid` lie outside the segment and read as -inf.
+__device__ __forceinline__ void mask_cols(uint32_t (&r)[32], int valid) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r[j] = j < valid ? r[j] : __float_as_uint(kNegInf);
+}
+
+__device__ __forceinline__ float cols_max(const uint32_t (&r)[32]) {
+#define V_(j) __uint_as_float(r[j])
+  float t0 = fmax3(V_(0), V_(1), V_(2)), t1 = fmax3(V_(3), V_(4), V_(5));
+  float t2 = fmax3(V_(6), V_(7), V_(8)), t3 = fmax3(V_(9), V_(10), V_(11));
+#pragma unroll
+  for (int j = 12; j < 28; j += 8) {
+    t0 = fmax3(t0, V_(j), V_(j + 1));
+    t1 = fmax3(t1, V_(j + 2), V_(j + 3));
+    t2 = fmax3(t2, V_(j + 4), V_(j + 5));
+    t3 = fmax3(t3, V_(j + 6), V_(j + 7));
+  }
+  return fmax3(fmax3(t0, t1, V_(28)), fmax3(t2, t3, V_(29)), fmaxf(V_(30), V_(31)));
+#undef V_
+}
+
+__device__ __forceinline__ void move_reference(float t, float& m, float& l, float2 (&a)[2]) {
+  if (t > m + 8.f) {   // also covers the first columns of a row (m = -inf, l = 0)
+    const float s = ex2(m - t);
+    const float2 a01 = __fadd2_rn(a[0], a[1]);
+    l = (l + (a01.x + a01.y)) * s;
+    a[0] = make_float2(0.f, 0.f);
+    a[1] = make_float2(0.f, 0.f);
+    m = t;
+  }
+}
+
+__device__ __forceinline__ void cols_exp_sum(const uint32_t (&r)[32], float2 c2, float2 nm2,
+                                             float2 (&a)[2]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
+                                c2, nm2);
+    a[j & 1] = __fadd2_rn(a[j & 1], make_float2(ex2(x.x), ex2(x.y)));
+  }
+}
+
 // One 128-column accumulator: two 32-column pieces in flight; the
 // accumulator is handed back to the MMA once all of it is in registers.
 // FULL: all 128 columns lie inside the segment (no masking).
@@ -514,21 +516,47 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int valid, const f
   tmem_ld32_async(taddr + 32, r1);
   tmem_wait_ld(r0);
   tmem_wait_ld(r1);
-  if (PASS == 1) row_softmax_chunk<FULL>(r0, valid, c, c2, m, l, acc);
-  else if (FULL || valid > 0) column_sum_chunk(r0, nl, c2, acc);
-  tmem_ld32_async(taddr + 64, r0);
-  if (PASS == 1) row_softmax_chunk<FULL>(r1, valid - 32, c, c2, m, l, acc);
-  else if (FULL || valid > 32) column_sum_chunk(r1, nl + 8, c2, acc);
-  tmem_ld32_async(taddr + 96, r1);
-  tmem_wait_ld(r0);
-  tmem_wait_ld(r1);
-  tc_fence_before();
-  __syncwarp();
-  mbar_arrive_lane0(acc_empty, lane);
-  if (PASS == 1) row_softmax_chunk<FULL>(r0, valid - 64, c, c2, m, l, acc);
-  else if (FULL || valid > 64) column_sum_chunk(r0, nl + 16, c2, acc);
-  if (PASS == 1) row_softmax_chunk<FULL>(r1, valid - 96, c, c2, m, l, acc);
-  else if (FULL || valid > 96) column_sum_chunk(r1, nl + 24, c2, acc);
+  if constexpr (PASS == 1) {
+    // row max over 64 columns at a time: one reference move per 64 columns
+    // and the exps of both 32-column pieces independent of each other
+    if (!FULL) {
+      mask_cols(r0, valid);
+      mask_cols(r1, valid - 32);
+    }
+    move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
+    float2 nm2 = make_float2(-m, -m);
+    cols_exp_sum(r0, c2, nm2, acc);
+    tmem_ld32_async(taddr + 64, r0);
+    if (FULL || valid > 32) cols_exp_sum(r1, c2, nm2, acc);
+    tmem_ld32_async(taddr + 96, r1);
+    tmem_wait_ld(r0);
+    tmem_wait_ld(r1);
+    tc_fence_before();
+    __syncwarp();
+    mbar_arrive_lane0(acc_empty, lane);
+    if (FULL || valid > 64) {
+      if (!FULL) {
+        mask_cols(r0, valid - 64);
+        mask_cols(r1, valid - 96);
+      }
+      move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
+      nm2 = make_float2(-m, -m);
+      cols_exp_sum(r0, c2, nm2, acc);
+      if (FULL || valid > 96) cols_exp_sum(r1, c2, nm2, acc);
+    }
+  } else {
+    if (FULL || valid > 0) column_sum_chunk(r0, nl, c2, acc);
+    tmem_ld32_async(taddr + 64, r0);
+    if (FULL || valid > 32) column_sum_chunk(r1, nl + 8, c2, acc);
+    tmem_ld32_async(taddr + 96, r1);
+    tmem_wait_ld(r0);
+    tmem_wait_ld(r1);
+    tc_fence_before();
+    __syncwarp();
+    mbar_arrive_lane0(acc_empty, lane);
+    if (FULL || valid > 64) column_sum_chunk(r0, nl + 16, c2, acc);
+    if (FULL || valid > 96) column_sum_chunk(r1, nl + 24, c2, acc);
+  }
 }
 
 template <int PASS, int D, bool FP8>
