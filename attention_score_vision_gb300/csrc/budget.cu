@@ -22,7 +22,7 @@
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
-#include "cluster_util.cuh"
+#include "launch_util.cuh"
 #include "common.cuh"
 
 namespace cg = cooperative_groups;
@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(kBudgetThreads)
   const int csize = int(cluster.num_blocks());
   const int r = int(blockIdx.x) / csize;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
+  pdl_wait();
 
   const int lo = req_off[r], hi = req_off[r + 1];
   if (tid == 0) {

@@ -102,6 +102,16 @@ __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
   atomicOr(status, bits);
 }
 
+// Programmatic dependent launch: let the next kernel on the stream launch
+// (its CTAs then wait in pdl_wait) ...
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ... and wait until the previous kernel on the stream has completed and its
+// memory is visible (returns at once for a kernel launched without PDL).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // fp32 bits -> uint32 with the same order; -0 maps to +0.
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);

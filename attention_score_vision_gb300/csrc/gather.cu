@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "launch_util.cuh"
 
 namespace tsel {
 
@@ -48,6 +49,8 @@ __global__ void __launch_bounds__(kGatherThreads)
                   int32_t* __restrict__ out_img, int32_t* __restrict__ out_cu,
                   uint32_t* status) {
   const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait();
   if (K_dev != nullptr) {
     // kept count produced on the device; K is the capacity the launch was sized for
     const int kd = __ldg(K_dev);
@@ -97,11 +100,10 @@ cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_
   const int64_t max_blocks = int64_t(num_sms) * (2048 / kGatherThreads);
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
-  gather_kernel<<<int(blocks), kGatherThreads, 0, stream>>>(
-      static_cast<const uint8_t*>(hidden), row_stride_bytes, row_bytes / 16, pos, pos_dim, cu_k,
-      G, Tk, keep_idx, K, K_dev, static_cast<uint8_t*>(out_hidden), out_pos, out_img, out_cu,
-      status);
-  return cudaPeekAtLastError();
+  return launch_kernel(gather_kernel, dim3(unsigned(blocks)), kGatherThreads, 0, stream, 1,
+                       static_cast<const uint8_t*>(hidden), row_stride_bytes, row_bytes / 16, pos,
+                       pos_dim, cu_k, G, Tk, keep_idx, K, K_dev, static_cast<uint8_t*>(out_hidden),
+                       out_pos, out_img, out_cu, status);
 }
 
 }  // namespace tsel

@@ -42,6 +42,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "launch_util.cuh"
 #include "ptx.cuh"
 
 namespace tsel {
@@ -184,6 +185,8 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
   uint2* units1 = reinterpret_cast<uint2*>(ws + L.units1);
   uint2* units2 = reinterpret_cast<uint2*>(ws + L.units2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  pdl_wait();   // cu_seqlens and the workspace belong to earlier kernels until here
 
   if (threadIdx.x == 0) {
     bad = 0;
@@ -640,6 +643,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Prologue done: the next kernel may launch; wait for the schedule kernel
+  // (unit lists) and, in pass 2, the row-LSE pass.
+  pdl_launch_dependents();
+  pdl_wait();
   const int total_units = *reinterpret_cast<const volatile int*>(p.num_units);
   const int group = p.H / p.Hkv;
 
@@ -927,6 +934,8 @@ __global__ void __launch_bounds__(kTile) imp_lse_import_kernel(
     const float* __restrict__ lse_in, int Tq, const int32_t* __restrict__ cu_q, int G,
     const int32_t* __restrict__ qtile_off, float* __restrict__ nlse2, int64_t lse_stride,
     const uint32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   if (*reinterpret_cast<const volatile uint32_t*>(status) & TSEL_DEV_SEQLENS) return;
   const int t = blockIdx.x, h = blockIdx.y;
   const int total = qtile_off[G];
@@ -955,8 +964,8 @@ __global__ void __launch_bounds__(kTile) imp_lse_import_kernel(
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
                             int max_q, int max_k, int H, int HG, uint8_t* ws,
                             const ImpWsLayout& L, cudaStream_t stream) {
-  imp_prep_kernel<<<1, 1024, 0, stream>>>(cu_q, cu_k, G, Tq, Tk, max_q, max_k, H, HG, ws, L);
-  return cudaPeekAtLastError();
+  return launch_kernel(imp_prep_kernel, dim3(1), 1024, 0, stream, 1, cu_q, cu_k, G, Tq, Tk, max_q,
+                       max_k, H, HG, ws, L);
 }
 
 template <int PASS, int D, bool FP8>
@@ -973,17 +982,16 @@ static cudaError_t launch_pass_t(const CUtensorMap* maps, const ImpPassParams& p
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 128) attr_set[dev] = true;
   }
-  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
-  return cudaPeekAtLastError();
+  return launch_kernel(kern, dim3(unsigned(grid)), kThreads, size_t(C::SMEM_BYTES), stream, 1,
+                       maps[0], maps[1], maps[2], maps[3], p);
 }
 
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
                               const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
                               int max_qtiles, int H, const uint32_t* status, cudaStream_t stream) {
   if (max_qtiles <= 0) return cudaSuccess;
-  imp_lse_import_kernel<<<dim3(unsigned(max_qtiles), unsigned(H)), kTile, 0, stream>>>(
-      lse_in, Tq, cu_q, G, qtile_off, nlse2, lse_stride, status);
-  return cudaPeekAtLastError();
+  return launch_kernel(imp_lse_import_kernel, dim3(unsigned(max_qtiles), unsigned(H)), kTile, 0,
+                       stream, 1, lse_in, Tq, cu_q, G, qtile_off, nlse2, lse_stride, status);
 }
 
 // maps: A64, A16, B64, B16 (pass 1: A = Q, B = K; pass 2: A = K, B = Q). For

@@ -1,6 +1,14 @@
-// Cluster-size helpers shared by the per-request cluster kernels (top-B and
-// dynamic budget): one thread-block cluster per request, sized from the
-// average request length, capped by what the device can co-schedule.
+// Launch helpers shared by every kernel of the library.
+//
+// Every kernel is launched with programmatic stream serialization (PDL): the
+// next kernel on the stream may start its prologue while the previous one
+// drains. Each kernel therefore calls pdl_launch_dependents() once all of its
+// CTAs are resident and pdl_wait() before it touches memory that an earlier
+// kernel on the stream writes or reads, so stream order holds for data.
+//
+// Cluster kernels (top-B, dynamic budget) run one thread-block cluster per
+// request, sized from the average request length and capped by what the
+// device can co-schedule.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -59,25 +67,41 @@ int usable_cluster_size(Kernel kernel, int want, int threads, size_t dyn, int (*
   return csize;
 }
 
+// Launches `kernel` on `stream` with programmatic stream serialization and,
+// when cluster_x > 1, clusters of cluster_x CTAs along x.
+template <typename Kernel, typename... Args>
+cudaError_t launch_kernel(Kernel kernel, dim3 grid, int threads, size_t dyn, cudaStream_t stream,
+                          int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(unsigned(threads));
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = unsigned(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = unsigned(n);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaPeekAtLastError();
+}
+
 // Launches `kernel` with one cluster of `csize` CTAs per request.
 template <typename Kernel, typename... Args>
 cudaError_t launch_clusters(Kernel kernel, int num_req, int csize, int threads, size_t dyn,
                             cudaStream_t stream, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(num_req) * unsigned(csize));
-  cfg.blockDim = dim3(unsigned(threads));
-  cfg.dynamicSmemBytes = dyn;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(csize);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
-  if (e != cudaSuccess) return e;
-  return cudaPeekAtLastError();
+  return launch_kernel(kernel, dim3(unsigned(num_req) * unsigned(csize)), threads, dyn, stream,
+                       csize, args...);
 }
 
 }  // namespace tsel

@@ -20,7 +20,7 @@
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
-#include "cluster_util.cuh"
+#include "launch_util.cuh"
 #include "common.cuh"
 
 namespace cg = cooperative_groups;
@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int csize = int(cluster.num_blocks());
   const int r = int(blockIdx.x) / csize;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
+  pdl_wait();
 
   // ---- request checks and output offset (identical in every CTA) --------
   int part = 0, neg = 0;

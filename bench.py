@@ -428,9 +428,10 @@ def gpu_arm(args) -> None:
     if tsel.tsel_read_device_status(ws) != 0:
         raise RuntimeError("device status set during warm-up")
 
-    # --- timed (device-resident inputs) -------------------------------------
-    names = ["prep", "pass1", "pass2", "topk", "gather"]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    # --- timed (device-resident inputs): the whole path per step, events only
+    # around it, so consecutive kernels overlap launch and drain (PDL) as in use
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
@@ -439,7 +440,32 @@ def gpu_arm(args) -> None:
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
-        e = evs[i]
+        evs[i][0].record(stream)
+        importance(0)
+        topk()
+        gather()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    status = tsel.tsel_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status 0x{status:x} after the timed loop")
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = reduce_max_over_ranks(ms_local, dev)
+    value = replica_throughput(Tk, world, ms)
+
+    # --- per-kernel times: the same steps with an event between the stages
+    # (events break the launch overlap, so these are each kernel alone) -------
+    names = ["prep", "pass1", "pass2", "topk", "gather"]
+    n_stage = max(5, min(args.steps, 50))
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_stage)]
+    for i in range(n_stage):
+        flush.fill_(i & 0xFF)
+        e = sevs[i]
         e[0].record(stream)
         importance(S1)
         e[1].record(stream)
@@ -452,22 +478,12 @@ def gpu_arm(args) -> None:
         gather()
         e[5].record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    wall = time.perf_counter() - wall0
-    clocks = sampler.stop()
     per = {n: [] for n in names}
-    step_ms = []
-    for e in evs:
+    for e in sevs:
         for j, n in enumerate(names):
             per[n].append(e[j].elapsed_time(e[j + 1]))
-        step_ms.append(e[0].elapsed_time(e[5]))
-    status = tsel.tsel_read_device_status(ws)
-    if status != 0:
-        raise RuntimeError(f"device status 0x{status:x} after the timed loop")
-    ms_local = sum(step_ms) / len(step_ms)
-    ms = reduce_max_over_ranks(ms_local, dev)
-    value = replica_throughput(Tk, world, ms)
+    if tsel.tsel_read_device_status(ws) != 0:
+        raise RuntimeError("device status set in the per-kernel loop")
 
     # --- LSE-provided mode: the attention kernel's LSE reused, column pass only ---
     lse_given = lse.clone()
@@ -699,6 +715,9 @@ def gpu_arm(args) -> None:
         "importance_roofline_frac": imp_roof / t_imp,
         "roofline": roofline,
         "kernels": kernels,
+        "kernel_timing": (f"per-kernel times from {n_stage} further steps with an event between "
+                          "the stages (each kernel alone, no launch overlap); the headline step "
+                          "has events only around the whole path"),
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "lse_provided": lse_provided,
