@@ -29,11 +29,14 @@ if ROOT not in sys.path:
 METRIC = "vision tokens scored+selected/sec at 1 GB300; importance % of roofline"
 DEFAULT_WORKLOAD = "thirty_images"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["attention_score_vision_gb300/csrc/importance.cu",
-                  "attention_score_vision_gb300/csrc/topk.cu",
-                  "attention_score_vision_gb300/csrc/gather.cu",
-                  "attention_score_vision_gb300/csrc/ptx.cuh",
-                  "attention_score_vision_gb300/csrc/common.cuh"]
+_CSRC = "attention_score_vision_gb300/csrc/"
+# Sources each kernel is built from (a traffic figure taken on other sources reads as null).
+KERNEL_SOURCES = {
+    "imp_pass_kernel": [_CSRC + f for f in ("importance.cu", "ptx.cuh", "common.cuh",
+                                            "launch_util.cuh")],
+    "topk_cluster_kernel": [_CSRC + f for f in ("topk.cu", "common.cuh", "launch_util.cuh")],
+    "gather_kernel": [_CSRC + f for f in ("gather.cu", "common.cuh", "launch_util.cuh")],
+}
 
 
 def parse_args(argv=None):
@@ -243,7 +246,7 @@ def load_traffic(kernel: str, workload: str):
     with open(p) as fh:
         d = json.load(fh)
     e = d.get(kernel, {}).get(workload)
-    if not e or e.get("src_hash") != src_hash(KERNEL_SOURCES):
+    if not e or e.get("src_hash") != src_hash(KERNEL_SOURCES[kernel.split("<")[0]]):
         return None
     return e.get("bytes_per_launch")
 
