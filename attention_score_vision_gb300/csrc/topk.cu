@@ -8,15 +8,17 @@
 // One thread-block cluster per request (up to 16 CTAs, one slice of the
 // request's tokens each, cached in shared memory):
 //   1. radix select, 8 bits per round from the top: every CTA builds
-//      warp-private histograms of its slice, adds them into CTA 0's histogram
-//      through distributed shared memory, and after one cluster barrier every
-//      CTA reads the merged histogram and picks the same digit. After four
-//      rounds the key of the B-th largest score is known (keys are fp32 bits
-//      mapped to an order-preserving uint32);
-//   2. each CTA counts its keys above / equal to that key, the counts are
-//      exchanged the same way, and each CTA writes its kept indices in index
-//      order through block-wide prefix sums: tokens above the key, and the
-//      lowest-index tokens equal to it. The output is deterministic.
+//      warp-private histograms of its slice and adds bin b into CTA
+//      (b % cluster size) through distributed shared memory (the merge is
+//      spread over the cluster); after one cluster barrier every CTA reads the
+//      merged bins and picks the same digit. After four rounds the key of the
+//      B-th largest score is known (keys are fp32 bits mapped to an
+//      order-preserving uint32);
+//   2. each CTA's counts of keys above / equal to that key follow from its
+//      own per-round histograms; they are sent to every CTA, and each CTA
+//      writes its kept indices in index order through block-wide prefix sums:
+//      tokens above the key, and the lowest-index tokens equal to it. The
+//      output is deterministic.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -63,8 +65,8 @@ __device__ __forceinline__ int topk_block_scan(int v, int* warp_sums, int& total
 
 struct TopkShared {
   int whist[kTopkWarps][256];      // warp-private histograms
-  int hist[4][256];                // merged histograms (rank 0's copy is the one used)
-  int cnt_gt[kTopkMaxCluster];     // per-CTA counts above / equal to the threshold (rank 0)
+  int hist[4][256];                // merged histograms (bin b lives in CTA b % csize)
+  int cnt_gt[kTopkMaxCluster];     // every CTA's counts above / equal to the threshold
   int cnt_eq[kTopkMaxCluster];
   int warp_sums[32];
   int digit, above, bad, nan_seen;
@@ -157,9 +159,13 @@ __global__ void __launch_bounds__(kTopkThreads)
   __syncthreads();
 
   // ---- radix select -------------------------------------------------------
-  int* hist0 = cluster.map_shared_rank(&sh.hist[0][0], 0);
+  // Bin b of each round is merged in CTA (b % csize), so the merge spreads
+  // over the cluster instead of queueing at one SM. Thread t keeps this
+  // CTA's count of bin t, from which the counts above / at the threshold
+  // follow without another pass over the keys.
   uint32_t prefix = 0, mask = 0;
   int remaining = B;  // how many still to take among keys matching `prefix`
+  int gt_part = 0, eq_part = 0;   // this CTA: keys above / equal to the threshold (bin tid)
 #pragma unroll 1
   for (int round = 0; round < 4; ++round) {
     const int shift = 24 - 8 * round;
@@ -176,12 +182,10 @@ __global__ void __launch_bounds__(kTopkThreads)
       if (match && (__ffs(peers) - 1) == lane) atomicAdd(&sh.whist[warp][d], __popc(peers));
     }
     __syncthreads();
-    {
-      int v = 0;
+    int v = 0;   // this CTA's count of bin tid
 #pragma unroll
-      for (int w = 0; w < kTopkWarps; ++w) v += sh.whist[w][tid];
-      if (v) atomicAdd(hist0 + round * 256 + tid, v);   // into CTA 0's shared memory
-    }
+    for (int w = 0; w < kTopkWarps; ++w) v += sh.whist[w][tid];
+    if (v) atomicAdd(cluster.map_shared_rank(&sh.hist[round][tid], tid % csize), v);
     cluster.sync();
     if (warp == 0) {
       // lane l owns bins 255-8l ... 248-8l (descending)
@@ -189,7 +193,8 @@ __global__ void __launch_bounds__(kTopkThreads)
       int sum = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = hist0[round * 256 + 255 - 8 * lane - j];
+        const int b = 255 - 8 * lane - j;
+        c[j] = *cluster.map_shared_rank(&sh.hist[round][b], b % csize);
         sum += c[j];
       }
       const int incl = warp_incl_scan(sum);
@@ -209,7 +214,10 @@ __global__ void __launch_bounds__(kTopkThreads)
       }
     }
     __syncthreads();
-    prefix |= uint32_t(sh.digit) << shift;
+    const int digit = sh.digit;
+    gt_part += tid > digit ? v : 0;
+    if (round == 3) eq_part = tid == digit ? v : 0;
+    prefix |= uint32_t(digit) << shift;
     mask |= 255u << shift;
     remaining -= sh.above;
     __syncthreads();
@@ -218,35 +226,30 @@ __global__ void __launch_bounds__(kTopkThreads)
   const uint32_t thr = prefix;
   const int need_eq = remaining;  // tokens equal to the threshold to keep (request-wide)
 
-  // ---- per-CTA counts, exchanged through CTA 0 -----------------------------
-  int gt = 0, eq = 0;
-  for (int i = tid; i < len; i += kTopkThreads) {
-    const uint32_t k = cached ? skeys[i] : order_key(s[i]);
-    gt += k > thr;
-    eq += k == thr;
-  }
+  // ---- per-CTA counts, sent to every CTA of the cluster ----------------------
   int gt_total, eq_total;
-  (void)topk_block_scan(gt, sh.warp_sums, gt_total);
-  (void)topk_block_scan(eq, sh.warp_sums, eq_total);
-  if (tid == 0) {
-    int* rg = cluster.map_shared_rank(&sh.cnt_gt[0], 0);
-    int* re = cluster.map_shared_rank(&sh.cnt_eq[0], 0);
-    rg[crank] = gt_total;
-    re[crank] = eq_total;
+  (void)topk_block_scan(gt_part, sh.warp_sums, gt_total);
+  (void)topk_block_scan(eq_part, sh.warp_sums, eq_total);
+  if (tid < csize) {
+    *cluster.map_shared_rank(&sh.cnt_gt[crank], tid) = gt_total;
+    *cluster.map_shared_rank(&sh.cnt_eq[crank], tid) = eq_total;
   }
-  cluster.sync();
-  int out_base = 0, eq_before = 0;
-  {
-    const int* rg = cluster.map_shared_rank(&sh.cnt_gt[0], 0);
-    const int* re = cluster.map_shared_rank(&sh.cnt_eq[0], 0);
-    for (int c = 0; c < crank; ++c) {
-      const int e = re[c];
-      const int take = max(0, min(e, need_eq - eq_before));
-      out_base += rg[c] + take;
-      eq_before += e;
+  cluster.sync();   // no CTA reads another CTA's shared memory after this point
+  if (warp == 0) {
+    // lane c: CTA c's counts; exclusive prefixes give this CTA's output slot
+    const int e = lane < csize ? sh.cnt_eq[lane] : 0;
+    const int g = lane < csize ? sh.cnt_gt[lane] : 0;
+    const int e_incl = warp_incl_scan(e);
+    const int e_before = e_incl - e;
+    const int take = max(0, min(e, need_eq - e_before));
+    const int t_incl = warp_incl_scan(g + take);
+    if (lane == crank) {
+      sh.above = t_incl - (g + take);   // output slots of CTAs before this one
+      sh.digit = e_before;              // tied tokens in CTAs before this one
     }
   }
-  cluster.sync();   // CTA 0's shared memory is no longer read after this point
+  __syncthreads();
+  const int out_base = sh.above, eq_before = sh.digit;
 
   // ---- compaction in index order --------------------------------------------
   int32_t* out = keep_idx + before + out_base;
