@@ -13,8 +13,9 @@
 // One thread-block cluster per request (up to 16 CTAs, one slice of the
 // request each, its keys cached in shared memory): the slice maxima meet in
 // CTA 0 (distributed shared memory) and give E; then four 8-bit radix rounds
-// over the order-preserving score keys build (count, quanta) histograms,
-// merged into CTA 0, from which every CTA picks the same digit. The first
+// over the order-preserving score keys build (count, quanta) histograms, bin
+// b merged in CTA (b % cluster size), from which every CTA picks the same
+// digit. The first
 // round's histogram also gives the request total M and the target T. After
 // the last round the key of the token that crosses T is known exactly; the
 // tokens tied on it carry equal quanta, so the number of them needed is one
@@ -60,7 +61,7 @@ __device__ __forceinline__ uint32_t quantum_of_key(uint32_t key, int E) {
 }
 
 struct BudgetShared {
-  int cnt[4][256];                   // merged histograms (CTA 0's copy is the one used)
+  int cnt[4][256];                   // merged histograms (bin b lives in CTA b % csize)
   unsigned long long mass[4][256];
   int lcnt[256];                     // this CTA's histogram of the current round
   unsigned long long lmass[256];
@@ -146,8 +147,6 @@ __global__ void __launch_bounds__(kBudgetThreads)
   const int E = smax_bits != 0 ? score_exponent(smax_bits) : 0;
 
   // ---- radix rounds on the score key, (count, quanta) histograms ---------
-  int* cnt0 = cluster.map_shared_rank(&sh.cnt[0][0], 0);
-  unsigned long long* mass0 = cluster.map_shared_rank(&sh.mass[0][0], 0);
   uint32_t prefix = 0, mask = 0;
   unsigned long long need = 0;   // quanta still to collect among keys matching prefix
   int cnt_above = 0;
@@ -178,9 +177,9 @@ __global__ void __launch_bounds__(kBudgetThreads)
     }
     __syncthreads();
     for (int b = tid; b < 256; b += kBudgetThreads) {
-      if (sh.lcnt[b]) {   // into CTA 0's shared memory
-        atomicAdd(cnt0 + round * 256 + b, sh.lcnt[b]);
-        atomicAdd(mass0 + round * 256 + b, sh.lmass[b]);
+      if (sh.lcnt[b]) {   // bin b is merged in CTA b % csize
+        atomicAdd(cluster.map_shared_rank(&sh.cnt[round][b], b % csize), sh.lcnt[b]);
+        atomicAdd(cluster.map_shared_rank(&sh.mass[round][b], b % csize), sh.lmass[b]);
       }
     }
     cluster.sync();
@@ -190,8 +189,9 @@ __global__ void __launch_bounds__(kBudgetThreads)
       int c8[8], csum = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        m8[j] = mass0[round * 256 + 255 - 8 * lane - j];
-        c8[j] = cnt0[round * 256 + 255 - 8 * lane - j];
+        const int b = 255 - 8 * lane - j;
+        m8[j] = *cluster.map_shared_rank(&sh.mass[round][b], b % csize);
+        c8[j] = *cluster.map_shared_rank(&sh.cnt[round][b], b % csize);
         msum += m8[j];
         csum += c8[j];
       }
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kBudgetThreads)
     keep_out[r] = int32_t(b_dyn);
     if (total_out != nullptr) atomicAdd(total_out, int32_t(b_dyn));
   }
-  cluster.sync();   // CTA 0's shared memory is no longer read after this point
+  cluster.sync();   // no CTA's shared memory is read remotely after this point
 }
 
 cudaError_t launch_budget(const float* scores, int total_tokens, const int32_t* req_off,
