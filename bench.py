@@ -133,6 +133,16 @@ def cpu_rate(res: dict) -> float:
     return res["full_tokens"] / t_full
 
 
+def workload_config(w, workload: str, world: int, l2: str) -> dict:
+    """The `config` object both arms report for one workload."""
+    return {"workload": workload, "images": w.num_seg, "visual_tokens": w.total_k,
+            "query_tokens": w.total_q, "heads": w.num_heads, "kv_heads": w.num_kv_heads,
+            "head_dim": w.head_dim, "hidden": int(w.hidden_bits.shape[1]),
+            "pos_dim": int(w.pos.shape[1]), "keep_total": w.total_keep,
+            "requests": int(w.keep_per_req.size), "attended_pairs": w.attended_pairs(),
+            "l2": l2, "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def reference_arm(args) -> None:
     """The fp64 oracle, as it stands, on a bounded sample per step (1 core)."""
     rank = int(os.environ.get("RANK", "0"))
@@ -158,7 +168,7 @@ def reference_arm(args) -> None:
             "ms_per_step": 1e3 * statistics.median(r["seconds"] for r in res),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": args.workload, "l2": "n/a (CPU)", "parallelism": "replicas"},
+            "config": workload_config(w, args.workload, args.gpus, "n/a (host cores)"),
             "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -710,11 +720,8 @@ def gpu_arm(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": args.workload, "images": G, "visual_tokens": Tk,
-                   "query_tokens": Tq, "heads": H, "kv_heads": Hkv, "head_dim": hd,
-                   "hidden": D, "pos_dim": P, "keep_total": K, "requests": R,
-                   "attended_pairs": E, "l2": "flushed (512 MiB write) between steps, untimed",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": workload_config(w, args.workload, world,
+                                  "flushed (512 MiB write) between steps, untimed"),
         "importance_roofline_frac": imp_roof / t_imp,
         "roofline": roofline,
         "kernels": kernels,
