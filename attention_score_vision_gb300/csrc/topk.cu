@@ -31,7 +31,7 @@ namespace tsel {
 
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkItems = 4;               // consecutive tokens per thread when compacting
+constexpr int kTopkItems = 16;              // consecutive tokens per thread when compacting
 constexpr int kTopkMaxCluster = kMaxClusterCtas;
 constexpr int kTopkCacheKeys = 16384;       // keys cached in shared memory per CTA
 
@@ -252,22 +252,41 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int out_base = sh.above, eq_before = sh.digit;
 
   // ---- compaction in index order --------------------------------------------
+  // kTopkItems consecutive tokens per thread; one block scan per pass gives
+  // both the tied tokens (for their rank) and the tokens above the threshold
+  // in front of each thread (16-bit halves: a pass has <= 4096 tokens).
   int32_t* out = keep_idx + before + out_base;
   int written = 0, eq_seen = eq_before;
   for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkItems) {
     const int ib = i0 + tid * kTopkItems;
     uint32_t k[kTopkItems];
-    int n_eq = 0;
+    if (cached && ib + kTopkItems <= len) {
+#pragma unroll
+      for (int j = 0; j < kTopkItems; j += 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(skeys + ib + j);
+        k[j] = v.x;
+        k[j + 1] = v.y;
+        k[j + 2] = v.z;
+        k[j + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kTopkItems; ++j) {
+        const int i = ib + j;
+        k[j] = i < len ? (cached ? skeys[i] : order_key(s[i])) : 0u;
+      }
+    }
+    int n_eq = 0, n_gt = 0;
 #pragma unroll
     for (int j = 0; j < kTopkItems; ++j) {
-      const int i = ib + j;
-      k[j] = i < len ? (cached ? skeys[i] : order_key(s[i])) : 0u;
-      n_eq += (i < len) && k[j] == thr;
+      const bool valid = ib + j < len;
+      n_eq += valid && k[j] == thr;
+      n_gt += valid && k[j] > thr;
     }
-    int eqt;
-    int eq_rank = eq_seen + topk_block_scan(n_eq, sh.warp_sums, eqt);
-    bool take[kTopkItems];
-    int n_take = 0;
+    int tot;
+    const int pre = topk_block_scan((n_eq << 16) | n_gt, sh.warp_sums, tot);
+    int eq_rank = eq_seen + (pre >> 16);
+    int pos = written + (pre & 0xFFFF) + max(0, min(pre >> 16, need_eq - eq_seen));
 #pragma unroll
     for (int j = 0; j < kTopkItems; ++j) {
       const bool valid = ib + j < len;
@@ -276,17 +295,11 @@ __global__ void __launch_bounds__(kTopkThreads)
         t = eq_rank < need_eq;
         ++eq_rank;
       }
-      take[j] = t;
-      n_take += t;
+      if (t) out[pos++] = lo + c0 + ib + j;
     }
-    int take_total;
-    int pos = written + topk_block_scan(n_take, sh.warp_sums, take_total);
-#pragma unroll
-    for (int j = 0; j < kTopkItems; ++j) {
-      if (take[j]) out[pos++] = lo + c0 + ib + j;
-    }
-    written += take_total;
-    eq_seen += eqt;
+    const int tot_eq = tot >> 16, tot_gt = tot & 0xFFFF;
+    written += tot_gt + max(0, min(tot_eq, need_eq - eq_seen));
+    eq_seen += tot_eq;
   }
 }
 
