@@ -29,7 +29,8 @@ namespace cg = cooperative_groups;
 
 namespace tsel {
 
-constexpr int kTopkThreads = 256;
+constexpr int kTopkThreads = 512;
+static_assert(kTopkThreads >= 256, "one thread per histogram bin");
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkItems = 16;              // consecutive tokens per thread when compacting
 constexpr int kTopkMaxCluster = kMaxClusterCtas;
@@ -182,9 +183,11 @@ __global__ void __launch_bounds__(kTopkThreads)
       if (match && (__ffs(peers) - 1) == lane) atomicAdd(&sh.whist[warp][d], __popc(peers));
     }
     __syncthreads();
-    int v = 0;   // this CTA's count of bin tid
+    int v = 0;   // this CTA's count of bin tid (threads >= 256 hold no bin)
+    if (tid < 256) {
 #pragma unroll
-    for (int w = 0; w < kTopkWarps; ++w) v += sh.whist[w][tid];
+      for (int w = 0; w < kTopkWarps; ++w) v += sh.whist[w][tid];
+    }
     if (v) atomicAdd(cluster.map_shared_rank(&sh.hist[round][tid], tid % csize), v);
     cluster.sync();
     if (warp == 0) {
