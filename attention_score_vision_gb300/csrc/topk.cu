@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int crank = int(cluster.block_rank());
   const int csize = int(cluster.num_blocks());
   const int r = int(blockIdx.x) / csize;
+  const bool solo = csize == 1;   // one CTA: plain block barriers, no exchange
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch_dependents();
   pdl_wait();
@@ -188,8 +189,13 @@ __global__ void __launch_bounds__(kTopkThreads)
 #pragma unroll
       for (int w = 0; w < kTopkWarps; ++w) v += sh.whist[w][tid];
     }
-    if (v) atomicAdd(cluster.map_shared_rank(&sh.hist[round][tid], tid % csize), v);
-    cluster.sync();
+    if (solo) {
+      if (tid < 256) sh.hist[round][tid] = v;
+      __syncthreads();
+    } else {
+      if (v) atomicAdd(cluster.map_shared_rank(&sh.hist[round][tid], tid % csize), v);
+      cluster.sync();
+    }
     if (warp == 0) {
       // lane l owns bins 255-8l ... 248-8l (descending)
       int c[8];
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(kTopkThreads)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int b = 255 - 8 * lane - j;
-        c[j] = *cluster.map_shared_rank(&sh.hist[round][b], b % csize);
+        c[j] = solo ? sh.hist[round][b] : *cluster.map_shared_rank(&sh.hist[round][b], b % csize);
         sum += c[j];
       }
       const int incl = warp_incl_scan(sum);
@@ -230,15 +236,22 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int need_eq = remaining;  // tokens equal to the threshold to keep (request-wide)
 
   // ---- per-CTA counts, sent to every CTA of the cluster ----------------------
-  int gt_total, eq_total;
-  (void)topk_block_scan(gt_part, sh.warp_sums, gt_total);
-  (void)topk_block_scan(eq_part, sh.warp_sums, eq_total);
-  if (tid < csize) {
-    *cluster.map_shared_rank(&sh.cnt_gt[crank], tid) = gt_total;
-    *cluster.map_shared_rank(&sh.cnt_eq[crank], tid) = eq_total;
+  if (!solo) {
+    int gt_total, eq_total;
+    (void)topk_block_scan(gt_part, sh.warp_sums, gt_total);
+    (void)topk_block_scan(eq_part, sh.warp_sums, eq_total);
+    if (tid < csize) {
+      *cluster.map_shared_rank(&sh.cnt_gt[crank], tid) = gt_total;
+      *cluster.map_shared_rank(&sh.cnt_eq[crank], tid) = eq_total;
+    }
+    cluster.sync();   // no CTA reads another CTA's shared memory after this point
   }
-  cluster.sync();   // no CTA reads another CTA's shared memory after this point
-  if (warp == 0) {
+  if (solo) {
+    if (tid == 0) {
+      sh.above = 0;
+      sh.digit = 0;
+    }
+  } else if (warp == 0) {
     // lane c: CTA c's counts; exclusive prefixes give this CTA's output slot
     const int e = lane < csize ? sh.cnt_eq[lane] : 0;
     const int g = lane < csize ? sh.cnt_gt[lane] : 0;
