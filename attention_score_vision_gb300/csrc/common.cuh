@@ -31,6 +31,30 @@ __host__ __device__ constexpr int64_t align_up(int64_t a, int64_t b) { return ce
 constexpr int kMaxHeadGroups = 8;
 constexpr int kPairRows = 256;   // A rows per unit (two 128-row tiles)
 
+// Pass-1 units may split a segment's key tiles into up to this many chunks,
+// when the problem has too few (head, query pair) units to fill the GPU; the
+// last chunk to finish a 32-row slice merges the chunks' (max, sum) pairs.
+constexpr int kMaxKeySplits = 8;
+
+// Key chunks per pass-1 unit for these sizes: the largest power of two (at
+// most kMaxKeySplits) that keeps the units within about one wave of CTAs
+// (128); a segment then uses min(chunks, key tiles / 2), so every chunk has
+// at least two key tiles. A pure function of the sizes, so the workspace
+// size and every launch agree on it.
+__host__ __device__ inline int pass1_key_splits(int G, int Tq, int H) {
+  const int64_t pairs = (int64_t(Tq) + kPairRows - 1) / kPairRows;
+  const int64_t est = int64_t(H) * (pairs > G ? pairs : G);
+  int ks = 1;
+  while (ks < kMaxKeySplits && est * ks * 2 <= 128) ks *= 2;
+  return ks;
+}
+
+// Key chunks of one segment with nkt key tiles.
+__host__ __device__ inline int segment_key_splits(int ks, int nkt) {
+  const int half = nkt / 2;
+  return ks < half ? ks : (half > 1 ? half : 1);
+}
+
 // Byte offsets of the importance workspace regions.
 struct ImpWsLayout {
   int64_t qtile_off;   // int32 [G+1]: per-segment first 128-row tile of the padded LSE rows
@@ -40,9 +64,12 @@ struct ImpWsLayout {
   int64_t units2;      // uint2 [U2]: pass-2 units (segment, head group<<24 | key pair)
   int64_t grp_ctr;     // int32 [n_grp]: arrivals per 32-key slice (head-group split)
   int64_t part;        // fp32 [kMaxHeadGroups][Tk]: per-head-group partial column sums
+  int64_t part1;       // float2 [ks][H][lse_stride]: per-key-chunk (max, sum) of pass 1 (ks > 1)
+  int64_t lse_ctr;     // int32 [H][lse_stride/32]: arrivals per 32-row slice (ks > 1)
   int64_t nlse2;       // fp32 [H][lse_stride]: -LSE*log2(e), 128-row padded per segment
   int64_t lse_stride;  // floats per head (multiple of 128)
   int64_t u1_max, u2_max, n_grp;
+  int ks;              // pass-1 key chunks
   int64_t total;
 };
 
@@ -55,7 +82,8 @@ __host__ __device__ inline ImpWsLayout imp_ws_layout(int G, int Tq, int Tk, int 
   off = align_up(off + 4 * (int64_t(G) + 1), 256);
   L.scratch = off;
   off = align_up(off + 32 * int64_t(G), 256);
-  L.u1_max = int64_t(H) * (ceil_div(Tq, kTile) + G);
+  L.ks = pass1_key_splits(G, Tq, H);
+  L.u1_max = int64_t(H) * (ceil_div(Tq, kTile) + G) * L.ks;
   L.u2_max = int64_t(kMaxHeadGroups) * (ceil_div(Tk, kPairRows) + G);
   L.units1 = off;
   off = align_up(off + 8 * L.u1_max, 256);
@@ -67,6 +95,10 @@ __host__ __device__ inline ImpWsLayout imp_ws_layout(int G, int Tq, int Tk, int 
   L.part = off;
   off = align_up(off + 4 * int64_t(kMaxHeadGroups) * Tk, 1024);
   L.lse_stride = int64_t(kTile) * (ceil_div(Tq, kTile) + G);
+  L.part1 = off;
+  if (L.ks > 1) off = align_up(off + 8 * int64_t(L.ks) * H * L.lse_stride, 256);
+  L.lse_ctr = off;
+  if (L.ks > 1) off = align_up(off + 4 * int64_t(H) * (L.lse_stride / 32), 1024);
   L.nlse2 = off;
   off = align_up(off + 4 * int64_t(H) * L.lse_stride, 256);
   L.total = off;
@@ -96,6 +128,10 @@ struct ImpPassParams {
   int32_t* grp_ctr;
   float* part;
   int sum_norm;          // 1: scores are total attention received (no division by H*Nq)
+  // pass 1, key split
+  int kspl;              // key chunks per (head, query pair) (1 = LSE written directly)
+  float2* part1;
+  int32_t* lse_ctr;
 };
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {

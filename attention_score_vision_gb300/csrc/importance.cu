@@ -1,92 +1,11 @@
-// Importance scores: mean softmax attention received by every key token.
-//
-// Follows the LiteVLM review (section 3.2, s_j = Attn(h, v_j)) and the
-// dynamic vision-token compression article (section 3.2: mean attention
-// received; probabilities recovered block by block from the row LSE and
-// reduced along columns; the attention matrix never leaves the chip).
-//
-// Three launches on one stream:
-//   prep   one CTA: checks cu_seqlens, sorts segments by cost (longest first)
-//          and writes the unit lists of both passes into the workspace.
-//   pass 1 units (segment, head, 256 query rows = two 128-row A tiles):
-//          S = Q K^T tile by tile on the tensor cores (tcgen05, accumulators
-//          in TMEM), each 128-key B tile multiplied by both A tiles, online
-//          max/sum per query row -> row LSE (kept as -LSE*log2 e, padded to
-//          128-row tiles per segment).
-//   pass 2 units (segment, 256 keys, group of query heads): S^T = K Q^T with
-//          the keys on the MMA M dimension, so each epilogue thread owns one
-//          key and sums exp2(S*c - LSE2) over the query columns in registers:
-//          the column reduction needs no shuffles. When the heads are split
-//          into groups (so that small requests still fill every SM), each
-//          group stores its partial sums and the last group to finish a
-//          32-key slice adds them up in group order: the result stays
-//          deterministic.
-// Two A tiles per unit halve the operand bytes each B tile costs per element
-// (the shared-memory feed, not the tensor cores, limited 128-row units).
-//
-// CTA layout (576 threads, one CTA per SM, persistent, units fetched from a
-// global counter in longest-first order):
-//   warp 0      TMA producer (A tile pairs, B tiles, LSE slices)
-//   warp 1      TMEM allocator + MMA issuer (one thread): per B tile, one
-//               128x128 accumulator for each A tile
-//   warps 2-17  four epilogue warpgroups; warpgroup 2*par + a owns TMEM
-//               accumulator 2*par + a (A tile a, B tiles of parity par);
-//               warp w reads TMEM lanes 32*(w%4).. . Each warp loads its
-//               128 columns in 32-column pieces, the next piece in flight
-//               while the current one is computed. The math is packed (f32x2
-//               FMA/ADD, 3-input max), one MUFU exp2 per element. The two
-//               warpgroups of an A tile merge their partials once per unit.
-// The issue slots, not only the MUFU, bound the epilogue: each warp walks its
-// own parity's tiles directly, full tiles run without column masks, waits
-// sleep on the barrier instead of spinning, and arrivals are predicated.
+// Importance scores: the schedule kernel, the LSE import of the LSE-provided
+// mode, and the dispatch to the pass kernels (imp_pass.cuh, instantiated in
+// imp_pass1.cu and imp_pass2.cu so the two passes compile in parallel).
 #include <cuda_runtime.h>
 
-#include "common.cuh"
-#include "launch_util.cuh"
-#include "ptx.cuh"
+#include "imp_pass.cuh"
 
 namespace tsel {
-
-using namespace ptx;
-
-constexpr float kNegInf = -__builtin_huge_valf();
-constexpr int kPair = 2 * kTile;    // A rows per unit: two 128-row A tiles
-constexpr int kAccBufs = 4;         // TMEM accumulators of 128 columns (512 columns)
-constexpr int kLseSlots = 8;        // LSE slices in flight (pass 2)
-constexpr int kSchedSlots = 4;      // scheduler ring depth
-constexpr int kEpiWarps = 16;       // four warpgroups
-constexpr int kEpiFirstWarp = 2;
-constexpr int kThreads = 32 * (kEpiFirstWarp + kEpiWarps);  // 576
-
-// Shared-memory tile geometry. bf16 rows are D*2 bytes, split into 64-column
-// chunks (128-byte swizzle) and 16-column chunks (32-byte swizzle). E4M3 rows
-// are padded to one 128-byte chunk (128 columns; the padding reads as zeros)
-// and the MMA runs ceil(D/32) K-steps of 32 over it.
-template <int D, bool FP8>
-struct TileCfg {
-  static_assert(D % 16 == 0 && D >= 64 && D <= 128, "head_dim");
-  static constexpr int N64 = FP8 ? 1 : D / 64;           // 128-byte swizzle chunks
-  static constexpr int N16 = FP8 ? 0 : (D % 64) / 16;    // 32-byte swizzle chunks
-  static constexpr int KSTEPS128 = FP8 ? (D + 31) / 32 : 4;  // MMA K-steps per 128-byte chunk
-  static constexpr int ROW_BYTES = FP8 ? 128 : D * 2;
-  static constexpr int TILE_BYTES = kTile * ROW_BYTES;   // one 128-row tile
-  static constexpr int A_BYTES = 4 * TILE_BYTES;         // 2 slots x 2 A tiles
-  static constexpr int STAGES_RAW = (200 * 1024 - A_BYTES - 8192) / TILE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = A_BYTES;
-  static constexpr int OFF_LSE = OFF_B + STAGES * TILE_BYTES;
-  static constexpr int OFF_COMB = OFF_LSE + kLseSlots * kTile * 4;
-  static constexpr int OFF_BAR = OFF_COMB + 2 * 2 * 2 * kTile * 4;
-  static constexpr int NUM_BARS = 2 + 2 + 2 * STAGES + 2 * kAccBufs + kLseSlots +
-                                  2 * kSchedSlots + 4 + 4 + 1;
-  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 256 + 64 + 1024;  // + alignment slack
-  static_assert(STAGES >= 2, "at least double-buffered B tiles");
-  static_assert(TILE_BYTES % 1024 == 0, "tiles stay 1024-byte aligned");
-  static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM (TMEM is allocated whole)");
-};
 
 // ---------------------------------------------------------------------------
 // Prep kernel
@@ -196,6 +115,10 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
     hdr->sched_ctr[1] = 0;
   }
   for (int64_t i = threadIdx.x; i < L.n_grp; i += 1024) grp_ctr[i] = 0;
+  if (L.ks > 1) {
+    int32_t* lse_ctr = reinterpret_cast<int32_t*>(ws + L.lse_ctr);
+    for (int64_t i = threadIdx.x; i < int64_t(H) * (L.lse_stride / 32); i += 1024) lse_ctr[i] = 0;
+  }
   if (G <= 32) {
     // Few segments: one warp checks, orders and scans them with shuffles.
     if (warp == 0) {
@@ -209,6 +132,7 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
       if (!any_bad) {
         const int nqt = int(ceil_div(nq, kTile)), nkt = int(ceil_div(nk, kTile));
         const int nqp = int(ceil_div(nq, kPair)), nkp = int(ceil_div(nk, kPair));
+        const int ksg = segment_key_splits(L.ks, nkt);   // key chunks of this segment
         // rank in descending cost (pass 1: key tiles, pass 2: query tiles),
         // ties by segment index; idle lanes rank last
         const int key1 = act ? nkt : -1, key2 = act ? nqt : -1;
@@ -227,8 +151,9 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
         // every lane takes part in the shuffles (a shuffle inside the
         // conditional would leave the idle lanes out of a full-mask exchange)
         const int nqp_g1 = __shfl_sync(0xffffffffu, nqp, g1);
+        const int ksg_g1 = __shfl_sync(0xffffffffu, ksg, g1);
         const int nkp_g2 = __shfl_sync(0xffffffffu, nkp, g2);
-        const int v1 = act ? H * nqp_g1 : 0;
+        const int v1 = act ? H * nqp_g1 * ksg_g1 : 0;
         const int v2 = act ? HG * nkp_g2 : 0;
         int t1, t2, tq, tk;
         const int s1 = warp_excl_scan(v1, t1);
@@ -287,9 +212,10 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
     for (int g = threadIdx.x; g < G; g += 1024) {
       const int nqp = int(ceil_div(cu_q[g + 1] - cu_q[g], kPair));
       const int nkp = int(ceil_div(cu_k[g + 1] - cu_k[g], kPair));
+      const int ksg = segment_key_splits(L.ks, int(ceil_div(cu_k[g + 1] - cu_k[g], kTile)));
       inv1[pos1[g]] = g;
       inv2[pos2[g]] = g;
-      start1[pos1[g]] = H * nqp;
+      start1[pos1[g]] = H * nqp * ksg;
       start2[pos2[g]] = HG * nkp;
     }
     __syncthreads();
@@ -309,11 +235,15 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
   for (int i = warp; i < G; i += 32) {
     const int g = inv1[i];
     const int nqp = int(ceil_div(cu_q[g + 1] - cu_q[g], kPair));
-    const int n = H * nqp;
+    const int ksg = segment_key_splits(L.ks, int(ceil_div(cu_k[g + 1] - cu_k[g], kTile)));
+    const int n = H * nqp * ksg;
     const int s = start1[i];
+    // the key chunks of one (head, query pair) are adjacent
     for (int j = lane; j < n; j += 32) {
-      const int h = j / nqp, qp = j - h * nqp;
-      units1[s + j] = make_uint2(uint32_t(g), (uint32_t(h) << 24) | uint32_t(qp));
+      const int t = j / ksg, kc = j - t * ksg;
+      const int h = t / nqp, qp = t - h * nqp;
+      units1[s + j] = make_uint2(uint32_t(g), (uint32_t(h) << 24) | (uint32_t(kc) << 20) |
+                                                  uint32_t(qp));
     }
     const int g2 = inv2[i];
     const int nkp = int(ceil_div(cu_k[g2 + 1] - cu_k[g2], kPair));
@@ -330,597 +260,6 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
     hdr->num_units[0] = totals[0];
     hdr->num_units[1] = totals[1];
   }
-}
-
-// ---------------------------------------------------------------------------
-// Pass kernel
-// ---------------------------------------------------------------------------
-
-struct Unit {
-  int g, h, pair, q0, nq, k0, nk;
-  int nA;          // valid 128-row A tiles in this unit's 256-row pair (1 or 2)
-  int qtile_base;  // first 128-row tile of the segment in the padded LSE rows
-  int h1;          // pass 2: query heads [h, h1) (pass 1: h + 1)
-  int hg;          // pass 2: head group of the unit
-  int valid;       // 1 for a unit, 0 for the end-of-work marker
-};
-
-static_assert(kSchedSlots * sizeof(Unit) <= 256, "scheduler ring fits its shared-memory slot");
-
-template <int PASS>
-__device__ __forceinline__ Unit decode_unit(const ImpPassParams& p, uint2 u) {
-  Unit r;
-  r.g = int(u.x);
-  r.pair = int(u.y & 0xFFFFFFu);
-  if (PASS == 1) {
-    r.h = int(u.y >> 24);
-    r.h1 = r.h + 1;
-    r.hg = 0;
-  } else {
-    r.hg = int(u.y >> 24);
-    const int per = p.H / p.hgroups;
-    r.h = r.hg * per;
-    r.h1 = r.h + per;
-  }
-  r.q0 = __ldg(p.cu_q + r.g);
-  r.nq = __ldg(p.cu_q + r.g + 1) - r.q0;
-  r.k0 = __ldg(p.cu_k + r.g);
-  r.nk = __ldg(p.cu_k + r.g + 1) - r.k0;
-  const int rows_left = (PASS == 1 ? r.nq : r.nk) - r.pair * kPair;
-  r.nA = rows_left > kTile ? 2 : 1;
-  r.qtile_base = __ldg(p.qtile_off + r.g);
-  r.valid = 1;
-  return r;
-}
-
-// Loads one 128-row tile of head `head` (columns [0, D)) starting at row y.
-// bf16: 2-D maps over [rows, heads*D] (x = head*D + column); E4M3: a 3-D map
-// over [rows, heads, D] whose 128-column box pads past D with zeros.
-template <int D, bool FP8>
-__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* m64,
-                                          const CUtensorMap* m16, uint64_t* bar, int head, int y) {
-  using C = TileCfg<D, FP8>;
-  if (FP8) {
-    tma_load_3d(dst, m64, bar, 0, head, y);
-  } else {
-    const int x0 = head * D;
-#pragma unroll
-    for (int c = 0; c < C::N64; ++c) tma_load_2d(dst + c * 16384, m64, bar, x0 + 64 * c, y);
-#pragma unroll
-    for (int j = 0; j < C::N16; ++j)
-      tma_load_2d(dst + C::N64 * 16384 + j * 4096, m16, bar, x0 + 64 * C::N64 + 16 * j, y);
-  }
-}
-
-// Issues the MMAs of one 128x128 tile: D = A * B^T over the head dimension.
-template <int D, bool FP8>
-__device__ __forceinline__ void issue_tile_mmas(uint32_t d_tmem, const uint8_t* a,
-                                                const uint8_t* b) {
-  using C = TileCfg<D, FP8>;
-  const uint32_t a0 = smem_u32(a), b0 = smem_u32(b);
-  uint32_t acc = 0;
-  if (FP8) {
-    constexpr uint32_t kIdesc = idesc_e4m3_f32(kTile, kTile);
-#pragma unroll
-    for (int k = 0; k < C::KSTEPS128; ++k) {
-      mma_f8(d_tmem, smem_desc(a0 + k * 32, 2, 1024), smem_desc(b0 + k * 32, 2, 1024), kIdesc,
-             acc);
-      acc = 1;
-    }
-    return;
-  }
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
-#pragma unroll
-  for (int c = 0; c < C::N64; ++c) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t off = c * 16384 + k * 32;
-      mma_bf16(d_tmem, smem_desc(a0 + off, 2, 1024), smem_desc(b0 + off, 2, 1024), kIdesc, acc);
-      acc = 1;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < C::N16; ++j) {
-    const uint32_t off = C::N64 * 16384 + j * 4096;
-    mma_bf16(d_tmem, smem_desc(a0 + off, 6, 256), smem_desc(b0 + off, 6, 256), kIdesc, acc);
-    acc = 1;
-  }
-}
-
-// Waits with the time limit only (used to drain copies before exit).
-__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
-  const int zero = 0;
-  return wait_bounded(bar, parity, &zero, timeout_ns);
-}
-
-// Epilogue waits: all lanes wait, and the outcome is made warp-uniform so a
-// timeout never leaves part of a warp in front of a .sync.aligned TMEM load.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort_flag, uint64_t timeout_ns) {
-  return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort_flag, timeout_ns));
-}
-
-
-// Adds exp2(S*c - LSE2) of 32 query columns into the packed per-key
-// accumulators (pass 2). nl holds -LSE2 of those columns (-inf for padding).
-__device__ __forceinline__ void column_sum_chunk(const uint32_t (&r)[32], const float4* nl,
-                                                 float2 c2, float2 (&acc)[2]) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float4 t = nl[j];
-    const float2 x01 = __ffma2_rn(
-        make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), c2,
-        make_float2(t.x, t.y));
-    const float2 x23 = __ffma2_rn(
-        make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), c2,
-        make_float2(t.z, t.w));
-    acc[0] = __fadd2_rn(acc[0], make_float2(ex2(x01.x), ex2(x01.y)));
-    acc[1] = __fadd2_rn(acc[1], make_float2(ex2(x23.x), ex2(x23.y)));
-  }
-}
-
-
-
-// Pass 1 (row LSE), on 32 columns held as raw TMEM words. Per query row, m
-// is a reference max of S*c and l the sum of exp2(S*c - m) before the
-// current accumulators a; m only moves when the max of the next 64 columns
-// exceeds it by more than 8 (terms stay below 2^8), so rescaling is rare.
-// Columns at or beyond `valid` lie outside the segment and read as -inf.
-__device__ __forceinline__ void mask_cols(uint32_t (&r)[32], int valid) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) r[j] = j < valid ? r[j] : __float_as_uint(kNegInf);
-}
-
-__device__ __forceinline__ float cols_max(const uint32_t (&r)[32]) {
-#define V_(j) __uint_as_float(r[j])
-  float t0 = fmax3(V_(0), V_(1), V_(2)), t1 = fmax3(V_(3), V_(4), V_(5));
-  float t2 = fmax3(V_(6), V_(7), V_(8)), t3 = fmax3(V_(9), V_(10), V_(11));
-#pragma unroll
-  for (int j = 12; j < 28; j += 8) {
-    t0 = fmax3(t0, V_(j), V_(j + 1));
-    t1 = fmax3(t1, V_(j + 2), V_(j + 3));
-    t2 = fmax3(t2, V_(j + 4), V_(j + 5));
-    t3 = fmax3(t3, V_(j + 6), V_(j + 7));
-  }
-  return fmax3(fmax3(t0, t1, V_(28)), fmax3(t2, t3, V_(29)), fmaxf(V_(30), V_(31)));
-#undef V_
-}
-
-__device__ __forceinline__ void move_reference(float t, float& m, float& l, float2 (&a)[2]) {
-  if (t > m + 8.f) {   // also covers the first columns of a row (m = -inf, l = 0)
-    const float s = ex2(m - t);
-    const float2 a01 = __fadd2_rn(a[0], a[1]);
-    l = (l + (a01.x + a01.y)) * s;
-    a[0] = make_float2(0.f, 0.f);
-    a[1] = make_float2(0.f, 0.f);
-    m = t;
-  }
-}
-
-__device__ __forceinline__ void cols_exp_sum(const uint32_t (&r)[32], float2 c2, float2 nm2,
-                                             float2 (&a)[2]) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
-                                c2, nm2);
-    a[j & 1] = __fadd2_rn(a[j & 1], make_float2(ex2(x.x), ex2(x.y)));
-  }
-}
-
-// One 128-column accumulator: two 32-column pieces in flight; the
-// accumulator is handed back to the MMA once all of it is in registers.
-// FULL: all 128 columns lie inside the segment (no masking).
-template <int PASS, bool FULL>
-__device__ __forceinline__ void epilogue_tile(uint32_t taddr, int valid, const float4* nl,
-                                              float c, float2 c2, float& m, float& l,
-                                              float2 (&acc)[2], uint64_t* acc_empty, int lane) {
-  uint32_t r0[32], r1[32];
-  tmem_ld32_async(taddr, r0);
-  tmem_ld32_async(taddr + 32, r1);
-  tmem_wait_ld(r0);
-  tmem_wait_ld(r1);
-  if constexpr (PASS == 1) {
-    // row max over 64 columns at a time: one reference move per 64 columns
-    // and the exps of both 32-column pieces independent of each other
-    if (!FULL) {
-      mask_cols(r0, valid);
-      mask_cols(r1, valid - 32);
-    }
-    move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
-    float2 nm2 = make_float2(-m, -m);
-    cols_exp_sum(r0, c2, nm2, acc);
-    tmem_ld32_async(taddr + 64, r0);
-    if (FULL || valid > 32) cols_exp_sum(r1, c2, nm2, acc);
-    tmem_ld32_async(taddr + 96, r1);
-    tmem_wait_ld(r0);
-    tmem_wait_ld(r1);
-    tc_fence_before();
-    __syncwarp();
-    mbar_arrive_lane0(acc_empty, lane);
-    if (FULL || valid > 64) {
-      if (!FULL) {
-        mask_cols(r0, valid - 64);
-        mask_cols(r1, valid - 96);
-      }
-      move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
-      nm2 = make_float2(-m, -m);
-      cols_exp_sum(r0, c2, nm2, acc);
-      if (FULL || valid > 96) cols_exp_sum(r1, c2, nm2, acc);
-    }
-  } else {
-    if (FULL || valid > 0) column_sum_chunk(r0, nl, c2, acc);
-    tmem_ld32_async(taddr + 64, r0);
-    if (FULL || valid > 32) column_sum_chunk(r1, nl + 8, c2, acc);
-    tmem_ld32_async(taddr + 96, r1);
-    tmem_wait_ld(r0);
-    tmem_wait_ld(r1);
-    tc_fence_before();
-    __syncwarp();
-    mbar_arrive_lane0(acc_empty, lane);
-    if (FULL || valid > 64) column_sum_chunk(r0, nl + 16, c2, acc);
-    if (FULL || valid > 96) column_sum_chunk(r1, nl + 24, c2, acc);
-  }
-}
-
-template <int PASS, int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
-    imp_pass_kernel(const __grid_constant__ CUtensorMap mapA64,
-                    const __grid_constant__ CUtensorMap mapA16,
-                    const __grid_constant__ CUtensorMap mapB64,
-                    const __grid_constant__ CUtensorMap mapB16, const ImpPassParams p) {
-  using C = TileCfg<D, FP8>;
-  constexpr int S = C::STAGES;
-  extern __shared__ uint8_t smem_dyn[];
-  // 128-byte swizzle atoms key off shared-address bits: align the carve-out
-  // on the shared-window address itself.
-  uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
-  uint8_t* sA = smem + C::OFF_A;   // [2 slots][2 tiles]
-  uint8_t* sB = smem + C::OFF_B;   // [S stages]
-  float* sLse = reinterpret_cast<float*>(smem + C::OFF_LSE);
-  float* sComb = reinterpret_cast<float*>(smem + C::OFF_COMB);  // [A half][buf][m|l][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* a_full = bars;
-  uint64_t* a_empty = a_full + 2;
-  uint64_t* b_full = a_empty + 2;
-  uint64_t* b_empty = b_full + S;
-  uint64_t* acc_full = b_empty + S;
-  uint64_t* acc_empty = acc_full + kAccBufs;
-  // The LSE slice of a B tile lands on that tile's b_full barrier; the
-  // epilogue reads it after acc_full, which the MMA thread commits only after
-  // it has seen b_full complete. lse_empty returns the slot to the producer.
-  uint64_t* lse_empty = acc_empty + kAccBufs;
-  uint64_t* sch_full = lse_empty + kLseSlots;
-  uint64_t* sch_empty = sch_full + kSchedSlots;
-  uint64_t* comb_full = sch_empty + kSchedSlots;  // [A half][buf]
-  uint64_t* comb_empty = comb_full + 4;
-  uint64_t* mma_done = comb_empty + 4;
-  Unit* sched = reinterpret_cast<Unit*>(smem + C::OFF_MISC);   // decoded units in flight
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC + 256);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 260);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint64_t T = p.timeout_ns;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], 1);
-      mbar_init(&a_empty[i], 1);
-    }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&comb_full[i], 4);
-      mbar_init(&comb_empty[i], 4);
-    }
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&b_full[i], 1);
-      mbar_init(&b_empty[i], 1);
-    }
-    for (int i = 0; i < kAccBufs; ++i) {
-      mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);           // the owning warpgroup
-    }
-    for (int i = 0; i < kLseSlots; ++i) {
-      mbar_init(&lse_empty[i], 8);           // both warpgroups of the B-tile parity
-    }
-    for (int i = 0; i < kSchedSlots; ++i) {
-      mbar_init(&sch_full[i], 1);
-      mbar_init(&sch_empty[i], 1 + kEpiWarps);
-    }
-    mbar_init(mma_done, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&mapA64);
-    prefetch_tensormap(&mapA16);
-    prefetch_tensormap(&mapB64);
-    prefetch_tensormap(&mapB16);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  // Prologue done: the next kernel may launch; wait for the schedule kernel
-  // (unit lists) and, in pass 2, the row-LSE pass.
-  pdl_launch_dependents();
-  pdl_wait();
-  const int total_units = *reinterpret_cast<const volatile int*>(p.num_units);
-  const int group = p.H / p.Hkv;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int s_it = 0, a_it = 0, b_it = 0;
-      bool ok = p.stall == 0;   // the test hook leaves the consumers waiting for work
-      while (ok) {
-        const int slot = s_it % kSchedSlots;
-        if (!wait_bounded(&sch_empty[slot], ((s_it / kSchedSlots) & 1) ^ 1, abort_flag, T)) {
-          ok = false;
-          break;
-        }
-        const int u = atomicAdd(p.sched_ctr, 1);
-        Unit w;
-        if (u < total_units) {
-          w = decode_unit<PASS>(p, p.units[u]);
-        } else {
-          w = Unit{};
-          w.valid = 0;
-        }
-        sched[slot] = w;   // consumers read the decoded unit from shared memory
-        mbar_arrive(&sch_full[slot]);
-        ++s_it;
-        if (!w.valid) break;
-        const int n_b = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
-        if (n_b == 0) continue;
-        // pass 2: one A tile pair per kv head the unit's query heads read
-        const int ag0 = PASS == 1 ? 0 : w.h / group;
-        const int ag1 = PASS == 1 ? 1 : (w.h1 - 1) / group + 1;
-        const int qtile_base = w.qtile_base;
-        for (int ag = ag0; ag < ag1 && ok; ++ag) {
-          const int as = a_it & 1;
-          if (!wait_bounded(&a_empty[as], ((a_it >> 1) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
-          mbar_arrive_expect_tx(&a_full[as], uint32_t(w.nA * C::TILE_BYTES));
-          const int ahead = PASS == 1 ? w.h : ag;
-          const int ay = (PASS == 1 ? w.q0 : w.k0) + w.pair * kPair;
-          for (int a = 0; a < w.nA; ++a)
-            load_tile<D, FP8>(sA + (as * 2 + a) * C::TILE_BYTES, &mapA64, &mapA16, &a_full[as],
-                              ahead, ay + a * kTile);
-          ++a_it;
-          const int hb0 = PASS == 1 ? w.h : max(w.h, ag * group);
-          const int hb1 = PASS == 1 ? w.h + 1 : min(w.h1, (ag + 1) * group);
-          for (int h = hb0; h < hb1 && ok; ++h) {
-            const int bhead = PASS == 1 ? w.h / group : h;
-            const int nbt = PASS == 1 ? n_b : int(ceil_div(w.nq, kTile));
-            for (int bt = 0; bt < nbt; ++bt) {
-              const int bs = b_it % S;
-              if (!wait_bounded(&b_empty[bs], ((b_it / S) & 1) ^ 1, abort_flag, T)) { ok = false; break; }
-              const int ls = b_it % kLseSlots;
-              if (PASS == 2 &&
-                  !wait_bounded(&lse_empty[ls], ((b_it / kLseSlots) & 1) ^ 1, abort_flag, T)) {
-                ok = false;
-                break;
-              }
-              mbar_arrive_expect_tx(&b_full[bs], C::TILE_BYTES + (PASS == 2 ? kTile * 4 : 0));
-              load_tile<D, FP8>(sB + bs * C::TILE_BYTES, &mapB64, &mapB16, &b_full[bs], bhead,
-                                (PASS == 1 ? w.k0 : w.q0) + bt * kTile);
-              if (PASS == 2)
-                bulk_load(sLse + ls * kTile,
-                          p.nlse2 + int64_t(h) * p.lse_stride + int64_t(qtile_base + bt) * kTile,
-                          kTile * 4, &b_full[bs]);
-              ++b_it;
-            }
-          }
-        }
-      }
-      if (!ok && p.stall == 0) {
-        *abort_flag = 1;
-        set_status(p.status, TSEL_DEV_TIMEOUT);
-      }
-      // Drain: every copy this thread issued has landed before the CTA exits.
-      for (int i = 0; i < S && i < b_it; ++i) {
-        const int n = b_it - 1 - i;
-        wait_drain(&b_full[n % S], (n / S) & 1, T);
-      }
-      for (int i = 0; i < 2 && i < a_it; ++i) {
-        const int n = a_it - 1 - i;
-        wait_drain(&a_full[n & 1], (n >> 1) & 1, T);
-      }
-
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int s_it = 0, a_it = 0, b_it = 0;
-      bool ok = true;
-      while (ok) {
-        const int slot = s_it % kSchedSlots;
-        if (!wait_bounded(&sch_full[slot], (s_it / kSchedSlots) & 1, abort_flag, T)) { ok = false; break; }
-        const Unit w = sched[slot];
-        mbar_arrive(&sch_empty[slot]);
-        ++s_it;
-        if (!w.valid) break;
-        const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
-        if (nbt == 0) continue;
-        const int ag0 = PASS == 1 ? 0 : w.h / group;
-        const int ag1 = PASS == 1 ? 1 : (w.h1 - 1) / group + 1;
-        for (int ag = ag0; ag < ag1 && ok; ++ag) {
-          const int as = a_it & 1;
-          if (!wait_bounded(&a_full[as], (a_it >> 1) & 1, abort_flag, T)) { ok = false; break; }
-          tc_fence_after();
-          const int n_b = PASS == 1
-                              ? nbt
-                              : (min(w.h1, (ag + 1) * group) - max(w.h, ag * group)) * nbt;
-          for (int bi = 0; bi < n_b; ++bi) {
-            const int bs = b_it % S;
-            if (!wait_bounded(&b_full[bs], (b_it / S) & 1, abort_flag, T)) { ok = false; break; }
-            const uint32_t use = uint32_t(b_it >> 1) & 1u;
-            for (int a = 0; a < 2; ++a) {
-              const int k = 2 * (b_it & 1) + a;
-              if (!wait_bounded(&acc_empty[k], use ^ 1u, abort_flag, T)) { ok = false; break; }
-              tc_fence_after();
-              if (a < w.nA)
-                issue_tile_mmas<D, FP8>(tmem_base + uint32_t(k * kTile),
-                                   sA + (as * 2 + a) * C::TILE_BYTES, sB + bs * C::TILE_BYTES);
-              mma_commit(&acc_full[k]);
-            }
-            if (!ok) break;
-            mma_commit(&b_empty[bs]);
-            ++b_it;
-          }
-          mma_commit(&a_empty[as]);
-          ++a_it;
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        set_status(p.status, TSEL_DEV_TIMEOUT);
-      }
-      // All MMAs issued by this thread have completed before TMEM is freed.
-      mma_commit(mma_done);
-      wait_drain(mma_done, 0, T);
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    // Warpgroup wg = 2*par + a owns TMEM accumulator k = 2*par + a: rows of
-    // A tile `a` against the B tiles of parity `par`.
-    const int wg = (warp - kEpiFirstWarp) >> 2;
-    const int a_half = wg & 1, par = wg >> 1;
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;
-    const int kbuf = 2 * par + a_half;
-    const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(kbuf * kTile);
-    const float c = p.c;
-    const float2 c2 = make_float2(c, c);
-    int s_it = 0, b_it = 0, unit_it = 0;
-    bool ok = true;
-    while (ok) {
-      const int slot = s_it % kSchedSlots;
-      if (!warp_wait(&sch_full[slot], (s_it / kSchedSlots) & 1, abort_flag, T)) { ok = false; break; }
-      const Unit w = sched[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sch_empty[slot]);
-      ++s_it;
-      if (!w.valid) break;
-      const bool mine = a_half < w.nA;   // this warpgroup's A tile holds rows of the unit
-      const int nbt = PASS == 1 ? int(ceil_div(w.nk, kTile)) : int(ceil_div(w.nq, kTile));
-      const int n_b = PASS == 1 ? nbt : (nbt > 0 ? (w.h1 - w.h) * nbt : 0);
-      float m = kNegInf, l = 0.f;           // pass 1
-      float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // pass 1: sum since m; pass 2: per-key sum
-      // This warpgroup's tiles: global B-tile indices of parity `par`; bt is
-      // the tile's column block within its head.
-      const int b_end = b_it + n_b;
-      int g = b_it + ((par ^ b_it) & 1);
-      int bt = g - b_it;
-      if (bt >= nbt) bt -= nbt;
-      for (; g < b_end; g += 2) {
-        const uint32_t use = uint32_t(g >> 1) & 1u;
-        if (!warp_wait(&acc_full[kbuf], use, abort_flag, T)) { ok = false; break; }
-        const int ls = g & (kLseSlots - 1);
-
-        tc_fence_after();
-        if (mine) {
-          const int valid = (PASS == 1 ? w.nk : w.nq) - bt * kTile;
-          const float4* nl = reinterpret_cast<const float4*>(sLse + ls * kTile);
-          if (valid >= kTile)
-            epilogue_tile<PASS, true>(taddr, valid, nl, c, c2, m, l, acc, &acc_empty[kbuf], lane);
-          else
-            epilogue_tile<PASS, false>(taddr, valid, nl, c, c2, m, l, acc, &acc_empty[kbuf], lane);
-        } else {
-          tc_fence_before();
-          __syncwarp();
-          mbar_arrive_lane0(&acc_empty[kbuf], lane);
-        }
-        if (PASS == 2) {
-          __syncwarp();
-          mbar_arrive_lane0(&lse_empty[ls], lane);
-        }
-        bt += 2;
-        if (bt >= nbt) bt -= nbt;
-        if (bt >= nbt) bt -= nbt;
-      }
-      if (!ok) break;
-      b_it = b_end;
-      // Merge the two warpgroups of the same A half (B-tile parities 0 and 1).
-      const int cb = unit_it & 1;
-      const uint32_t cpar = (unit_it >> 1) & 1;
-      float* comb = sComb + (a_half * 2 + cb) * 2 * kTile;
-      uint64_t* cfull = &comb_full[a_half * 2 + cb];
-      uint64_t* cempty = &comb_empty[a_half * 2 + cb];
-      const float2 accs = __fadd2_rn(acc[0], acc[1]);
-      const float part = accs.x + accs.y;   // pass 1: sum since m; pass 2: per-key sum
-      if (par == 1) {
-        if (!warp_wait(cempty, cpar ^ 1, abort_flag, T)) { ok = false; break; }
-        comb[row] = PASS == 1 ? m : part;
-        comb[kTile + row] = PASS == 1 ? l + part : 0.f;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cfull);
-      } else {
-        if (!warp_wait(cfull, cpar, abort_flag, T)) { ok = false; break; }
-        const float o0 = comb[row], o1 = comb[kTile + row];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cempty);
-        if (mine) {
-          if (PASS == 1) {
-            const float l0 = l + part;
-            const float M = fmaxf(m, o0);
-            float Lsum = 0.f;
-            if (M > kNegInf) Lsum = l0 * ex2(m - M) + o1 * ex2(o0 - M);
-            const int qrow = w.pair * kPair + a_half * kTile + row;
-            const bool valid = qrow < w.nq;
-            const float lse2 = Lsum > 0.f ? M + log2f(Lsum) : kNegInf;
-            const int qtile = w.qtile_base + w.pair * 2 + a_half;
-            p.nlse2[int64_t(w.h) * p.lse_stride + int64_t(qtile) * kTile + row] =
-                (valid && Lsum > 0.f) ? -lse2 : kNegInf;
-            if (valid && p.lse_out != nullptr)
-              p.lse_out[int64_t(w.h) * p.Tq + w.q0 + qrow] = lse2 * 0.69314718055994531f;
-          } else {
-            const int krow = w.pair * kPair + a_half * kTile + row;
-            const float total = part + o0;
-            const float rows = p.sum_norm ? 1.f : float(p.H * w.nq);
-            if (p.hgroups == 1) {
-              if (krow < w.nk) p.scores[w.k0 + krow] = w.nq > 0 ? total / rows : 0.f;
-            } else {
-              // Partial sums of this head group; the last group of the 32-key
-              // slice adds all groups' partials in group order.
-              if (krow < w.nk) p.part[int64_t(w.hg) * p.Tk + w.k0 + krow] = total;
-              __threadfence();
-              __syncwarp();
-              int old = 0;
-              if (lane == 0) {
-                const int slice = (__ldg(p.kpair_off + w.g) + w.pair) * 8 + a_half * 4 + quad;
-                old = atomicAdd(p.grp_ctr + slice, 1);
-                if (old == p.hgroups - 1) p.grp_ctr[slice] = 0;   // no other arrival follows
-              }
-              old = __shfl_sync(0xffffffffu, old, 0);
-              if (old == p.hgroups - 1) {
-                __threadfence();
-                if (krow < w.nk) {
-                  float sum = 0.f;
-                  for (int gi = 0; gi < p.hgroups; ++gi)
-                    sum += __ldcg(p.part + int64_t(gi) * p.Tk + w.k0 + krow);
-                  p.scores[w.k0 + krow] = w.nq > 0 ? sum / rows : 0.f;
-                }
-              }
-            }
-          }
-        }
-      }
-      ++unit_it;
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      set_status(p.status, TSEL_DEV_TIMEOUT);
-    }
-  }
-
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -968,24 +307,6 @@ cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int
                        max_k, H, HG, ws, L);
 }
 
-template <int PASS, int D, bool FP8>
-static cudaError_t launch_pass_t(const CUtensorMap* maps, const ImpPassParams& p, int grid,
-                                 cudaStream_t stream) {
-  using C = TileCfg<D, FP8>;
-  auto kern = imp_pass_kernel<PASS, D, FP8>;
-  static bool attr_set[128] = {};  // per device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 128) attr_set[dev] = true;
-  }
-  return launch_kernel(kern, dim3(unsigned(grid)), kThreads, size_t(C::SMEM_BYTES), stream, 1,
-                       maps[0], maps[1], maps[2], maps[3], p);
-}
-
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
                               const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
                               int max_qtiles, int H, const uint32_t* status, cudaStream_t stream) {
@@ -994,27 +315,17 @@ cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, 
                        stream, 1, lse_in, Tq, cu_q, G, qtile_off, nlse2, lse_stride, status);
 }
 
+cudaError_t launch_imp_pass1(int head_dim, bool fp8, bool ksplit, const CUtensorMap* maps,
+                             const ImpPassParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_imp_pass2(int head_dim, bool fp8, const CUtensorMap* maps,
+                             const ImpPassParams& p, int grid, cudaStream_t stream);
+
 // maps: A64, A16, B64, B16 (pass 1: A = Q, B = K; pass 2: A = K, B = Q). For
 // E4M3 inputs A64 / B64 are the 3-D maps and A16 / B16 are unused.
 cudaError_t launch_imp_pass(int pass, int head_dim, bool fp8, const CUtensorMap* maps,
                             const ImpPassParams& p, int grid, cudaStream_t stream) {
-#define TSEL_PASS_CASE(DD)                                                                    \
-  case DD:                                                                                    \
-    if (fp8)                                                                                  \
-      return pass == 1 ? launch_pass_t<1, DD, true>(maps, p, grid, stream)                    \
-                       : launch_pass_t<2, DD, true>(maps, p, grid, stream);                   \
-    return pass == 1 ? launch_pass_t<1, DD, false>(maps, p, grid, stream)                     \
-                     : launch_pass_t<2, DD, false>(maps, p, grid, stream);
-  switch (head_dim) {
-    TSEL_PASS_CASE(64)
-    TSEL_PASS_CASE(80)
-    TSEL_PASS_CASE(96)
-    TSEL_PASS_CASE(112)
-    TSEL_PASS_CASE(128)
-    default:
-      return cudaErrorInvalidValue;
-  }
-#undef TSEL_PASS_CASE
+  if (pass == 1) return launch_imp_pass1(head_dim, fp8, p.kspl > 1, maps, p, grid, stream);
+  return launch_imp_pass2(head_dim, fp8, maps, p, grid, stream);
 }
 
 }  // namespace tsel

@@ -303,6 +303,9 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     p1.units = reinterpret_cast<const uint2*>(ws + L.units1);
     p1.num_units = &hdr->num_units[0];
     p1.sched_ctr = &hdr->sched_ctr[0];
+    p1.kspl = L.ks;
+    p1.part1 = reinterpret_cast<float2*>(ws + L.part1);
+    p1.lse_ctr = reinterpret_cast<int32_t*>(ws + L.lse_ctr);
     const int grid = int(L.u1_max < sms ? L.u1_max : sms);
     e = launch_imp_pass(1, head_dim, fp8, maps, p1, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pass-1 launch");

@@ -32,8 +32,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 _CSRC = "attention_score_vision_gb300/csrc/"
 # Sources each kernel is built from (a traffic figure taken on other sources reads as null).
 KERNEL_SOURCES = {
-    "imp_pass_kernel": [_CSRC + f for f in ("importance.cu", "ptx.cuh", "common.cuh",
-                                            "launch_util.cuh")],
+    "imp_pass_kernel": [_CSRC + f for f in ("imp_pass.cuh", "imp_pass1.cu", "imp_pass2.cu",
+                                            "ptx.cuh", "common.cuh", "launch_util.cuh")],
     "topk_cluster_kernel": [_CSRC + f for f in ("topk.cu", "common.cuh", "launch_util.cuh")],
     "gather_kernel": [_CSRC + f for f in ("gather.cu", "common.cuh", "launch_util.cuh")],
 }
