@@ -23,9 +23,9 @@ constexpr int kMaxClusterCtas = 16;
 // per-request offsets): small requests need no cluster.
 inline int cluster_size_for(int total_tokens, int num_req) {
   const int64_t avg = num_req > 0 ? (int64_t(total_tokens) + num_req - 1) / num_req : 0;
-  if (avg >= 16384) return 16;
-  if (avg >= 4096) return 8;
-  if (avg >= 1024) return 4;
+  if (avg >= 32768) return 16;
+  if (avg >= 16384) return 8;
+  if (avg >= 8192) return 4;
   return 1;
 }
 
