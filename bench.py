@@ -49,6 +49,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--cpu-child", nargs=2, metavar=("WORKLOAD", "PAIRS"), help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -275,6 +276,60 @@ def reduce_max_over_ranks(x: float, device=None) -> float:
 def replica_throughput(tokens_per_replica: int, world: int, ms_max: float) -> float:
     """Whole-job tokens/s: every rank processed its own replica of the workload."""
     return world * tokens_per_replica / (ms_max * 1e-3)
+
+
+def workload_throughput(tsel, w, dev, flush, stream, ex2_peak, bf16_peak, steps: int = 20,
+                        warmup: int = 3) -> dict:
+    """Whole-path throughput of one workload (events around each step, L2 flushed
+    in between, untimed) and its importance time against the importance roofline."""
+    import numpy as np
+    import torch
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    q, k, hidden = bf16(w.q_bits), bf16(w.k_bits), bf16(w.hidden_bits)
+    cq, ck, ro, kp, pos = (i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.req_tok_offsets),
+                           i32(w.keep_per_req), i32(w.pos))
+    G, Tq, Tk, H, K = w.num_seg, w.total_q, w.total_k, w.num_heads, w.total_keep
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(G, Tq, Tk, H), dtype=torch.uint8, device=dev)
+    scores = torch.empty(Tk, device=dev)
+    lse = torch.empty((H, Tq), device=dev)
+    keep_idx = torch.empty(K, dtype=torch.int32, device=dev)
+    cu_keep = torch.empty(w.keep_per_req.size + 1, dtype=torch.int32, device=dev)
+    oh = torch.empty((K, hidden.shape[1]), dtype=torch.bfloat16, device=dev)
+    op = torch.empty((K, w.pos.shape[1]), dtype=torch.int32, device=dev)
+    oi = torch.empty(K, dtype=torch.int32, device=dev)
+    oc = torch.empty(G + 1, dtype=torch.int32, device=dev)
+    step, imp = [], []
+    for i in range(warmup + steps):
+        flush.fill_(i & 0xFF)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record(stream)
+        tsel.tsel_importance(q, k, cq, ck, w.max_seqlen_q, w.max_seqlen_k, lse=lse, scores=scores,
+                             workspace=ws, stream=stream)
+        ev[1].record(stream)
+        tsel.tsel_select_topk(scores, ro, kp, K, keep_idx=keep_idx, cu_keep=cu_keep, workspace=ws,
+                              stream=stream)
+        tsel.tsel_gather_compact(hidden, pos, ck, keep_idx, out_hidden=oh, out_pos=op, out_img_id=oi,
+                                 out_cu_seqlens=oc, workspace=ws, stream=stream)
+        ev[2].record(stream)
+        if i >= warmup:
+            step.append(ev)
+    torch.cuda.synchronize()
+    if tsel.tsel_read_device_status(ws) != 0:
+        raise RuntimeError(f"device status set for {w.name}")
+    t_step = sum(e[0].elapsed_time(e[2]) for e in step) / len(step)
+    t_imp = sum(e[0].elapsed_time(e[1]) for e in step) / len(step)
+    E = w.attended_pairs()
+    roof = max(4 * w.head_dim * E / bf16_peak, 2 * E / ex2_peak)
+    return {"tokens": Tk, "ms_per_step": t_step, "tokens_per_s": Tk / (t_step * 1e-3),
+            "importance_ms": t_imp, "importance_roofline_frac": roof / (t_imp * 1e-3),
+            "note": f"{steps} steps, importance timed with an event after it (no overlap with "
+                    "the selection)"}
 
 
 def small_request_latency(tsel, w, dev, flush, stream, reps: int = 20) -> dict:
@@ -650,6 +705,16 @@ def gpu_arm(args) -> None:
         for name in ("single_image_256", "six_views_1536", "text_query_3072"):
             small[name] = small_request_latency(tsel, W.make(name), dev, flush, stream)
 
+    # --- the other seeded workloads: throughput and importance roofline -------
+    sweep = {}
+    if not args.no_sweep:
+        peaks_s, _ = load_peaks()
+        for name in W.WORKLOADS:
+            if name == args.workload:
+                continue
+            sweep[name] = workload_throughput(tsel, W.make(name), dev, flush, stream, ex2_peak,
+                                              peaks_s["bf16_tflops"] * 1e12)
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -734,6 +799,7 @@ def gpu_arm(args) -> None:
         "dynamic_budget": dynamic,
         "fp8": fp8,
         "small_requests": small,
+        "workloads": sweep,
         "gpu_launches": 5 * args.steps,
         "clocks": clocks,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
