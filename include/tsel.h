@@ -62,7 +62,7 @@ extern "C" {
 typedef enum tsel_status {
   TSEL_OK = 0,
   TSEL_ERR_INVALID_VALUE = 1, /* bad pointer, size, stride or alignment */
-  TSEL_ERR_UNSUPPORTED = 2,   /* valid request this build does not handle */
+  TSEL_ERR_UNSUPPORTED = 2,   /* valid request this library does not handle */
   TSEL_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned */
   TSEL_ERR_CUDA = 4,          /* CUDA runtime/driver error (launch, device) */
   TSEL_ERR_DEVICE_CHECK = 5   /* a device-side check fired (see status word) */
