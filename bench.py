@@ -761,6 +761,11 @@ def gpu_arm(args) -> None:
                  "hbm_frac": topk_bytes / (mean["topk"] * 1e-3) / hbm_peak},
         "gather": {"ms": mean["gather"], "GB/s": gather_bytes / (mean["gather"] * 1e-3) / 1e9,
                    "hbm_frac": gather_bytes / (mean["gather"] * 1e-3) / hbm_peak},
+        # top-B + compaction as one selection step (each alone is timed above)
+        "selection": {"ms": mean["topk"] + mean["gather"],
+                      "GB/s": (topk_bytes + gather_bytes) / ((mean["topk"] + mean["gather"]) * 1e-3) / 1e9,
+                      "hbm_frac": (topk_bytes + gather_bytes)
+                                  / ((mean["topk"] + mean["gather"]) * 1e-3) / hbm_peak},
     }
 
     if fp8 is not None:
