@@ -81,6 +81,27 @@ def test_long_segment_4096_and_cross_lengths(tsel):
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
 
 
+def test_very_long_segment_8192(tsel):
+    # one 8,192-token image (64 key tiles per row; 32 query pairs per head)
+    w = W.make_segments([8192], [8192], 1, 1, 64, seed=308, sink_counts=[100], hidden_dim=64)
+    s, lse, st = _importance(tsel, w)
+    assert st == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
+
+
+@pytest.mark.parametrize("H,Hkv,d", [(32, 8, 64), (64, 64, 64), (40, 5, 128), (255, 255, 64)])
+def test_many_heads(tsel, H, Hkv, d):
+    w = W.make_segments([130, 300, 1], [130, 300, 1], H, Hkv, d, seed=309 + H, sink_counts=[2, 3, 0],
+                        hidden_dim=64)
+    s, lse, st = _importance(tsel, w)
+    assert st == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=1e-4)
+
+
 def test_empty_segments_and_missing_queries(tsel):
     # segment 1 is empty, segment 2 has keys but no queries (scores 0),
     # segment 3 has queries but no keys (lse -inf)
