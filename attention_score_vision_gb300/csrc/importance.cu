@@ -82,7 +82,9 @@ __device__ __forceinline__ int warp_excl_scan(int v, int& total) {
   return x - v;
 }
 
-__global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restrict__ cu_q,
+// THREADS = 1024: any number of segments; fewer threads: up to 32 segments.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) imp_prep_kernel(const int32_t* __restrict__ cu_q,
                                                         const int32_t* __restrict__ cu_k, int G,
                                                         int Tq, int Tk, int max_q, int max_k,
                                                         int H, int HG, uint8_t* ws,
@@ -114,10 +116,16 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
     hdr->sched_ctr[0] = 0;
     hdr->sched_ctr[1] = 0;
   }
-  for (int64_t i = threadIdx.x; i < L.n_grp; i += 1024) grp_ctr[i] = 0;
+  for (int64_t i = threadIdx.x; i < L.n_grp; i += THREADS) grp_ctr[i] = 0;
   if (L.ks > 1) {
     int32_t* lse_ctr = reinterpret_cast<int32_t*>(ws + L.lse_ctr);
-    for (int64_t i = threadIdx.x; i < int64_t(H) * (L.lse_stride / 32); i += 1024) lse_ctr[i] = 0;
+    for (int64_t i = threadIdx.x; i < int64_t(H) * (L.lse_stride / 32); i += THREADS) lse_ctr[i] = 0;
+  }
+  if constexpr (THREADS < 1024) {
+    if (G > 32) {   // the launcher sends larger segment counts to the 1024-thread form
+      if (threadIdx.x == 0) set_status(&hdr->status, TSEL_DEV_SEQLENS);
+      return;
+    }
   }
   if (G <= 32) {
     // Few segments: one warp checks, orders and scans them with shuffles.
@@ -181,7 +189,7 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
       if (threadIdx.x == 0) set_status(&hdr->status, TSEL_DEV_SEQLENS);
       return;
     }
-  } else {
+  } else if constexpr (THREADS == 1024) {
     if (threadIdx.x == 0 &&
         (cu_q[0] != 0 || cu_k[0] != 0 || cu_q[G] != Tq || cu_k[G] != Tk))
       bad = 1;
@@ -230,9 +238,9 @@ __global__ void __launch_bounds__(1024) imp_prep_kernel(const int32_t* __restric
       totals[1] = total2;
     }
     __syncthreads();
-  }
+    }
   // Unit lists in descending-cost segment order.
-  for (int i = warp; i < G; i += 32) {
+  for (int i = warp; i < G; i += THREADS / 32) {
     const int g = inv1[i];
     const int nqp = int(ceil_div(cu_q[g + 1] - cu_q[g], kPair));
     const int ksg = segment_key_splits(L.ks, int(ceil_div(cu_k[g + 1] - cu_k[g], kTile)));
@@ -303,8 +311,11 @@ __global__ void __launch_bounds__(kTile) imp_lse_import_kernel(
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
                             int max_q, int max_k, int H, int HG, uint8_t* ws,
                             const ImpWsLayout& L, cudaStream_t stream) {
-  return launch_kernel(imp_prep_kernel, dim3(1), 1024, 0, stream, 1, cu_q, cu_k, G, Tq, Tk, max_q,
-                       max_k, H, HG, ws, L);
+  if (G <= 32)   // one warp orders the segments; a small block writes the units
+    return launch_kernel(imp_prep_kernel<128>, dim3(1), 128, 0, stream, 1, cu_q, cu_k, G, Tq, Tk,
+                         max_q, max_k, H, HG, ws, L);
+  return launch_kernel(imp_prep_kernel<1024>, dim3(1), 1024, 0, stream, 1, cu_q, cu_k, G, Tq, Tk,
+                       max_q, max_k, H, HG, ws, L);
 }
 
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
