@@ -311,7 +311,9 @@ __global__ void __launch_bounds__(kTile) imp_lse_import_kernel(
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
                             int max_q, int max_k, int H, int HG, uint8_t* ws,
                             const ImpWsLayout& L, cudaStream_t stream) {
-  if (G <= 32)   // one warp orders the segments; a small block writes the units
+  // Few segments and few units: a small block (one warp orders the segments,
+  // four write the units); otherwise all 32 warps write the unit lists.
+  if (G <= 32 && L.u1_max + L.u2_max <= 1024)
     return launch_kernel(imp_prep_kernel<128>, dim3(1), 128, 0, stream, 1, cu_q, cu_k, G, Tq, Tk,
                          max_q, max_k, H, HG, ws, L);
   return launch_kernel(imp_prep_kernel<1024>, dim3(1), 1024, 0, stream, 1, cu_q, cu_k, G, Tq, Tk,
