@@ -23,6 +23,7 @@ __all__ = [
     "tsel_gather_compact_workspace_size", "tsel_gather_compact", "tsel_gather_compact_counted",
     "tsel_dynamic_budget", "TSEL_KEEP_FROM_DEVICE",
     "tsel_keep_count", "tsel_read_device_status", "tsel_clear_device_status",
+    "tsel_importance_redo_pairs",
     "tsel_status_string", "tsel_last_error", "tsel_probe_ex2",
     "TSEL_DEV_SEQLENS", "TSEL_DEV_REQUESTS", "TSEL_DEV_KEEP_IDX", "TSEL_DEV_TIMEOUT", "TSEL_DEV_NAN",
     "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_SCORE_SUM", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
@@ -72,6 +73,7 @@ _SIGNATURES = {
     "tsel_keep_count": (_c_int, [_c_int, _c_int]),
     "tsel_read_device_status": (_c_int, [_p, ctypes.POINTER(ctypes.c_uint32), _p]),
     "tsel_clear_device_status": (_c_int, [_p, _p]),
+    "tsel_importance_redo_pairs": (_c_int, [_p, ctypes.POINTER(ctypes.c_int32), _p]),
     "tsel_status_string": (ctypes.c_char_p, [_c_int]),
     "tsel_last_error": (ctypes.c_char_p, []),
     "tsel_probe_ex2": (_c_int, [_c_int, _c_int, _p, _p]),
@@ -388,6 +390,15 @@ def tsel_read_device_status(workspace: torch.Tensor, stream=None) -> int:
     if st not in (TSEL_OK, TSEL_ERR_DEVICE_CHECK):
         _check(st)
     return int(bits.value)
+
+
+def tsel_importance_redo_pairs(workspace: torch.Tensor, stream=None) -> int:
+    """(head, query pair)s the last importance call on `workspace` redid with a
+    moving reference (synchronises the stream)."""
+    n = ctypes.c_int32(0)
+    _check(load_library().tsel_importance_redo_pairs(_ptr(workspace), ctypes.byref(n),
+                                                     _stream(stream, workspace.device)))
+    return int(n.value)
 
 
 def tsel_clear_device_status(workspace: torch.Tensor, stream=None) -> None:

@@ -20,6 +20,10 @@ struct WsHeader {
   uint32_t pad1[30];
   int32_t num_units[2];   // units of the two passes (written by the prep kernel)
   uint32_t pad2[30];
+  int32_t fix_ctr;        // unit counter of the pass-1 redo launch
+  uint32_t pad3[31];
+  int32_t redo_count;     // pass-1 units queued for an exact redo
+  uint32_t pad4[31];
 };
 static_assert(sizeof(WsHeader) <= kWsHeaderBytes, "header too large");
 
@@ -62,6 +66,8 @@ struct ImpWsLayout {
   int64_t scratch;     // int32 [8*G]: sort positions, inverses and unit starts (prep kernel)
   int64_t units1;      // uint2 [U1]: pass-1 units (segment, head<<24 | query pair)
   int64_t units2;      // uint2 [U2]: pass-2 units (segment, head group<<24 | key pair)
+  int64_t redo_units;  // uint2 [H][lse_stride/128]: (head, query pair)s queued for an exact redo
+  int64_t redo_flags;  // int32 [H][lse_stride/128]: pair already queued (index: its first tile)
   int64_t grp_ctr;     // int32 [n_grp]: arrivals per 32-key slice (head-group split)
   int64_t part;        // fp32 [kMaxHeadGroups][Tk]: per-head-group partial column sums
   int64_t part1;       // float2 [ks][H][lse_stride]: per-key-chunk (max, sum) of pass 1 (ks > 1)
@@ -89,12 +95,16 @@ __host__ __device__ inline ImpWsLayout imp_ws_layout(int G, int Tq, int Tk, int 
   off = align_up(off + 8 * L.u1_max, 256);
   L.units2 = off;
   off = align_up(off + 8 * L.u2_max, 256);
+  L.lse_stride = int64_t(kTile) * (ceil_div(Tq, kTile) + G);
+  L.redo_units = off;
+  off = align_up(off + 8 * int64_t(H) * (L.lse_stride / kTile), 256);
+  L.redo_flags = off;
+  off = align_up(off + 4 * int64_t(H) * (L.lse_stride / kTile), 256);
   L.n_grp = 8 * (ceil_div(Tk, kPairRows) + G);
   L.grp_ctr = off;
   off = align_up(off + 4 * L.n_grp, 256);
   L.part = off;
   off = align_up(off + 4 * int64_t(kMaxHeadGroups) * Tk, 1024);
-  L.lse_stride = int64_t(kTile) * (ceil_div(Tq, kTile) + G);
   L.part1 = off;
   if (L.ks > 1) off = align_up(off + 8 * int64_t(L.ks) * H * L.lse_stride, 256);
   L.lse_ctr = off;
@@ -132,6 +142,13 @@ struct ImpPassParams {
   int kspl;              // key chunks per (head, query pair) (1 = LSE written directly)
   float2* part1;
   int32_t* lse_ctr;
+  // pass 1, fixed row reference: a (head, query pair) with a row whose sum
+  // overflows is queued; a second launch (exact = 1, units = the queue)
+  // redoes it with a moving reference
+  int exact;
+  uint2* redo_units;
+  int32_t* redo_flags;
+  int32_t* redo_count;
 };
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {

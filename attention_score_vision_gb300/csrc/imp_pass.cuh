@@ -12,7 +12,13 @@
 //          S = Q K^T tile by tile on the tensor cores (tcgen05, accumulators
 //          in TMEM), each 128-key B tile multiplied by both A tiles, online
 //          max/sum per query row -> row LSE (kept as -LSE*log2 e, padded to
-//          128-row tiles per segment).
+//          128-row tiles per segment). Each row fixes its reference max on
+//          its first 64 columns; a (head, query pair) with a row whose sum
+//          then overflows fp32 is queued, and a second launch of the same
+//          kernel redoes the queue with a reference that follows the row
+//          max (nothing is queued unless the logits of a row climb more than
+//          ~88 above the maximum of its first 64 keys; the launch then exits
+//          at once).
 //   pass 2 units (segment, 256 keys, group of query heads): S^T = K Q^T with
 //          the keys on the MMA M dimension, so each epilogue thread owns one
 //          key and sums exp2(S*c - LSE2) over the query columns in registers:
@@ -242,9 +248,12 @@ __device__ __forceinline__ void column_sum_chunk(const uint32_t (&r)[32], const 
 
 
 // Pass 1 (row LSE), on 32 columns held as raw TMEM words. Per query row, m
-// is a reference max of S*c and l the sum of exp2(S*c - m) before the
-// current accumulators a; m only moves when the max of the next 64 columns
-// exceeds it by more than 8 (terms stay below 2^8), so rescaling is rare.
+// is a reference for S*c and l the sum of exp2(S*c - m) before the current
+// accumulators a. First launch (lazy): m is the max of the row's first 64
+// columns and stays there — the terms of later columns may exceed 1, and a
+// row whose logits climb ~128 (log2) above m overflows to inf, which the
+// unit end detects. Redo launch (exact): m moves whenever the max of the
+// next 64 columns exceeds it by more than 8 (terms stay below 2^8).
 // Columns at or beyond `valid` lie outside the segment and read as -inf.
 __device__ __forceinline__ void mask_cols(uint32_t (&r)[32], int valid) {
 #pragma unroll
@@ -292,7 +301,7 @@ __device__ __forceinline__ void cols_exp_sum(const uint32_t (&r)[32], float2 c2,
 // FULL: all 128 columns lie inside the segment (no masking).
 template <int PASS, bool FULL>
 __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int valid, const float4* nl,
-                                              float c, float2 c2, float& m, float& l,
+                                              float c, float2 c2, bool lazy, float& m, float& l,
                                               float2 (&acc)[2], uint64_t* acc_empty, int lane) {
   uint32_t r0[32], r1[32];
   tmem_ld32_async(taddr, r0);
@@ -306,7 +315,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int valid, const f
       mask_cols(r0, valid);
       mask_cols(r1, valid - 32);
     }
-    move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
+    if (!lazy || m == kNegInf) move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
     float2 nm2 = make_float2(-m, -m);
     cols_exp_sum(r0, c2, nm2, acc);
     tmem_ld32_async(taddr + 64, r0);
@@ -322,7 +331,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int valid, const f
         mask_cols(r0, valid - 64);
         mask_cols(r1, valid - 96);
       }
-      move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
+      if (!lazy) move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
       nm2 = make_float2(-m, -m);
       cols_exp_sum(r0, c2, nm2, acc);
       if (FULL || valid > 96) cols_exp_sum(r1, c2, nm2, acc);
@@ -381,6 +390,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t T = p.timeout_ns;
+
+  if (PASS == 1 && p.exact != 0) {
+    // Redo launch: the queue is complete once the first launch has finished;
+    // it is almost always empty, so leave before any set-up.
+    pdl_wait();
+    if (*reinterpret_cast<const volatile int*>(p.num_units) == 0) {
+      pdl_launch_dependents();
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -573,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(kbuf * kTile);
     const float c = p.c;
     const float2 c2 = make_float2(c, c);
+    const bool lazy = PASS == 1 && p.exact == 0;
     int s_it = 0, b_it = 0, unit_it = 0;
     bool ok = true;
     while (ok) {
@@ -620,9 +640,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int valid = vbase - bt * kTile;
           const float4* nl = reinterpret_cast<const float4*>(sLse + ls * kTile);
           if (valid >= kTile)
-            epilogue_tile<PASS, true>(taddr, valid, nl, c, c2, m, l, acc, &acc_empty[kbuf], lane);
+            epilogue_tile<PASS, true>(taddr, valid, nl, c, c2, lazy, m, l, acc, &acc_empty[kbuf], lane);
           else
-            epilogue_tile<PASS, false>(taddr, valid, nl, c, c2, m, l, acc, &acc_empty[kbuf], lane);
+            epilogue_tile<PASS, false>(taddr, valid, nl, c, c2, lazy, m, l, acc, &acc_empty[kbuf], lane);
         } else {
           tc_fence_before();
           __syncwarp();
@@ -701,6 +721,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               p.nlse2[lrow] = (valid && Lsum > 0.f) ? -lse2 : kNegInf;
               if (valid && p.lse_out != nullptr)
                 p.lse_out[int64_t(w.h) * p.Tq + w.q0 + qrow] = lse2 * 0.69314718055994531f;
+              // A sum past the fp32 range (inf, or NaN from inf * 0) under the
+              // fixed reference: queue the (head, query pair) for the redo
+              // launch, once (the flag is indexed by the pair's first tile).
+              const bool over = lazy && valid && !(Lsum <= 3.402823466e38f);
+              if (__any_sync(0xffffffffu, over) && lane == 0) {
+                const int64_t fi = int64_t(w.h) * (p.lse_stride / kTile) + w.qtile_base + 2 * w.pair;
+                if (atomicExch(p.redo_flags + fi, 1) == 0) {
+                  const int slot_r = atomicAdd(p.redo_count, 1);
+                  p.redo_units[slot_r] = make_uint2(uint32_t(w.g), (uint32_t(w.h) << 24) | uint32_t(w.pair));
+                }
+              }
             }
           } else {
             const int krow = w.pair * kPair + a_half * kTile + row;

@@ -115,8 +115,14 @@ __global__ void __launch_bounds__(THREADS) imp_prep_kernel(const int32_t* __rest
     hdr->num_units[1] = 0;
     hdr->sched_ctr[0] = 0;
     hdr->sched_ctr[1] = 0;
+    hdr->redo_count = 0;
+    hdr->fix_ctr = 0;
   }
   for (int64_t i = threadIdx.x; i < L.n_grp; i += THREADS) grp_ctr[i] = 0;
+  {
+    int32_t* redo_flags = reinterpret_cast<int32_t*>(ws + L.redo_flags);
+    for (int64_t i = threadIdx.x; i < int64_t(H) * (L.lse_stride / kTile); i += THREADS) redo_flags[i] = 0;
+  }
   if (L.ks > 1) {
     int32_t* lse_ctr = reinterpret_cast<int32_t*>(ws + L.lse_ctr);
     for (int64_t i = threadIdx.x; i < int64_t(H) * (L.lse_stride / 32); i += THREADS) lse_ctr[i] = 0;

@@ -306,9 +306,25 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     p1.kspl = L.ks;
     p1.part1 = reinterpret_cast<float2*>(ws + L.part1);
     p1.lse_ctr = reinterpret_cast<int32_t*>(ws + L.lse_ctr);
+    p1.redo_units = reinterpret_cast<uint2*>(ws + L.redo_units);
+    p1.redo_flags = reinterpret_cast<int32_t*>(ws + L.redo_flags);
+    p1.redo_count = &hdr->redo_count;
     const int grid = int(L.u1_max < sms ? L.u1_max : sms);
     e = launch_imp_pass(1, head_dim, fp8, maps, p1, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pass-1 launch");
+    // The redo launch: (head, query pair)s whose rows overflowed under the
+    // fixed reference, whole (no key chunks), with a moving reference.
+    ImpPassParams pr = p1;
+    pr.exact = 1;
+    pr.stall = 0;
+    pr.kspl = 1;
+    pr.units = p1.redo_units;
+    pr.num_units = &hdr->redo_count;
+    pr.sched_ctr = &hdr->fix_ctr;
+    const int64_t redo_max = int64_t(num_heads) * (L.lse_stride / kTile);
+    const int grid_r = int(redo_max < sms ? redo_max : sms);
+    e = launch_imp_pass(1, head_dim, fp8, maps, pr, grid_r, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "pass-1 redo launch");
   }
   if (stages & TSEL_IMP_STAGE_PASS2) {
     const CUtensorMap maps[4] = {km64, km16, qm64, qm16};
@@ -460,6 +476,15 @@ tsel_status tsel_read_device_status(const void* workspace, uint32_t* bits, void*
   if (e != cudaSuccess) return cuda_fail(e, "read status");
   if (bits) *bits = word;
   return word == 0 ? TSEL_OK : fail(TSEL_ERR_DEVICE_CHECK, "device status 0x%x", word);
+}
+
+tsel_status tsel_importance_redo_pairs(const void* workspace, int32_t* pairs, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (workspace == nullptr || pairs == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "null argument");
+  const auto* hdr = static_cast<const WsHeader*>(workspace);
+  cudaError_t e = cudaMemcpyAsync(pairs, &hdr->redo_count, sizeof(int32_t), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "read redo count");
 }
 
 tsel_status tsel_clear_device_status(void* workspace, void* stream_) {

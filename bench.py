@@ -552,6 +552,7 @@ def gpu_arm(args) -> None:
             per[n].append(e[j].elapsed_time(e[j + 1]))
     if tsel.tsel_read_device_status(ws) != 0:
         raise RuntimeError("device status set in the per-kernel loop")
+    redo_pairs = tsel.tsel_importance_redo_pairs(ws)
 
     # --- LSE-provided mode: the attention kernel's LSE reused, column pass only ---
     lse_given = lse.clone()
@@ -755,7 +756,9 @@ def gpu_arm(args) -> None:
     gather_bytes = K * (2 * 2 * D + 2 * 4 * P + 4 + 4) + 4 * 2 * (G + 1)
     kernels = {
         "prep": {"ms": mean["prep"]},
-        "pass1": {"ms": mean["pass1"], **roof1},
+        # the row-LSE pass and its redo launch (which exits at once when no
+        # row overflowed the fixed reference: redo_pairs = 0)
+        "pass1": {"ms": mean["pass1"], **roof1, "redo_pairs": redo_pairs},
         "pass2": {"ms": mean["pass2"], **roof2},
         "topk": {"ms": mean["topk"], "GB/s": topk_bytes / (mean["topk"] * 1e-3) / 1e9,
                  "hbm_frac": topk_bytes / (mean["topk"] * 1e-3) / hbm_peak},
@@ -805,7 +808,8 @@ def gpu_arm(args) -> None:
         "fp8": fp8,
         "small_requests": small,
         "workloads": sweep,
-        "gpu_launches": 5 * args.steps,
+        # per step: schedule, row-LSE pass, its redo launch, column pass, top-B, gather
+        "gpu_launches": 6 * args.steps,
         "clocks": clocks,
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
                   "ex2_per_s": ex2_peak, "ex2_per_clk_per_sm_at_max":

@@ -144,6 +144,14 @@ TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int tot
  * scores       out fp32 [total_k].
  * workspace    >= tsel_importance_workspace_size(num_seg, total_q, total_k,
  *              num_heads) bytes; holds the status word and the schedule.
+ *
+ * Kernels, in order on `stream` (no host synchronisation; capturable): the
+ * schedule kernel, the row-LSE pass, its redo launch, the column pass. The
+ * row-LSE pass fixes each row's reference max on its first 64 keys; a query
+ * pair with a row whose sum then leaves the fp32 range (logits more than ~88
+ * above that maximum) is redone by the redo launch with a moving reference,
+ * which otherwise exits at once. Results do not depend on which rows took
+ * the redo beyond fp32 rounding.
  */
 TSEL_API tsel_status tsel_importance(const void* q, int64_t q_row_stride,
                             const void* k, int64_t k_row_stride,
@@ -319,6 +327,12 @@ TSEL_API int tsel_keep_count(int n_tokens, int keep_permille);
  * word is zero, TSEL_ERR_DEVICE_CHECK when any bit is set, TSEL_ERR_CUDA on a
  * CUDA error. */
 TSEL_API tsel_status tsel_read_device_status(const void* workspace, uint32_t* bits, void* stream);
+
+/* Reads, after synchronising `stream`, how many (head, 256-query-row pair)s
+ * the last tsel_importance call on `workspace` sent to its redo launch (rows
+ * whose sum overflowed the fixed reference; see tsel_importance). 0 for
+ * nearly every input; a diagnostic, not needed for correct results. */
+TSEL_API tsel_status tsel_importance_redo_pairs(const void* workspace, int32_t* pairs, void* stream);
 
 /* Enqueues a reset of the device status word to zero. */
 TSEL_API tsel_status tsel_clear_device_status(void* workspace, void* stream);

@@ -209,6 +209,47 @@ def make_segments(lengths_q, lengths_k, num_heads, num_kv_heads, head_dim, *,
     )
 
 
+def make_far_keys(lengths, num_heads, num_kv_heads, head_dim, *, seed, far_positions,
+                  far_value, head_signs, noise=0.1, q_lead=4.0, name="far_keys") -> Workload:
+    """Self-attention segments whose logits climb far above the first keys.
+
+    Every Q and K entry is N(0, noise^2); query rows of head h add
+    ``q_lead * head_signs[h]`` to dimension 0, and the keys at the local
+    positions ``far_positions`` of every segment (those that exist) have
+    dimension 0 set to ``far_value`` on every KV head. With the default
+    1/sqrt(d) scale, such a key's logit is about
+    ``q_lead * far_value / sqrt(d) * sign`` while every other logit stays
+    within a few tenths of zero — a controlled gap between the largest logit
+    of a row and the largest logit among its first keys.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lk = np.asarray(lengths, dtype=np.int64)
+    cu = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    t = int(cu[-1])
+    q = _normal_f32(rng, (t, num_heads, head_dim)) * np.float32(noise)
+    k = _normal_f32(rng, (t, num_kv_heads, head_dim)) * np.float32(noise)
+    q[:, :, 0] += np.float32(q_lead) * np.asarray(head_signs, dtype=np.float32)[None, :]
+    for g in range(lk.shape[0]):
+        for p in far_positions:
+            if p < lk[g]:
+                k[cu[g] + p, :, 0] = np.float32(far_value)
+    hidden = _normal_f32(rng, (t, 16))
+    req_off = np.array([0, t], dtype=np.int32)
+    return Workload(
+        name=name,
+        q_bits=f32_to_bf16_bits(q),
+        k_bits=f32_to_bf16_bits(k),
+        cu_seqlens_q=cu,
+        cu_seqlens_k=cu.copy(),
+        req_tok_offsets=req_off,
+        keep_per_req=np.array([t // 2], dtype=np.int32),
+        hidden_bits=f32_to_bf16_bits(hidden),
+        pos=_pos_index(t),
+        softmax_scale=float(1.0 / np.sqrt(head_dim)),
+        meta={"seed": seed, "far_positions": list(far_positions), "far_value": far_value},
+    )
+
+
 def keep_floor(n: int, permille: int) -> int:
     """floor(n * permille / 1000) in integer arithmetic (budget rounding)."""
     return (int(n) * int(permille)) // 1000
