@@ -26,7 +26,7 @@ __all__ = [
     "tsel_importance_redo_pairs",
     "tsel_status_string", "tsel_last_error", "tsel_probe_ex2",
     "TSEL_DEV_SEQLENS", "TSEL_DEV_REQUESTS", "TSEL_DEV_KEEP_IDX", "TSEL_DEV_TIMEOUT", "TSEL_DEV_NAN",
-    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_SCORE_SUM", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
+    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_SCORE_SUM", "TSEL_IMP_ROWREF_FIXED", "TSEL_IMP_ROWREF_MOVING", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
 ]
 
 TSEL_OK = 0
@@ -47,6 +47,8 @@ TSEL_KEEP_FROM_DEVICE = -1
 TSEL_IMP_LSE_PROVIDED = 0x1
 TSEL_IMP_FP8_E4M3 = 0x2
 TSEL_IMP_SCORE_SUM = 0x4
+TSEL_IMP_ROWREF_FIXED = 0x8
+TSEL_IMP_ROWREF_MOVING = 0x20
 TSEL_IMP_TEST_STALL = 0x10000
 TSEL_IMP_STAGE_PREP = 0x100
 TSEL_IMP_STAGE_PASS1 = 0x200

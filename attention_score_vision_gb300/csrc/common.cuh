@@ -142,10 +142,11 @@ struct ImpPassParams {
   int kspl;              // key chunks per (head, query pair) (1 = LSE written directly)
   float2* part1;
   int32_t* lse_ctr;
-  // pass 1, fixed row reference: a (head, query pair) with a row whose sum
-  // overflows is queued; a second launch (exact = 1, units = the queue)
-  // redoes it with a moving reference
+  // pass 1, fixed row reference (exact = 0): a (head, query pair) with a row
+  // whose sum overflows is queued; a second launch (redo = 1, exact = 1,
+  // units = the queue) redoes it with a moving reference
   int exact;
+  int redo;
   uint2* redo_units;
   int32_t* redo_flags;
   int32_t* redo_count;

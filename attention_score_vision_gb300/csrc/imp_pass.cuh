@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t T = p.timeout_ns;
 
-  if (PASS == 1 && p.exact != 0) {
+  if (PASS == 1 && p.redo != 0) {
     // Redo launch: the queue is complete once the first launch has finished;
     // it is almost always empty, so leave before any set-up.
     pdl_wait();

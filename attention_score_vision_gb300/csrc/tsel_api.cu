@@ -15,6 +15,10 @@
 #include "common.cuh"
 
 namespace tsel {
+// Attended-pair bound above which the row-LSE pass fixes its row reference
+// (2^28: ~43 us of pass 1; the redo launch costs ~4 us in the chain).
+constexpr double kFixedRefMinPairs = 268435456.0;
+
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
                             int max_q, int max_k, int H, int HG, uint8_t* ws,
                             const ImpWsLayout& L, cudaStream_t stream);
@@ -199,9 +203,11 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   if (!(head_dim == 64 || head_dim == 80 || head_dim == 96 || head_dim == 112 || head_dim == 128))
     return fail(TSEL_ERR_UNSUPPORTED, "head_dim=%d (supported: 64, 80, 96, 112, 128)", head_dim);
   if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_FP8_E4M3 | TSEL_IMP_SCORE_SUM |
-                 TSEL_IMP_TEST_STALL | TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 |
-                 TSEL_IMP_STAGE_PASS2)) != 0)
+                 TSEL_IMP_ROWREF_FIXED | TSEL_IMP_ROWREF_MOVING | TSEL_IMP_TEST_STALL |
+                 TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2)) != 0)
     return fail(TSEL_ERR_UNSUPPORTED, "flags=0x%x", flags);
+  if ((flags & TSEL_IMP_ROWREF_FIXED) && (flags & TSEL_IMP_ROWREF_MOVING))
+    return fail(TSEL_ERR_INVALID_VALUE, "TSEL_IMP_ROWREF_FIXED and _MOVING are exclusive");
   const bool lse_provided = (flags & TSEL_IMP_LSE_PROVIDED) != 0;
   if (lse_provided && total_q > 0 && lse == nullptr)
     return fail(TSEL_ERR_INVALID_VALUE, "TSEL_IMP_LSE_PROVIDED needs the lse input");
@@ -310,12 +316,22 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     p1.redo_flags = reinterpret_cast<int32_t*>(ws + L.redo_flags);
     p1.redo_count = &hdr->redo_count;
     const int grid = int(L.u1_max < sms ? L.u1_max : sms);
+    // Fixed row reference (and its redo launch) only where the pass is long
+    // enough for the saved max to outweigh one more launch in the chain; the
+    // bound is H * total_q * max_seqlen_k attended pairs, about 40 us of
+    // pass 1 at the GB300 exp2 rate.
+    const bool fixed_ref =
+        (flags & TSEL_IMP_ROWREF_FIXED) ||
+        (!(flags & TSEL_IMP_ROWREF_MOVING) &&
+         double(num_heads) * double(total_q) * double(max_seqlen_k) >= kFixedRefMinPairs);
+    p1.exact = fixed_ref ? 0 : 1;
     e = launch_imp_pass(1, head_dim, fp8, maps, p1, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "pass-1 launch");
     // The redo launch: (head, query pair)s whose rows overflowed under the
     // fixed reference, whole (no key chunks), with a moving reference.
     ImpPassParams pr = p1;
     pr.exact = 1;
+    pr.redo = 1;
     pr.stall = 0;
     pr.kspl = 1;
     pr.units = p1.redo_units;
@@ -323,8 +339,10 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     pr.sched_ctr = &hdr->fix_ctr;
     const int64_t redo_max = int64_t(num_heads) * (L.lse_stride / kTile);
     const int grid_r = int(redo_max < sms ? redo_max : sms);
-    e = launch_imp_pass(1, head_dim, fp8, maps, pr, grid_r, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "pass-1 redo launch");
+    if (fixed_ref) {
+      e = launch_imp_pass(1, head_dim, fp8, maps, pr, grid_r, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "pass-1 redo launch");
+    }
   }
   if (stages & TSEL_IMP_STAGE_PASS2) {
     const CUtensorMap maps[4] = {km64, km16, qm64, qm16};

@@ -88,6 +88,10 @@ typedef enum tsel_status {
                                         softmax_scale ([LiteVLM] FP8 deployment) */
 #define TSEL_IMP_SCORE_SUM    0x4u   /* scores are the total attention received,
                                         sum_h sum_i P, not divided by H * Nq_g */
+#define TSEL_IMP_ROWREF_FIXED  0x8u  /* row-LSE pass: fixed row reference + redo launch, */
+#define TSEL_IMP_ROWREF_MOVING 0x20u /*   or moving reference, one launch; neither = chosen
+                                        by size (fixed from 2^28 = H*total_q*max_seqlen_k
+                                        attended pairs). Same results up to fp32 rounding. */
 #define TSEL_IMP_TEST_STALL   0x10000u /* test hook for failure detection: the pass kernels'
                                           scheduler publishes no work, every bounded wait
                                           runs out after ~50 ms and TSEL_DEV_TIMEOUT is set;
@@ -146,7 +150,8 @@ TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int tot
  *              num_heads) bytes; holds the status word and the schedule.
  *
  * Kernels, in order on `stream` (no host synchronisation; capturable): the
- * schedule kernel, the row-LSE pass, its redo launch, the column pass. The
+ * schedule kernel, the row-LSE pass, its redo launch (large problems only),
+ * the column pass. On large problems (or with TSEL_IMP_ROWREF_FIXED) the
  * row-LSE pass fixes each row's reference max on its first 64 keys; a query
  * pair with a row whose sum then leaves the fp32 range (logits more than ~88
  * above that maximum) is redone by the redo launch with a moving reference,

@@ -39,14 +39,16 @@ def _expected_pairs(lengths, signs):
     return pairs * sum(1 for s in signs if s > 0)
 
 
-def _run(tsel, w, ws=None):
+def _run(tsel, w, ws=None, flags=None):
+    # these problems are below the size that picks the fixed reference by itself
+    flags = tsel.TSEL_IMP_ROWREF_FIXED if flags is None else flags
     d = to_device(w)
     if ws is None:
         ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k,
                                                              w.num_heads), dtype=torch.uint8,
                          device="cuda")
     s, lse = tsel.tsel_importance(d["q"], d["k"], d["cu_q"], d["cu_k"], w.max_seqlen_q,
-                                  w.max_seqlen_k, workspace=ws)
+                                  w.max_seqlen_k, workspace=ws, flags=flags)
     torch.cuda.synchronize()
     return s.cpu().numpy(), lse.cpu().numpy(), tsel.tsel_importance_redo_pairs(ws), ws
 
@@ -112,6 +114,23 @@ def test_no_redo_on_seeded_workloads(tsel):
         assert redo == 0, name
 
 
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_moving_reference_needs_no_redo(tsel, name):
+    # the one-launch mode handles the same gap by moving its reference
+    w = _case(name, 128.0, seed=940 + len(name))
+    s, lse, redo, _ = _run(tsel, w, flags=tsel.TSEL_IMP_ROWREF_MOVING)
+    assert redo == 0
+    _check(w, s, lse)
+
+
+def test_fixed_and_moving_reference_agree(tsel):
+    w = W.make("six_views_1536")
+    s_f, lse_f, _, _ = _run(tsel, w, flags=tsel.TSEL_IMP_ROWREF_FIXED)
+    s_m, lse_m, _, _ = _run(tsel, w, flags=tsel.TSEL_IMP_ROWREF_MOVING)
+    np.testing.assert_allclose(lse_f, lse_m, rtol=1e-6, atol=1e-5)
+    np.testing.assert_allclose(s_f, s_m, rtol=1e-4, atol=0)
+
+
 def test_overflow_redo_e4m3(tsel):
     c = CASES["key_chunks"]
     w = W.to_e4m3(_case("key_chunks", 128.0, seed=930))
@@ -122,7 +141,8 @@ def test_overflow_redo_e4m3(tsel):
     cq = torch.from_numpy(w.cu_seqlens_q).cuda()
     ck = torch.from_numpy(w.cu_seqlens_k).cuda()
     s, lse = tsel.tsel_importance(q, k, cq, ck, w.max_seqlen_q, w.max_seqlen_k,
-                                  softmax_scale=w.softmax_scale, workspace=ws)
+                                  softmax_scale=w.softmax_scale, workspace=ws,
+                                  flags=tsel.TSEL_IMP_ROWREF_FIXED)
     assert tsel.tsel_importance_redo_pairs(ws) == _expected_pairs(c["lengths"], c["signs"])
     assert tsel.tsel_read_device_status(ws) == 0
     _check(w, s.cpu().numpy(), lse.cpu().numpy(), fmt="e4m3")
