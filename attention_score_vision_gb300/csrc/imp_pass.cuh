@@ -30,11 +30,14 @@
 // Two A tiles per unit halve the operand bytes each B tile costs per element
 // (the shared-memory feed, not the tensor cores, limited 128-row units).
 //
-// CTA layout (576 threads, one CTA per SM, persistent, units fetched from a
+// CTA layout (608 threads, one CTA per SM, persistent, units fetched from a
 // global counter in longest-first order):
 //   warp 0      TMA producer (A tile pairs, B tiles, LSE slices)
-//   warp 1      TMEM allocator + MMA issuer (one thread): per B tile, one
-//               128x128 accumulator for each A tile
+//   warp 1      TMEM allocator + MMA issuer for the B tiles of parity 0 (one
+//               thread): per B tile, one 128x128 accumulator for each A tile
+//   warp 18     MMA issuer for the B tiles of parity 1. With one issuer for
+//               both parities, a warpgroup that released its accumulator
+//               late held up the other parity's next tile as well.
 //   warps 2-17  four epilogue warpgroups; warpgroup 2*par + a owns TMEM
 //               accumulator 2*par + a (A tile a, B tiles of parity par);
 //               warp w reads TMEM lanes 32*(w%4).. . Each warp loads its
@@ -64,7 +67,8 @@ constexpr int kLseSlots = 8;        // LSE slices in flight (pass 2)
 constexpr int kSchedSlots = 4;      // scheduler ring depth
 constexpr int kEpiWarps = 16;       // four warpgroups
 constexpr int kEpiFirstWarp = 2;
-constexpr int kThreads = 32 * (kEpiFirstWarp + kEpiWarps);  // 576
+constexpr int kMma1Warp = kEpiFirstWarp + kEpiWarps;        // second MMA issuer
+constexpr int kThreads = 32 * (kEpiFirstWarp + kEpiWarps + 1);  // 608
 
 // Shared-memory tile geometry. bf16 rows are D*2 bytes, split into 64-column
 // chunks (128-byte swizzle) and 16-column chunks (32-byte swizzle). E4M3 rows
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&a_full[i], 1);
-      mbar_init(&a_empty[i], 1);
+      mbar_init(&a_empty[i], 2);             // both MMA issuers
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&comb_full[i], 4);
@@ -423,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kSchedSlots; ++i) {
       mbar_init(&sch_full[i], 1);
-      mbar_init(&sch_empty[i], 1 + kEpiWarps);
+      mbar_init(&sch_empty[i], 2 + kEpiWarps);
     }
-    mbar_init(mma_done, 1);
+    mbar_init(mma_done, 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -528,9 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kMma1Warp) {
+    // ------------------------------------------------------------ MMA issuers
+    // Each walks every unit and B tile, and issues the tiles of its parity.
     if (lane == 0) {
+      const int mypar = warp == 1 ? 0 : 1;
       int s_it = 0, a_it = 0, b_it = 0;
       bool ok = true;
       while (ok) {
@@ -552,6 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                               ? nbt
                               : (min(w.h1, (ag + 1) * group) - max(w.h, ag * group)) * nbt;
           for (int bi = 0; bi < n_b; ++bi) {
+            if ((b_it & 1) != mypar) {
+              ++b_it;
+              continue;
+            }
             const int bs = b_it % S;
             if (!wait_bounded(&b_full[bs], (b_it / S) & 1, abort_flag, T)) { ok = false; break; }
             const uint32_t use = uint32_t(b_it >> 1) & 1u;
@@ -682,7 +692,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float l0 = l + part;
             float M = fmaxf(m, o0);
             float Lsum = 0.f;
-            if (M > kNegInf) Lsum = l0 * ex2(m - M) + o1 * ex2(o0 - M);
+            // Which warpgroup holds the even tiles of the unit depends on
+            // the CTA's earlier units: the merge is written symmetric (two
+            // rounded products, one add; no contraction into an FMA) so the
+            // result does not.
+            if (M > kNegInf) Lsum = __fadd_rn(__fmul_rn(l0, ex2(m - M)), __fmul_rn(o1, ex2(o0 - M)));
             const int qrow = w.pair * kPair + a_half * kTile + row;
             const bool valid = qrow < w.nq;
             const int qtile = w.qtile_base + w.pair * 2 + a_half;

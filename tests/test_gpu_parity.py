@@ -88,3 +88,27 @@ def test_determinism_bitwise(tsel):
         b = run_path(tsel, w, dev)
         assert np.array_equal(a["scores"].view(np.uint32), b["scores"].view(np.uint32))
         assert np.array_equal(a["keep_idx"], b["keep_idx"])
+
+
+@pytest.mark.parametrize("flags_name", ["TSEL_IMP_ROWREF_FIXED", "TSEL_IMP_ROWREF_MOVING"])
+def test_determinism_bitwise_uneven_units(tsel, flags_name):
+    """Images of 256..4096 tokens give units with odd B-tile counts, so which
+    epilogue warpgroup takes the even tiles of a unit changes with the
+    scheduling history of its CTA; the row LSE and the scores must not."""
+    w = W.make("thirty_images")
+    dev = to_device(w)
+    flags = getattr(tsel, flags_name)
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k,
+                                                         w.num_heads), dtype=torch.uint8,
+                     device="cuda")
+    ref = None
+    for _ in range(4):
+        s, lse = tsel.tsel_importance(dev["q"], dev["k"], dev["cu_q"], dev["cu_k"], w.max_seqlen_q,
+                                      w.max_seqlen_k, flags=flags, workspace=ws)
+        got = (s.view(torch.int32).cpu().numpy(), lse.view(torch.int32).cpu().numpy())
+        if ref is None:
+            ref = got
+        else:
+            assert np.array_equal(ref[0], got[0])
+            assert np.array_equal(ref[1], got[1])
+    assert tsel.tsel_read_device_status(ws) == 0
