@@ -31,8 +31,9 @@ void record_error(const char* msg);  // tsel_api.cu
 
 namespace {
 
-// 16 MiB: enough for the schedule and padded row-LSE buffer of, e.g., 16
-// heads over 131072 query tokens in 128 segments (about 9.5 MB).
+// 16 MiB: enough for the schedule, the per-head-group partial sums and the
+// padded row-LSE buffer of, e.g., 16 heads over 131072 query and key tokens
+// in 128 segments (about 14.1 MB).
 constexpr size_t kNoallocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
