@@ -117,6 +117,29 @@ def test_empty_segments_and_missing_queries(tsel):
     np.testing.assert_allclose(lse[fin], lse_ref[fin], rtol=1e-5, atol=1e-4)
 
 
+@pytest.mark.parametrize("G,max_len,H,Hkv", [(1500, 40, 4, 2), (4000, 8, 2, 1)])
+def test_thousands_of_small_segments(tsel, G, max_len, H, Hkv):
+    # more segments than the schedule kernel has threads: its block-wide
+    # bucket sort, scans and unit lists loop; many segments share a tile
+    rng = np.random.default_rng(G)
+    L = rng.integers(0, max_len + 1, size=G)
+    n_req = 7
+    cuts = np.linspace(0, G, n_req + 1).astype(int)
+    groups = np.diff(cuts).tolist()
+    per_req = np.add.reduceat(L, cuts[:-1])
+    keep = [int(x) // 3 for x in per_req]
+    w = W.make_segments(L, L, H, Hkv, 64, seed=310 + G, hidden_dim=64, requests=groups,
+                        keep_per_req=keep)
+    out = run_path(tsel, w)
+    assert out["status"] == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(out["scores"], s_ref) <= REL_TOL
+    fin = np.isfinite(lse_ref)
+    np.testing.assert_allclose(out["lse"][fin], lse_ref[fin], rtol=1e-5, atol=1e-4)
+    assert np.all(np.isneginf(out["lse"][~fin]))
+    check_selection_exact(w, out)
+
+
 def test_zero_queries_uniform_and_one_hot_closed_form(tsel):
     nq, nk, d, H = 130, 300, 64, 2
     q = np.zeros((nq, H, d), np.float32)
@@ -194,6 +217,21 @@ def test_topk_many_requests_and_negative_zero(tsel):
     got, cu, st = _topk(tsel, s, off, keep)
     ref, cref = oracle.select_topk(np.where(s == 0, 0.0, s).astype(np.float32), off, keep)
     assert st == 0 and np.array_equal(got, ref) and np.array_equal(cu, cref)
+
+
+@pytest.mark.parametrize("big", [4096, 4097, 9000])
+def test_topk_small_requests_with_one_large(tsel, big):
+    # one CTA per request (the average request is small); requests from
+    # empty to thousands of tokens, sizes on both sides of 4096
+    rng = np.random.default_rng(big)
+    sizes = [big] + [10, 0, 37, 1, 256, 3, 99, 64]
+    off = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    s = (rng.integers(0, 50, off[-1]).astype(np.float32) * 0.25)   # many ties
+    keep = [big // 3, 10, 0, 20, 1, 255, 0, 99, 7]
+    got, cu, st = _topk(tsel, s, off, keep)
+    ref, cref = oracle.select_topk(s, off, keep)
+    assert st == 0
+    assert np.array_equal(got, ref) and np.array_equal(cu, cref)
 
 
 def test_gather_fp32_rows_and_no_pos(tsel):
