@@ -6,19 +6,27 @@
 // keep ratio r.
 //
 // One thread-block cluster per request (up to 16 CTAs, one slice of the
-// request's tokens each, cached in shared memory):
-//   1. radix select, 8 bits per round from the top: every CTA builds
-//      warp-private histograms of its slice and adds bin b into CTA
-//      (b % cluster size) through distributed shared memory (the merge is
-//      spread over the cluster); after one cluster barrier every CTA reads the
-//      merged bins and picks the same digit. After four rounds the key of the
-//      B-th largest score is known (keys are fp32 bits mapped to an
-//      order-preserving uint32);
-//   2. each CTA's counts of keys above / equal to that key follow from its
-//      own per-round histograms; they are sent to every CTA, and each CTA
-//      writes its kept indices in index order through block-wide prefix sums:
-//      tokens above the key, and the lowest-index tokens equal to it. The
-//      output is deterministic.
+// request's tokens each, cached in shared memory; keys are fp32 bits mapped
+// to an order-preserving uint32):
+//   1. radix select in three rounds of 11, 11 and 10 bits from the top. Every
+//      CTA counts the digits of its slice's still-matching keys into a
+//      2048-bin histogram; group g of four bins is added into CTA
+//      (g % cluster size) through distributed shared memory, so the merge
+//      spreads over the cluster. After one cluster barrier each thread reads
+//      its four merged bins and a block-wide suffix scan (descending bins)
+//      finds the digit holding the B-th largest key; every CTA picks the same
+//      digit. After the last round the key of the B-th largest score and the
+//      number of tokens equal to it that are kept are known;
+//   2. before the last barrier each CTA publishes, per bin group of the last
+//      round, its count of keys above that group (the keys above the prefix
+//      in the first two rounds plus the last round's higher groups). After
+//      the barrier each CTA reads the other CTAs' counts at the chosen digit,
+//      so its output offset needs no further exchange;
+//   3. each CTA writes its kept indices in index order: per pass of 4096
+//      tokens one block-wide prefix sum gives every thread's slots (tokens
+//      above the key, and the lowest-index tokens equal to it), the indices
+//      are staged in shared memory and stored with coalesced writes.
+// The output is deterministic and independent of the cluster size.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -30,11 +38,18 @@ namespace cg = cooperative_groups;
 namespace tsel {
 
 constexpr int kTopkThreads = 512;
-static_assert(kTopkThreads >= 256, "one thread per histogram bin");
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kTopkItems = 16;              // consecutive tokens per thread when compacting
-constexpr int kTopkMaxCluster = kMaxClusterCtas;
-constexpr int kTopkCacheKeys = 16384;       // keys cached in shared memory per CTA
+constexpr int kTopkBins = 2048;                    // 11-bit digits (the last round uses 1024)
+constexpr int kTopkGroups = kTopkBins / 4;         // one group of four bins per thread
+static_assert(kTopkGroups == kTopkThreads, "one bin group per thread");
+constexpr int kTopkItems = 8;                      // consecutive tokens per thread when compacting
+constexpr int kTopkPass = kTopkThreads * kTopkItems;   // tokens per compaction pass (<= 65535)
+constexpr int kTopkCacheKeys = 16384;              // keys cached in shared memory per CTA
+constexpr int kTopkLoad = 8;                       // score loads in flight per thread
+
+// Digit of round `round` (0, 1, 2): bits 31..21, 20..10, 9..0.
+__device__ __forceinline__ int topk_shift(int round) { return round == 0 ? 21 : (round == 1 ? 10 : 0); }
+__device__ __forceinline__ uint32_t topk_dmask(int round) { return round == 2 ? 1023u : 2047u; }
 
 __device__ __forceinline__ int warp_incl_scan(int x) {
   const int lane = threadIdx.x & 31;
@@ -43,6 +58,23 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
+  return x;
+}
+
+// Sum over this lane and the lanes above it.
+__device__ __forceinline__ int warp_suffix_scan(int x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  return x;
+}
+
+__device__ __forceinline__ int warp_sum(int x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
 }
 
@@ -64,14 +96,31 @@ __device__ __forceinline__ int topk_block_scan(int v, int* warp_sums, int& total
   return excl;
 }
 
-struct TopkShared {
-  int whist[kTopkWarps][256];      // warp-private histograms
-  int hist[4][256];                // merged histograms (bin b lives in CTA b % csize)
-  int cnt_gt[kTopkMaxCluster];     // every CTA's counts above / equal to the threshold
-  int cnt_eq[kTopkMaxCluster];
+// Sum of w[i] over the warps i > warp (16 per-warp values).
+__device__ __forceinline__ int sum_warps_above(const int* w, int warp) {
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < kTopkWarps; i += 4) {
+    const int4 v = *reinterpret_cast<const int4*>(w + i);
+    s += (i > warp ? v.x : 0) + (i + 1 > warp ? v.y : 0) + (i + 2 > warp ? v.z : 0) +
+         (i + 3 > warp ? v.w : 0);
+  }
+  return s;
+}
+
+struct __align__(16) TopkShared {
+  int local[3][kTopkBins];    // this CTA's digit counts per round
+  int merged[3][kTopkBins];   // cluster-wide counts; group g lives in CTA g % cluster size
+  int above_grp[kTopkGroups]; // last round: this CTA's keys above bin group g (see step 2)
+  int stage[kTopkPass];       // kept indices of one compaction pass
+  __align__(16) int wsum[kTopkWarps];
+  __align__(16) int wsum2[kTopkWarps];
   int warp_sums[32];
-  int digit, above, bad, nan_seen;
+  int sel_digit[3], sel_above[3];
+  int out_base, eq_before;
+  int bad, nan_seen;
 };
+static_assert(sizeof(TopkShared) % 16 == 0, "key cache follows at a 16-byte boundary");
 
 __global__ void __launch_bounds__(kTopkThreads)
     topk_cluster_kernel(const float* __restrict__ scores, int total_tokens,
@@ -79,16 +128,47 @@ __global__ void __launch_bounds__(kTopkThreads)
                         const int32_t* __restrict__ keep, int total_keep,
                         int32_t* __restrict__ keep_idx, int32_t* __restrict__ cu_keep,
                         uint32_t* status) {
-  __shared__ TopkShared sh;
-  extern __shared__ uint32_t skeys[];  // kTopkCacheKeys
+  extern __shared__ __align__(16) unsigned char topk_smem[];
+  TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
+  uint32_t* skeys = reinterpret_cast<uint32_t*>(topk_smem + sizeof(TopkShared));  // kTopkCacheKeys
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = int(cluster.block_rank());
   const int csize = int(cluster.num_blocks());
   const int r = int(blockIdx.x) / csize;
-  const bool solo = csize == 1;   // one CTA: plain block barriers, no exchange
+  const bool solo = csize == 1;   // one CTA: no distributed shared memory, no cluster barrier
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch_dependents();
+
+  // Histograms start at zero in every CTA before any remote add (the first
+  // cluster barrier below orders the two). `local` and `merged` are adjacent.
+  {
+    int4* h = reinterpret_cast<int4*>(&sh.local[0][0]);
+    for (int i = tid; i < 6 * kTopkBins / 4; i += kTopkThreads) h[i] = make_int4(0, 0, 0, 0);
+    if (tid == 0) sh.nan_seen = 0;
+    if (tid < 3) {
+      sh.sel_digit[tid] = 0;
+      sh.sel_above[tid] = 0;
+    }
+  }
   pdl_wait();
+
+  // ---- this CTA's slice; its first scores in flight during the checks ------
+  const int lo_raw = req_off[r], hi_raw = req_off[r + 1];
+  const int B = keep[r];
+  const int lo = min(max(lo_raw, 0), total_tokens);
+  const int hi = min(max(hi_raw, lo), total_tokens);
+  const int n = hi - lo;
+  const int chunk = (n + csize - 1) / csize;
+  const int c0 = min(n, crank * chunk), c1 = min(n, c0 + chunk);
+  const int len = c1 - c0;
+  const float* s = scores + lo + c0;
+  const bool cached = len <= kTopkCacheKeys;
+  float f[kTopkLoad];
+#pragma unroll
+  for (int j = 0; j < kTopkLoad; ++j) {
+    const int i = j * kTopkThreads + tid;
+    f[j] = i < len ? __ldcg(s + i) : 0.f;
+  }
 
   // ---- request checks and output offset (identical in every CTA) --------
   int part = 0, neg = 0;
@@ -97,13 +177,13 @@ __global__ void __launch_bounds__(kTopkThreads)
     part += b;
     neg |= b < 0;
   }
+  neg = __syncthreads_or(neg);
   int before;
   (void)topk_block_scan(part, sh.warp_sums, before);
-  const int lo = req_off[r], hi = req_off[r + 1];
-  const int B = keep[r];
   if (tid == 0) {
     int bad = neg;
-    if (lo < 0 || hi < lo || hi > total_tokens || B < 0 || B > hi - lo) bad = 1;
+    if (lo_raw < 0 || hi_raw < lo_raw || hi_raw > total_tokens || B < 0 || B > hi_raw - lo_raw)
+      bad = 1;
     if (before < 0) bad = 1;
     if (total_keep >= 0) {
       if (int64_t(before) + B > total_keep) bad = 1;
@@ -112,12 +192,6 @@ __global__ void __launch_bounds__(kTopkThreads)
       bad = 1;   // budgets from the device: keep_idx has room for total_tokens entries
     }
     sh.bad = bad;
-    sh.nan_seen = 0;
-  }
-  for (int i = tid; i < 4 * 256; i += kTopkThreads) (&sh.hist[0][0])[i] = 0;
-  if (tid < kTopkMaxCluster) {
-    sh.cnt_gt[tid] = 0;
-    sh.cnt_eq[tid] = 0;
   }
   __syncthreads();
   if (sh.bad) {
@@ -129,28 +203,22 @@ __global__ void __launch_bounds__(kTopkThreads)
     if (r == 0) cu_keep[0] = 0;
     cu_keep[r + 1] = before + B;
   }
-  const int n = hi - lo;
   if (B == 0) return;
 
-  // This CTA's slice of the request.
-  const int chunk = (n + csize - 1) / csize;
-  const int c0 = min(n, crank * chunk), c1 = min(n, c0 + chunk);
-  const int len = c1 - c0;
-  const float* s = scores + lo + c0;
-  const bool cached = len <= kTopkCacheKeys;
-  // Histograms are zeroed everywhere before any remote add: arrive now, wait
-  // after the slice is loaded.
+  // Zeroed histograms are released to the cluster now; the wait comes after
+  // the slice is loaded.
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   int nan_local = 0;
-  for (int i0 = 0; i0 < len; i0 += kTopkThreads * 8) {
-    float f[8];
+  for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkLoad) {
+    if (i0 > 0) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {   // eight independent loads in flight per thread
-      const int i = i0 + j * kTopkThreads + tid;
-      f[j] = i < len ? __ldcg(s + i) : 0.f;
+      for (int j = 0; j < kTopkLoad; ++j) {
+        const int i = i0 + j * kTopkThreads + tid;
+        f[j] = i < len ? __ldcg(s + i) : 0.f;
+      }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kTopkLoad; ++j) {
       const int i = i0 + j * kTopkThreads + tid;
       nan_local |= (f[j] != f[j]);
       if (cached && i < len) skeys[i] = order_key(f[j]);
@@ -161,111 +229,132 @@ __global__ void __launch_bounds__(kTopkThreads)
   __syncthreads();
 
   // ---- radix select -------------------------------------------------------
-  // Bin b of each round is merged in CTA (b % csize), so the merge spreads
-  // over the cluster instead of queueing at one SM. Thread t keeps this
-  // CTA's count of bin t, from which the counts above / at the threshold
-  // follow without another pass over the keys.
   uint32_t prefix = 0, mask = 0;
-  int remaining = B;  // how many still to take among keys matching `prefix`
-  int gt_part = 0, eq_part = 0;   // this CTA: keys above / equal to the threshold (bin tid)
+  int remaining = B;   // how many still to take among keys matching `prefix`
+  int gt_part = 0;     // this thread's bin groups: this CTA's keys above the prefix
+  int4 lv = make_int4(0, 0, 0, 0);   // this thread's four bins of this CTA's counts
 #pragma unroll 1
-  for (int round = 0; round < 4; ++round) {
-    const int shift = 24 - 8 * round;
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&sh.whist[0][0])[i] = 0;
-    __syncthreads();
+  for (int round = 0; round < 3; ++round) {
+    const int shift = topk_shift(round);
+    const uint32_t dmask = topk_dmask(round);
+    int* loc = sh.local[round];
     for (int i0 = 0; i0 < len; i0 += kTopkThreads) {
       const int i = i0 + tid;
       const bool in = i < len;
       const uint32_t k = in ? (cached ? skeys[i] : order_key(s[i])) : 0u;
       const bool match = in && (k & mask) == prefix;
-      const uint32_t d = (k >> shift) & 255u;
-      // aggregate equal digits within the warp: one shared atomic per value
-      const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0x100u);
-      if (match && (__ffs(peers) - 1) == lane) atomicAdd(&sh.whist[warp][d], __popc(peers));
+      const uint32_t d = (k >> shift) & dmask;
+      if (round == 0) {
+        // the top digits of real scores take few values: one shared atomic
+        // per distinct digit of the warp
+        const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0xFFFFFFFFu);
+        if (match && (__ffs(peers) - 1) == lane) atomicAdd(&loc[d], __popc(peers));
+      } else if (match) {
+        atomicAdd(&loc[d], 1);
+      }
     }
     __syncthreads();
-    int v = 0;   // this CTA's count of bin tid (threads >= 256 hold no bin)
-    if (tid < 256) {
-#pragma unroll
-      for (int w = 0; w < kTopkWarps; ++w) v += sh.whist[w][tid];
-    }
-    if (solo) {
-      if (tid < 256) sh.hist[round][tid] = v;
-      __syncthreads();
-    } else {
-      if (v) atomicAdd(cluster.map_shared_rank(&sh.hist[round][tid], tid % csize), v);
+    lv = reinterpret_cast<const int4*>(loc)[tid];
+    int* mrg = sh.merged[round];
+    if (!solo) {
+      int* dst = cluster.map_shared_rank(mrg + 4 * tid, tid % csize);
+      if (lv.x) atomicAdd(dst, lv.x);
+      if (lv.y) atomicAdd(dst + 1, lv.y);
+      if (lv.z) atomicAdd(dst + 2, lv.z);
+      if (lv.w) atomicAdd(dst + 3, lv.w);
+      if (round == 2) {
+        // Step 2: this CTA's keys above bin group tid = keys above the prefix
+        // in rounds 0-1 (summed over the block) + last-round keys in groups > tid.
+        const int sum4 = lv.x + lv.y + lv.z + lv.w;
+        const int g01 = warp_sum(gt_part);
+        const int sfx = warp_suffix_scan(sum4);
+        if (lane == 0) {
+          sh.wsum[warp] = g01;
+          sh.wsum2[warp] = sfx;
+        }
+        __syncthreads();
+        const int all01 = sum_warps_above(sh.wsum, -1);
+        sh.above_grp[tid] = all01 + (sfx - sum4) + sum_warps_above(sh.wsum2, warp);
+        __syncthreads();   // wsum is reused by the digit search below
+      }
       cluster.sync();
     }
-    if (warp == 0) {
-      // lane l owns bins 255-8l ... 248-8l (descending)
-      int c[8];
-      int sum = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int b = 255 - 8 * lane - j;
-        c[j] = solo ? sh.hist[round][b] : *cluster.map_shared_rank(&sh.hist[round][b], b % csize);
-        sum += c[j];
-      }
-      const int incl = warp_incl_scan(sum);
-      int above = incl - sum;  // count in bins above this lane's bins
-      int found = -1, found_above = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (found < 0 && above < remaining && above + c[j] >= remaining) {
-          found = 255 - 8 * lane - j;
-          found_above = above;
+    const int4 c = solo ? lv
+                        : *reinterpret_cast<const int4*>(
+                              cluster.map_shared_rank(mrg + 4 * tid, tid % csize));
+
+    // Digit search, bins descending: thread t holds bins 4t+3 .. 4t.
+    const int sum4 = c.x + c.y + c.z + c.w;
+    const int x = warp_suffix_scan(sum4);
+    if (lane == 0) sh.wsum[warp] = x;
+    __syncthreads();
+    int a = x - sum4 + sum_warps_above(sh.wsum, warp);   // keys in higher bins
+    if (a < remaining) {
+      int dg = -1;
+      if (a + c.w >= remaining) {
+        dg = 4 * tid + 3;
+      } else {
+        a += c.w;
+        if (a + c.z >= remaining) {
+          dg = 4 * tid + 2;
+        } else {
+          a += c.z;
+          if (a + c.y >= remaining) {
+            dg = 4 * tid + 1;
+          } else {
+            a += c.y;
+            if (a + c.x >= remaining) dg = 4 * tid;
+          }
         }
-        above += c[j];
       }
-      if (found >= 0) {
-        sh.digit = found;
-        sh.above = found_above;
+      if (dg >= 0) {
+        sh.sel_digit[round] = dg;
+        sh.sel_above[round] = a;
       }
     }
     __syncthreads();
-    const int digit = sh.digit;
-    gt_part += tid > digit ? v : 0;
-    if (round == 3) eq_part = tid == digit ? v : 0;
+    const int digit = sh.sel_digit[round];
+    if (round < 2) {
+      const int b0 = 4 * tid;
+      gt_part += (b0 > digit ? lv.x : 0) + (b0 + 1 > digit ? lv.y : 0) +
+                 (b0 + 2 > digit ? lv.z : 0) + (b0 + 3 > digit ? lv.w : 0);
+    }
     prefix |= uint32_t(digit) << shift;
-    mask |= 255u << shift;
-    remaining -= sh.above;
-    __syncthreads();
+    mask |= dmask << shift;
+    remaining -= sh.sel_above[round];
   }
   if (tid == 0 && sh.nan_seen) set_status(status, TSEL_DEV_NAN);   // this CTA's slice
   const uint32_t thr = prefix;
-  const int need_eq = remaining;  // tokens equal to the threshold to keep (request-wide)
+  const int need_eq = remaining;   // tokens equal to the threshold to keep (request-wide)
 
-  // ---- per-CTA counts, sent to every CTA of the cluster ----------------------
+  // ---- output offset: the other CTAs' counts at the chosen digit -------------
   if (!solo) {
-    int gt_total, eq_total;
-    (void)topk_block_scan(gt_part, sh.warp_sums, gt_total);
-    (void)topk_block_scan(eq_part, sh.warp_sums, eq_total);
-    if (tid < csize) {
-      *cluster.map_shared_rank(&sh.cnt_gt[crank], tid) = gt_total;
-      *cluster.map_shared_rank(&sh.cnt_eq[crank], tid) = eq_total;
+    if (warp == 0) {
+      const int d2 = sh.sel_digit[2];
+      const int g = d2 >> 2, j = d2 & 3;
+      int gt = 0, eq = 0;
+      if (lane < csize) {
+        const int ab = *cluster.map_shared_rank(&sh.above_grp[g], lane);
+        const int4 l = *reinterpret_cast<const int4*>(cluster.map_shared_rank(&sh.local[2][4 * g], lane));
+        gt = ab + (j < 3 ? l.w : 0) + (j < 2 ? l.z : 0) + (j < 1 ? l.y : 0);
+        eq = j == 3 ? l.w : (j == 2 ? l.z : (j == 1 ? l.y : l.x));
+      }
+      // lane c: CTA c's counts; exclusive prefixes give this CTA's output slot
+      const int e_incl = warp_incl_scan(eq);
+      const int e_before = e_incl - eq;
+      const int take = max(0, min(eq, need_eq - e_before));
+      const int t_incl = warp_incl_scan(gt + take);
+      if (lane == crank) {
+        sh.out_base = t_incl - (gt + take);   // output slots of CTAs before this one
+        sh.eq_before = e_before;              // tied tokens in CTAs before this one
+      }
     }
-    cluster.sync();   // no CTA reads another CTA's shared memory after this point
+    // This CTA reads no other CTA's shared memory after this point; no CTA
+    // leaves before every CTA has arrived here (wait at the end).
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    __syncthreads();
   }
-  if (solo) {
-    if (tid == 0) {
-      sh.above = 0;
-      sh.digit = 0;
-    }
-  } else if (warp == 0) {
-    // lane c: CTA c's counts; exclusive prefixes give this CTA's output slot
-    const int e = lane < csize ? sh.cnt_eq[lane] : 0;
-    const int g = lane < csize ? sh.cnt_gt[lane] : 0;
-    const int e_incl = warp_incl_scan(e);
-    const int e_before = e_incl - e;
-    const int take = max(0, min(e, need_eq - e_before));
-    const int t_incl = warp_incl_scan(g + take);
-    if (lane == crank) {
-      sh.above = t_incl - (g + take);   // output slots of CTAs before this one
-      sh.digit = e_before;              // tied tokens in CTAs before this one
-    }
-  }
-  __syncthreads();
-  const int out_base = sh.above, eq_before = sh.digit;
+  const int out_base = solo ? 0 : sh.out_base, eq_before = solo ? 0 : sh.eq_before;
 
   // ---- compaction in index order --------------------------------------------
   // kTopkItems consecutive tokens per thread; one block scan per pass gives
@@ -273,7 +362,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   // in front of each thread (16-bit halves: a pass has <= 4096 tokens).
   int32_t* out = keep_idx + before + out_base;
   int written = 0, eq_seen = eq_before;
-  for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkItems) {
+  for (int i0 = 0; i0 < len; i0 += kTopkPass) {
     const int ib = i0 + tid * kTopkItems;
     uint32_t k[kTopkItems];
     if (cached && ib + kTopkItems <= len) {
@@ -302,7 +391,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     int tot;
     const int pre = topk_block_scan((n_eq << 16) | n_gt, sh.warp_sums, tot);
     int eq_rank = eq_seen + (pre >> 16);
-    int pos = written + (pre & 0xFFFF) + max(0, min(pre >> 16, need_eq - eq_seen));
+    int pos = (pre & 0xFFFF) + max(0, min(pre >> 16, need_eq - eq_seen));
 #pragma unroll
     for (int j = 0; j < kTopkItems; ++j) {
       const bool valid = ib + j < len;
@@ -311,19 +400,24 @@ __global__ void __launch_bounds__(kTopkThreads)
         t = eq_rank < need_eq;
         ++eq_rank;
       }
-      if (t) out[pos++] = lo + c0 + ib + j;
+      if (t) sh.stage[pos++] = lo + c0 + ib + j;
     }
     const int tot_eq = tot >> 16, tot_gt = tot & 0xFFFF;
-    written += tot_gt + max(0, min(tot_eq, need_eq - eq_seen));
+    const int cnt = tot_gt + max(0, min(tot_eq, need_eq - eq_seen));
+    __syncthreads();
+    for (int i = tid; i < cnt; i += kTopkThreads) out[written + i] = sh.stage[i];
+    written += cnt;
     eq_seen += tot_eq;
+    if (i0 + kTopkPass < len) __syncthreads();   // the stage is refilled
   }
+  if (!solo) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
                         int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
                         int32_t* cu_keep, uint32_t* status, cudaStream_t stream) {
   static int cache[128][5] = {};
-  const size_t dyn = size_t(kTopkCacheKeys) * sizeof(uint32_t);
+  const size_t dyn = sizeof(TopkShared) + size_t(kTopkCacheKeys) * sizeof(uint32_t);
   cudaError_t e = cudaSuccess;
   const int csize = usable_cluster_size(topk_cluster_kernel,
                                         cluster_size_for(total_tokens, num_req), kTopkThreads,

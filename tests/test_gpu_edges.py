@@ -234,6 +234,26 @@ def test_topk_small_requests_with_one_large(tsel, big):
     assert np.array_equal(got, ref) and np.array_equal(cu, cref)
 
 
+@pytest.mark.parametrize("sizes", [[10000] * 4, [20000, 20001], [40000], [300000]])
+def test_topk_cluster_sizes_and_uncached_slices(tsel, sizes):
+    # clusters of 4, 8 and 16 CTAs (average request 10K, 20K, 40K tokens) and,
+    # at 300K tokens, slices too long for the per-CTA key cache; scores span
+    # many binades (every digit of every round is used), with negative values,
+    # signed zeros and long runs of ties
+    rng = np.random.default_rng(sum(sizes))
+    off = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    n = off[-1]
+    s = (np.exp2(rng.uniform(-40, 40, n)) * rng.choice([-1.0, 1.0], n, p=[0.1, 0.9])).astype(np.float32)
+    s[rng.integers(0, n, n // 5)] = np.float32(0.75)
+    s[rng.integers(0, n, n // 50)] = np.float32(-0.0)
+    s[rng.integers(0, n, n // 50)] = np.float32(0.0)
+    keep = [(i * 37 + 11) * sz // 97 % (sz + 1) for i, sz in enumerate(sizes)]
+    got, cu, st = _topk(tsel, s, off, keep)
+    ref, cref = oracle.select_topk(np.where(s == 0, 0.0, s).astype(np.float32), off, keep)
+    assert st == 0
+    assert np.array_equal(got, ref) and np.array_equal(cu, cref)
+
+
 def test_gather_fp32_rows_and_no_pos(tsel):
     hidden = torch.randn(500, 12, device="cuda", dtype=torch.float32)
     cu = i32([0, 100, 100, 500])
