@@ -10,18 +10,19 @@
 // to an order-preserving uint32):
 //   1. radix select in three rounds of 11, 11 and 10 bits from the top. Every
 //      CTA counts the digits of its slice's still-matching keys into a
-//      2048-bin histogram; group g of four bins is added into CTA
-//      (g % cluster size) through distributed shared memory, so the merge
-//      spreads over the cluster. After one cluster barrier each thread reads
-//      its four merged bins and a block-wide suffix scan (descending bins)
-//      finds the digit holding the B-th largest key; every CTA picks the same
-//      digit. After the last round the key of the B-th largest score and the
-//      number of tokens equal to it that are kept are known;
-//   2. before the last barrier each CTA publishes, per bin group of the last
-//      round, its count of keys above that group (the keys above the prefix
-//      in the first two rounds plus the last round's higher groups). After
-//      the barrier each CTA reads the other CTAs' counts at the chosen digit,
-//      so its output offset needs no further exchange;
+//      2048-bin histogram (shared atomics); group g of four bins is added
+//      into CTA (g % cluster size) through distributed shared memory, so the
+//      merge spreads over the cluster. After one cluster barrier each thread
+//      gathers its four merged bins, and after one block barrier every warp
+//      finds the digit holding the B-th largest key on its own (warp totals,
+//      then the groups of one warp, then the bins of one group; bins
+//      descending). After the last round the key of the B-th largest score
+//      and the number of tokens equal to it still to keep are known;
+//   2. before the last cluster barrier each CTA publishes, per warp and per
+//      bin group of the last round, its counts of keys above the first two
+//      rounds' prefix and in higher groups. After the barrier one warp of
+//      each CTA reads every CTA's counts at the chosen digit, so the output
+//      offset needs no further exchange;
 //   3. each CTA writes its kept indices in index order: per pass of 4096
 //      tokens one block-wide prefix sum gives every thread's slots (tokens
 //      above the key, and the lowest-index tokens equal to it), the indices
@@ -78,22 +79,24 @@ __device__ __forceinline__ int warp_sum(int x) {
   return x;
 }
 
-// Exclusive scan of one value per thread over the block; `total` gets the sum.
+// Exclusive scan of one value per thread over the block; `total` gets the
+// sum. One block barrier: every warp adds the totals of the warps below it.
+// The caller separates two calls by a barrier (warp_sums is rewritten).
 __device__ __forceinline__ int topk_block_scan(int v, int* warp_sums, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int x = warp_incl_scan(v);
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
-  if (warp == 0) {
-    const int w = lane < kTopkWarps ? warp_sums[lane] : 0;
-    const int s = warp_incl_scan(w);
-    if (lane < kTopkWarps) warp_sums[lane] = s;
+  int below = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < kTopkWarps; i += 4) {
+    const int4 w = *reinterpret_cast<const int4*>(warp_sums + i);
+    below += (i < warp ? w.x : 0) + (i + 1 < warp ? w.y : 0) + (i + 2 < warp ? w.z : 0) +
+             (i + 3 < warp ? w.w : 0);
+    all += w.x + w.y + w.z + w.w;
   }
-  __syncthreads();
-  const int excl = x - v + (warp > 0 ? warp_sums[warp - 1] : 0);
-  total = warp_sums[kTopkWarps - 1];
-  __syncthreads();
-  return excl;
+  total = all;
+  return x - v + below;
 }
 
 // Sum of w[i] over the warps i > warp (16 per-warp values).
@@ -110,17 +113,59 @@ __device__ __forceinline__ int sum_warps_above(const int* w, int warp) {
 
 struct __align__(16) TopkShared {
   int local[3][kTopkBins];    // this CTA's digit counts per round
-  int merged[3][kTopkBins];   // cluster-wide counts; group g lives in CTA g % cluster size
-  int above_grp[kTopkGroups]; // last round: this CTA's keys above bin group g (see step 2)
+  int merged[3][kTopkBins];   // cluster-wide counts; bin group g lives in CTA g % cluster size
+  int bins[kTopkBins];        // this round's cluster-wide counts, gathered for the digit search
+  int grp_sfx[kTopkGroups];   // last round: this CTA's keys in the groups above g of g's warp
   int stage[kTopkPass];       // kept indices of one compaction pass
-  __align__(16) int wsum[kTopkWarps];
-  __align__(16) int wsum2[kTopkWarps];
-  int warp_sums[32];
-  int sel_digit[3], sel_above[3];
+  __align__(16) int wtot[kTopkWarps];       // digit search: per-warp bin totals
+  __align__(16) int gt_w[kTopkWarps];       // last round: per-warp keys above the rounds 0-1 prefix
+  __align__(16) int grp_w[kTopkWarps];      // last round: per-warp totals of this CTA's counts
+  __align__(16) int warp_sums[kTopkWarps];  // compaction scan
+  __align__(16) long long pre_w[kTopkWarps];  // budgets of earlier requests, per warp
+  int neg_w[kTopkWarps];
   int out_base, eq_before;
-  int bad, nan_seen;
+  int nan_seen;
+  int pad_[3];
 };
 static_assert(sizeof(TopkShared) % 16 == 0, "key cache follows at a 16-byte boundary");
+
+// Finds the bin holding the `remaining`-th largest key, bins descending, in
+// every warp at once (no further block barrier): the warp totals give the
+// warp whose bin groups hold it, that warp's 32 groups give the group, the
+// group's four bins give the bin. Returns the digit; `above` gets the keys
+// in higher bins. wtot[w] = sum of the bins of groups 32w .. 32w+31.
+__device__ __forceinline__ int find_digit(const int* bins, const int* wtot, int remaining,
+                                          int& above) {
+  const int lane = threadIdx.x & 31;
+  const int v = lane < kTopkWarps ? wtot[lane] : 0;
+  const int xs = warp_suffix_scan(v);
+  const unsigned hw = __ballot_sync(0xffffffffu, lane < kTopkWarps && xs - v < remaining && xs >= remaining);
+  const int w = hw ? __ffs(hw) - 1 : 0;
+  const int above_w = __shfl_sync(0xffffffffu, xs - v, w);
+  const int4 c = reinterpret_cast<const int4*>(bins)[32 * w + lane];
+  const int sum4 = c.x + c.y + c.z + c.w;
+  const int xg = warp_suffix_scan(sum4);
+  const int a0 = above_w + xg - sum4;   // keys in groups above this lane's
+  const unsigned hg = __ballot_sync(0xffffffffu, a0 < remaining && a0 + sum4 >= remaining);
+  const int g = hg ? __ffs(hg) - 1 : 0;
+  int a = __shfl_sync(0xffffffffu, a0, g);
+  const int cw = __shfl_sync(0xffffffffu, c.w, g), cz = __shfl_sync(0xffffffffu, c.z, g);
+  const int cy = __shfl_sync(0xffffffffu, c.y, g);
+  const int base = 4 * (32 * w + g);
+  int digit;
+  if (a + cw >= remaining) {
+    digit = base + 3;
+  } else if ((a += cw) + cz >= remaining) {
+    digit = base + 2;
+  } else if ((a += cz) + cy >= remaining) {
+    digit = base + 1;
+  } else {
+    a += cy;
+    digit = base;
+  }
+  above = a;
+  return digit;
+}
 
 __global__ void __launch_bounds__(kTopkThreads)
     topk_cluster_kernel(const float* __restrict__ scores, int total_tokens,
@@ -145,10 +190,6 @@ __global__ void __launch_bounds__(kTopkThreads)
     int4* h = reinterpret_cast<int4*>(&sh.local[0][0]);
     for (int i = tid; i < 6 * kTopkBins / 4; i += kTopkThreads) h[i] = make_int4(0, 0, 0, 0);
     if (tid == 0) sh.nan_seen = 0;
-    if (tid < 3) {
-      sh.sel_digit[tid] = 0;
-      sh.sel_above[tid] = 0;
-    }
   }
   pdl_wait();
 
@@ -170,35 +211,43 @@ __global__ void __launch_bounds__(kTopkThreads)
     f[j] = i < len ? __ldcg(s + i) : 0.f;
   }
 
-  // ---- request checks and output offset (identical in every CTA) --------
-  int part = 0, neg = 0;
+  // ---- request checks and output offset (every thread, every CTA alike) ----
+  long long part = 0;
+  int neg = 0;
   for (int i = tid; i < r; i += kTopkThreads) {
     const int b = keep[i];
     part += b;
     neg |= b < 0;
   }
-  neg = __syncthreads_or(neg);
-  int before;
-  (void)topk_block_scan(part, sh.warp_sums, before);
-  if (tid == 0) {
-    int bad = neg;
-    if (lo_raw < 0 || hi_raw < lo_raw || hi_raw > total_tokens || B < 0 || B > hi_raw - lo_raw)
-      bad = 1;
-    if (before < 0) bad = 1;
-    if (total_keep >= 0) {
-      if (int64_t(before) + B > total_keep) bad = 1;
-      if (r == num_req - 1 && int64_t(before) + B != total_keep) bad = 1;
-    } else if (int64_t(before) + B > total_tokens) {
-      bad = 1;   // budgets from the device: keep_idx has room for total_tokens entries
-    }
-    sh.bad = bad;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  neg = __any_sync(0xffffffffu, neg);
+  if (lane == 0) {
+    sh.pre_w[warp] = part;
+    sh.neg_w[warp] = neg;
   }
   __syncthreads();
-  if (sh.bad) {
+  long long before64 = 0;
+  bool bad = false;
+#pragma unroll
+  for (int w = 0; w < kTopkWarps; ++w) {
+    before64 += sh.pre_w[w];
+    bad |= sh.neg_w[w] != 0;
+  }
+  if (lo_raw < 0 || hi_raw < lo_raw || hi_raw > total_tokens || B < 0 || B > hi_raw - lo_raw)
+    bad = true;
+  if (total_keep >= 0) {
+    if (before64 + B > total_keep) bad = true;
+    if (r == num_req - 1 && before64 + B != total_keep) bad = true;
+  } else if (before64 + B > total_tokens) {
+    bad = true;   // budgets from the device: keep_idx has room for total_tokens entries
+  }
+  if (bad) {
     // every CTA of the cluster takes this branch together (same request)
     if (tid == 0 && crank == 0) set_status(status, TSEL_DEV_REQUESTS);
     return;
   }
+  const int before = int(before64);
   if (tid == 0 && crank == 0) {
     if (r == 0) cu_keep[0] = 0;
     cu_keep[r + 1] = before + B;
@@ -232,88 +281,59 @@ __global__ void __launch_bounds__(kTopkThreads)
   uint32_t prefix = 0, mask = 0;
   int remaining = B;   // how many still to take among keys matching `prefix`
   int gt_part = 0;     // this thread's bin groups: this CTA's keys above the prefix
-  int4 lv = make_int4(0, 0, 0, 0);   // this thread's four bins of this CTA's counts
+  int digit = 0;
 #pragma unroll 1
   for (int round = 0; round < 3; ++round) {
     const int shift = topk_shift(round);
     const uint32_t dmask = topk_dmask(round);
     int* loc = sh.local[round];
-    for (int i0 = 0; i0 < len; i0 += kTopkThreads) {
-      const int i = i0 + tid;
-      const bool in = i < len;
-      const uint32_t k = in ? (cached ? skeys[i] : order_key(s[i])) : 0u;
-      const bool match = in && (k & mask) == prefix;
-      const uint32_t d = (k >> shift) & dmask;
-      if (round == 0) {
-        // the top digits of real scores take few values: one shared atomic
-        // per distinct digit of the warp
-        const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0xFFFFFFFFu);
-        if (match && (__ffs(peers) - 1) == lane) atomicAdd(&loc[d], __popc(peers));
-      } else if (match) {
-        atomicAdd(&loc[d], 1);
+    if (round == 2 && !solo) {
+      const int g = warp_sum(gt_part);
+      if (lane == 0) sh.gt_w[warp] = g;
+    }
+    for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkLoad) {
+      uint32_t kk[kTopkLoad];
+#pragma unroll
+      for (int j = 0; j < kTopkLoad; ++j) {
+        const int i = i0 + j * kTopkThreads + tid;
+        kk[j] = i < len ? (cached ? skeys[i] : order_key(s[i])) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < kTopkLoad; ++j) {
+        const bool match = i0 + j * kTopkThreads + tid < len && (kk[j] & mask) == prefix;
+        if (match) atomicAdd(&loc[(kk[j] >> shift) & dmask], 1);
       }
     }
     __syncthreads();
-    lv = reinterpret_cast<const int4*>(loc)[tid];
-    int* mrg = sh.merged[round];
+    const int4 lv = reinterpret_cast<const int4*>(loc)[tid];   // bins 4 tid .. 4 tid + 3
+    const int* bins = loc;
     if (!solo) {
+      int* mrg = sh.merged[round];
       int* dst = cluster.map_shared_rank(mrg + 4 * tid, tid % csize);
       if (lv.x) atomicAdd(dst, lv.x);
       if (lv.y) atomicAdd(dst + 1, lv.y);
       if (lv.z) atomicAdd(dst + 2, lv.z);
       if (lv.w) atomicAdd(dst + 3, lv.w);
       if (round == 2) {
-        // Step 2: this CTA's keys above bin group tid = keys above the prefix
-        // in rounds 0-1 (summed over the block) + last-round keys in groups > tid.
+        // published for the other CTAs' output offsets (read after the barrier)
         const int sum4 = lv.x + lv.y + lv.z + lv.w;
-        const int g01 = warp_sum(gt_part);
-        const int sfx = warp_suffix_scan(sum4);
-        if (lane == 0) {
-          sh.wsum[warp] = g01;
-          sh.wsum2[warp] = sfx;
-        }
-        __syncthreads();
-        const int all01 = sum_warps_above(sh.wsum, -1);
-        sh.above_grp[tid] = all01 + (sfx - sum4) + sum_warps_above(sh.wsum2, warp);
-        __syncthreads();   // wsum is reused by the digit search below
+        const int x = warp_suffix_scan(sum4);
+        sh.grp_sfx[tid] = x - sum4;
+        if (lane == 0) sh.grp_w[warp] = x;
       }
       cluster.sync();
-    }
-    const int4 c = solo ? lv
-                        : *reinterpret_cast<const int4*>(
-                              cluster.map_shared_rank(mrg + 4 * tid, tid % csize));
-
-    // Digit search, bins descending: thread t holds bins 4t+3 .. 4t.
-    const int sum4 = c.x + c.y + c.z + c.w;
-    const int x = warp_suffix_scan(sum4);
-    if (lane == 0) sh.wsum[warp] = x;
-    __syncthreads();
-    int a = x - sum4 + sum_warps_above(sh.wsum, warp);   // keys in higher bins
-    if (a < remaining) {
-      int dg = -1;
-      if (a + c.w >= remaining) {
-        dg = 4 * tid + 3;
-      } else {
-        a += c.w;
-        if (a + c.z >= remaining) {
-          dg = 4 * tid + 2;
-        } else {
-          a += c.z;
-          if (a + c.y >= remaining) {
-            dg = 4 * tid + 1;
-          } else {
-            a += c.y;
-            if (a + c.x >= remaining) dg = 4 * tid;
-          }
-        }
-      }
-      if (dg >= 0) {
-        sh.sel_digit[round] = dg;
-        sh.sel_above[round] = a;
-      }
+      const int4 c = *reinterpret_cast<const int4*>(cluster.map_shared_rank(mrg + 4 * tid, tid % csize));
+      reinterpret_cast<int4*>(sh.bins)[tid] = c;
+      const int t = warp_sum(c.x + c.y + c.z + c.w);
+      if (lane == 0) sh.wtot[warp] = t;
+      bins = sh.bins;
+    } else {
+      const int t = warp_sum(lv.x + lv.y + lv.z + lv.w);
+      if (lane == 0) sh.wtot[warp] = t;
     }
     __syncthreads();
-    const int digit = sh.sel_digit[round];
+    int above;
+    digit = find_digit(bins, sh.wtot, remaining, above);
     if (round < 2) {
       const int b0 = 4 * tid;
       gt_part += (b0 > digit ? lv.x : 0) + (b0 + 1 > digit ? lv.y : 0) +
@@ -321,7 +341,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     }
     prefix |= uint32_t(digit) << shift;
     mask |= dmask << shift;
-    remaining -= sh.sel_above[round];
+    remaining -= above;
   }
   if (tid == 0 && sh.nan_seen) set_status(status, TSEL_DEV_NAN);   // this CTA's slice
   const uint32_t thr = prefix;
@@ -330,13 +350,22 @@ __global__ void __launch_bounds__(kTopkThreads)
   // ---- output offset: the other CTAs' counts at the chosen digit -------------
   if (!solo) {
     if (warp == 0) {
-      const int d2 = sh.sel_digit[2];
-      const int g = d2 >> 2, j = d2 & 3;
+      const int g = digit >> 2, j = digit & 3;
       int gt = 0, eq = 0;
       if (lane < csize) {
-        const int ab = *cluster.map_shared_rank(&sh.above_grp[g], lane);
-        const int4 l = *reinterpret_cast<const int4*>(cluster.map_shared_rank(&sh.local[2][4 * g], lane));
-        gt = ab + (j < 3 ? l.w : 0) + (j < 2 ? l.z : 0) + (j < 1 ? l.y : 0);
+        const TopkShared* o = cluster.map_shared_rank(&sh, lane);
+        int tot = 0;
+#pragma unroll
+        for (int w = 0; w < kTopkWarps; w += 4) {
+          const int4 a = *reinterpret_cast<const int4*>(o->gt_w + w);
+          const int4 b = *reinterpret_cast<const int4*>(o->grp_w + w);
+          tot += a.x + a.y + a.z + a.w;
+          const int gw = g >> 5;
+          tot += (w > gw ? b.x : 0) + (w + 1 > gw ? b.y : 0) + (w + 2 > gw ? b.z : 0) +
+                 (w + 3 > gw ? b.w : 0);
+        }
+        const int4 l = *reinterpret_cast<const int4*>(&o->local[2][4 * g]);
+        gt = tot + o->grp_sfx[g] + (j < 3 ? l.w : 0) + (j < 2 ? l.z : 0) + (j < 1 ? l.y : 0);
         eq = j == 3 ? l.w : (j == 2 ? l.z : (j == 1 ? l.y : l.x));
       }
       // lane c: CTA c's counts; exclusive prefixes give this CTA's output slot
@@ -352,16 +381,16 @@ __global__ void __launch_bounds__(kTopkThreads)
     // This CTA reads no other CTA's shared memory after this point; no CTA
     // leaves before every CTA has arrived here (wait at the end).
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    __syncthreads();
   }
-  const int out_base = solo ? 0 : sh.out_base, eq_before = solo ? 0 : sh.eq_before;
 
   // ---- compaction in index order --------------------------------------------
   // kTopkItems consecutive tokens per thread; one block scan per pass gives
   // both the tied tokens (for their rank) and the tokens above the threshold
-  // in front of each thread (16-bit halves: a pass has <= 4096 tokens).
-  int32_t* out = keep_idx + before + out_base;
-  int written = 0, eq_seen = eq_before;
+  // in front of each thread (16-bit halves: a pass has <= 4096 tokens). The
+  // output offset written by warp 0 above is read after the first scan's
+  // barrier.
+  int32_t* out = keep_idx + before;
+  int written = 0, eq_seen = 0;
   for (int i0 = 0; i0 < len; i0 += kTopkPass) {
     const int ib = i0 + tid * kTopkItems;
     uint32_t k[kTopkItems];
@@ -390,6 +419,10 @@ __global__ void __launch_bounds__(kTopkThreads)
     }
     int tot;
     const int pre = topk_block_scan((n_eq << 16) | n_gt, sh.warp_sums, tot);
+    if (i0 == 0 && !solo) {
+      out += sh.out_base;
+      eq_seen = sh.eq_before;
+    }
     int eq_rank = eq_seen + (pre >> 16);
     int pos = (pre & 0xFFFF) + max(0, min(pre >> 16, need_eq - eq_seen));
 #pragma unroll
@@ -405,10 +438,11 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int tot_eq = tot >> 16, tot_gt = tot & 0xFFFF;
     const int cnt = tot_gt + max(0, min(tot_eq, need_eq - eq_seen));
     __syncthreads();
+    // (every thread has read warp_sums and the stage is read here before the
+    // next pass's first barrier, so the next pass may rewrite both)
     for (int i = tid; i < cnt; i += kTopkThreads) out[written + i] = sh.stage[i];
     written += cnt;
     eq_seen += tot_eq;
-    if (i0 + kTopkPass < len) __syncthreads();   // the stage is refilled
   }
   if (!solo) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
