@@ -7,9 +7,11 @@
 // independent copy and the new per-image boundaries are lower bounds of the
 // old ones in keep_idx.
 //
-// Rows are copied with 16-byte vector loads/stores, one warp per row, several
-// rows in flight per warp (HBM-bound: the algorithmic bytes are the kept rows
-// read once and written once).
+// Rows are copied with 16-byte streaming loads/stores. Each warp takes two
+// consecutive kept rows at a time and issues every load of both rows before
+// its stores (rows of up to 4 KB stay in registers), so each lane keeps up to
+// 16 loads in flight (HBM-bound: the algorithmic bytes are the kept rows read
+// once and written once).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -18,7 +20,8 @@
 namespace tsel {
 
 constexpr int kGatherThreads = 256;
-constexpr int kGatherUnroll = 4;
+constexpr int kGatherRows = 2;     // kept rows per warp per step
+constexpr int kGatherMaxVpl = 8;   // 16-byte vectors per lane per row held in registers
 
 __device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int v) {
   int lo = 0, hi = n;
@@ -40,6 +43,9 @@ __device__ __forceinline__ int lower_bound_i32(const int32_t* a, int n, int v) {
   return lo;
 }
 
+// VPL = 16-byte vectors per lane per row (rows of up to 32 * VPL vectors in
+// registers); VPL = 0 copies rows of any length in a loop.
+template <int VPL>
 __global__ void __launch_bounds__(kGatherThreads)
     gather_kernel(const uint8_t* __restrict__ hidden, int64_t row_stride_bytes, int row_vecs,
                   const int32_t* __restrict__ pos, int pos_dim,
@@ -67,27 +73,99 @@ __global__ void __launch_bounds__(kGatherThreads)
   for (int g = gtid; g <= G; g += gridDim.x * kGatherThreads)
     out_cu[g] = lower_bound_i32(keep_idx, K, __ldg(cu_k + g));
 
-  for (int k = gwarp; k < K; k += nwarps) {
-    const int t = __ldg(keep_idx + k);
-    const bool ok = t >= 0 && t < Tk && (k == 0 || __ldg(keep_idx + k - 1) < t);
-    if (!ok) {
-      if (lane == 0) set_status(status, TSEL_DEV_KEEP_IDX);
-      continue;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(hidden + int64_t(t) * row_stride_bytes);
-    uint4* dst = reinterpret_cast<uint4*>(out_hidden + int64_t(k) * row_vecs * 16);
-    int v = lane;
-    for (; v + 32 * (kGatherUnroll - 1) < row_vecs; v += 32 * kGatherUnroll) {
-      uint4 x[kGatherUnroll];
+  // Image of a token: boundaries <= t, minus one (a ballot when they fit a warp).
+  const bool few_images = G < 32;
+  const int cu_lane = few_images && lane <= G ? __ldg(cu_k + lane) : 0x7FFFFFFF;
+
+  for (int k0 = kGatherRows * gwarp; k0 < K; k0 += kGatherRows * nwarps) {
+    int t[kGatherRows];
+    bool ok[kGatherRows];
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) x[u] = __ldcs(src + v + 32 * u);
-#pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) __stcs(dst + v + 32 * u, x[u]);
+    for (int r = 0; r < kGatherRows; ++r) {
+      const int k = k0 + r;
+      t[r] = k < K ? __ldg(keep_idx + k) : -1;
+      const int prev = k > 0 && k < K ? __ldg(keep_idx + k - 1) : -1;
+      ok[r] = k < K && t[r] >= 0 && t[r] < Tk && prev < t[r];
+      if (k < K && !ok[r] && lane == 0) set_status(status, TSEL_DEV_KEEP_IDX);
     }
-    for (; v < row_vecs; v += 32) __stcs(dst + v, __ldcs(src + v));
-    if (lane < pos_dim) out_pos[int64_t(k) * pos_dim + lane] = __ldg(pos + int64_t(t) * pos_dim + lane);
-    if (lane == 0) out_img[k] = upper_bound_i32(cu_k, G + 1, t) - 1;
+    if (VPL > 0) {
+      uint4 x[kGatherRows][VPL > 0 ? VPL : 1];
+#pragma unroll
+      for (int r = 0; r < kGatherRows; ++r) {
+        const uint4* src = reinterpret_cast<const uint4*>(hidden + int64_t(t[r]) * row_stride_bytes);
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+          const int v = lane + 32 * u;
+          if (ok[r] && v < row_vecs) x[r][u] = __ldcs(src + v);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kGatherRows; ++r) {
+        uint4* dst = reinterpret_cast<uint4*>(out_hidden + int64_t(k0 + r) * row_vecs * 16);
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+          const int v = lane + 32 * u;
+          if (ok[r] && v < row_vecs) __stcs(dst + v, x[r][u]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < kGatherRows; ++r) {
+        if (!ok[r]) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(hidden + int64_t(t[r]) * row_stride_bytes);
+        uint4* dst = reinterpret_cast<uint4*>(out_hidden + int64_t(k0 + r) * row_vecs * 16);
+        int v = lane;
+        for (; v + 32 * (kGatherMaxVpl - 1) < row_vecs; v += 32 * kGatherMaxVpl) {
+          uint4 x[kGatherMaxVpl];
+#pragma unroll
+          for (int u = 0; u < kGatherMaxVpl; ++u) x[u] = __ldcs(src + v + 32 * u);
+#pragma unroll
+          for (int u = 0; u < kGatherMaxVpl; ++u) __stcs(dst + v + 32 * u, x[u]);
+        }
+        for (; v < row_vecs; v += 32) __stcs(dst + v, __ldcs(src + v));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kGatherRows; ++r) {
+      if (!ok[r]) continue;
+      const int k = k0 + r;
+      if (lane < pos_dim)
+        out_pos[int64_t(k) * pos_dim + lane] = __ldg(pos + int64_t(t[r]) * pos_dim + lane);
+      if (few_images) {
+        const int img = __popc(__ballot_sync(0xffffffffu, cu_lane <= t[r])) - 1;
+        if (lane == 0) out_img[k] = img;
+      } else if (lane == 0) {
+        out_img[k] = upper_bound_i32(cu_k, G + 1, t[r]) - 1;
+      }
+    }
   }
+}
+
+template <int VPL>
+static cudaError_t launch_gather_vpl(int num_sms, int64_t warps_needed, cudaStream_t stream,
+                                     const uint8_t* hidden, int64_t row_stride_bytes, int row_vecs,
+                                     const int32_t* pos, int pos_dim, const int32_t* cu_k, int G,
+                                     int Tk, const int32_t* keep_idx, int K, const int32_t* K_dev,
+                                     uint8_t* out_hidden, int32_t* out_pos, int32_t* out_img,
+                                     int32_t* out_cu, uint32_t* status) {
+  static int resident[128] = {};   // blocks per SM, per device (0 = not asked yet)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = dev >= 0 && dev < 128 ? resident[dev] : 0;
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gather_kernel<VPL>, kGatherThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    if (dev >= 0 && dev < 128) resident[dev] = per_sm;
+  }
+  int64_t blocks = (warps_needed * 32 + kGatherThreads - 1) / kGatherThreads;
+  const int64_t max_blocks = int64_t(num_sms) * per_sm;
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(gather_kernel<VPL>, dim3(unsigned(blocks)), kGatherThreads, 0, stream, 1,
+                       hidden, row_stride_bytes, row_vecs, pos, pos_dim, cu_k, G, Tk, keep_idx, K,
+                       K_dev, out_hidden, out_pos, out_img, out_cu, status);
 }
 
 cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_bytes,
@@ -95,15 +173,33 @@ cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_
                           const int32_t* keep_idx, int K, const int32_t* K_dev,
                           void* out_hidden, int32_t* out_pos, int32_t* out_img, int32_t* out_cu,
                           uint32_t* status, int num_sms, cudaStream_t stream) {
-  const int64_t warps_needed = K > G + 1 ? K : G + 1;
-  int64_t blocks = (warps_needed * 32 + kGatherThreads - 1) / kGatherThreads;
-  const int64_t max_blocks = int64_t(num_sms) * (2048 / kGatherThreads);
-  if (blocks > max_blocks) blocks = max_blocks;
-  if (blocks < 1) blocks = 1;
-  return launch_kernel(gather_kernel, dim3(unsigned(blocks)), kGatherThreads, 0, stream, 1,
-                       static_cast<const uint8_t*>(hidden), row_stride_bytes, row_bytes / 16, pos,
-                       pos_dim, cu_k, G, Tk, keep_idx, K, K_dev, static_cast<uint8_t*>(out_hidden),
-                       out_pos, out_img, out_cu, status);
+  const int row_vecs = row_bytes / 16;
+  const int64_t row_warps = (int64_t(K) + kGatherRows - 1) / kGatherRows;
+  const int64_t warps_needed = row_warps > G + 1 ? row_warps : G + 1;
+  const int vpl = (row_vecs + 31) / 32;
+  const auto* h = static_cast<const uint8_t*>(hidden);
+  auto* oh = static_cast<uint8_t*>(out_hidden);
+#define TSEL_GATHER_CASE(N)                                                                    \
+  case N:                                                                                      \
+    return launch_gather_vpl<N>(num_sms, warps_needed, stream, h, row_stride_bytes, row_vecs,  \
+                                pos, pos_dim, cu_k, G, Tk, keep_idx, K, K_dev, oh, out_pos,    \
+                                out_img, out_cu, status);
+  switch (vpl) {
+    TSEL_GATHER_CASE(1)
+    TSEL_GATHER_CASE(2)
+    TSEL_GATHER_CASE(3)
+    TSEL_GATHER_CASE(4)
+    TSEL_GATHER_CASE(5)
+    TSEL_GATHER_CASE(6)
+    TSEL_GATHER_CASE(7)
+    TSEL_GATHER_CASE(8)
+    default:
+      // no hidden rows (vpl 0) or rows longer than 4 KB
+      return launch_gather_vpl<0>(num_sms, warps_needed, stream, h, row_stride_bytes, row_vecs,
+                                  pos, pos_dim, cu_k, G, Tk, keep_idx, K, K_dev, oh, out_pos,
+                                  out_img, out_cu, status);
+  }
+#undef TSEL_GATHER_CASE
 }
 
 }  // namespace tsel

@@ -3,8 +3,10 @@
 // Every kernel is launched with programmatic stream serialization (PDL): the
 // next kernel on the stream may start its prologue while the previous one
 // drains. Each kernel therefore calls pdl_launch_dependents() once all of its
-// CTAs are resident and pdl_wait() before it touches memory that an earlier
-// kernel on the stream writes or reads, so stream order holds for data.
+// CTAs are resident (the top-B kernel only after its radix rounds, so the
+// compaction's CTAs do not sit on its SMs meanwhile) and pdl_wait() before it
+// touches memory that an earlier kernel on the stream writes or reads, so
+// stream order holds for data.
 //
 // Cluster kernels (top-B, dynamic budget) run one thread-block cluster per
 // request, sized from the average request length and capped by what the

@@ -182,7 +182,6 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int r = int(blockIdx.x) / csize;
   const bool solo = csize == 1;   // one CTA: no distributed shared memory, no cluster barrier
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_launch_dependents();
 
   // Histograms start at zero in every CTA before any remote add (the first
   // cluster barrier below orders the two). `local` and `merged` are adjacent.
@@ -344,6 +343,9 @@ __global__ void __launch_bounds__(kTopkThreads)
     remaining -= above;
   }
   if (tid == 0 && sh.nan_seen) set_status(status, TSEL_DEV_NAN);   // this CTA's slice
+  // The compaction kernel that follows may launch now: its CTAs would only
+  // wait on this request's SMs during the rounds.
+  pdl_launch_dependents();
   const uint32_t thr = prefix;
   const int need_eq = remaining;   // tokens equal to the threshold to keep (request-wide)
 

@@ -554,12 +554,17 @@ def gpu_arm(args) -> None:
         raise RuntimeError("device status set in the per-kernel loop")
     redo_pairs = tsel.tsel_importance_redo_pairs(ws)
 
-    # --- top-B + compaction back to back, as the path runs them: the
-    # compaction launches while the top-B runs and waits for it on the device
-    # (programmatic dependent launch), so one launch latency is hidden -------
+    # --- top-B + compaction back to back inside the step, as the path runs
+    # them (the compaction launches while the top-B runs and waits for it on
+    # the device); events only around those two launches. Directly after the
+    # flush, the compaction would also pay for writing back the flush's dirty
+    # L2 lines, which the importance passes absorb in a real step -------------
     sel_evs = []
     for i in range(n_stage):
         flush.fill_(i & 0xFF)
+        importance(S1)
+        importance(S2)
+        importance(S3)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         topk()
