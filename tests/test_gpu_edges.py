@@ -265,6 +265,52 @@ def test_gather_fp32_rows_and_no_pos(tsel):
     assert oc.tolist() == [0, 3, 3, 5]
 
 
+@pytest.mark.parametrize("sizes,keep", [([100000, 5, 0, 3000, 1], [1000, 5, 0, 0, 1]),
+                                        ([70000, 7], [69999, 2]),
+                                        ([3, 65000, 40000, 2], [1, 0, 40000, 1])])
+def test_topk_uneven_requests_in_clusters(tsel, sizes, keep):
+    # the cluster size follows the average request, so small requests run on
+    # clusters whose CTAs mostly hold no token; budgets of 0, all and all but one
+    rng = np.random.default_rng(len(sizes) + sizes[0])
+    off = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    s = rng.random(off[-1]).astype(np.float32)
+    s[rng.integers(0, off[-1], off[-1] // 3)] = np.float32(0.5)   # ties across slices
+    got, cu, st = _topk(tsel, s, off, keep)
+    ref, cref = oracle.select_topk(s, off, keep)
+    assert st == 0
+    assert np.array_equal(got, ref) and np.array_equal(cu, cref)
+
+
+@pytest.mark.parametrize("D,dtype,G", [(8, torch.bfloat16, 1), (256, torch.bfloat16, 31),
+                                       (1280, torch.bfloat16, 32), (2048, torch.bfloat16, 33),
+                                       (1792, torch.bfloat16, 5), (5120, torch.bfloat16, 3),
+                                       (700, torch.float32, 40), (4, torch.float64, 200)])
+def test_gather_row_widths_and_segment_counts(tsel, D, dtype, G):
+    # rows held whole in registers (1 to 8 16-byte vectors per lane) and rows
+    # past 4 KB (5120 bf16, the hidden size of a 32B VLM) copied in a loop;
+    # image ids by ballot (up to 31 segments) and by binary search (more);
+    # rows read through a stride wider than the row; an odd number of kept rows
+    rng = np.random.default_rng(D + G)
+    L = rng.integers(0, 60, G)
+    L[0] = max(L[0], 1)
+    cu = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    Tk = int(cu[-1])
+    full = torch.randn(Tk, D + 24, device="cuda").to(dtype)
+    hidden = full[:, 8:8 + D]               # row stride D + 24 elements
+    pos = torch.from_numpy(rng.integers(-1000, 1000, (Tk, 3)).astype(np.int32)).cuda()
+    keep = np.sort(rng.choice(Tk, size=max(1, (Tk * 3) // 5) | 1, replace=False)).astype(np.int32)
+    oh, op, oi, oc = tsel.tsel_gather_compact(hidden, pos, i32(cu), i32(keep))
+    h_np = hidden.view(torch.int16 if dtype == torch.bfloat16 else
+                       (torch.int32 if dtype == torch.float32 else torch.int64)).cpu().numpy()
+    rh, rp, ri, rc = oracle.gather_compact(h_np, pos.cpu().numpy(), cu, keep)
+    o_np = oh.view(torch.int16 if dtype == torch.bfloat16 else
+                   (torch.int32 if dtype == torch.float32 else torch.int64)).cpu().numpy()
+    assert np.array_equal(o_np, rh)
+    assert np.array_equal(op.cpu().numpy(), rp)
+    assert np.array_equal(oi.cpu().numpy(), ri)
+    assert np.array_equal(oc.cpu().numpy(), rc)
+
+
 def test_full_selection_bit_exact_on_mid_size(tsel):
     w = W.make_segments([333, 1200, 17], [333, 1200, 17], 4, 4, 64, seed=305, hidden_dim=1280,
                         pos_dim=3, requests=[2, 1], keep_per_req=[900, 5])
