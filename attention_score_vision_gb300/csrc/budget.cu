@@ -12,14 +12,16 @@
 //
 // One thread-block cluster per request (up to 16 CTAs, one slice of the
 // request each, its keys cached in shared memory): the slice maxima meet in
-// CTA 0 (distributed shared memory) and give E; then four 8-bit radix rounds
-// over the order-preserving score keys build (count, quanta) histograms, bin
-// b merged in CTA (b % cluster size), from which every CTA picks the same
-// digit. The first
-// round's histogram also gives the request total M and the target T. After
-// the last round the key of the token that crosses T is known exactly; the
-// tokens tied on it carry equal quanta, so the number of them needed is one
-// division.
+// every CTA through distributed shared memory and give E; then three radix
+// rounds of 11, 11 and 10 bits over the order-preserving score keys build
+// (count, quanta) histograms of 2048 bins, bin group g (four bins) merged in
+// CTA (g % cluster size). After one cluster barrier each thread gathers its
+// merged group, and after one block barrier every warp finds the digit on
+// its own (warp totals, then the groups of one warp, then the bins of one
+// group; bins descending). The first round's totals also give the request
+// total M and the target T. After the last round the key of the token that
+// crosses T is known exactly; the tokens tied on it carry equal quanta, so
+// the number of them needed is one division.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -30,9 +32,13 @@ namespace cg = cooperative_groups;
 
 namespace tsel {
 
-constexpr int kBudgetThreads = 256;
+
+constexpr int kBudgetThreads = 512;
 constexpr int kBudgetWarps = kBudgetThreads / 32;
-constexpr int kBudgetCacheKeys = 16384;    // keys cached in shared memory per CTA
+constexpr int kBudgetBins = 2048;                // 11-bit digits (the last round uses 1024)
+static_assert(kBudgetBins / 4 == kBudgetThreads, "one bin group per thread");
+constexpr int kBudgetCacheKeys = 16384;          // keys cached in shared memory per CTA
+constexpr int kBudgetLoad = 8;                   // score loads in flight per thread
 
 // Binary exponent E with s in [2^(E-1), 2^E) for a positive fp32 bit pattern.
 __device__ __forceinline__ int score_exponent(uint32_t bits) {
@@ -60,44 +66,131 @@ __device__ __forceinline__ uint32_t quantum_of_key(uint32_t key, int E) {
   return score_quantum(bits, E);
 }
 
-struct BudgetShared {
-  int cnt[4][256];                   // merged histograms (bin b lives in CTA b % csize)
-  unsigned long long mass[4][256];
-  int lcnt[256];                     // this CTA's histogram of the current round
-  unsigned long long lmass[256];
-  uint32_t red[kBudgetWarps];
-  uint32_t smax;                     // CTA 0: largest positive score bits of the request
-  int bad, nan_seen, digit, cnt_above;
-  unsigned long long mass_above, target;
-};
+// Digit of round `round` (0, 1, 2): bits 31..21, 20..10, 9..0 of the key.
+__device__ __forceinline__ int budget_shift(int round) { return round == 0 ? 21 : (round == 1 ? 10 : 0); }
+__device__ __forceinline__ uint32_t budget_dmask(int round) { return round == 2 ? 1023u : 2047u; }
 
-__global__ void __launch_bounds__(kBudgetThreads)
+template <typename T>
+__device__ __forceinline__ T budget_warp_sum(T x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Sum over this lane and the lanes above it.
+template <typename T>
+__device__ __forceinline__ T budget_suffix_scan(T x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_down_sync(0xffffffffu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  return x;
+}
+
+struct __align__(16) BudgetShared {
+  unsigned long long lmass[kBudgetBins];      // this CTA's quanta per digit (current round)
+  unsigned long long mmass[3][kBudgetBins];   // merged; bin group g lives in CTA g % csize
+  unsigned long long bmass[kBudgetBins];      // the round's merged quanta, gathered
+  int lcnt[kBudgetBins];                      // this CTA's token count per digit
+  int mcnt[3][kBudgetBins];
+  int bcnt[kBudgetBins];
+  unsigned long long wmass[kBudgetWarps];     // per-warp totals of the gathered bins
+  int wcnt[kBudgetWarps];
+  uint32_t wmax[kBudgetWarps];                // per-warp largest positive score bits
+  uint32_t cmax[kMaxClusterCtas];             // every CTA's slice maximum
+  int nan_seen;
+  int pad_[3];
+};
+static_assert(sizeof(BudgetShared) % 16 == 0, "key cache follows at a 16-byte boundary");
+
+// Finds, in every warp at once, the bin (descending) where the quanta of the
+// higher bins plus its own first reach `need`. Returns the digit; mass_above
+// and cnt_above get the quanta and the tokens of the higher bins.
+__device__ __forceinline__ int budget_find_digit(const BudgetShared& sh, unsigned long long need,
+                                                 unsigned long long& mass_above, int& cnt_above) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long vm = lane < kBudgetWarps ? sh.wmass[lane] : 0ull;
+  const int vc = lane < kBudgetWarps ? sh.wcnt[lane] : 0;
+  const unsigned long long xm = budget_suffix_scan(vm);
+  const int xc = budget_suffix_scan(vc);
+  const unsigned hw = __ballot_sync(0xffffffffu, lane < kBudgetWarps && xm - vm < need && xm >= need);
+  const int w = hw ? __ffs(hw) - 1 : 0;
+  const unsigned long long am_w = __shfl_sync(0xffffffffu, xm - vm, w);
+  const int ac_w = __shfl_sync(0xffffffffu, xc - vc, w);
+  const int grp = 32 * w + lane;
+  const int4 c4 = reinterpret_cast<const int4*>(sh.bcnt)[grp];
+  const ulonglong2 m01 = reinterpret_cast<const ulonglong2*>(sh.bmass)[2 * grp];
+  const ulonglong2 m23 = reinterpret_cast<const ulonglong2*>(sh.bmass)[2 * grp + 1];
+  const unsigned long long sm = m01.x + m01.y + m23.x + m23.y;
+  const int sc = c4.x + c4.y + c4.z + c4.w;
+  const unsigned long long xg = budget_suffix_scan(sm);
+  const int xgc = budget_suffix_scan(sc);
+  const unsigned long long a0 = am_w + xg - sm;
+  const int a0c = ac_w + xgc - sc;
+  const unsigned hg = __ballot_sync(0xffffffffu, a0 < need && a0 + sm >= need);
+  const int g = hg ? __ffs(hg) - 1 : 0;
+  unsigned long long a = __shfl_sync(0xffffffffu, a0, g);
+  int ac = __shfl_sync(0xffffffffu, a0c, g);
+  const unsigned long long m3 = __shfl_sync(0xffffffffu, m23.y, g);
+  const unsigned long long m2 = __shfl_sync(0xffffffffu, m23.x, g);
+  const unsigned long long m1 = __shfl_sync(0xffffffffu, m01.y, g);
+  const int k3 = __shfl_sync(0xffffffffu, c4.w, g), k2 = __shfl_sync(0xffffffffu, c4.z, g);
+  const int k1 = __shfl_sync(0xffffffffu, c4.y, g);
+  const int base = 4 * (32 * w + g);
+  int digit;
+  if (a + m3 >= need) {
+    digit = base + 3;
+  } else {
+    a += m3;
+    ac += k3;
+    if (a + m2 >= need) {
+      digit = base + 2;
+    } else {
+      a += m2;
+      ac += k2;
+      if (a + m1 >= need) {
+        digit = base + 1;
+      } else {
+        a += m1;
+        ac += k1;
+        digit = base;
+      }
+    }
+  }
+  mass_above = a;
+  cnt_above = ac;
+  return digit;
+}
+
+__global__ void __launch_bounds__(kBudgetThreads, 1)
     budget_cluster_kernel(const float* __restrict__ scores, int total_tokens,
                           const int32_t* __restrict__ req_off, int mass_pm, int min_pm,
                           int max_pm, int32_t* __restrict__ keep_out, int32_t* total_out,
                           uint32_t* status) {
-  __shared__ BudgetShared sh;
-  extern __shared__ uint32_t skeys[];   // kBudgetCacheKeys
+  extern __shared__ __align__(16) unsigned char budget_smem[];
+  BudgetShared& sh = *reinterpret_cast<BudgetShared*>(budget_smem);
+  uint32_t* skeys = reinterpret_cast<uint32_t*>(budget_smem + sizeof(BudgetShared));
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = int(cluster.block_rank());
   const int csize = int(cluster.num_blocks());
   const int r = int(blockIdx.x) / csize;
+  const bool solo = csize == 1;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_launch_dependents();
+
+  // Histograms start at zero before any remote add (ordered by the first
+  // cluster barrier below).
+  {
+    int4* h = reinterpret_cast<int4*>(&sh.lmass[0]);
+    constexpr int n16 = int((offsetof(BudgetShared, wmass)) / 16);
+    for (int i = tid; i < n16; i += kBudgetThreads) h[i] = make_int4(0, 0, 0, 0);
+    if (tid == 0) sh.nan_seen = 0;
+  }
   pdl_wait();
 
   const int lo = req_off[r], hi = req_off[r + 1];
-  if (tid == 0) {
-    sh.bad = (lo < 0 || hi < lo || hi > total_tokens) ? 1 : 0;
-    sh.nan_seen = 0;
-    sh.smax = 0u;
-  }
-  for (int i = tid; i < 4 * 256; i += kBudgetThreads) {
-    (&sh.cnt[0][0])[i] = 0;
-    (&sh.mass[0][0])[i] = 0ull;
-  }
-  __syncthreads();
-  if (sh.bad) {
+  if (lo < 0 || hi < lo || hi > total_tokens) {
     // every CTA of the cluster takes this branch together (same request)
     if (tid == 0 && crank == 0) {
       set_status(status, TSEL_DEV_REQUESTS);
@@ -111,20 +204,20 @@ __global__ void __launch_bounds__(kBudgetThreads)
   const int len = c1 - c0;
   const float* s = scores + lo + c0;
   const bool cached = len <= kBudgetCacheKeys;
-  // CTA 0's histograms and max are zeroed before any remote update: arrive
-  // now, wait after the slice is loaded.
+  // Zeroed histograms released to the cluster now; the wait (which also
+  // makes sure every CTA runs before any remote access) follows the loads.
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   uint32_t mx = 0;
   int nan_local = 0;
-  for (int i0 = 0; i0 < len; i0 += kBudgetThreads * 8) {
-    float f[8];
+  for (int i0 = 0; i0 < len; i0 += kBudgetThreads * kBudgetLoad) {
+    float f[kBudgetLoad];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {   // eight independent loads in flight per thread
+    for (int j = 0; j < kBudgetLoad; ++j) {
       const int i = i0 + j * kBudgetThreads + tid;
       f[j] = i < len ? __ldcg(s + i) : 0.f;
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kBudgetLoad; ++j) {
       const int i = i0 + j * kBudgetThreads + tid;
       nan_local |= (f[j] != f[j]);
       if (f[j] > 0.f) mx = max(mx, __float_as_uint(f[j]));
@@ -132,124 +225,109 @@ __global__ void __launch_bounds__(kBudgetThreads)
     }
   }
   mx = __reduce_max_sync(0xffffffffu, mx);
-  if (lane == 0) sh.red[warp] = mx;
+  if (lane == 0) sh.wmax[warp] = mx;
   if (nan_local) atomicOr(&sh.nan_seen, 1);
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   __syncthreads();
-  uint32_t* smax0 = cluster.map_shared_rank(&sh.smax, 0);
-  if (tid == 0) {
-    uint32_t m = 0;
-    for (int w = 0; w < kBudgetWarps; ++w) m = max(m, sh.red[w]);
-    if (m) atomicMax(smax0, m);
+  // this slice's maximum into slot crank of every CTA
+  if (warp == 0) {
+    uint32_t m = lane < kBudgetWarps ? sh.wmax[lane] : 0u;
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane < csize) *cluster.map_shared_rank(&sh.cmax[crank], lane) = m;
   }
   cluster.sync();
-  const uint32_t smax_bits = *smax0;
+  uint32_t smax_bits = 0;
+  for (int c = 0; c < csize; ++c) smax_bits = max(smax_bits, sh.cmax[c]);
   const int E = smax_bits != 0 ? score_exponent(smax_bits) : 0;
 
   // ---- radix rounds on the score key, (count, quanta) histograms ---------
   uint32_t prefix = 0, mask = 0;
   unsigned long long need = 0;   // quanta still to collect among keys matching prefix
   int cnt_above = 0;
-  bool done = smax_bits == 0;    // no positive score: nothing to collect
+  bool done = smax_bits == 0;    // no positive score: nothing to collect (same in every CTA)
 #pragma unroll 1
-  for (int round = 0; round < 4 && !done; ++round) {
-    const int shift = 24 - 8 * round;
-    for (int i = tid; i < 256; i += kBudgetThreads) {
-      sh.lcnt[i] = 0;
-      sh.lmass[i] = 0ull;
-    }
-    __syncthreads();
-    for (int i0 = 0; i0 < len; i0 += kBudgetThreads) {
-      const int i = i0 + tid;
-      const bool in = i < len;
-      const uint32_t k = in ? (cached ? skeys[i] : order_key(__ldcg(s + i))) : 0u;
-      const bool match = in && (k & mask) == prefix;
-      const uint32_t d = (k >> shift) & 255u;
-      const uint32_t q = match ? quantum_of_key(k, E) : 0u;
-      // one shared atomic per distinct digit of the warp; quanta < 2^24, so
-      // a group's sum fits 32 bits
-      const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0x100u);
-      const uint32_t gsum = __reduce_add_sync(peers, q);
-      if (match && (__ffs(peers) - 1) == lane) {
-        atomicAdd(&sh.lcnt[d], __popc(peers));
-        atomicAdd(&sh.lmass[d], (unsigned long long)gsum);
-      }
-    }
-    __syncthreads();
-    for (int b = tid; b < 256; b += kBudgetThreads) {
-      if (sh.lcnt[b]) {   // bin b is merged in CTA b % csize
-        atomicAdd(cluster.map_shared_rank(&sh.cnt[round][b], b % csize), sh.lcnt[b]);
-        atomicAdd(cluster.map_shared_rank(&sh.mass[round][b], b % csize), sh.lmass[b]);
-      }
-    }
-    cluster.sync();
-    if (warp == 0) {
-      // lane l owns bins 255-8l ... 248-8l (descending)
-      unsigned long long m8[8], msum = 0;
-      int c8[8], csum = 0;
+  for (int round = 0; round < 3 && !done; ++round) {
+    const int shift = budget_shift(round);
+    const uint32_t dmask = budget_dmask(round);
+    for (int i0 = 0; i0 < len; i0 += kBudgetThreads * kBudgetLoad) {
+      uint32_t kk[kBudgetLoad];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int b = 255 - 8 * lane - j;
-        m8[j] = *cluster.map_shared_rank(&sh.mass[round][b], b % csize);
-        c8[j] = *cluster.map_shared_rank(&sh.cnt[round][b], b % csize);
-        msum += m8[j];
-        csum += c8[j];
+      for (int j = 0; j < kBudgetLoad; ++j) {
+        const int i = i0 + j * kBudgetThreads + tid;
+        kk[j] = i < len ? (cached ? skeys[i] : order_key(__ldcg(s + i))) : 0u;
       }
-      unsigned long long mi = msum;
-      int ci = csum;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, mi, o);
-        const int yc = __shfl_up_sync(0xffffffffu, ci, o);
-        if (lane >= o) {
-          mi += y;
-          ci += yc;
+      for (int j = 0; j < kBudgetLoad; ++j) {
+        const bool match = i0 + j * kBudgetThreads + tid < len && (kk[j] & mask) == prefix;
+        const uint32_t d = (kk[j] >> shift) & dmask;
+        const uint32_t q = match ? quantum_of_key(kk[j], E) : 0u;
+        // one shared atomic pair per distinct digit of the warp (the 64-bit
+        // adds would otherwise serialise on the few top digits of real
+        // scores); quanta < 2^24, so a group's sum fits 32 bits
+        const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0xFFFFFFFFu);
+        const uint32_t gsum = __reduce_add_sync(peers, q);
+        if (match && (__ffs(peers) - 1) == lane) {
+          atomicAdd(&sh.lcnt[d], __popc(peers));
+          if (gsum) atomicAdd(&sh.lmass[d], (unsigned long long)gsum);
         }
       }
-      if (round == 0) {
-        // request total = every bin of the first round; T = ceil(tau * M)
-        const unsigned long long M = __shfl_sync(0xffffffffu, mi, 31);
-        const unsigned long long a = M / 1000ull, b = M % 1000ull;
-        const unsigned long long T = a * (unsigned long long)mass_pm +
-                                     (b * (unsigned long long)mass_pm + 999ull) / 1000ull;
-        if (lane == 0) sh.target = T;
-        need = T;
-      }
-      unsigned long long m_before = mi - msum;
-      int c_before = ci - csum;
-      int found = -1;
-      unsigned long long f_mass = 0;
-      int f_cnt = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (found < 0 && m_before < need && m_before + m8[j] >= need) {
-          found = 255 - 8 * lane - j;
-          f_mass = m_before;
-          f_cnt = c_before;
-        }
-        m_before += m8[j];
-        c_before += c8[j];
-      }
-      if (found >= 0) {
-        sh.digit = found;
-        sh.mass_above = f_mass;
-        sh.cnt_above = f_cnt;
-      }
+    }
+    __syncthreads();
+    // this thread's group: read, re-zero for the next round, merge
+    int4 c4 = reinterpret_cast<const int4*>(sh.lcnt)[tid];
+    ulonglong2 m01 = reinterpret_cast<const ulonglong2*>(sh.lmass)[2 * tid];
+    ulonglong2 m23 = reinterpret_cast<const ulonglong2*>(sh.lmass)[2 * tid + 1];
+    reinterpret_cast<int4*>(sh.lcnt)[tid] = make_int4(0, 0, 0, 0);
+    reinterpret_cast<ulonglong2*>(sh.lmass)[2 * tid] = make_ulonglong2(0ull, 0ull);
+    reinterpret_cast<ulonglong2*>(sh.lmass)[2 * tid + 1] = make_ulonglong2(0ull, 0ull);
+    if (!solo) {
+      const int owner = tid % csize;
+      int* dc = cluster.map_shared_rank(&sh.mcnt[round][4 * tid], owner);
+      unsigned long long* dm = cluster.map_shared_rank(&sh.mmass[round][4 * tid], owner);
+      if (c4.x) atomicAdd(dc, c4.x);
+      if (c4.y) atomicAdd(dc + 1, c4.y);
+      if (c4.z) atomicAdd(dc + 2, c4.z);
+      if (c4.w) atomicAdd(dc + 3, c4.w);
+      if (m01.x) atomicAdd(dm, m01.x);
+      if (m01.y) atomicAdd(dm + 1, m01.y);
+      if (m23.x) atomicAdd(dm + 2, m23.x);
+      if (m23.y) atomicAdd(dm + 3, m23.y);
+      cluster.sync();
+      c4 = *reinterpret_cast<const int4*>(dc);
+      m01 = *reinterpret_cast<const ulonglong2*>(dm);
+      m23 = *reinterpret_cast<const ulonglong2*>(dm + 2);
+    }
+    reinterpret_cast<int4*>(sh.bcnt)[tid] = c4;
+    reinterpret_cast<ulonglong2*>(sh.bmass)[2 * tid] = m01;
+    reinterpret_cast<ulonglong2*>(sh.bmass)[2 * tid + 1] = m23;
+    const unsigned long long wm = budget_warp_sum(m01.x + m01.y + m23.x + m23.y);
+    const int wc = budget_warp_sum(c4.x + c4.y + c4.z + c4.w);
+    if (lane == 0) {
+      sh.wmass[warp] = wm;
+      sh.wcnt[warp] = wc;
     }
     __syncthreads();
     if (round == 0) {
-      need = sh.target;
+      // request total = every bin of the first round; T = ceil(tau * M)
+      unsigned long long M = 0;
+#pragma unroll
+      for (int w = 0; w < kBudgetWarps; ++w) M += sh.wmass[w];
+      const unsigned long long a = M / 1000ull, b = M % 1000ull;
+      need = a * (unsigned long long)mass_pm + (b * (unsigned long long)mass_pm + 999ull) / 1000ull;
       if (need == 0) {
         done = true;
         break;
       }
     }
-    prefix |= uint32_t(sh.digit) << shift;
-    mask |= 255u << shift;
-    need -= sh.mass_above;
-    cnt_above += sh.cnt_above;
-    __syncthreads();
+    unsigned long long mass_above;
+    int cnt_r;
+    const int digit = budget_find_digit(sh, need, mass_above, cnt_r);
+    prefix |= uint32_t(digit) << shift;
+    mask |= dmask << shift;
+    need -= mass_above;
+    cnt_above += cnt_r;
   }
+  pdl_launch_dependents();
   if (tid == 0 && sh.nan_seen) set_status(status, TSEL_DEV_NAN);   // this CTA's slice
   if (tid == 0 && crank == 0) {
     long long b_dyn = 0;
@@ -266,7 +344,7 @@ __global__ void __launch_bounds__(kBudgetThreads)
     keep_out[r] = int32_t(b_dyn);
     if (total_out != nullptr) atomicAdd(total_out, int32_t(b_dyn));
   }
-  cluster.sync();   // no CTA's shared memory is read remotely after this point
+  if (!solo) cluster.sync();   // no CTA's shared memory is read remotely after this point
 }
 
 cudaError_t launch_budget(const float* scores, int total_tokens, const int32_t* req_off,
@@ -277,7 +355,7 @@ cudaError_t launch_budget(const float* scores, int total_tokens, const int32_t* 
     cudaError_t e = cudaMemsetAsync(total_out, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return e;
   }
-  const size_t dyn = size_t(kBudgetCacheKeys) * sizeof(uint32_t);
+  const size_t dyn = sizeof(BudgetShared) + size_t(kBudgetCacheKeys) * sizeof(uint32_t);
   cudaError_t e = cudaSuccess;
   const int csize = usable_cluster_size(budget_cluster_kernel,
                                         cluster_size_for(total_tokens, num_req), kBudgetThreads,

@@ -55,6 +55,13 @@ def _score_sets():
     # one large request across many blocks
     e = rng.exponential(1e-4, 70000).astype(np.float32)
     sets.append(("large", e, [0, 70000]))
+    # clusters of 4 and 8 CTAs (average request 10K and 20K tokens); slices
+    # longer than the per-CTA key cache (300K tokens on 16 CTAs)
+    f = (rng.random(40000) ** 3).astype(np.float32) * np.float32(3e-3)
+    sets.append(("clusters4", f, [0, 9000, 20000, 30001, 40000]))
+    sets.append(("clusters8", f, [0, 17000, 40000]))
+    h = rng.exponential(1e-5, 300000).astype(np.float32)
+    sets.append(("uncached", h, [0, 300000]))
     return sets
 
 
