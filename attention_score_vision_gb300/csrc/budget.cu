@@ -89,9 +89,28 @@ __device__ __forceinline__ T budget_suffix_scan(T x) {
   return x;
 }
 
+// Quanta sums are 64-bit but kept as two 32-bit words (low, high): a sum is
+// added with a native 32-bit atomic on the low word that returns the old
+// value, and the carry it produces goes into the high word. Once every add
+// has landed, high * 2^32 + low is the exact sum. (64-bit adds to shared
+// and distributed shared memory took several times longer on the few hot
+// bins of real scores.)
+__device__ __forceinline__ void add_u64_split(uint32_t* lo, uint32_t* hi, unsigned long long x) {
+  const uint32_t xl = uint32_t(x), xh = uint32_t(x >> 32);
+  const uint32_t old = atomicAdd(lo, xl);
+  const uint32_t up = xh + (old + xl < old ? 1u : 0u);
+  if (up) atomicAdd(hi, up);
+}
+
+__device__ __forceinline__ unsigned long long join_u64(uint32_t lo, uint32_t hi) {
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
 struct __align__(16) BudgetShared {
-  unsigned long long lmass[kBudgetBins];      // this CTA's quanta per digit (current round)
-  unsigned long long mmass[3][kBudgetBins];   // merged; bin group g lives in CTA g % csize
+  uint32_t lmlo[kBudgetBins];                 // this CTA's quanta per digit (current round)
+  uint32_t lmhi[kBudgetBins];
+  uint32_t mmlo[3][kBudgetBins];              // merged; bin group g lives in CTA g % csize
+  uint32_t mmhi[3][kBudgetBins];
   unsigned long long bmass[kBudgetBins];      // the round's merged quanta, gathered
   int lcnt[kBudgetBins];                      // this CTA's token count per digit
   int mcnt[3][kBudgetBins];
@@ -182,7 +201,7 @@ __global__ void __launch_bounds__(kBudgetThreads, 1)
   // Histograms start at zero before any remote add (ordered by the first
   // cluster barrier below).
   {
-    int4* h = reinterpret_cast<int4*>(&sh.lmass[0]);
+    int4* h = reinterpret_cast<int4*>(&sh.lmlo[0]);
     constexpr int n16 = int((offsetof(BudgetShared, wmass)) / 16);
     for (int i = tid; i < n16; i += kBudgetThreads) h[i] = make_int4(0, 0, 0, 0);
     if (tid == 0) sh.nan_seen = 0;
@@ -261,42 +280,53 @@ __global__ void __launch_bounds__(kBudgetThreads, 1)
         const bool match = i0 + j * kBudgetThreads + tid < len && (kk[j] & mask) == prefix;
         const uint32_t d = (kk[j] >> shift) & dmask;
         const uint32_t q = match ? quantum_of_key(kk[j], E) : 0u;
-        // one shared atomic pair per distinct digit of the warp (the 64-bit
-        // adds would otherwise serialise on the few top digits of real
-        // scores); quanta < 2^24, so a group's sum fits 32 bits
-        const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0xFFFFFFFFu);
-        const uint32_t gsum = __reduce_add_sync(peers, q);
-        if (match && (__ffs(peers) - 1) == lane) {
-          atomicAdd(&sh.lcnt[d], __popc(peers));
-          if (gsum) atomicAdd(&sh.lmass[d], (unsigned long long)gsum);
+        if (round == 0) {
+          // the top digits of real scores take few values: one add per
+          // distinct digit of the warp (quanta < 2^24, so a group's sum
+          // fits 32 bits). In later rounds the digits of a warp are mostly
+          // distinct and the grouping itself would serialise.
+          const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0xFFFFFFFFu);
+          const uint32_t gsum = __reduce_add_sync(peers, q);
+          if (match && (__ffs(peers) - 1) == lane) {
+            atomicAdd(&sh.lcnt[d], __popc(peers));
+            if (gsum) add_u64_split(&sh.lmlo[d], &sh.lmhi[d], gsum);
+          }
+        } else if (match) {
+          atomicAdd(&sh.lcnt[d], 1);
+          if (q) add_u64_split(&sh.lmlo[d], &sh.lmhi[d], q);
         }
       }
     }
     __syncthreads();
     // this thread's group: read, re-zero for the next round, merge
     int4 c4 = reinterpret_cast<const int4*>(sh.lcnt)[tid];
-    ulonglong2 m01 = reinterpret_cast<const ulonglong2*>(sh.lmass)[2 * tid];
-    ulonglong2 m23 = reinterpret_cast<const ulonglong2*>(sh.lmass)[2 * tid + 1];
+    uint4 lo4 = reinterpret_cast<const uint4*>(sh.lmlo)[tid];
+    uint4 hi4 = reinterpret_cast<const uint4*>(sh.lmhi)[tid];
     reinterpret_cast<int4*>(sh.lcnt)[tid] = make_int4(0, 0, 0, 0);
-    reinterpret_cast<ulonglong2*>(sh.lmass)[2 * tid] = make_ulonglong2(0ull, 0ull);
-    reinterpret_cast<ulonglong2*>(sh.lmass)[2 * tid + 1] = make_ulonglong2(0ull, 0ull);
+    reinterpret_cast<uint4*>(sh.lmlo)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(sh.lmhi)[tid] = make_uint4(0u, 0u, 0u, 0u);
     if (!solo) {
       const int owner = tid % csize;
       int* dc = cluster.map_shared_rank(&sh.mcnt[round][4 * tid], owner);
-      unsigned long long* dm = cluster.map_shared_rank(&sh.mmass[round][4 * tid], owner);
+      uint32_t* dlo = cluster.map_shared_rank(&sh.mmlo[round][4 * tid], owner);
+      uint32_t* dhi = cluster.map_shared_rank(&sh.mmhi[round][4 * tid], owner);
       if (c4.x) atomicAdd(dc, c4.x);
       if (c4.y) atomicAdd(dc + 1, c4.y);
       if (c4.z) atomicAdd(dc + 2, c4.z);
       if (c4.w) atomicAdd(dc + 3, c4.w);
-      if (m01.x) atomicAdd(dm, m01.x);
-      if (m01.y) atomicAdd(dm + 1, m01.y);
-      if (m23.x) atomicAdd(dm + 2, m23.x);
-      if (m23.y) atomicAdd(dm + 3, m23.y);
+      const unsigned long long v0 = join_u64(lo4.x, hi4.x), v1 = join_u64(lo4.y, hi4.y);
+      const unsigned long long v2 = join_u64(lo4.z, hi4.z), v3 = join_u64(lo4.w, hi4.w);
+      if (v0) add_u64_split(dlo, dhi, v0);
+      if (v1) add_u64_split(dlo + 1, dhi + 1, v1);
+      if (v2) add_u64_split(dlo + 2, dhi + 2, v2);
+      if (v3) add_u64_split(dlo + 3, dhi + 3, v3);
       cluster.sync();
       c4 = *reinterpret_cast<const int4*>(dc);
-      m01 = *reinterpret_cast<const ulonglong2*>(dm);
-      m23 = *reinterpret_cast<const ulonglong2*>(dm + 2);
+      lo4 = *reinterpret_cast<const uint4*>(dlo);
+      hi4 = *reinterpret_cast<const uint4*>(dhi);
     }
+    const ulonglong2 m01 = make_ulonglong2(join_u64(lo4.x, hi4.x), join_u64(lo4.y, hi4.y));
+    const ulonglong2 m23 = make_ulonglong2(join_u64(lo4.z, hi4.z), join_u64(lo4.w, hi4.w));
     reinterpret_cast<int4*>(sh.bcnt)[tid] = c4;
     reinterpret_cast<ulonglong2*>(sh.bmass)[2 * tid] = m01;
     reinterpret_cast<ulonglong2*>(sh.bmass)[2 * tid + 1] = m23;
