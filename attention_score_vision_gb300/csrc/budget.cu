@@ -14,14 +14,15 @@
 // request each, its keys cached in shared memory): the slice maxima meet in
 // every CTA through distributed shared memory and give E; then three radix
 // rounds of 11, 11 and 10 bits over the order-preserving score keys build
-// (count, quanta) histograms of 2048 bins, bin group g (four bins) merged in
-// CTA (g % cluster size). After one cluster barrier each thread gathers its
-// merged group, and after one block barrier every warp finds the digit on
-// its own (warp totals, then the groups of one warp, then the bins of one
-// group; bins descending). The first round's totals also give the request
-// total M and the target T. After the last round the key of the token that
-// crosses T is known exactly; the tokens tied on it carry equal quanta, so
-// the number of them needed is one division.
+// (count, quanta) histograms of 2048 bins (shared atomics), bin group g
+// (four bins) merged in CTA (g % cluster size). After one cluster barrier
+// each thread gathers its merged group, and after one block barrier every
+// warp finds the digit on its own (warp totals, then the groups of one
+// warp, then the bins of one group; bins descending). The first round's
+// totals also give the request total M and the target T. After the last
+// round the key of the token that crosses T is known exactly; the tokens
+// tied on it carry equal quanta, so the number of them needed is one
+// division.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -92,9 +93,10 @@ __device__ __forceinline__ T budget_suffix_scan(T x) {
 // Quanta sums are 64-bit but kept as two 32-bit words (low, high): a sum is
 // added with a native 32-bit atomic on the low word that returns the old
 // value, and the carry it produces goes into the high word. Once every add
-// has landed, high * 2^32 + low is the exact sum. (64-bit adds to shared
-// and distributed shared memory took several times longer on the few hot
-// bins of real scores.)
+// has landed, high * 2^32 + low is the exact sum. Every key adds its own
+// count and quantum (no warp grouping: on the seeded scores that was slower
+// in every round, and in later rounds, where a warp's digits are mostly
+// distinct, it serialised).
 __device__ __forceinline__ void add_u64_split(uint32_t* lo, uint32_t* hi, unsigned long long x) {
   const uint32_t xl = uint32_t(x), xh = uint32_t(x >> 32);
   const uint32_t old = atomicAdd(lo, xl);
@@ -279,20 +281,9 @@ __global__ void __launch_bounds__(kBudgetThreads, 1)
       for (int j = 0; j < kBudgetLoad; ++j) {
         const bool match = i0 + j * kBudgetThreads + tid < len && (kk[j] & mask) == prefix;
         const uint32_t d = (kk[j] >> shift) & dmask;
-        const uint32_t q = match ? quantum_of_key(kk[j], E) : 0u;
-        if (round == 0) {
-          // the top digits of real scores take few values: one add per
-          // distinct digit of the warp (quanta < 2^24, so a group's sum
-          // fits 32 bits). In later rounds the digits of a warp are mostly
-          // distinct and the grouping itself would serialise.
-          const uint32_t peers = __match_any_sync(0xffffffffu, match ? d : 0xFFFFFFFFu);
-          const uint32_t gsum = __reduce_add_sync(peers, q);
-          if (match && (__ffs(peers) - 1) == lane) {
-            atomicAdd(&sh.lcnt[d], __popc(peers));
-            if (gsum) add_u64_split(&sh.lmlo[d], &sh.lmhi[d], gsum);
-          }
-        } else if (match) {
+        if (match) {
           atomicAdd(&sh.lcnt[d], 1);
+          const uint32_t q = quantum_of_key(kk[j], E);
           if (q) add_u64_split(&sh.lmlo[d], &sh.lmhi[d], q);
         }
       }
