@@ -252,7 +252,8 @@ TSEL_API tsel_status tsel_select_topk(const float* scores, int total_tokens,
  * keep_per_req    out int32 [num_req] device.
  * total_keep      out int32 device scalar = sum_r B_r (may be NULL).
  * workspace       >= tsel_select_topk_workspace_size(num_req) bytes (status).
- * Requests of up to 2^31 tokens; one CTA per request.
+ * Requests of up to 2^31 - 1 tokens; one thread-block cluster (up to 16 CTAs)
+ * per request.
  */
 TSEL_API tsel_status tsel_dynamic_budget(const float* scores, int total_tokens,
                                          const int32_t* req_tok_offsets, int num_req,
