@@ -77,6 +77,21 @@ def test_dynamic_budget_matches_oracle_exactly(tsel, tau, lo, hi):
         assert total == int(ref.sum())
 
 
+def test_dynamic_budget_slice_past_two_to_the_twenty(tsel):
+    # 300 small requests and one of 1.1M tokens: the average request is small,
+    # so one CTA holds every key of the large one (more than 2^20, past its
+    # key cache: every round re-reads the scores), and its per-bin quanta sums
+    # pass 2^32
+    rng = np.random.default_rng(902)
+    sizes = [1_100_000] + rng.integers(1, 40, 300).tolist()
+    off = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    s = rng.exponential(1e-6, off[-1]).astype(np.float32)
+    keep, total, st = _budget(tsel, s, off, 900, 0, 1000)
+    ref = oracle.dynamic_budget(s, off, 900, 0, 1000)
+    assert st == 0
+    assert np.array_equal(keep, ref) and total == int(ref.sum())
+
+
 def test_dynamic_budget_flags_nan_and_bad_offsets(tsel):
     s = np.asarray([0.5, np.nan, 0.25, 0.125], np.float32)
     keep, _, st = _budget(tsel, s, [0, 4], 1000, 0, 1000)

@@ -281,6 +281,27 @@ def test_topk_uneven_requests_in_clusters(tsel, sizes, keep):
     assert np.array_equal(got, ref) and np.array_equal(cu, cref)
 
 
+def test_topk_nan_in_cluster_slices(tsel):
+    # NaN scores in several slices of a 16-CTA cluster: the status flags them;
+    # their rank is unspecified, but every other kept token must be one of the
+    # best non-NaN tokens (score descending, lowest index first), B in total,
+    # ascending and in range
+    rng = np.random.default_rng(77)
+    n, B = 50000, 20000
+    s = rng.random(n).astype(np.float32)
+    nan_at = np.sort(rng.choice(n, 12, replace=False))
+    s[nan_at] = np.float32(np.nan)
+    got, cu, st = _topk(tsel, s, [0, n], [B])
+    assert st & tsel.TSEL_DEV_NAN
+    assert got.shape == (B,) and cu.tolist() == [0, B]
+    assert np.all(np.diff(got) > 0) and got[0] >= 0 and got[-1] < n
+    is_nan = np.isnan(s[got])
+    rest = got[~is_nan]
+    clean = np.where(np.isnan(s), np.float32(-1.0), s).astype(np.float32)
+    ref, _ = oracle.select_topk(clean, [0, n], [rest.size])
+    assert np.array_equal(rest, ref)
+
+
 @pytest.mark.parametrize("D,dtype,G", [(8, torch.bfloat16, 1), (256, torch.bfloat16, 31),
                                        (1280, torch.bfloat16, 32), (2048, torch.bfloat16, 33),
                                        (1792, torch.bfloat16, 5), (5120, torch.bfloat16, 3),
