@@ -378,9 +378,9 @@ cudaError_t launch_budget(const float* scores, int total_tokens, const int32_t* 
   }
   const size_t dyn = sizeof(BudgetShared) + size_t(kBudgetCacheKeys) * sizeof(uint32_t);
   cudaError_t e = cudaSuccess;
-  const int csize = usable_cluster_size(budget_cluster_kernel,
-                                        cluster_size_for(total_tokens, num_req), kBudgetThreads,
-                                        dyn, cache, &e);
+  const int want = cluster_size_for(total_tokens, num_req);
+  const int csize =
+      cluster_size_for_grid(budget_cluster_kernel, want, num_req, kBudgetThreads, dyn, cache, &e);
   if (e != cudaSuccess) return e;
   return launch_clusters(budget_cluster_kernel, num_req, csize, kBudgetThreads, dyn, stream,
                          scores, total_tokens, req_off, mass_pm, min_pm, max_pm, keep_out,

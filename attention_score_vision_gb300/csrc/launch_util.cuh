@@ -31,42 +31,54 @@ inline int cluster_size_for(int total_tokens, int num_req) {
   return 1;
 }
 
-// Largest power-of-two cluster size <= want that `kernel` (threads per CTA,
-// dyn bytes of dynamic shared memory) can co-schedule on the current device.
-// cache[dev][log2 size] keeps 1 + the answer (0 = unknown); the kernel's
-// attributes are set on the first query per device.
+// Cluster size for num_clusters clusters of `kernel` (threads per CTA, dyn
+// bytes of dynamic shared memory): the largest power of two <= want at which
+// the device can hold every one of them at once, else 1. A cluster that has
+// to wait for another one to finish would double these latency-bound
+// kernels' time (at most 7 clusters of 16 top-B CTAs fit on a GB300).
+// cache[dev][0] notes that the kernel's attributes are set on that device;
+// cache[dev][k] keeps 1 + the number of resident clusters of 2^k CTAs.
 template <typename Kernel>
-int usable_cluster_size(Kernel kernel, int want, int threads, size_t dyn, int (*cache)[5],
-                        cudaError_t* err) {
+int cluster_size_for_grid(Kernel kernel, int want, int num_clusters, int threads, size_t dyn,
+                          int (*cache)[5], cudaError_t* err) {
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return 1;
+  const bool cacheable = dev >= 0 && dev < 128;
   int lw = 0;
   while ((1 << (lw + 1)) <= want && lw < 4) ++lw;
-  if (dev >= 0 && dev < 128 && cache[dev][lw] > 0) return cache[dev][lw] - 1;
-  *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
-  if (*err != cudaSuccess) return 1;
-  *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (*err != cudaSuccess) return 1;
-  int csize = 1 << lw;
-  for (; csize > 1; csize /= 2) {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(csize);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(unsigned(csize));
-    cfg.blockDim = dim3(unsigned(threads));
-    cfg.dynamicSmemBytes = dyn;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) == cudaSuccess && active > 0) break;
-    (void)cudaGetLastError();
+  if (!cacheable || cache[dev][0] == 0) {
+    *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn));
+    if (*err != cudaSuccess) return 1;
+    *err = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (*err != cudaSuccess) return 1;
+    if (cacheable) cache[dev][0] = 1;
   }
-  if (dev >= 0 && dev < 128) cache[dev][lw] = csize + 1;
-  return csize;
+  for (; lw > 0; --lw) {
+    int active = 0;
+    if (cacheable && cache[dev][lw] > 0) {
+      active = cache[dev][lw] - 1;
+    } else {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1u << lw;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(1u << lw);
+      cfg.blockDim = dim3(unsigned(threads));
+      cfg.dynamicSmemBytes = dyn;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) != cudaSuccess) {
+        active = 0;
+        (void)cudaGetLastError();
+      }
+      if (cacheable) cache[dev][lw] = active + 1;
+    }
+    if (active >= num_clusters) return 1 << lw;
+  }
+  return 1;
 }
 
 // Launches `kernel` on `stream` with programmatic stream serialization and,

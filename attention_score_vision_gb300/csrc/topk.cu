@@ -455,9 +455,9 @@ cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* re
   static int cache[128][5] = {};
   const size_t dyn = sizeof(TopkShared) + size_t(kTopkCacheKeys) * sizeof(uint32_t);
   cudaError_t e = cudaSuccess;
-  const int csize = usable_cluster_size(topk_cluster_kernel,
-                                        cluster_size_for(total_tokens, num_req), kTopkThreads,
-                                        dyn, cache, &e);
+  const int want = cluster_size_for(total_tokens, num_req);
+  const int csize =
+      cluster_size_for_grid(topk_cluster_kernel, want, num_req, kTopkThreads, dyn, cache, &e);
   if (e != cudaSuccess) return e;
   return launch_clusters(topk_cluster_kernel, num_req, csize, kTopkThreads, dyn, stream, scores,
                          total_tokens, req_off, num_req, keep, total_keep, keep_idx, cu_keep,

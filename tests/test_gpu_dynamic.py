@@ -92,6 +92,17 @@ def test_dynamic_budget_slice_past_two_to_the_twenty(tsel):
     assert np.array_equal(keep, ref) and total == int(ref.sum())
 
 
+def test_dynamic_budget_many_large_requests(tsel):
+    # twelve 40K-token requests (more than the device holds clusters of 16)
+    rng = np.random.default_rng(903)
+    off = (np.arange(13) * 40000).tolist()
+    s = (rng.random(off[-1]) ** 4).astype(np.float32) * np.float32(1e-3)
+    keep, total, st = _budget(tsel, s, off, 800, 50, 950)
+    ref = oracle.dynamic_budget(s, off, 800, 50, 950)
+    assert st == 0
+    assert np.array_equal(keep, ref) and total == int(ref.sum())
+
+
 def test_dynamic_budget_flags_nan_and_bad_offsets(tsel):
     s = np.asarray([0.5, np.nan, 0.25, 0.125], np.float32)
     keep, _, st = _budget(tsel, s, [0, 4], 1000, 0, 1000)

@@ -281,6 +281,21 @@ def test_topk_uneven_requests_in_clusters(tsel, sizes, keep):
     assert np.array_equal(got, ref) and np.array_equal(cu, cref)
 
 
+def test_topk_more_large_requests_than_resident_clusters(tsel):
+    # twelve 40K-token requests: clusters of 16 CTAs would not all fit on the
+    # device at once, so the launch takes a smaller cluster size
+    rng = np.random.default_rng(12)
+    sizes = [40000] * 11 + [39999]
+    off = np.concatenate([[0], np.cumsum(sizes)]).tolist()
+    s = rng.random(off[-1]).astype(np.float32)
+    s[rng.integers(0, off[-1], off[-1] // 4)] = np.float32(0.25)   # ties across slices
+    keep = [(7919 * (i + 1)) % (sz + 1) for i, sz in enumerate(sizes)]
+    got, cu, st = _topk(tsel, s, off, keep)
+    ref, cref = oracle.select_topk(s, off, keep)
+    assert st == 0
+    assert np.array_equal(got, ref) and np.array_equal(cu, cref)
+
+
 def test_topk_nan_in_cluster_slices(tsel):
     # NaN scores in several slices of a 16-CTA cluster: the status flags them;
     # their rank is unspecified, but every other kept token must be one of the
