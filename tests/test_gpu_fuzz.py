@@ -4,7 +4,8 @@ self- and cross-attention lengths, every head_dim, GQA ratios, explicit
 scales, several requests per call, random budgets — each compared with the
 fp64 oracle (scores, LSE) and bit for bit on the selection and compaction fed
 the same fp32 scores; the dynamic budget and the LSE-provided mode ride
-along."""
+along. A second set draws request layouts for the selection kernels alone
+(one to sixty requests of up to 100K tokens, so every cluster size occurs)."""
 import numpy as np
 import pytest
 import torch
@@ -93,3 +94,56 @@ def test_random_problem_lse_provided(tsel, seed):
                                 max(w.max_seqlen_k, 1), softmax_scale=scale,
                                 flags=tsel.TSEL_IMP_LSE_PROVIDED, lse=lse_in)
     assert max_rel_err(s.cpu().numpy(), s_ref) <= REL_TOL
+
+
+def _random_selection_problem(seed):
+    """Random request layouts for the selection kernels alone: from one to
+    sixty requests, each empty to 100K tokens (so every cluster size and
+    slices of every length occur), score sets with heavy ties, signed zeros
+    and values over many binades."""
+    rng = np.random.default_rng(50_000 + seed)
+    R = int(rng.choice([1, 2, 3, 8, 13, 60]))
+    big = rng.random() < 0.5
+    sizes = rng.integers(0, 100_000 if big else 5_000, size=R)
+    if rng.random() < 0.3:
+        sizes[rng.integers(R)] = 0
+    n = int(sizes.sum())
+    kind = int(rng.integers(4))
+    if kind == 0:
+        s = rng.random(n)
+    elif kind == 1:
+        s = rng.integers(0, 5, n) * 0.125                     # five values: ties everywhere
+    elif kind == 2:
+        s = np.exp2(rng.uniform(-60, 10, n))                  # many binades
+    else:
+        s = rng.exponential(1e-4, n)                          # attention-like
+    s = s.astype(np.float32)
+    if n:
+        s[rng.integers(0, n, n // 50 + 1)] = np.float32(0.0)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64).tolist()
+    keep = [int(rng.integers(0, int(z) + 1)) for z in sizes]
+    return s, off, keep
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_selection_layouts(tsel, seed):
+    s, off, keep = _random_selection_problem(seed)
+    sd = torch.from_numpy(s).cuda()
+    ws = torch.zeros(tsel.tsel_select_topk_workspace_size(len(keep)), dtype=torch.uint8, device="cuda")
+    ki, cu = tsel.tsel_select_topk(sd, i32(off), i32(keep), int(sum(keep)), workspace=ws)
+    ref, cref = oracle.select_topk(s, off, keep)
+    assert tsel.tsel_read_device_status(ws) == 0
+    assert np.array_equal(ki.cpu().numpy(), ref) and np.array_equal(cu.cpu().numpy(), cref)
+    # the dynamic budget on the same layout, and the device-count selection it feeds
+    rng = np.random.default_rng(seed)
+    tau, lo = int(rng.choice([1, 300, 900, 1000])), int(rng.choice([0, 100]))
+    hi = int(rng.choice([lo, 900, 1000]))
+    bk, bt = tsel.tsel_dynamic_budget(sd, i32(off), tau, lo, hi, workspace=ws)
+    bref = oracle.dynamic_budget(s, off, tau, lo, hi)
+    assert tsel.tsel_read_device_status(ws) == 0
+    assert np.array_equal(bk.cpu().numpy(), bref) and int(bt.item()) == int(bref.sum())
+    ki2, cu2 = tsel.tsel_select_topk(sd, i32(off), bk, tsel.TSEL_KEEP_FROM_DEVICE, workspace=ws)
+    ref2, cref2 = oracle.select_topk(s, off, bref)
+    n_kept = int(cu2[-1].item())
+    assert n_kept == int(bref.sum())
+    assert np.array_equal(ki2[:n_kept].cpu().numpy(), ref2) and np.array_equal(cu2.cpu().numpy(), cref2)
