@@ -137,6 +137,38 @@ def _new_workspace(nbytes: int, device) -> torch.Tensor:
     return torch.zeros(max(nbytes, 1024), dtype=torch.uint8, device=device)
 
 
+def _check_qk(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torch.Tensor,
+              cu_seqlens_k: torch.Tensor, allow_fp8: bool):
+    """Checks the importance inputs the C ABI cannot see (dtypes, devices, the
+    [rows, heads, head_dim] layout the TMA maps are built from); returns
+    (Tq, H, d, Tk, Hkv, fp8)."""
+    fp8_types = (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
+    fp8 = allow_fp8 and q.dtype in fp8_types and k.dtype in fp8_types
+    if fp8:
+        if not (q.is_cuda and k.is_cuda):
+            raise TypeError("q and k must be CUDA tensors")
+    else:
+        _need(q, torch.bfloat16, "q")
+        _need(k, torch.bfloat16, "k")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q and k must be [rows, heads, head_dim] tensors")
+    tq, H, d = q.shape
+    tk, Hkv, dk = k.shape
+    if dk != d:
+        raise ValueError("q and k head_dim differ")
+    for t, name in ((q, "q"), (k, "k")):
+        if t.stride(2) != 1 or t.stride(1) != d:
+            raise ValueError(f"{name} must have contiguous [heads, head_dim] rows")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel():
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    for t in (k, cu_seqlens_q, cu_seqlens_k):
+        if t.device != q.device:
+            raise ValueError("q, k and cu_seqlens must be on the same device")
+    return tq, H, d, tk, Hkv, fp8
+
+
 # ---------------------------------------------------------------------------
 # Importance
 # ---------------------------------------------------------------------------
@@ -159,23 +191,9 @@ def tsel_importance(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torch.Tensor
     log) is an input and only the column pass runs. uint8 / float8_e4m3fn q and
     k are E4M3 inputs; softmax_scale then includes their dequantisation scales.
     """
-    fp8_types = (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))
-    if q.dtype in fp8_types and k.dtype in fp8_types:
+    tq, H, d, tk, Hkv, fp8 = _check_qk(q, k, cu_seqlens_q, cu_seqlens_k, allow_fp8=True)
+    if fp8:
         flags |= TSEL_IMP_FP8_E4M3   # E4M3 bytes; softmax_scale must carry the dequant scales
-        if not (q.is_cuda and k.is_cuda):
-            raise TypeError("q and k must be CUDA tensors")
-    else:
-        _need(q, torch.bfloat16, "q")
-        _need(k, torch.bfloat16, "k")
-    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
-    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
-    tq, H, d = q.shape
-    tk, Hkv, dk = k.shape
-    if dk != d:
-        raise ValueError("q and k head_dim differ")
-    for t, name in ((q, "q"), (k, "k")):
-        if t.stride(2) != 1 or t.stride(1) != d:
-            raise ValueError(f"{name} must have contiguous [heads, head_dim] rows")
     G = cu_seqlens_k.numel() - 1
     dev = q.device
     if scores is None:
@@ -186,10 +204,12 @@ def tsel_importance(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torch.Tensor
     if workspace is None:
         workspace = _new_workspace(nbytes, dev)
     lib = load_library()
-    st = lib.tsel_importance(_ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(cu_seqlens_q),
-                             _ptr(cu_seqlens_k), G, tq, tk, int(max_seqlen_q), int(max_seqlen_k),
-                             H, Hkv, d, float(softmax_scale), int(flags), _ptr(lse), _ptr(scores),
-                             _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    with torch.cuda.device(dev):   # the library works on the current device
+        st = lib.tsel_importance(_ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), G, tq, tk, int(max_seqlen_q),
+                                 int(max_seqlen_k), H, Hkv, d, float(softmax_scale), int(flags),
+                                 _ptr(lse), _ptr(scores), _ptr(workspace), workspace.numel(),
+                                 _stream(stream, dev))
     _check(st)
     return scores, lse
 
@@ -204,20 +224,23 @@ def tsel_importance_noalloc(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torc
     workspace (for callers that cannot allocate device memory). Output
     tensors passed in are used as they are; calls on one device must not
     overlap on the GPU."""
-    _need(q, torch.bfloat16, "q")
-    _need(k, torch.bfloat16, "k")
-    tq, H, d = q.shape
-    tk, Hkv, _ = k.shape
+    tq, H, d, tk, Hkv, _ = _check_qk(q, k, cu_seqlens_q, cu_seqlens_k, allow_fp8=False)
+    if device_status is not None:
+        _need(device_status, torch.int32, "device_status")
+        if device_status.device != q.device:
+            raise ValueError("device_status must be on q's device")
     G = cu_seqlens_k.numel() - 1
     dev = q.device
     if scores is None:
         scores = torch.empty(tk, dtype=torch.float32, device=dev)
     if lse is None and want_lse:
         lse = torch.empty((H, tq), dtype=torch.float32, device=dev)
-    st = load_library().tsel_importance_noalloc(
-        _ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), G, tq,
-        tk, int(max_seqlen_q), int(max_seqlen_k), H, Hkv, d, float(softmax_scale), _ptr(lse),
-        _ptr(scores), _ptr(device_status), _stream(stream, dev))
+    # the static scratch array is looked up on the current device: make it q's
+    with torch.cuda.device(dev):
+        st = load_library().tsel_importance_noalloc(
+            _ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), G,
+            tq, tk, int(max_seqlen_q), int(max_seqlen_k), H, Hkv, d, float(softmax_scale),
+            _ptr(lse), _ptr(scores), _ptr(device_status), _stream(stream, dev))
     _check(st)
     return scores, lse
 

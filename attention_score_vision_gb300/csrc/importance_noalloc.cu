@@ -33,7 +33,7 @@ namespace {
 
 // 16 MiB: enough for the schedule, the per-head-group partial sums and the
 // padded row-LSE buffer of, e.g., 16 heads over 131072 query and key tokens
-// in 128 segments (about 14.1 MB).
+// in 128 segments (about 14.1 MB; 30 images of 61,385 tokens need about 6 MB).
 constexpr size_t kNoallocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -83,6 +83,23 @@ extern "C" TSEL_API tsel_status tsel_importance_noalloc(
              (long long)need, kNoallocScratchBytes);
     tsel::record_error(msg);
     return TSEL_ERR_WORKSPACE;
+  }
+  if (stream != nullptr) {
+    // The scratch array used is the current device's; a stream of another
+    // device would run the kernels there against this device's address.
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(stream, &sdev) != cudaSuccess) {
+      tsel::record_error("tsel_importance_noalloc: cannot query the current or the stream's device");
+      return TSEL_ERR_CUDA;
+    }
+    if (sdev != cur) {
+      char msg[160];
+      snprintf(msg, sizeof(msg),
+               "tsel_importance_noalloc: the stream belongs to device %d, the current device is %d",
+               sdev, cur);
+      tsel::record_error(msg);
+      return TSEL_ERR_INVALID_VALUE;
+    }
   }
   void* scratch = nullptr;
   cudaError_t e = scratch_for_current_device(&scratch);

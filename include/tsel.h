@@ -187,6 +187,8 @@ TSEL_API tsel_status tsel_importance(const void* q, int64_t q_row_stride,
  *
  * Arguments are those of tsel_importance (flags fixed to 0). device_status,
  * if not NULL, is a device uint32 that receives this call's TSEL_DEV_* bits.
+ * The array used is the one of the calling thread's current device, so
+ * `stream` must belong to that device (else TSEL_ERR_INVALID_VALUE).
  */
 TSEL_API tsel_status tsel_importance_noalloc(const void* q, int64_t q_row_stride,
                                              const void* k, int64_t k_row_stride,

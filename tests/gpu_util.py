@@ -106,3 +106,35 @@ def segment_slice(w, g):
     q0, q1 = int(w.cu_seqlens_q[g]), int(w.cu_seqlens_q[g + 1])
     k0, k1 = int(w.cu_seqlens_k[g]), int(w.cu_seqlens_k[g + 1])
     return w.q_bits[q0:q1], w.k_bits[k0:k1], [0, q1 - q0], [0, k1 - k0], (q0, q1, k0, k1)
+
+
+_ORACLE_FULL = {}
+
+
+def oracle_full(name: str):
+    """(lse, scores) of the fp64 oracle over a whole named workload (bf16 inputs),
+    segments spread over a pool of host processes; computed once per test run."""
+    if name not in _ORACLE_FULL:
+        import workloads as W
+        from oracle_pool import importance_by_segment
+        _ORACLE_FULL[name] = importance_by_segment(W.make(name))
+    return _ORACLE_FULL[name]
+
+
+def keep_set_flips(w, keep_idx, ref_scores):
+    """Tokens kept by exactly one of `keep_idx` and the oracle's top-B of
+    `ref_scores`, with each one's relative distance from its request's B-th
+    oracle score. Returns (flipped token indices, distances)."""
+    k_ref, _ = oracle.select_topk(ref_scores, w.req_tok_offsets, w.keep_per_req)
+    flips = np.array(sorted(set(np.asarray(keep_idx).tolist()) ^ set(k_ref.tolist())),
+                     dtype=np.int64)
+    dist = np.zeros(flips.size)
+    off = w.req_tok_offsets
+    for r in range(len(off) - 1):
+        lo, hi, B = int(off[r]), int(off[r + 1]), int(w.keep_per_req[r])
+        sel = (flips >= lo) & (flips < hi)
+        if not np.any(sel):
+            continue
+        bth = np.sort(ref_scores[lo:hi])[::-1][B - 1]
+        dist[sel] = np.abs(ref_scores[flips[sel]] - bth) / bth
+    return flips, dist

@@ -12,7 +12,7 @@ import torch
 import oracle
 import workloads as W
 from gpu_util import (REL_TOL, check_keep_set_agreement, check_selection_exact, max_rel_err,
-                      run_path, segment_slice, to_device)
+                      oracle_full, run_path, segment_slice, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -64,6 +64,22 @@ def test_full_size_workloads_sampled(tsel, name):
         assert err <= REL_TOL, (g, err)
         np.testing.assert_allclose(out["lse"][:, q0:q1], lse_ref, rtol=1e-5, atol=1e-4)
     check_selection_exact(w, out)
+
+
+@pytest.mark.parametrize("name", ["thirty_images", "batch_8x16x1024"])
+def test_full_size_workloads_full_oracle_keep_set(tsel, name):
+    """Full size against the oracle over every image (segments spread over
+    host processes): every score within 2e-3, and the end-to-end keep set
+    equal to the oracle's except for tokens within 2e-3 of a request's B-th
+    oracle score (the 8-request batch: every request's pool)."""
+    w = W.make(name)
+    out = run_path(tsel, w)
+    assert out["status"] == 0
+    lse_ref, s_ref = oracle_full(name)
+    assert max_rel_err(out["scores"], s_ref) <= REL_TOL
+    np.testing.assert_allclose(out["lse"], lse_ref, rtol=1e-5, atol=1e-4)
+    check_selection_exact(w, out)
+    check_keep_set_agreement(w, out, s_ref)
 
 
 def test_varlen_pool_end_to_end(tsel):

@@ -33,11 +33,17 @@ import numpy as np
 SEED_BASE = 0x75E10000
 
 
-def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round fp32 values to bf16 (round to nearest, ties to even); return bits."""
+def f32_to_bf16_bits(x: np.ndarray, chunk: int = 1 << 20) -> np.ndarray:
+    """Round fp32 values to bf16 (round to nearest, ties to even); return bits.
+    Works in cache-sized chunks (the result does not depend on the chunking)."""
     b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    rounding = np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))
-    return ((b + rounding) >> np.uint32(16)).astype(np.uint16)
+    flat = b.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint16)
+    for i in range(0, flat.size, chunk):
+        v = flat[i:i + chunk]
+        rounding = np.uint32(0x7FFF) + ((v >> np.uint32(16)) & np.uint32(1))
+        out[i:i + chunk] = (v + rounding) >> np.uint32(16)
+    return out.reshape(b.shape)
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
