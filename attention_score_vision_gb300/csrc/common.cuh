@@ -24,6 +24,8 @@ struct WsHeader {
   uint32_t pad3[31];
   int32_t redo_count;     // pass-1 units queued for an exact redo
   uint32_t pad4[31];
+  int32_t hist_ok;        // 1: the request offsets are valid and the score histograms are built
+  uint32_t pad5[31];
 };
 static_assert(sizeof(WsHeader) <= kWsHeaderBytes, "header too large");
 
@@ -115,6 +117,24 @@ __host__ __device__ inline ImpWsLayout imp_ws_layout(int G, int Tq, int Tk, int 
   return L;
 }
 
+// Per-request score histograms the column pass builds for the top-B (fused
+// score + select path): bins of the first 11 bits of the order-preserving
+// score key (the top-B's first radix digit) followed by bins of its first 16
+// bits, int32 counts.
+constexpr int kHistCoarse = 2048;
+constexpr int kHistFine = 65536;
+constexpr int64_t kHistWords = kHistCoarse + kHistFine;
+constexpr int kHistMaxReq = 64;   // more requests: the fused path runs without histograms
+
+// Histogram region of a fused score + select workspace (after the importance
+// layout); 0 bytes when the requests get no histograms.
+__host__ __device__ inline int64_t sel_hist_offset(const ImpWsLayout& L) {
+  return align_up(L.total, 1024);
+}
+__host__ __device__ inline int64_t sel_hist_bytes(int R) {
+  return (R >= 1 && R <= kHistMaxReq) ? int64_t(R) * kHistWords * 4 : 0;
+}
+
 struct ImpPassParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
@@ -150,6 +170,13 @@ struct ImpPassParams {
   uint2* redo_units;
   int32_t* redo_flags;
   int32_t* redo_count;
+  // fused score + select: per-request score histograms (pass 1 zeroes them,
+  // pass 2 adds every score it writes); null when not requested
+  int32_t* hist;
+  int64_t hist_words;        // R * kHistWords
+  const int32_t* req_off;    // [R+1] request token offsets
+  int R;
+  const int32_t* hist_ok;    // header word written by the schedule kernel
 };
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
@@ -171,6 +198,37 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Adds the scores of a warp's tokens to their requests' histograms (coarse:
+// first 11 bits of the key, fine: first 16 bits). Lanes holding the same bin
+// add once (match_any); lanes with valid == false or tokens outside every
+// request add nothing. Every lane of the warp must call it.
+__device__ __forceinline__ void hist_add_warp(int32_t* hist, const int32_t* req_off, int R,
+                                              int tok, float s, bool valid) {
+  const int lane = threadIdx.x & 31;
+  int r = -1;
+  uint32_t key = 0;
+  if (valid) {
+    int lo = 0, hi = R + 1;   // first i in [0, R] with req_off[i] > tok
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(req_off + mid) <= tok) lo = mid + 1;
+      else hi = mid;
+    }
+    r = lo - 1 < R ? lo - 1 : -1;
+    key = order_key(s);
+  }
+  const bool in = r >= 0;
+  const uint32_t tc = in ? (uint32_t(r) << 11) | (key >> 21) : 0xFFFFFFFFu;
+  const uint32_t tf = in ? (uint32_t(r) << 16) | (key >> 16) : 0xFFFFFFFFu;
+  const unsigned mc = __match_any_sync(0xffffffffu, tc);
+  const unsigned mf = __match_any_sync(0xffffffffu, tf);
+  if (in) {
+    int32_t* h = hist + int64_t(r) * kHistWords;
+    if (lane == __ffs(mc) - 1) atomicAdd(h + (key >> 21), __popc(mc));
+    if (lane == __ffs(mf) - 1) atomicAdd(h + kHistCoarse + (key >> 16), __popc(mf));
+  }
 }
 
 // Inverse of order_key (for keys of non-negative scores).

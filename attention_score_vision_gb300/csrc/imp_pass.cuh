@@ -453,6 +453,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   const int total_units = *reinterpret_cast<const volatile int*>(p.num_units);
   const int group = p.H / p.Hkv;
+  if (PASS == 1 && p.hist != nullptr && warp >= kEpiFirstWarp && warp < kMma1Warp) {
+    // Fused score + select: zero the per-request score histograms the column
+    // pass adds into (the epilogue warps have nothing to do yet).
+    constexpr int kZeroThreads = 32 * kEpiWarps;
+    const int t = (warp - kEpiFirstWarp) * 32 + lane;
+    int4* h4 = reinterpret_cast<int4*>(p.hist);
+    for (int64_t i = int64_t(blockIdx.x) * kZeroThreads + t; i < p.hist_words / 4;
+         i += int64_t(gridDim.x) * kZeroThreads)
+      h4[i] = make_int4(0, 0, 0, 0);
+  }
+  const bool add_hist =
+      PASS == 2 && p.hist != nullptr && *reinterpret_cast<const volatile int32_t*>(p.hist_ok) != 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -752,7 +764,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float total = part + o0;
             const float rows = p.sum_norm ? 1.f : float(p.H * w.nq);
             if (p.hgroups == 1) {
-              if (krow < w.nk) p.scores[w.k0 + krow] = w.nq > 0 ? total / rows : 0.f;
+              const float sc = w.nq > 0 ? total / rows : 0.f;
+              if (krow < w.nk) p.scores[w.k0 + krow] = sc;
+              if (add_hist) hist_add_warp(p.hist, p.req_off, p.R, w.k0 + krow, sc, krow < w.nk);
             } else {
               // Partial sums of this head group; the last group of the 32-key
               // slice adds all groups' partials in group order.
@@ -768,12 +782,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               old = __shfl_sync(0xffffffffu, old, 0);
               if (old == p.hgroups - 1) {
                 __threadfence();
+                float sc = 0.f;
                 if (krow < w.nk) {
                   float sum = 0.f;
                   for (int gi = 0; gi < p.hgroups; ++gi)
                     sum += __ldcg(p.part + int64_t(gi) * p.Tk + w.k0 + krow);
-                  p.scores[w.k0 + krow] = w.nq > 0 ? sum / rows : 0.f;
+                  sc = w.nq > 0 ? sum / rows : 0.f;
+                  p.scores[w.k0 + krow] = sc;
                 }
+                if (add_hist) hist_add_warp(p.hist, p.req_off, p.R, w.k0 + krow, sc, krow < w.nk);
               }
             }
           }

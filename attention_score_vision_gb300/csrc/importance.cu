@@ -88,7 +88,9 @@ __global__ void __launch_bounds__(THREADS) imp_prep_kernel(const int32_t* __rest
                                                         const int32_t* __restrict__ cu_k, int G,
                                                         int Tq, int Tk, int max_q, int max_k,
                                                         int H, int HG, uint8_t* ws,
-                                                        ImpWsLayout L) {
+                                                        ImpWsLayout L,
+                                                        const int32_t* __restrict__ req_off,
+                                                        int R) {
   __shared__ int bad;
   __shared__ int totals[2];
   __shared__ int hist[1024];
@@ -117,6 +119,21 @@ __global__ void __launch_bounds__(THREADS) imp_prep_kernel(const int32_t* __rest
     hdr->sched_ctr[1] = 0;
     hdr->redo_count = 0;
     hdr->fix_ctr = 0;
+  }
+  if (warp == 1) {
+    // Fused score + select (req_off given): the column pass builds per-request
+    // score histograms only for requests that cover ordered token ranges
+    // (0 <= o[0] <= ... <= o[R] <= Tk) and when both passes run.
+    bool ok = req_off != nullptr && R >= 1 && R <= kHistMaxReq && Tq > 0 && Tk > 0 && G > 0;
+    if (ok) {
+      for (int r = lane; r <= R; r += 32) {
+        const int o = req_off[r];
+        const int prev = r > 0 ? req_off[r - 1] : 0;
+        if (o < prev || o > Tk) ok = false;
+      }
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (lane == 0) hdr->hist_ok = ok ? 1 : 0;
   }
   for (int64_t i = threadIdx.x; i < L.n_grp; i += THREADS) grp_ctr[i] = 0;
   {
@@ -286,9 +303,17 @@ __global__ void __launch_bounds__(THREADS) imp_prep_kernel(const int32_t* __rest
 __global__ void __launch_bounds__(kTile) imp_lse_import_kernel(
     const float* __restrict__ lse_in, int Tq, const int32_t* __restrict__ cu_q, int G,
     const int32_t* __restrict__ qtile_off, float* __restrict__ nlse2, int64_t lse_stride,
-    const uint32_t* status) {
+    const uint32_t* status, int32_t* hist, int64_t hist_words) {
   pdl_launch_dependents();
   pdl_wait();
+  if (hist != nullptr) {
+    // the column pass that follows adds into zeroed histograms
+    const int64_t cta = int64_t(blockIdx.y) * gridDim.x + blockIdx.x;
+    const int64_t ctas = int64_t(gridDim.x) * gridDim.y;
+    int4* h4 = reinterpret_cast<int4*>(hist);
+    for (int64_t i = cta * kTile + threadIdx.x; i < hist_words / 4; i += ctas * kTile)
+      h4[i] = make_int4(0, 0, 0, 0);
+  }
   if (*reinterpret_cast<const volatile uint32_t*>(status) & TSEL_DEV_SEQLENS) return;
   const int t = blockIdx.x, h = blockIdx.y;
   const int total = qtile_off[G];
@@ -316,22 +341,25 @@ __global__ void __launch_bounds__(kTile) imp_lse_import_kernel(
 
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
                             int max_q, int max_k, int H, int HG, uint8_t* ws,
-                            const ImpWsLayout& L, cudaStream_t stream) {
+                            const ImpWsLayout& L, const int32_t* req_off, int R,
+                            cudaStream_t stream) {
   // Few segments and few units: a small block (one warp orders the segments,
   // four write the units); otherwise all 32 warps write the unit lists.
   if (G <= 32 && L.u1_max + L.u2_max <= 1024)
     return launch_kernel(imp_prep_kernel<128>, dim3(1), 128, 0, stream, 1, cu_q, cu_k, G, Tq, Tk,
-                         max_q, max_k, H, HG, ws, L);
+                         max_q, max_k, H, HG, ws, L, req_off, R);
   return launch_kernel(imp_prep_kernel<1024>, dim3(1), 1024, 0, stream, 1, cu_q, cu_k, G, Tq, Tk,
-                       max_q, max_k, H, HG, ws, L);
+                       max_q, max_k, H, HG, ws, L, req_off, R);
 }
 
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
                               const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
-                              int max_qtiles, int H, const uint32_t* status, cudaStream_t stream) {
+                              int max_qtiles, int H, const uint32_t* status, int32_t* hist,
+                              int64_t hist_words, cudaStream_t stream) {
   if (max_qtiles <= 0) return cudaSuccess;
   return launch_kernel(imp_lse_import_kernel, dim3(unsigned(max_qtiles), unsigned(H)), kTile, 0,
-                       stream, 1, lse_in, Tq, cu_q, G, qtile_off, nlse2, lse_stride, status);
+                       stream, 1, lse_in, Tq, cu_q, G, qtile_off, nlse2, lse_stride, status, hist,
+                       hist_words);
 }
 
 cudaError_t launch_imp_pass1(int head_dim, bool fp8, bool ksplit, const CUtensorMap* maps,

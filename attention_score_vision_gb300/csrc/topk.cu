@@ -28,6 +28,18 @@
 //      above the key, and the lowest-index tokens equal to it), the indices
 //      are staged in shared memory and stored with coalesced writes.
 // The output is deterministic and independent of the cluster size.
+//
+// Histogram-seeded start (fused score + select path): the column pass that
+// wrote the scores also counted them per request by their first 11 and first
+// 16 key bits. The top-B then reads the 2048 first-digit counts with its
+// slice (no first round), and the 32 counts under the chosen digit give the
+// threshold's first 16 bits. When at most kTopkCand keys share them, every
+// CTA sends those candidates (key, index) and its count of keys above them to
+// every CTA of the cluster: one cluster barrier, after which each CTA finds
+// the threshold among the candidates alone (two 8-bit rounds in shared
+// memory, block barriers only) and knows its output offset. More candidates,
+// or counts that do not add up to the request's tokens, fall back to the
+// radix rounds above (from the second digit, or from the first).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -47,6 +59,8 @@ constexpr int kTopkItems = 8;                      // consecutive tokens per thr
 constexpr int kTopkPass = kTopkThreads * kTopkItems;   // tokens per compaction pass (<= 65535)
 constexpr int kTopkCacheKeys = 16384;              // keys cached in shared memory per CTA
 constexpr int kTopkLoad = 8;                       // score loads in flight per thread
+constexpr int kTopkCand = 2048;                    // histogram start: candidates exchanged in the cluster
+static_assert(2 * kTopkCand <= kTopkPass, "candidates are staged in the compaction stage buffer");
 
 // Digit of round `round` (0, 1, 2): bits 31..21, 20..10, 9..0.
 __device__ __forceinline__ int topk_shift(int round) { return round == 0 ? 21 : (round == 1 ? 10 : 0); }
@@ -117,6 +131,15 @@ struct __align__(16) TopkShared {
   int bins[kTopkBins];        // this round's cluster-wide counts, gathered for the digit search
   int grp_sfx[kTopkGroups];   // last round: this CTA's keys in the groups above g of g's warp
   int stage[kTopkPass];       // kept indices of one compaction pass
+  // histogram start: every CTA's candidates (keys sharing the threshold's
+  // first 16 bits) and per-CTA counts, written by the CTAs that hold them
+  uint32_t cand_key[kTopkCand];
+  int cand_idx[kTopkCand];
+  int gt16_of[kMaxClusterCtas];   // per CTA: its keys above the candidates' 16-bit prefix
+  int cls_gt[kMaxClusterCtas];    // per CTA: its candidates above the threshold
+  int cls_eq[kMaxClusterCtas];    // per CTA: its candidates equal to the threshold
+  int cbase[kMaxClusterCtas];     // this CTA's first slot in each CTA's candidate list
+  int cand_n, loc_n;
   __align__(16) int wtot[kTopkWarps];       // digit search: per-warp bin totals
   __align__(16) int gt_w[kTopkWarps];       // last round: per-warp keys above the rounds 0-1 prefix
   __align__(16) int grp_w[kTopkWarps];      // last round: per-warp totals of this CTA's counts
@@ -125,7 +148,7 @@ struct __align__(16) TopkShared {
   int neg_w[kTopkWarps];
   int out_base, eq_before;
   int nan_seen;
-  int pad_[3];
+  int pad_[1];
 };
 static_assert(sizeof(TopkShared) % 16 == 0, "key cache follows at a 16-byte boundary");
 
@@ -167,12 +190,41 @@ __device__ __forceinline__ int find_digit(const int* bins, const int* wtot, int 
   return digit;
 }
 
+// find_digit over 256 bins (the candidates' last two rounds): lane l holds
+// bins 8l .. 8l + 7. Every warp finds the same digit.
+__device__ __forceinline__ int find_digit256(const int* bins, int remaining, int& above) {
+  const int lane = threadIdx.x & 31;
+  const int4 lo4 = reinterpret_cast<const int4*>(bins)[2 * lane];
+  const int4 hi4 = reinterpret_cast<const int4*>(bins)[2 * lane + 1];
+  const int b[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+  const int sum8 = lo4.x + lo4.y + lo4.z + lo4.w + hi4.x + hi4.y + hi4.z + hi4.w;
+  const int xs = warp_suffix_scan(sum8);
+  const int a0 = xs - sum8;   // keys in the bins of higher lanes
+  const unsigned hb = __ballot_sync(0xffffffffu, a0 < remaining && xs >= remaining);
+  const int g = hb ? __ffs(hb) - 1 : 0;
+  int a = __shfl_sync(0xffffffffu, a0, g);
+  int bg[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) bg[j] = __shfl_sync(0xffffffffu, b[j], g);
+  int digit = 8 * g;
+#pragma unroll
+  for (int j = 7; j >= 0; --j) {
+    if (a + bg[j] >= remaining) {
+      digit = 8 * g + j;
+      break;
+    }
+    a += bg[j];
+  }
+  above = a;
+  return digit;
+}
+
 __global__ void __launch_bounds__(kTopkThreads)
     topk_cluster_kernel(const float* __restrict__ scores, int total_tokens,
                         const int32_t* __restrict__ req_off, int num_req,
                         const int32_t* __restrict__ keep, int total_keep,
                         int32_t* __restrict__ keep_idx, int32_t* __restrict__ cu_keep,
-                        uint32_t* status) {
+                        uint32_t* status, const int32_t* hist, const int32_t* hist_ok) {
   extern __shared__ __align__(16) unsigned char topk_smem[];
   TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
   uint32_t* skeys = reinterpret_cast<uint32_t*>(topk_smem + sizeof(TopkShared));  // kTopkCacheKeys
@@ -188,7 +240,18 @@ __global__ void __launch_bounds__(kTopkThreads)
   {
     int4* h = reinterpret_cast<int4*>(&sh.local[0][0]);
     for (int i = tid; i < 6 * kTopkBins / 4; i += kTopkThreads) h[i] = make_int4(0, 0, 0, 0);
-    if (tid == 0) sh.nan_seen = 0;
+    if (tid < kMaxClusterCtas) {
+      sh.gt16_of[tid] = 0;
+      sh.cls_gt[tid] = 0;
+      sh.cls_eq[tid] = 0;
+    }
+    if (tid == 0) {
+      sh.nan_seen = 0;
+      sh.cand_n = 0;
+      sh.loc_n = 0;
+      sh.out_base = 0;
+      sh.eq_before = 0;
+    }
   }
   pdl_wait();
 
@@ -209,6 +272,10 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int i = j * kTopkThreads + tid;
     f[j] = i < len ? __ldcg(s + i) : 0.f;
   }
+  // histogram start: this request's first-digit counts (bins 4 tid .. 4 tid + 3)
+  const bool use_hist = hist != nullptr && *reinterpret_cast<const volatile int32_t*>(hist_ok) != 0;
+  const int32_t* hreq = use_hist ? hist + int64_t(r) * kHistWords : nullptr;
+  const int4 hc = use_hist ? __ldcg(reinterpret_cast<const int4*>(hreq) + tid) : make_int4(0, 0, 0, 0);
 
   // ---- request checks and output offset (every thread, every CTA alike) ----
   long long part = 0;
@@ -276,13 +343,161 @@ __global__ void __launch_bounds__(kTopkThreads)
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   __syncthreads();
 
-  // ---- radix select -------------------------------------------------------
+  // ---- threshold -----------------------------------------------------------
   uint32_t prefix = 0, mask = 0;
   int remaining = B;   // how many still to take among keys matching `prefix`
-  int gt_part = 0;     // this thread's bin groups: this CTA's keys above the prefix
+  int gt_part = 0;     // this thread's share: this CTA's keys above the prefix
   int digit = 0;
+  int round0 = 0;      // first radix round still to run
+  bool cand_mode = false;
+  uint32_t pfx16 = 0;  // candidates: keys whose first 16 bits are pfx16
+  int cnt16 = 0;
+  uint32_t thr = 0;
+  int need_eq = 0;     // tokens equal to the threshold to keep (request-wide)
+  if (use_hist) {
+    reinterpret_cast<int4*>(sh.bins)[tid] = hc;
+    const int t = warp_sum(hc.x + hc.y + hc.z + hc.w);
+    if (lane == 0) sh.wtot[warp] = t;
+    __syncthreads();
+    int counted = 0;
+#pragma unroll
+    for (int w = 0; w < kTopkWarps; w += 4) {
+      const int4 v = *reinterpret_cast<const int4*>(sh.wtot + w);
+      counted += v.x + v.y + v.z + v.w;
+    }
+    // Every token of the request counted (else the scores did not all come
+    // from the column pass that built the histogram): the same outcome in
+    // every CTA of the cluster, which all read the same counts.
+    if (counted == n) {
+      int above0;
+      const int d0 = find_digit(sh.bins, sh.wtot, remaining, above0);
+      const int rem0 = remaining - above0;
+      // the 32 first-16-bit bins under d0, bins descending = lanes descending
+      const int fb = __ldcg(hreq + kHistCoarse + d0 * 32 + lane);
+      const int xs = warp_suffix_scan(fb);
+      const unsigned hb = __ballot_sync(0xffffffffu, xs - fb < rem0 && xs >= rem0);
+      const int d1 = hb ? __ffs(hb) - 1 : 0;
+      const int above1 = __shfl_sync(0xffffffffu, xs - fb, d1);
+      cnt16 = __shfl_sync(0xffffffffu, fb, d1);
+      if (cnt16 <= kTopkCand) {
+        cand_mode = true;
+        pfx16 = (uint32_t(d0) << 5) | uint32_t(d1);
+        remaining = rem0 - above1;
+      } else {
+        // too many candidates: radix rounds from the second digit on
+        round0 = 1;
+        prefix = uint32_t(d0) << 21;
+        mask = 0x7FFu << 21;
+        remaining = rem0;
+        for (int i = tid; i < len; i += kTopkThreads) {
+          const uint32_t kk = cached ? skeys[i] : order_key(s[i]);
+          gt_part += (kk >> 21) > uint32_t(d0);
+        }
+      }
+    }
+  }
+
+  if (cand_mode) {
+    // This CTA's keys above the 16-bit prefix, and its candidates (staged in
+    // the compaction buffer: keys, then indices).
+    int gt16 = 0;
+    for (int i = tid; i < len; i += kTopkThreads) {
+      const uint32_t kk = cached ? skeys[i] : order_key(s[i]);
+      const uint32_t top = kk >> 16;
+      if (top > pfx16) {
+        ++gt16;
+      } else if (top == pfx16) {
+        const int slot = atomicAdd(&sh.loc_n, 1);
+        if (slot < kTopkCand) {
+          sh.stage[slot] = int(kk);
+          sh.stage[kTopkCand + slot] = lo + c0 + i;
+        }
+      }
+    }
+    gt16 = warp_sum(gt16);
+    if (lane == 0) sh.gt_w[warp] = gt16;
+    __syncthreads();
+    const int nloc = min(sh.loc_n, kTopkCand);
+    if (tid < csize) {
+      int gsum = 0;
+#pragma unroll
+      for (int w = 0; w < kTopkWarps; ++w) gsum += sh.gt_w[w];
+      int* cn = solo ? &sh.cand_n : cluster.map_shared_rank(&sh.cand_n, tid);
+      sh.cbase[tid] = atomicAdd(cn, nloc);
+      int* g16 = solo ? &sh.gt16_of[crank] : cluster.map_shared_rank(&sh.gt16_of[crank], tid);
+      *g16 = gsum;
+    }
+    __syncthreads();
+    for (int j = 0; j < csize; ++j) {
+      const int base = sh.cbase[j];
+      uint32_t* dk = solo ? sh.cand_key : cluster.map_shared_rank(sh.cand_key, j);
+      int* di = solo ? sh.cand_idx : cluster.map_shared_rank(sh.cand_idx, j);
+      for (int t = tid; t < nloc && base + t < kTopkCand; t += kTopkThreads) {
+        dk[base + t] = uint32_t(sh.stage[t]);
+        di[base + t] = sh.stage[kTopkCand + t];
+      }
+    }
+    // The one exchange: after it no CTA touches another's shared memory.
+    if (!solo) cluster.sync();
+    __syncthreads();
+    if (sh.cand_n != cnt16) {
+      // the candidates do not match the counts: radix rounds from the start
+      // (the same outcome in every CTA: each received every candidate)
+      cand_mode = false;
+      round0 = 0;
+      prefix = 0;
+      mask = 0;
+      remaining = B;
+      gt_part = 0;
+    }
+  }
+
+  if (cand_mode) {
+    // The threshold among the candidates: two 8-bit rounds over their low
+    // 16 bits (local[0], local[1]: zeroed at entry, unused on this path).
+    const int ncand = cnt16;
+    int* binsA = sh.local[0];
+    int* binsB = sh.local[1];
+    for (int i = tid; i < ncand; i += kTopkThreads) atomicAdd(&binsA[(sh.cand_key[i] >> 8) & 255u], 1);
+    __syncthreads();
+    int aboveA;
+    const int dA = find_digit256(binsA, remaining, aboveA);
+    remaining -= aboveA;
+    const uint32_t pfx24 = (pfx16 << 8) | uint32_t(dA);
+    for (int i = tid; i < ncand; i += kTopkThreads) {
+      const uint32_t kk = sh.cand_key[i];
+      if ((kk >> 8) == pfx24) atomicAdd(&binsB[kk & 255u], 1);
+    }
+    __syncthreads();
+    int aboveB;
+    const int dB = find_digit256(binsB, remaining, aboveB);
+    remaining -= aboveB;
+    thr = (pfx24 << 8) | uint32_t(dB);
+    need_eq = remaining;
+    // per CTA (the slice holding the index): candidates above / equal to thr
+    for (int i = tid; i < ncand; i += kTopkThreads) {
+      const uint32_t kk = sh.cand_key[i];
+      if (kk >= thr) {
+        const int src = min(csize - 1, (sh.cand_idx[i] - lo) / chunk);
+        atomicAdd(kk > thr ? &sh.cls_gt[src] : &sh.cls_eq[src], 1);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int base = 0, eqb = 0;
+      for (int c = 0; c < crank; ++c) {
+        const int take = max(0, min(sh.cls_eq[c], need_eq - eqb));
+        base += sh.gt16_of[c] + sh.cls_gt[c] + take;
+        eqb += sh.cls_eq[c];
+      }
+      sh.out_base = base;     // read after the compaction's first block barrier
+      sh.eq_before = eqb;
+    }
+    if (tid == 0 && sh.nan_seen) set_status(status, TSEL_DEV_NAN);   // this CTA's slice
+    pdl_launch_dependents();
+  } else {
 #pragma unroll 1
-  for (int round = 0; round < 3; ++round) {
+  for (int round = round0; round < 3; ++round) {
     const int shift = topk_shift(round);
     const uint32_t dmask = topk_dmask(round);
     int* loc = sh.local[round];
@@ -346,8 +561,8 @@ __global__ void __launch_bounds__(kTopkThreads)
   // The compaction kernel that follows may launch now: its CTAs would only
   // wait on this request's SMs during the rounds.
   pdl_launch_dependents();
-  const uint32_t thr = prefix;
-  const int need_eq = remaining;   // tokens equal to the threshold to keep (request-wide)
+  thr = prefix;
+  need_eq = remaining;
 
   // ---- output offset: the other CTAs' counts at the chosen digit -------------
   if (!solo) {
@@ -383,6 +598,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     // This CTA reads no other CTA's shared memory after this point; no CTA
     // leaves before every CTA has arrived here (wait at the end).
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  }
   }
 
   // ---- compaction in index order --------------------------------------------
@@ -421,7 +637,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     }
     int tot;
     const int pre = topk_block_scan((n_eq << 16) | n_gt, sh.warp_sums, tot);
-    if (i0 == 0 && !solo) {
+    if (i0 == 0) {   // (0 for one CTA on the radix-round path)
       out += sh.out_base;
       eq_seen = sh.eq_before;
     }
@@ -446,12 +662,60 @@ __global__ void __launch_bounds__(kTopkThreads)
     written += cnt;
     eq_seen += tot_eq;
   }
-  if (!solo) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (!solo && !cand_mode) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Per-request histograms of given scores (tsel_select_topk_hist), into a
+// zeroed region: one warp per 32 consecutive tokens. Every CTA checks the
+// request offsets itself (ordered, inside the tokens) and adds nothing when
+// they are not; CTA 0 records the outcome for the top-B that follows.
+constexpr int kHistThreads = 256;
+
+__global__ void __launch_bounds__(kHistThreads)
+    topk_hist_kernel(const float* __restrict__ scores, int total_tokens,
+                     const int32_t* __restrict__ req_off, int R, int32_t* hist, int32_t* hist_ok) {
+  __shared__ int ok_s;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    bool ok = R >= 1 && R <= kHistMaxReq;
+    for (int r = lane; ok && r <= R; r += 32) {
+      const int o = __ldg(req_off + r);
+      const int prev = r > 0 ? __ldg(req_off + r - 1) : 0;
+      if (o < prev || o > total_tokens) ok = false;
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (lane == 0) {
+      ok_s = ok ? 1 : 0;
+      if (blockIdx.x == 0) *hist_ok = ok_s;
+    }
+  }
+  __syncthreads();
+  if (!ok_s) return;
+  const int64_t warps = int64_t(gridDim.x) * (kHistThreads / 32);
+  for (int64_t w = int64_t(blockIdx.x) * (kHistThreads / 32) + warp; w * 32 < total_tokens; w += warps) {
+    const int tok = int(w * 32) + lane;
+    const bool valid = tok < total_tokens;
+    const float sc = valid ? __ldcg(scores + tok) : 0.f;
+    hist_add_warp(hist, req_off, R, tok, sc, valid);
+  }
+}
+
+cudaError_t launch_topk_hist(const float* scores, int total_tokens, const int32_t* req_off, int R,
+                             int32_t* hist, int32_t* hist_ok, int num_sms, cudaStream_t stream) {
+  const int64_t warps = (int64_t(total_tokens) + 31) / 32;
+  int64_t blocks = (warps + kHistThreads / 32 - 1) / (kHistThreads / 32);
+  if (blocks > 4 * int64_t(num_sms)) blocks = 4 * int64_t(num_sms);
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(topk_hist_kernel, dim3(unsigned(blocks)), kHistThreads, 0, stream, 1, scores,
+                       total_tokens, req_off, R, hist, hist_ok);
 }
 
 cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
                         int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
-                        int32_t* cu_keep, uint32_t* status, cudaStream_t stream) {
+                        int32_t* cu_keep, uint32_t* status, const int32_t* hist,
+                        const int32_t* hist_ok, cudaStream_t stream) {
   static int cache[128][5] = {};
   const size_t dyn = sizeof(TopkShared) + size_t(kTopkCacheKeys) * sizeof(uint32_t);
   cudaError_t e = cudaSuccess;
@@ -461,7 +725,7 @@ cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* re
   if (e != cudaSuccess) return e;
   return launch_clusters(topk_cluster_kernel, num_req, csize, kTopkThreads, dyn, stream, scores,
                          total_tokens, req_off, num_req, keep, total_keep, keep_idx, cu_keep,
-                         status);
+                         status, hist, hist_ok);
 }
 
 }  // namespace tsel

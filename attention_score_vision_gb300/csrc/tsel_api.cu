@@ -21,15 +21,20 @@ constexpr double kFixedRefMinPairs = 268435456.0;
 
 cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int Tq, int Tk,
                             int max_q, int max_k, int H, int HG, uint8_t* ws,
-                            const ImpWsLayout& L, cudaStream_t stream);
+                            const ImpWsLayout& L, const int32_t* req_off, int R,
+                            cudaStream_t stream);
 cudaError_t launch_imp_pass(int pass, int head_dim, bool fp8, const CUtensorMap* maps,
                             const ImpPassParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
                               const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
-                              int max_qtiles, int H, const uint32_t* status, cudaStream_t stream);
+                              int max_qtiles, int H, const uint32_t* status, int32_t* hist,
+                              int64_t hist_words, cudaStream_t stream);
 cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
                         int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
-                        int32_t* cu_keep, uint32_t* status, cudaStream_t stream);
+                        int32_t* cu_keep, uint32_t* status, const int32_t* hist,
+                        const int32_t* hist_ok, cudaStream_t stream);
+cudaError_t launch_topk_hist(const float* scores, int total_tokens, const int32_t* req_off, int R,
+                             int32_t* hist, int32_t* hist_ok, int num_sms, cudaStream_t stream);
 cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_bytes,
                           const int32_t* pos, int pos_dim, const int32_t* cu_k, int G, int Tk,
                           const int32_t* keep_idx, int K, const int32_t* K_dev,
@@ -188,14 +193,26 @@ size_t tsel_select_topk_workspace_size(int num_req) {
 
 size_t tsel_gather_compact_workspace_size(void) { return kWsHeaderBytes; }
 
-tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
+}  // extern "C"
+
+namespace {
+
+// Histograms the column pass builds for the top-B of the fused path.
+struct SelHist {
+  const int32_t* req_off;   // [R+1]
+  int R;
+  int32_t* hist;            // R * kHistWords int32 (null: no histograms)
+};
+
+// Importance: the schedule kernel, the row-LSE pass (or the LSE import) and
+// the column pass; with `sel` the column pass also builds the histograms.
+tsel_status importance_impl(const void* q, int64_t q_row_stride, const void* k,
                             int64_t k_row_stride, const int32_t* cu_seqlens_q,
                             const int32_t* cu_seqlens_k, int num_seg, int total_q, int total_k,
                             int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
                             int head_dim, float softmax_scale, unsigned flags, float* lse,
                             float* scores, void* workspace, size_t workspace_bytes,
-                            void* stream_) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+                            size_t workspace_needed, const SelHist& sel, cudaStream_t stream) {
   if (num_seg < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
     return fail(TSEL_ERR_INVALID_VALUE, "negative size");
   if (num_heads < 1 || num_heads > 256 || num_kv_heads < 1 || num_heads % num_kv_heads != 0)
@@ -204,7 +221,8 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     return fail(TSEL_ERR_UNSUPPORTED, "head_dim=%d (supported: 64, 80, 96, 112, 128)", head_dim);
   if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_FP8_E4M3 | TSEL_IMP_SCORE_SUM |
                  TSEL_IMP_ROWREF_FIXED | TSEL_IMP_ROWREF_MOVING | TSEL_IMP_TEST_STALL |
-                 TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2)) != 0)
+                 TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2 |
+                 (sel.req_off != nullptr ? TSEL_SEL_STAGE_TOPK : 0u))) != 0)
     return fail(TSEL_ERR_UNSUPPORTED, "flags=0x%x", flags);
   if ((flags & TSEL_IMP_ROWREF_FIXED) && (flags & TSEL_IMP_ROWREF_MOVING))
     return fail(TSEL_ERR_INVALID_VALUE, "TSEL_IMP_ROWREF_FIXED and _MOVING are exclusive");
@@ -231,10 +249,11 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return fail(TSEL_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   const ImpWsLayout L = imp_ws_layout(num_seg, total_q, total_k, num_heads);
-  if (workspace_bytes < size_t(L.total))
-    return fail(TSEL_ERR_WORKSPACE, "workspace %zu < %lld bytes", workspace_bytes,
-                (long long)L.total);
-  const unsigned stage_bits = TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2;
+  if (workspace_bytes < workspace_needed)
+    return fail(TSEL_ERR_WORKSPACE, "workspace %zu < %zu bytes", workspace_bytes,
+                workspace_needed);
+  const unsigned stage_bits = TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2 |
+                              TSEL_SEL_STAGE_TOPK;
   const unsigned stages = (flags & stage_bits) ? (flags & stage_bits) : stage_bits;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
@@ -245,7 +264,8 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
 
   if (stages & TSEL_IMP_STAGE_PREP) {
     e = launch_imp_prep(cu_seqlens_q, cu_seqlens_k, num_seg, total_q, total_k, max_seqlen_q,
-                        max_seqlen_k, num_heads, hgroups, ws, L, stream);
+                        max_seqlen_k, num_heads, hgroups, ws, L, sel.hist ? sel.req_off : nullptr,
+                        sel.R, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prep launch");
   }
   if (total_k == 0 || num_seg == 0) return TSEL_OK;
@@ -296,12 +316,17 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   p.stall = (flags & TSEL_IMP_TEST_STALL) ? 1 : 0;
   p.sum_norm = (flags & TSEL_IMP_SCORE_SUM) ? 1 : 0;
   if (p.stall) p.timeout_ns = 50ull * 1000000ull;
+  p.hist = sel.hist;
+  p.hist_words = sel.hist ? int64_t(sel.R) * kHistWords : 0;
+  p.req_off = sel.req_off;
+  p.R = sel.R;
+  p.hist_ok = &hdr->hist_ok;
 
   if ((stages & TSEL_IMP_STAGE_PASS1) && lse_provided) {
     // The caller's LSE replaces the row-LSE pass.
     e = launch_lse_import(lse, total_q, cu_seqlens_q, num_seg, p.qtile_off, p.nlse2, L.lse_stride,
                           int(ceil_div(total_q, kTile) + num_seg), num_heads, &hdr->status,
-                          stream);
+                          p.hist, p.hist_words, stream);
     if (e != cudaSuccess) return cuda_fail(e, "LSE import launch");
   } else if (stages & TSEL_IMP_STAGE_PASS1) {
     const CUtensorMap maps[4] = {qm64, qm16, km64, km16};
@@ -335,6 +360,7 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
     pr.stall = 0;
     pr.kspl = 1;
     pr.units = p1.redo_units;
+    pr.hist = nullptr;   // the histograms were zeroed by the first launch
     pr.num_units = &hdr->redo_count;
     pr.sched_ctr = &hdr->fix_ctr;
     const int64_t redo_max = int64_t(num_heads) * (L.lse_stride / kTile);
@@ -362,19 +388,97 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
   return TSEL_OK;
 }
 
+// Host checks of the top-B arguments (tsel_select_topk and the fused path).
+tsel_status check_select_args(const float* scores, int total_tokens, const int32_t* req_tok_offsets,
+                              int num_req, const int32_t* keep_per_req, int total_keep,
+                              int32_t* keep_idx, int32_t* cu_keep) {
+  if (num_req < 0 || total_tokens < 0 || (total_keep < 0 && total_keep != TSEL_KEEP_FROM_DEVICE))
+    return fail(TSEL_ERR_INVALID_VALUE, "negative size");
+  const int capacity = total_keep == TSEL_KEEP_FROM_DEVICE ? total_tokens : total_keep;
+  if (req_tok_offsets == nullptr || keep_per_req == nullptr || cu_keep == nullptr ||
+      (total_tokens > 0 && scores == nullptr) || (capacity > 0 && keep_idx == nullptr))
+    return fail(TSEL_ERR_INVALID_VALUE, "null pointer");
+  return TSEL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
+                            int64_t k_row_stride, const int32_t* cu_seqlens_q,
+                            const int32_t* cu_seqlens_k, int num_seg, int total_q, int total_k,
+                            int max_seqlen_q, int max_seqlen_k, int num_heads, int num_kv_heads,
+                            int head_dim, float softmax_scale, unsigned flags, float* lse,
+                            float* scores, void* workspace, size_t workspace_bytes,
+                            void* stream_) {
+  if (num_seg < 0 || total_q < 0 || total_k < 0 || num_heads < 1)
+    return fail(TSEL_ERR_INVALID_VALUE, "negative size or no heads");
+  const SelHist none{nullptr, 0, nullptr};
+  const size_t need = size_t(imp_ws_layout(num_seg, total_q, total_k, num_heads).total);
+  return importance_impl(q, q_row_stride, k, k_row_stride, cu_seqlens_q, cu_seqlens_k, num_seg,
+                         total_q, total_k, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
+                         head_dim, softmax_scale, flags, lse, scores, workspace, workspace_bytes,
+                         need, none, static_cast<cudaStream_t>(stream_));
+}
+
+size_t tsel_score_select_workspace_size(int num_seg, int total_q, int total_k, int num_heads,
+                                        int num_req) {
+  if (num_seg < 0 || total_q < 0 || total_k < 0 || num_heads < 1 || num_req < 0) return 0;
+  const ImpWsLayout L = imp_ws_layout(num_seg, total_q, total_k, num_heads);
+  return size_t(sel_hist_offset(L) + sel_hist_bytes(num_req));
+}
+
+tsel_status tsel_score_select(const void* q, int64_t q_row_stride, const void* k,
+                              int64_t k_row_stride, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_k, int num_seg, int total_q, int total_k,
+                              int max_seqlen_q, int max_seqlen_k, int num_heads,
+                              int num_kv_heads, int head_dim, float softmax_scale, unsigned flags,
+                              float* lse, float* scores, const int32_t* req_tok_offsets,
+                              int num_req, const int32_t* keep_per_req, int total_keep,
+                              int32_t* keep_idx, int32_t* cu_keep, void* workspace,
+                              size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (num_seg < 0 || total_q < 0 || total_k < 0 || num_heads < 1)
+    return fail(TSEL_ERR_INVALID_VALUE, "negative size or no heads");
+  tsel_status st = check_select_args(scores, total_k, req_tok_offsets, num_req, keep_per_req,
+                                     total_keep, keep_idx, cu_keep);
+  if (st != TSEL_OK) return st;
+  const ImpWsLayout L = imp_ws_layout(num_seg, total_q, total_k, num_heads);
+  const int64_t hbytes = sel_hist_bytes(num_req);
+  SelHist sel{req_tok_offsets, num_req, nullptr};
+  if (hbytes > 0 && workspace != nullptr)
+    sel.hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + sel_hist_offset(L));
+  const size_t need = size_t(sel_hist_offset(L) + hbytes);
+  st = importance_impl(q, q_row_stride, k, k_row_stride, cu_seqlens_q, cu_seqlens_k, num_seg,
+                       total_q, total_k, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
+                       head_dim, softmax_scale, flags, lse, scores, workspace, workspace_bytes,
+                       need, sel, stream);
+  if (st != TSEL_OK) return st;
+  const unsigned stage_bits = TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2 |
+                              TSEL_SEL_STAGE_TOPK;
+  if ((flags & stage_bits) && !(flags & TSEL_SEL_STAGE_TOPK)) return TSEL_OK;
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  cudaError_t e;
+  if (num_req == 0) {
+    e = cudaMemsetAsync(cu_keep, 0, sizeof(int32_t), stream);
+    return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "memset cu_keep");
+  }
+  e = launch_topk(scores, total_k, req_tok_offsets, num_req, keep_per_req, total_keep, keep_idx,
+                  cu_keep, &hdr->status, sel.hist, &hdr->hist_ok, stream);
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "top-k launch");
+}
+
 tsel_status tsel_select_topk(const float* scores, int total_tokens,
                              const int32_t* req_tok_offsets, int num_req,
                              const int32_t* keep_per_req, int total_keep, int32_t* keep_idx,
                              int32_t* cu_keep, void* workspace, size_t workspace_bytes,
                              void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (num_req < 0 || total_tokens < 0 || (total_keep < 0 && total_keep != TSEL_KEEP_FROM_DEVICE))
-    return fail(TSEL_ERR_INVALID_VALUE, "negative size");
-  const int capacity = total_keep == TSEL_KEEP_FROM_DEVICE ? total_tokens : total_keep;
-  if (req_tok_offsets == nullptr || keep_per_req == nullptr || cu_keep == nullptr ||
-      workspace == nullptr || (total_tokens > 0 && scores == nullptr) ||
-      (capacity > 0 && keep_idx == nullptr))
-    return fail(TSEL_ERR_INVALID_VALUE, "null pointer");
+  tsel_status st = check_select_args(scores, total_tokens, req_tok_offsets, num_req, keep_per_req,
+                                     total_keep, keep_idx, cu_keep);
+  if (st != TSEL_OK) return st;
+  if (workspace == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "null workspace");
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < kWsHeaderBytes)
     return fail(TSEL_ERR_WORKSPACE, "workspace must be >= %d bytes, 256-byte aligned",
                 kWsHeaderBytes);
@@ -384,7 +488,49 @@ tsel_status tsel_select_topk(const float* scores, int total_tokens,
   }
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   cudaError_t e = launch_topk(scores, total_tokens, req_tok_offsets, num_req, keep_per_req,
-                              total_keep, keep_idx, cu_keep, &hdr->status, stream);
+                              total_keep, keep_idx, cu_keep, &hdr->status, nullptr, nullptr,
+                              stream);
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "top-k launch");
+}
+
+size_t tsel_select_topk_hist_workspace_size(int num_req) {
+  if (num_req < 0) return 0;
+  return size_t(kWsHeaderBytes + sel_hist_bytes(num_req));
+}
+
+tsel_status tsel_select_topk_hist(const float* scores, int total_tokens,
+                                  const int32_t* req_tok_offsets, int num_req,
+                                  const int32_t* keep_per_req, int total_keep, int32_t* keep_idx,
+                                  int32_t* cu_keep, void* workspace, size_t workspace_bytes,
+                                  void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  tsel_status st = check_select_args(scores, total_tokens, req_tok_offsets, num_req, keep_per_req,
+                                     total_keep, keep_idx, cu_keep);
+  if (st != TSEL_OK) return st;
+  if (workspace == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "null workspace");
+  const int64_t hbytes = sel_hist_bytes(num_req);
+  const size_t need = size_t(kWsHeaderBytes + hbytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || workspace_bytes < need)
+    return fail(TSEL_ERR_WORKSPACE, "workspace must be >= %zu bytes, 256-byte aligned", need);
+  if (num_req == 0) {
+    cudaError_t e = cudaMemsetAsync(cu_keep, 0, sizeof(int32_t), stream);
+    return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "memset cu_keep");
+  }
+  WsHeader* hdr = static_cast<WsHeader*>(workspace);
+  int32_t* hist = nullptr;
+  cudaError_t e;
+  if (hbytes > 0 && total_tokens > 0) {
+    int sms = 0;
+    if (sm_count(&sms) != 0) return fail(TSEL_ERR_CUDA, "cannot query the SM count");
+    hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kWsHeaderBytes);
+    e = cudaMemsetAsync(hist, 0, size_t(hbytes), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "memset histograms");
+    e = launch_topk_hist(scores, total_tokens, req_tok_offsets, num_req, hist, &hdr->hist_ok, sms,
+                         stream);
+    if (e != cudaSuccess) return cuda_fail(e, "histogram launch");
+  }
+  e = launch_topk(scores, total_tokens, req_tok_offsets, num_req, keep_per_req, total_keep,
+                  keep_idx, cu_keep, &hdr->status, hist, hist ? &hdr->hist_ok : nullptr, stream);
   return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "top-k launch");
 }
 

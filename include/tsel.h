@@ -102,6 +102,8 @@ typedef enum tsel_status {
 #define TSEL_IMP_STAGE_PASS2  0x400u /*   Stages run in order on one stream/workspace; each
                                           pass needs a schedule stage after the previous
                                           run of that pass (it resets the pass's counters). */
+#define TSEL_SEL_STAGE_TOPK   0x800u /* tsel_score_select only: the top-B stage (listed with
+                                        the TSEL_IMP_STAGE_* bits to time the stages apart) */
 
 /* ------------------------------------------------------------------------ */
 /* Importance scores                                                        */
@@ -200,6 +202,50 @@ TSEL_API tsel_status tsel_importance_noalloc(const void* q, int64_t q_row_stride
                                              uint32_t* device_status, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Importance and pooled top-B in one call                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of workspace tsel_score_select needs: the importance workspace plus,
+ * for 1 to 64 requests, 270,336 bytes of score histograms per request. */
+TSEL_API size_t tsel_score_select_workspace_size(int num_seg, int total_q, int total_k,
+                                                 int num_heads, int num_req);
+
+/*
+ * tsel_importance followed by tsel_select_topk on its scores, with the same
+ * results (scores and LSE bit for bit, keep_idx and cu_keep identical), and
+ * the selection started from histograms built while the scores are written:
+ * the column pass also counts every request's scores by the first 11 and the
+ * first 16 bits of their order-preserving keys, so the top-B needs no radix
+ * round over the request's scores for those bits, and usually resolves the
+ * rest with one exchange among its CTAs. [VTC] section 3.2 (one global budget
+ * per request, decided from the per-token importance scores the reduction
+ * kernel writes) and section 4 (fusing the steps of one decision into one
+ * kernel flow); [LiteVLM] section 3.2 (keep ratio r).
+ *
+ * Arguments: those of tsel_importance (q ... scores, flags) followed by those
+ * of tsel_select_topk (req_tok_offsets ... cu_keep) for the key tokens
+ * (total_tokens = total_k), and the workspace. flags may also list
+ * TSEL_SEL_STAGE_TOPK with the TSEL_IMP_STAGE_* bits to run the stages
+ * separately (in order, on one workspace). Requests whose offsets are not
+ * ordered, more than 64 requests, or scores not all written by this call's
+ * column pass make the top-B run its plain radix rounds (same results).
+ * workspace: >= tsel_score_select_workspace_size(...) bytes, 256-byte aligned;
+ * its status word collects the device checks of both steps.
+ */
+TSEL_API tsel_status tsel_score_select(const void* q, int64_t q_row_stride,
+                                       const void* k, int64_t k_row_stride,
+                                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                       int num_seg, int total_q, int total_k,
+                                       int max_seqlen_q, int max_seqlen_k,
+                                       int num_heads, int num_kv_heads, int head_dim,
+                                       float softmax_scale, unsigned flags,
+                                       float* lse, float* scores,
+                                       const int32_t* req_tok_offsets, int num_req,
+                                       const int32_t* keep_per_req, int total_keep,
+                                       int32_t* keep_idx, int32_t* cu_keep,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Pooled global top-B                                                      */
 /* ------------------------------------------------------------------------ */
 
@@ -231,6 +277,24 @@ TSEL_API tsel_status tsel_select_topk(const float* scores, int total_tokens,
                              const int32_t* keep_per_req, int total_keep,
                              int32_t* keep_idx, int32_t* cu_keep,
                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace tsel_select_topk_hist needs: 1 KB plus, for 1 to 64
+ * requests, 270,336 bytes of histograms per request. */
+TSEL_API size_t tsel_select_topk_hist_workspace_size(int num_req);
+
+/*
+ * tsel_select_topk (same arguments, same results) for scores that did not come
+ * from tsel_score_select, e.g. from another scoring kernel: one launch counts
+ * the scores into per-request histograms of their first 11 and 16 key bits
+ * (after a memset of that region), then the top-B starts from them as in
+ * tsel_score_select. More than 64 requests: the plain top-B.
+ * workspace: >= tsel_select_topk_hist_workspace_size(num_req) bytes.
+ */
+TSEL_API tsel_status tsel_select_topk_hist(const float* scores, int total_tokens,
+                                           const int32_t* req_tok_offsets, int num_req,
+                                           const int32_t* keep_per_req, int total_keep,
+                                           int32_t* keep_idx, int32_t* cu_keep,
+                                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Dynamic keep budget per request from its scores ([VTC] section 6.2 leaves a
