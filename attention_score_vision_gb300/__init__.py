@@ -20,10 +20,12 @@ __all__ = [
     "TselError", "load_library", "build",
     "tsel_importance_workspace_size", "tsel_importance", "tsel_importance_noalloc",
     "tsel_select_topk_workspace_size", "tsel_select_topk",
+    "tsel_score_select_workspace_size", "tsel_score_select",
+    "tsel_select_topk_hist_workspace_size", "tsel_select_topk_hist", "TSEL_SEL_STAGE_TOPK",
     "tsel_gather_compact_workspace_size", "tsel_gather_compact", "tsel_gather_compact_counted",
     "tsel_dynamic_budget", "TSEL_KEEP_FROM_DEVICE",
     "tsel_keep_count", "tsel_read_device_status", "tsel_clear_device_status",
-    "tsel_importance_redo_pairs",
+    "tsel_importance_redo_pairs", "tsel_select_path_counts",
     "tsel_status_string", "tsel_last_error", "tsel_probe_ex2",
     "TSEL_DEV_SEQLENS", "TSEL_DEV_REQUESTS", "TSEL_DEV_KEEP_IDX", "TSEL_DEV_TIMEOUT", "TSEL_DEV_NAN",
     "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_SCORE_SUM", "TSEL_IMP_ROWREF_FIXED", "TSEL_IMP_ROWREF_MOVING", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
@@ -53,6 +55,7 @@ TSEL_IMP_TEST_STALL = 0x10000
 TSEL_IMP_STAGE_PREP = 0x100
 TSEL_IMP_STAGE_PASS1 = 0x200
 TSEL_IMP_STAGE_PASS2 = 0x400
+TSEL_SEL_STAGE_TOPK = 0x800
 
 _c_int, _c_i64, _c_size, _c_float, _c_uint, _p = (ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
                                                    ctypes.c_float, ctypes.c_uint, ctypes.c_void_p)
@@ -76,9 +79,17 @@ _SIGNATURES = {
     "tsel_read_device_status": (_c_int, [_p, ctypes.POINTER(ctypes.c_uint32), _p]),
     "tsel_clear_device_status": (_c_int, [_p, _p]),
     "tsel_importance_redo_pairs": (_c_int, [_p, ctypes.POINTER(ctypes.c_int32), _p]),
+    "tsel_select_path_counts": (_c_int, [_p, ctypes.POINTER(ctypes.c_int32), _p]),
     "tsel_status_string": (ctypes.c_char_p, [_c_int]),
     "tsel_last_error": (ctypes.c_char_p, []),
     "tsel_probe_ex2": (_c_int, [_c_int, _c_int, _p, _p]),
+    "tsel_score_select_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "tsel_score_select": (_c_int, [_p, _c_i64, _p, _c_i64, _p, _p, _c_int, _c_int, _c_int, _c_int,
+                                   _c_int, _c_int, _c_int, _c_int, _c_float, _c_uint, _p, _p,
+                                   _p, _c_int, _p, _c_int, _p, _p, _p, _c_size, _p]),
+    "tsel_select_topk_hist_workspace_size": (_c_size, [_c_int]),
+    "tsel_select_topk_hist": (_c_int, [_p, _c_int, _p, _c_int, _p, _c_int, _p, _p, _p, _c_size,
+                                       _p]),
     "tsel_importance_noalloc": (_c_int, [_p, _c_i64, _p, _c_i64, _p, _p, _c_int, _c_int, _c_int,
                                          _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _p, _p,
                                          _p, _p]),
@@ -245,6 +256,53 @@ def tsel_importance_noalloc(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torc
     return scores, lse
 
 
+def tsel_score_select_workspace_size(num_seg: int, total_q: int, total_k: int, num_heads: int,
+                                     num_req: int) -> int:
+    return int(load_library().tsel_score_select_workspace_size(num_seg, total_q, total_k,
+                                                                num_heads, num_req))
+
+
+def tsel_score_select(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                      cu_seqlens_k: torch.Tensor, max_seqlen_q: int, max_seqlen_k: int,
+                      req_tok_offsets: torch.Tensor, keep_per_req: torch.Tensor, total_keep: int,
+                      *, softmax_scale: float = 0.0, flags: int = 0,
+                      lse: Optional[torch.Tensor] = None, scores: Optional[torch.Tensor] = None,
+                      keep_idx: Optional[torch.Tensor] = None,
+                      cu_keep: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, want_lse: bool = True,
+                      stream=None):
+    """tsel_importance + tsel_select_topk in one call (the top-B starts from the
+    score histograms the column pass builds); returns (scores, lse, keep_idx, cu_keep)."""
+    tq, H, d, tk, Hkv, fp8 = _check_qk(q, k, cu_seqlens_q, cu_seqlens_k, allow_fp8=True)
+    if fp8:
+        flags |= TSEL_IMP_FP8_E4M3
+    _need(req_tok_offsets, torch.int32, "req_tok_offsets")
+    _need(keep_per_req, torch.int32, "keep_per_req")
+    G = cu_seqlens_k.numel() - 1
+    R = keep_per_req.numel()
+    dev = q.device
+    if scores is None:
+        scores = torch.empty(tk, dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((H, tq), dtype=torch.float32, device=dev)
+    if keep_idx is None:
+        cap = tk if int(total_keep) == TSEL_KEEP_FROM_DEVICE else int(total_keep)
+        keep_idx = torch.empty(cap, dtype=torch.int32, device=dev)
+    if cu_keep is None:
+        cu_keep = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _new_workspace(tsel_score_select_workspace_size(G, tq, tk, H, R), dev)
+    with torch.cuda.device(dev):
+        st = load_library().tsel_score_select(
+            _ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), G,
+            tq, tk, int(max_seqlen_q), int(max_seqlen_k), H, Hkv, d, float(softmax_scale),
+            int(flags), _ptr(lse), _ptr(scores), _ptr(req_tok_offsets), R, _ptr(keep_per_req),
+            int(total_keep), _ptr(keep_idx), _ptr(cu_keep), _ptr(workspace), workspace.numel(),
+            _stream(stream, dev))
+    _check(st)
+    return scores, lse, keep_idx, cu_keep
+
+
 # ---------------------------------------------------------------------------
 # Top-B
 # ---------------------------------------------------------------------------
@@ -279,6 +337,39 @@ def tsel_select_topk(scores: torch.Tensor, req_tok_offsets: torch.Tensor,
                                          _ptr(keep_per_req), int(total_keep), _ptr(keep_idx),
                                          _ptr(cu_keep), _ptr(workspace), workspace.numel(),
                                          _stream(stream, dev))
+    _check(st)
+    return keep_idx, cu_keep
+
+
+def tsel_select_topk_hist_workspace_size(num_req: int) -> int:
+    return int(load_library().tsel_select_topk_hist_workspace_size(num_req))
+
+
+def tsel_select_topk_hist(scores: torch.Tensor, req_tok_offsets: torch.Tensor,
+                          keep_per_req: torch.Tensor, total_keep: int, *,
+                          keep_idx: Optional[torch.Tensor] = None,
+                          cu_keep: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """tsel_select_topk started from per-request score histograms (built by one
+    extra launch); same results. Returns (keep_idx, cu_keep)."""
+    _need(scores, torch.float32, "scores")
+    _need(req_tok_offsets, torch.int32, "req_tok_offsets")
+    _need(keep_per_req, torch.int32, "keep_per_req")
+    R = keep_per_req.numel()
+    dev = scores.device
+    if keep_idx is None:
+        cap = scores.numel() if int(total_keep) == TSEL_KEEP_FROM_DEVICE else int(total_keep)
+        keep_idx = torch.empty(cap, dtype=torch.int32, device=dev)
+    if cu_keep is None:
+        cu_keep = torch.empty(R + 1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = _new_workspace(tsel_select_topk_hist_workspace_size(R), dev)
+    with torch.cuda.device(dev):
+        st = load_library().tsel_select_topk_hist(
+            _ptr(scores), scores.numel(), _ptr(req_tok_offsets), R, _ptr(keep_per_req),
+            int(total_keep), _ptr(keep_idx), _ptr(cu_keep), _ptr(workspace), workspace.numel(),
+            _stream(stream, dev))
     _check(st)
     return keep_idx, cu_keep
 
@@ -424,6 +515,16 @@ def tsel_importance_redo_pairs(workspace: torch.Tensor, stream=None) -> int:
     _check(load_library().tsel_importance_redo_pairs(_ptr(workspace), ctypes.byref(n),
                                                      _stream(stream, workspace.device)))
     return int(n.value)
+
+
+def tsel_select_path_counts(workspace: torch.Tensor, stream=None) -> list:
+    """Top-B requests per threshold path on `workspace` since it was zeroed:
+    [radix rounds, histogram + rounds, histogram + candidates, candidates
+    rejected] (synchronises the stream)."""
+    c = (ctypes.c_int32 * 4)()
+    _check(load_library().tsel_select_path_counts(_ptr(workspace), c,
+                                                  _stream(stream, workspace.device)))
+    return [int(x) for x in c]
 
 
 def tsel_clear_device_status(workspace: torch.Tensor, stream=None) -> None:

@@ -26,6 +26,8 @@ struct WsHeader {
   uint32_t pad4[31];
   int32_t hist_ok;        // 1: the request offsets are valid and the score histograms are built
   uint32_t pad5[31];
+  int32_t sel_paths[4];   // top-B requests per threshold path (tsel_select_path_counts)
+  uint32_t pad6[28];
 };
 static_assert(sizeof(WsHeader) <= kWsHeaderBytes, "header too large");
 

@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   int cnt16 = 0;
   uint32_t thr = 0;
   int need_eq = 0;     // tokens equal to the threshold to keep (request-wide)
+  int path = 0;        // 0 radix rounds, 1 histogram + rounds, 2 candidates, 3 candidates rejected
   if (use_hist) {
     reinterpret_cast<int4*>(sh.bins)[tid] = hc;
     const int t = warp_sum(hc.x + hc.y + hc.z + hc.w);
@@ -377,13 +378,13 @@ __global__ void __launch_bounds__(kTopkThreads)
       const int xs = warp_suffix_scan(fb);
       const unsigned hb = __ballot_sync(0xffffffffu, xs - fb < rem0 && xs >= rem0);
       const int d1 = hb ? __ffs(hb) - 1 : 0;
-      const int above1 = __shfl_sync(0xffffffffu, xs - fb, d1);
       cnt16 = __shfl_sync(0xffffffffu, fb, d1);
       if (cnt16 <= kTopkCand) {
-        cand_mode = true;
+        cand_mode = true;   // (remaining is set from the exchanged counts)
+        path = 2;
         pfx16 = (uint32_t(d0) << 5) | uint32_t(d1);
-        remaining = rem0 - above1;
       } else {
+        path = 1;
         // too many candidates: radix rounds from the second digit on
         round0 = 1;
         prefix = uint32_t(d0) << 21;
@@ -422,8 +423,10 @@ __global__ void __launch_bounds__(kTopkThreads)
       int gsum = 0;
 #pragma unroll
       for (int w = 0; w < kTopkWarps; ++w) gsum += sh.gt_w[w];
+      // the full count (a CTA with more candidates than fit stores only the
+      // first kTopkCand; the total then exceeds the list and is rejected below)
       int* cn = solo ? &sh.cand_n : cluster.map_shared_rank(&sh.cand_n, tid);
-      sh.cbase[tid] = atomicAdd(cn, nloc);
+      sh.cbase[tid] = atomicAdd(cn, sh.loc_n);
       int* g16 = solo ? &sh.gt16_of[crank] : cluster.map_shared_rank(&sh.gt16_of[crank], tid);
       *g16 = gsum;
     }
@@ -440,16 +443,30 @@ __global__ void __launch_bounds__(kTopkThreads)
     // The one exchange: after it no CTA touches another's shared memory.
     if (!solo) cluster.sync();
     __syncthreads();
-    if (sh.cand_n != cnt16) {
-      // the candidates do not match the counts: radix rounds from the start
-      // (the same outcome in every CTA: each received every candidate)
+    // The threshold lies among the candidates when the keys above their
+    // prefix (counted in the slices, not taken from the histograms) number
+    // fewer than B and the candidates make up the rest; every CTA holds the
+    // same counts, so every CTA takes the same branch.
+    int above16 = 0;
+    for (int c = 0; c < csize; ++c) above16 += sh.gt16_of[c];
+    if (sh.cand_n <= kTopkCand && above16 < B && B <= above16 + sh.cand_n) {
+      remaining = B - above16;
+      cnt16 = sh.cand_n;
+    } else {
+      // radix rounds from the start
       cand_mode = false;
+      path = 3;
       round0 = 0;
       prefix = 0;
       mask = 0;
       remaining = B;
       gt_part = 0;
     }
+  }
+
+  if (tid == 0 && crank == 0) {
+    // the status word heads the workspace header: count this request's path
+    atomicAdd(&reinterpret_cast<WsHeader*>(status)->sel_paths[path], 1);
   }
 
   if (cand_mode) {
@@ -608,7 +625,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   // output offset written by warp 0 above is read after the first scan's
   // barrier.
   int32_t* out = keep_idx + before;
-  int written = 0, eq_seen = 0;
+  int written = 0, eq_seen = 0, room = B;
   for (int i0 = 0; i0 < len; i0 += kTopkPass) {
     const int ib = i0 + tid * kTopkItems;
     uint32_t k[kTopkItems];
@@ -639,6 +656,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int pre = topk_block_scan((n_eq << 16) | n_gt, sh.warp_sums, tot);
     if (i0 == 0) {   // (0 for one CTA on the radix-round path)
       out += sh.out_base;
+      room = B - sh.out_base;
       eq_seen = sh.eq_before;
     }
     int eq_rank = eq_seen + (pre >> 16);
@@ -658,7 +676,8 @@ __global__ void __launch_bounds__(kTopkThreads)
     __syncthreads();
     // (every thread has read warp_sums and the stage is read here before the
     // next pass's first barrier, so the next pass may rewrite both)
-    for (int i = tid; i < cnt; i += kTopkThreads) out[written + i] = sh.stage[i];
+    // (stores stay inside the request's B slots whatever the counts said)
+    for (int i = tid; i < cnt && written + i < room; i += kTopkThreads) out[written + i] = sh.stage[i];
     written += cnt;
     eq_seen += tot_eq;
   }

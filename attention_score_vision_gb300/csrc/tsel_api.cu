@@ -651,6 +651,16 @@ tsel_status tsel_importance_redo_pairs(const void* workspace, int32_t* pairs, vo
   return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "read redo count");
 }
 
+tsel_status tsel_select_path_counts(const void* workspace, int32_t* counts, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (workspace == nullptr || counts == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "null argument");
+  const auto* hdr = static_cast<const WsHeader*>(workspace);
+  cudaError_t e = cudaMemcpyAsync(counts, hdr->sel_paths, sizeof(hdr->sel_paths),
+                                  cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "read path counts");
+}
+
 tsel_status tsel_clear_device_status(void* workspace, void* stream_) {
   if (workspace == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "null workspace");
   cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream_));

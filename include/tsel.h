@@ -406,6 +406,14 @@ TSEL_API tsel_status tsel_read_device_status(const void* workspace, uint32_t* bi
  * nearly every input; a diagnostic, not needed for correct results. */
 TSEL_API tsel_status tsel_importance_redo_pairs(const void* workspace, int32_t* pairs, void* stream);
 
+/* Reads, after synchronising `stream`, how many requests the top-B calls on
+ * `workspace` resolved by each threshold path since the workspace was zeroed:
+ * counts[0] radix rounds over the scores (no histograms), counts[1] first
+ * digit from the histograms then radix rounds, counts[2] histograms and one
+ * candidate exchange, counts[3] candidate exchange rejected (its counts did not
+ * bracket the budget), radix rounds from the start. A diagnostic. */
+TSEL_API tsel_status tsel_select_path_counts(const void* workspace, int32_t* counts, void* stream);
+
 /* Enqueues a reset of the device status word to zero. */
 TSEL_API tsel_status tsel_clear_device_status(void* workspace, void* stream);
 
