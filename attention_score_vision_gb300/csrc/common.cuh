@@ -205,7 +205,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // Adds the scores of a warp's tokens to their requests' histograms (coarse:
 // first 11 bits of the key, fine: first 16 bits). Lanes holding the same bin
 // add once (match_any); lanes with valid == false or tokens outside every
-// request add nothing. Every lane of the warp must call it.
+// request add nothing. Every lane of the warp must call it. req_off: the
+// R + 1 request offsets, staged in shared memory by the caller.
 __device__ __forceinline__ void hist_add_warp(int32_t* hist, const int32_t* req_off, int R,
                                               int tok, float s, bool valid) {
   const int lane = threadIdx.x & 31;
@@ -215,7 +216,7 @@ __device__ __forceinline__ void hist_add_warp(int32_t* hist, const int32_t* req_
     int lo = 0, hi = R + 1;   // first i in [0, R] with req_off[i] > tok
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
-      if (__ldg(req_off + mid) <= tok) lo = mid + 1;
+      if (req_off[mid] <= tok) lo = mid + 1;
       else hi = mid;
     }
     r = lo - 1 < R ? lo - 1 : -1;

@@ -465,6 +465,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const bool add_hist =
       PASS == 2 && p.hist != nullptr && *reinterpret_cast<const volatile int32_t*>(p.hist_ok) != 0;
+  // request offsets for the histogram adds, read once per CTA
+  __shared__ int32_t s_req_off[kHistMaxReq + 1];
+  if (add_hist && warp >= kEpiFirstWarp && warp < kMma1Warp) {
+    const int t = (warp - kEpiFirstWarp) * 32 + lane;
+    if (t <= p.R) s_req_off[t] = __ldg(p.req_off + t);
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");   // the epilogue warps
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -766,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (p.hgroups == 1) {
               const float sc = w.nq > 0 ? total / rows : 0.f;
               if (krow < w.nk) p.scores[w.k0 + krow] = sc;
-              if (add_hist) hist_add_warp(p.hist, p.req_off, p.R, w.k0 + krow, sc, krow < w.nk);
+              if (add_hist) hist_add_warp(p.hist, s_req_off, p.R, w.k0 + krow, sc, krow < w.nk);
             } else {
               // Partial sums of this head group; the last group of the 32-key
               // slice adds all groups' partials in group order.
@@ -790,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   sc = w.nq > 0 ? sum / rows : 0.f;
                   p.scores[w.k0 + krow] = sc;
                 }
-                if (add_hist) hist_add_warp(p.hist, p.req_off, p.R, w.k0 + krow, sc, krow < w.nk);
+                if (add_hist) hist_add_warp(p.hist, s_req_off, p.R, w.k0 + krow, sc, krow < w.nk);
               }
             }
           }

@@ -35,6 +35,7 @@ cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* re
                         const int32_t* hist_ok, cudaStream_t stream);
 cudaError_t launch_topk_hist(const float* scores, int total_tokens, const int32_t* req_off, int R,
                              int32_t* hist, int32_t* hist_ok, int num_sms, cudaStream_t stream);
+int topk_cluster_size(int total_tokens, int num_req, cudaError_t* e);
 cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_bytes,
                           const int32_t* pos, int pos_dim, const int32_t* cu_k, int G, int Tk,
                           const int32_t* keep_idx, int K, const int32_t* K_dev,
@@ -447,7 +448,12 @@ tsel_status tsel_score_select(const void* q, int64_t q_row_stride, const void* k
   const ImpWsLayout L = imp_ws_layout(num_seg, total_q, total_k, num_heads);
   const int64_t hbytes = sel_hist_bytes(num_req);
   SelHist sel{req_tok_offsets, num_req, nullptr};
-  if (hbytes > 0 && workspace != nullptr)
+  // Histograms only for requests the top-B splits over a cluster of CTAs
+  // (one CTA per request runs its radix rounds without cluster barriers).
+  cudaError_t ce = cudaSuccess;
+  const bool clustered = num_req > 0 && topk_cluster_size(total_k, num_req, &ce) > 1;
+  if (ce != cudaSuccess) return cuda_fail(ce, "top-B cluster size");
+  if (hbytes > 0 && workspace != nullptr && clustered)
     sel.hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + sel_hist_offset(L));
   const size_t need = size_t(sel_hist_offset(L) + hbytes);
   st = importance_impl(q, q_row_stride, k, k_row_stride, cu_seqlens_q, cu_seqlens_k, num_seg,
@@ -518,8 +524,10 @@ tsel_status tsel_select_topk_hist(const float* scores, int total_tokens,
   }
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   int32_t* hist = nullptr;
-  cudaError_t e;
-  if (hbytes > 0 && total_tokens > 0) {
+  cudaError_t e = cudaSuccess;
+  const bool clustered = topk_cluster_size(total_tokens, num_req, &e) > 1;
+  if (e != cudaSuccess) return cuda_fail(e, "top-B cluster size");
+  if (hbytes > 0 && total_tokens > 0 && clustered) {
     int sms = 0;
     if (sm_count(&sms) != 0) return fail(TSEL_ERR_CUDA, "cannot query the SM count");
     hist = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + kWsHeaderBytes);

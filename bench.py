@@ -357,41 +357,60 @@ def workload_throughput(tsel, w, dev, flush, stream, ex2_peak, bf16_peak, steps:
     cq, ck, ro, kp, pos = (i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.req_tok_offsets),
                            i32(w.keep_per_req), i32(w.pos))
     G, Tq, Tk, H, K = w.num_seg, w.total_q, w.total_k, w.num_heads, w.total_keep
-    ws = torch.zeros(tsel.tsel_importance_workspace_size(G, Tq, Tk, H), dtype=torch.uint8, device=dev)
+    R = w.keep_per_req.size
+    ws = torch.zeros(tsel.tsel_score_select_workspace_size(G, Tq, Tk, H, R), dtype=torch.uint8,
+                     device=dev)
     scores = torch.empty(Tk, device=dev)
     lse = torch.empty((H, Tq), device=dev)
     keep_idx = torch.empty(K, dtype=torch.int32, device=dev)
-    cu_keep = torch.empty(w.keep_per_req.size + 1, dtype=torch.int32, device=dev)
+    cu_keep = torch.empty(R + 1, dtype=torch.int32, device=dev)
     oh = torch.empty((K, hidden.shape[1]), dtype=torch.bfloat16, device=dev)
     op = torch.empty((K, w.pos.shape[1]), dtype=torch.int32, device=dev)
     oi = torch.empty(K, dtype=torch.int32, device=dev)
     oc = torch.empty(G + 1, dtype=torch.int32, device=dev)
-    step, imp = [], []
-    for i in range(warmup + steps):
-        flush.fill_(i & 0xFF)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        ev[0].record(stream)
-        tsel.tsel_importance(q, k, cq, ck, w.max_seqlen_q, w.max_seqlen_k, lse=lse, scores=scores,
-                             workspace=ws, stream=stream)
-        ev[1].record(stream)
-        tsel.tsel_select_topk(scores, ro, kp, K, keep_idx=keep_idx, cu_keep=cu_keep, workspace=ws,
-                              stream=stream)
+    IMP = tsel.TSEL_IMP_STAGE_PREP | tsel.TSEL_IMP_STAGE_PASS1 | tsel.TSEL_IMP_STAGE_PASS2
+
+    def score_select(flags):
+        tsel.tsel_score_select(q, k, cq, ck, w.max_seqlen_q, w.max_seqlen_k, ro, kp, K, flags=flags,
+                               lse=lse, scores=scores, keep_idx=keep_idx, cu_keep=cu_keep,
+                               workspace=ws, stream=stream)
+
+    def gather():
         tsel.tsel_gather_compact(hidden, pos, ck, keep_idx, out_hidden=oh, out_pos=op, out_img_id=oi,
                                  out_cu_seqlens=oc, workspace=ws, stream=stream)
-        ev[2].record(stream)
+
+    whole, stage = [], []
+    for i in range(warmup + steps):       # the path as it runs: one fused call + compaction
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        score_select(0)
+        gather()
+        b.record(stream)
         if i >= warmup:
-            step.append(ev)
+            whole.append((a, b))
+    for i in range(warmup + steps):       # importance stages apart, for its roofline
+        flush.fill_(i & 0xFF)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        score_select(IMP)
+        ev[1].record(stream)
+        score_select(tsel.TSEL_SEL_STAGE_TOPK)
+        gather()
+        if i >= warmup:
+            stage.append(ev)
     torch.cuda.synchronize()
     if tsel.tsel_read_device_status(ws) != 0:
         raise RuntimeError(f"device status set for {w.name}")
-    t_step = sum(e[0].elapsed_time(e[2]) for e in step) / len(step)
-    t_imp = sum(e[0].elapsed_time(e[1]) for e in step) / len(step)
+    t_step = sum(a.elapsed_time(b) for a, b in whole) / len(whole)
+    t_imp = sum(e[0].elapsed_time(e[1]) for e in stage) / len(stage)
     E = w.attended_pairs()
     roof = max(4 * w.head_dim * E / bf16_peak, 2 * E / ex2_peak)
     return {"tokens": Tk, "ms_per_step": t_step, "tokens_per_s": Tk / (t_step * 1e-3),
             "importance_ms": t_imp, "importance_roofline_frac": roof / (t_imp * 1e-3),
-            "note": f"{steps} steps, importance timed with an event after it (no overlap with "
-                    "the selection)"}
+            "topk_paths": tsel.tsel_select_path_counts(ws),
+            "note": f"{steps} steps of the fused score + select call and the compaction; "
+                    "importance timed apart (its three stages, then an event)"}
 
 
 def small_request_latency(tsel, w, dev, flush, stream, reps: int = 20) -> dict:
@@ -411,21 +430,22 @@ def small_request_latency(tsel, w, dev, flush, stream, reps: int = 20) -> dict:
     cq, ck, ro, kp, pos = (i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), i32(w.req_tok_offsets),
                            i32(w.keep_per_req), i32(w.pos))
     G, Tq, Tk, H, K = w.num_seg, w.total_q, w.total_k, w.num_heads, w.total_keep
-    ws = torch.zeros(tsel.tsel_importance_workspace_size(G, Tq, Tk, H), dtype=torch.uint8, device=dev)
+    R = w.keep_per_req.size
+    ws = torch.zeros(tsel.tsel_score_select_workspace_size(G, Tq, Tk, H, R), dtype=torch.uint8,
+                     device=dev)
     scores = torch.empty(Tk, device=dev)
     lse = torch.empty((H, Tq), device=dev)
     keep_idx = torch.empty(K, dtype=torch.int32, device=dev)
-    cu_keep = torch.empty(w.keep_per_req.size + 1, dtype=torch.int32, device=dev)
+    cu_keep = torch.empty(R + 1, dtype=torch.int32, device=dev)
     oh = torch.empty((K, hidden.shape[1]), dtype=torch.bfloat16, device=dev)
     op = torch.empty((K, w.pos.shape[1]), dtype=torch.int32, device=dev)
     oi = torch.empty(K, dtype=torch.int32, device=dev)
     oc = torch.empty(G + 1, dtype=torch.int32, device=dev)
 
     def path(st):
-        tsel.tsel_importance(q, k, cq, ck, w.max_seqlen_q, w.max_seqlen_k, lse=lse, scores=scores,
-                             workspace=ws, stream=st)
-        tsel.tsel_select_topk(scores, ro, kp, K, keep_idx=keep_idx, cu_keep=cu_keep, workspace=ws,
-                              stream=st)
+        tsel.tsel_score_select(q, k, cq, ck, w.max_seqlen_q, w.max_seqlen_k, ro, kp, K, lse=lse,
+                               scores=scores, keep_idx=keep_idx, cu_keep=cu_keep, workspace=ws,
+                               stream=st)
         tsel.tsel_gather_compact(hidden, pos, ck, keep_idx, out_hidden=oh, out_pos=op, out_img_id=oi,
                                  out_cu_seqlens=oc, workspace=ws, stream=st)
 
@@ -499,11 +519,13 @@ def gpu_arm(args) -> None:
     K = w.total_keep
     D = w.hidden_bits.shape[1]
     P = w.pos.shape[1]
-    ws = torch.zeros(tsel.tsel_importance_workspace_size(G, Tq, Tk, H), dtype=torch.uint8, device=dev)
+    R = w.keep_per_req.size
+    ws = torch.zeros(tsel.tsel_score_select_workspace_size(G, Tq, Tk, H, R), dtype=torch.uint8,
+                     device=dev)
     scores = torch.empty(Tk, dtype=torch.float32, device=dev)
     lse = torch.empty((H, Tq), dtype=torch.float32, device=dev)
     keep_idx = torch.empty(K, dtype=torch.int32, device=dev)
-    cu_keep = torch.empty(w.keep_per_req.size + 1, dtype=torch.int32, device=dev)
+    cu_keep = torch.empty(R + 1, dtype=torch.int32, device=dev)
     out_h = torch.empty((K, D), dtype=torch.bfloat16, device=dev)
     out_p = torch.empty((K, P), dtype=torch.int32, device=dev)
     out_i = torch.empty(K, dtype=torch.int32, device=dev)
@@ -511,6 +533,18 @@ def gpu_arm(args) -> None:
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     S1, S2, S3 = tsel.TSEL_IMP_STAGE_PREP, tsel.TSEL_IMP_STAGE_PASS1, tsel.TSEL_IMP_STAGE_PASS2
+    S4 = tsel.TSEL_SEL_STAGE_TOPK
+
+    def score_select(flags, q=None, k=None, cu_q=None, cu_k=None, req_off=None, keep=None):
+        # importance and the pooled top-B in one call (the product path)
+        tsel.tsel_score_select(q if q is not None else d["q"], k if k is not None else d["k"],
+                               cu_q if cu_q is not None else d["cu_q"],
+                               cu_k if cu_k is not None else d["cu_k"],
+                               w.max_seqlen_q, w.max_seqlen_k,
+                               req_off if req_off is not None else d["req_off"],
+                               keep if keep is not None else d["keep"], K, flags=flags, lse=lse,
+                               scores=scores, keep_idx=keep_idx, cu_keep=cu_keep, workspace=ws,
+                               stream=stream)
 
     def importance(flags, q=None, k=None, cu_q=None, cu_k=None):
         tsel.tsel_importance(q if q is not None else d["q"], k if k is not None else d["k"],
@@ -551,8 +585,7 @@ def gpu_arm(args) -> None:
     # --- warm-up -----------------------------------------------------------
     for _ in range(args.warmup):
         flush.fill_(1)
-        importance(0)
-        topk()
+        score_select(0)
         gather()
     torch.cuda.synchronize()
     if tsel.tsel_read_device_status(ws) != 0:
@@ -571,8 +604,7 @@ def gpu_arm(args) -> None:
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         evs[i][0].record(stream)
-        importance(0)
-        topk()
+        score_select(0)
         gather()
         evs[i][1].record(stream)
     torch.cuda.synchronize()
@@ -590,23 +622,27 @@ def gpu_arm(args) -> None:
 
     # --- per-kernel times: the same steps with an event between the stages
     # (events break the launch overlap, so these are each kernel alone) -------
-    names = ["prep", "pass1", "pass2", "topk", "gather"]
+    # topk: the histogram-started top-B of the fused call; topk_plain: the
+    # plain top-B (tsel_select_topk) on the same scores, for comparison
+    names = ["prep", "pass1", "pass2", "topk", "gather", "topk_plain"]
     n_stage = max(5, min(args.steps, 50))
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_stage)]
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n_stage)]
     for i in range(n_stage):
         flush.fill_(i & 0xFF)
         e = sevs[i]
         e[0].record(stream)
-        importance(S1)
+        score_select(S1)
         e[1].record(stream)
-        importance(S2)
+        score_select(S2)
         e[2].record(stream)
-        importance(S3)
+        score_select(S3)
         e[3].record(stream)
-        topk()
+        score_select(S4)
         e[4].record(stream)
         gather()
         e[5].record(stream)
+        topk()
+        e[6].record(stream)
     torch.cuda.synchronize()
     per = {n: [] for n in names}
     for e in sevs:
@@ -615,6 +651,7 @@ def gpu_arm(args) -> None:
     if tsel.tsel_read_device_status(ws) != 0:
         raise RuntimeError("device status set in the per-kernel loop")
     redo_pairs = tsel.tsel_importance_redo_pairs(ws)
+    topk_paths = tsel.tsel_select_path_counts(ws)
 
     # --- top-B + compaction back to back inside the step, as the path runs
     # them (the compaction launches while the top-B runs and waits for it on
@@ -624,12 +661,10 @@ def gpu_arm(args) -> None:
     sel_evs = []
     for i in range(n_stage):
         flush.fill_(i & 0xFF)
-        importance(S1)
-        importance(S2)
-        importance(S3)
+        score_select(S1 | S2 | S3)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        topk()
+        score_select(S4)
         gather()
         b.record(stream)
         sel_evs.append((a, b))
@@ -637,6 +672,26 @@ def gpu_arm(args) -> None:
     sel_span = [a.elapsed_time(b) for a, b in sel_evs]
     if tsel.tsel_read_device_status(ws) != 0:
         raise RuntimeError("device status set in the selection loop")
+
+    # --- the same path as three separate calls (importance, plain top-B,
+    # compaction), for comparison with the fused call ------------------------
+    sep = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        importance(0)
+        topk()
+        gather()
+        b.record(stream)
+        if i >= args.warmup:
+            sep.append((a, b))
+    torch.cuda.synchronize()
+    sep_ms = reduce_max_over_ranks(sum(x.elapsed_time(y) for x, y in sep) / len(sep), dev)
+    separate_calls = {"ms_per_step": sep_ms, "value": replica_throughput(Tk, world, sep_ms),
+                      "unit": "tokens/s",
+                      "note": "tsel_importance + tsel_select_topk (radix rounds over the scores) "
+                              "+ tsel_gather_compact"}
 
     # --- LSE-provided mode: the attention kernel's LSE reused, column pass only ---
     lse_given = lse.clone()
@@ -661,7 +716,6 @@ def gpu_arm(args) -> None:
 
     # --- dynamic keep budget: importance -> budget -> top-B -> compaction, with
     # the kept count staying on the device (no host round trip) ----------------
-    R = w.keep_per_req.size
     dyn_keep = torch.empty(R, dtype=torch.int32, device=dev)
     dyn_total = torch.empty(1, dtype=torch.int32, device=dev)
     dyn_idx = torch.empty(Tk, dtype=torch.int32, device=dev)
@@ -768,8 +822,7 @@ def gpu_arm(args) -> None:
                 ev_late = torch.cuda.Event()
                 ev_late.record(copy_stream)
             stream.wait_event(ev_first)
-            importance(0, db["q"], db["k"], db["cu_q"], db["cu_k"])
-            topk(db["req_off"], db["keep"])
+            score_select(0, db["q"], db["k"], db["cu_q"], db["cu_k"], db["req_off"], db["keep"])
             stream.wait_event(ev_late)
             gather(db["hidden"], db["pos"], db["cu_k"])
             done = torch.cuda.Event()
@@ -863,8 +916,14 @@ def gpu_arm(args) -> None:
         # row overflowed the fixed reference: redo_pairs = 0)
         "pass1": {"ms": mean["pass1"], **roof1, "redo_pairs": redo_pairs},
         "pass2": {"ms": mean["pass2"], **roof2},
+        # the fused call's top-B, started from the column pass's histograms
         "topk": {"ms": mean["topk"], "GB/s": topk_bytes / (mean["topk"] * 1e-3) / 1e9,
-                 "hbm_frac": topk_bytes / (mean["topk"] * 1e-3) / hbm_peak},
+                 "hbm_frac": topk_bytes / (mean["topk"] * 1e-3) / hbm_peak,
+                 "paths": dict(zip(["radix", "hist_rounds", "hist_candidates", "rejected"],
+                                   topk_paths))},
+        "topk_plain": {"ms": mean["topk_plain"],
+                       "GB/s": topk_bytes / (mean["topk_plain"] * 1e-3) / 1e9,
+                       "note": "tsel_select_topk on the same scores (three radix rounds)"},
         "gather": {"ms": mean["gather"], "GB/s": gather_bytes / (mean["gather"] * 1e-3) / 1e9,
                    "hbm_frac": gather_bytes / (mean["gather"] * 1e-3) / hbm_peak,
                    **gather_dram_rate(args.workload, mean["gather"], gather_bytes, hbm_peak)},
@@ -909,9 +968,11 @@ def gpu_arm(args) -> None:
         "kernels": kernels,
         "kernel_timing": (f"per-kernel times from {n_stage} further steps with an event between "
                           "the stages (each kernel alone, no launch overlap); the headline step "
-                          "has events only around the whole path"),
+                          "(tsel_score_select + tsel_gather_compact) has events only around the "
+                          "whole path"),
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
+        "separate_calls": separate_calls,
         "lse_provided": lse_provided,
         "dynamic_budget": dynamic,
         "fp8": fp8,
