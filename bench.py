@@ -47,12 +47,16 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["tsel", "reference"], default="tsel")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--images", type=int, default=0,
+                    help="only the first N images of the workload, as one 60%% request "
+                         "(a smaller case of the same shapes, e.g. for counter captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-small", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-fp8", action="store_true")
-    ap.add_argument("--cpu-child", nargs=2, metavar=("WORKLOAD", "PAIRS"), help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-child", nargs=3, metavar=("WORKLOAD", "PAIRS", "IMAGES"),
+                    help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -133,10 +137,12 @@ def oracle_pool(workers: int):
     return cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn"))
 
 
-def cpu_child(workload: str, pair_budget: float) -> dict:
+def cpu_child(workload: str, pair_budget: float, images: int = 0) -> dict:
     """The oracle over the workload (every image when pair_budget covers it)."""
     import workloads as W
     w = W.make(workload)
+    if images > 0:
+        w = W.first_images(w, images)
     chosen, _ = oracle_sample(w, pair_budget)
     workers = host_cores()
     with oracle_pool(workers) as pool:
@@ -153,12 +159,13 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def run_cpu_child(workload: str, pair_budget: float) -> dict:
+def run_cpu_child(workload: str, pair_budget: float, images: int = 0) -> dict:
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[v] = "1"
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", workload,
-                        str(pair_budget)], capture_output=True, text=True, env=env, timeout=900)
+                        str(pair_budget), str(images)], capture_output=True, text=True, env=env,
+                       timeout=900)
     if r.returncode != 0:
         raise RuntimeError(r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])
@@ -169,6 +176,12 @@ def cpu_rate(res: dict) -> float:
     images by attended pairs when only a sample was run)."""
     t_full = res["seconds"] * res["full_pairs"] / max(res["pairs"], 1)
     return res["full_tokens"] / t_full
+
+
+def make_workload(args):
+    import workloads as W
+    w = W.make(args.workload)
+    return W.first_images(w, args.images) if args.images > 0 else w
 
 
 def workload_config(w, workload: str, world: int, l2: str) -> dict:
@@ -188,8 +201,7 @@ def reference_arm(args) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import workloads as W
-    w = W.make(args.workload)
+    w = make_workload(args)
     workers = host_cores()
     budget = REFERENCE_PAIRS_PER_S * workers * 120.0 / max(1, args.steps + args.warmup)
     chosen, pairs = oracle_sample(w, budget)
@@ -489,7 +501,7 @@ def gpu_arm(args) -> None:
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         try:
-            cpu = run_cpu_child(args.workload, float("inf"))
+            cpu = run_cpu_child(args.workload, float("inf"), args.images)
         except Exception as exc:  # reported, never fatal
             cpu = {"error": str(exc)[-300:]}
 
@@ -502,7 +514,7 @@ def gpu_arm(args) -> None:
     tsel.build()
     tsel.load_library()
 
-    w = W.make(args.workload)
+    w = make_workload(args)
     dev = torch.device("cuda", local)
 
     def bf16(bits):
@@ -1005,7 +1017,8 @@ def main():
     if args.cpu_child or args.impl == "reference":
         _single_thread_blas()   # before numpy is imported
     if args.cpu_child:
-        print(json.dumps(cpu_child(args.cpu_child[0], float(args.cpu_child[1]))))
+        print(json.dumps(cpu_child(args.cpu_child[0], float(args.cpu_child[1]),
+                                   int(args.cpu_child[2]))))
         return
     if args.impl == "reference":
         reference_arm(args)

@@ -256,6 +256,21 @@ def make_far_keys(lengths, num_heads, num_kv_heads, head_dim, *, seed, far_posit
     )
 
 
+def first_images(w: "Workload", n_images: int, keep_permille: int = 600) -> "Workload":
+    """The first n_images segments of a workload as one request keeping
+    floor(keep_permille / 1000 of its tokens) (a smaller case of the same
+    shapes, e.g. for profiling)."""
+    g = max(1, min(int(n_images), w.num_seg))
+    q1, k1 = int(w.cu_seqlens_q[g]), int(w.cu_seqlens_k[g])
+    return Workload(name=f"{w.name}[:{g}]", q_bits=w.q_bits[:q1], k_bits=w.k_bits[:k1],
+                    cu_seqlens_q=w.cu_seqlens_q[:g + 1].copy(),
+                    cu_seqlens_k=w.cu_seqlens_k[:g + 1].copy(),
+                    req_tok_offsets=np.array([0, k1], dtype=np.int32),
+                    keep_per_req=np.array([keep_floor(k1, keep_permille)], dtype=np.int32),
+                    hidden_bits=w.hidden_bits[:k1], pos=w.pos[:k1],
+                    softmax_scale=w.softmax_scale, meta=dict(w.meta, first_images=g))
+
+
 def keep_floor(n: int, permille: int) -> int:
     """floor(n * permille / 1000) in integer arithmetic (budget rounding)."""
     return (int(n) * int(permille)) // 1000
