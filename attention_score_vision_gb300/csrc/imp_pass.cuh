@@ -478,13 +478,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int s_it = 0, a_it = 0, b_it = 0;
       bool ok = p.stall == 0;   // the test hook leaves the consumers waiting for work
+      // No more units than CTAs: each CTA takes the unit of its own index
+      // (no round trip to the counter for it, nor for the end of the work).
+      const bool one_each = total_units <= int(gridDim.x);
       while (ok) {
         const int slot = s_it % kSchedSlots;
         if (!wait_bounded(&sch_empty[slot], ((s_it / kSchedSlots) & 1) ^ 1, abort_flag, T)) {
           ok = false;
           break;
         }
-        const int u = atomicAdd(p.sched_ctr, 1);
+        const int u = one_each ? (s_it == 0 ? int(blockIdx.x) : total_units)
+                               : atomicAdd(p.sched_ctr, 1);
         Unit w;
         if (u < total_units) {
           w = decode_unit<PASS, KSPLIT>(p, p.units[u]);

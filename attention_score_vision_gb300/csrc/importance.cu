@@ -108,8 +108,10 @@ __global__ void __launch_bounds__(THREADS) imp_prep_kernel(const int32_t* __rest
   uint2* units1 = reinterpret_cast<uint2*>(ws + L.units1);
   uint2* units2 = reinterpret_cast<uint2*>(ws + L.units2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_launch_dependents();
   pdl_wait();   // cu_seqlens and the workspace belong to earlier kernels until here
+  // Released only now: every kernel of this call that launches early may
+  // then read the caller's inputs, which no earlier kernel still writes.
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     bad = 0;

@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(kTopkThreads)
                         const int32_t* __restrict__ req_off, int num_req,
                         const int32_t* __restrict__ keep, int total_keep,
                         int32_t* __restrict__ keep_idx, int32_t* __restrict__ cu_keep,
-                        uint32_t* status, const int32_t* hist, const int32_t* hist_ok) {
+                        uint32_t* status, const int32_t* hist, const int32_t* hist_ok,
+                        int inputs_final) {
   extern __shared__ __align__(16) unsigned char topk_smem[];
   TopkShared& sh = *reinterpret_cast<TopkShared*>(topk_smem);
   uint32_t* skeys = reinterpret_cast<uint32_t*>(topk_smem + sizeof(TopkShared));  // kTopkCacheKeys
@@ -260,11 +261,24 @@ __global__ void __launch_bounds__(kTopkThreads)
       sh.eq_before = 0;
     }
   }
+  // The request's offsets and budget: read before the wait for the scores
+  // when no kernel still running may write them (the fused score + select
+  // call: its schedule kernel released its dependents after the caller's
+  // earlier work had completed), else after it.
+  int lo_raw = 0, hi_raw = 0, B = 0;
+  if (inputs_final) {
+    lo_raw = req_off[r];
+    hi_raw = req_off[r + 1];
+    B = keep[r];
+  }
   pdl_wait();
+  if (!inputs_final) {
+    lo_raw = req_off[r];
+    hi_raw = req_off[r + 1];
+    B = keep[r];
+  }
 
   // ---- this CTA's slice; its first scores in flight during the checks ------
-  const int lo_raw = req_off[r], hi_raw = req_off[r + 1];
-  const int B = keep[r];
   const int lo = min(max(lo_raw, 0), total_tokens);
   const int hi = min(max(hi_raw, lo), total_tokens);
   const int n = hi - lo;
@@ -813,14 +827,14 @@ int topk_cluster_size(int total_tokens, int num_req, cudaError_t* e) {
 cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
                         int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
                         int32_t* cu_keep, uint32_t* status, const int32_t* hist,
-                        const int32_t* hist_ok, cudaStream_t stream) {
+                        const int32_t* hist_ok, int inputs_final, cudaStream_t stream) {
   const size_t dyn = kTopkDyn;
   cudaError_t e = cudaSuccess;
   const int csize = topk_cluster_size(total_tokens, num_req, &e);
   if (e != cudaSuccess) return e;
   return launch_clusters(topk_cluster_kernel, num_req, csize, kTopkThreads, dyn, stream, scores,
                          total_tokens, req_off, num_req, keep, total_keep, keep_idx, cu_keep,
-                         status, hist, hist_ok);
+                         status, hist, hist_ok, inputs_final);
 }
 
 }  // namespace tsel

@@ -32,7 +32,7 @@ cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, 
 cudaError_t launch_topk(const float* scores, int total_tokens, const int32_t* req_off,
                         int num_req, const int32_t* keep, int total_keep, int32_t* keep_idx,
                         int32_t* cu_keep, uint32_t* status, const int32_t* hist,
-                        const int32_t* hist_ok, cudaStream_t stream);
+                        const int32_t* hist_ok, int inputs_final, cudaStream_t stream);
 cudaError_t launch_topk_hist(const float* scores, int total_tokens, const int32_t* req_off, int R,
                              int32_t* hist, int32_t* hist_ok, int num_sms, cudaStream_t stream);
 int topk_cluster_size(int total_tokens, int num_req, cudaError_t* e);
@@ -470,8 +470,11 @@ tsel_status tsel_score_select(const void* q, int64_t q_row_stride, const void* k
     e = cudaMemsetAsync(cu_keep, 0, sizeof(int32_t), stream);
     return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "memset cu_keep");
   }
+  // After the schedule stage of this call the caller's inputs are final
+  // (its launch releases the later kernels only after its own wait).
+  const bool chained = (flags & stage_bits) == 0;
   e = launch_topk(scores, total_k, req_tok_offsets, num_req, keep_per_req, total_keep, keep_idx,
-                  cu_keep, &hdr->status, sel.hist, &hdr->hist_ok, stream);
+                  cu_keep, &hdr->status, sel.hist, &hdr->hist_ok, chained ? 1 : 0, stream);
   return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "top-k launch");
 }
 
@@ -494,7 +497,7 @@ tsel_status tsel_select_topk(const float* scores, int total_tokens,
   }
   WsHeader* hdr = static_cast<WsHeader*>(workspace);
   cudaError_t e = launch_topk(scores, total_tokens, req_tok_offsets, num_req, keep_per_req,
-                              total_keep, keep_idx, cu_keep, &hdr->status, nullptr, nullptr,
+                              total_keep, keep_idx, cu_keep, &hdr->status, nullptr, nullptr, 0,
                               stream);
   return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "top-k launch");
 }
@@ -538,7 +541,7 @@ tsel_status tsel_select_topk_hist(const float* scores, int total_tokens,
     if (e != cudaSuccess) return cuda_fail(e, "histogram launch");
   }
   e = launch_topk(scores, total_tokens, req_tok_offsets, num_req, keep_per_req, total_keep,
-                  keep_idx, cu_keep, &hdr->status, hist, hist ? &hdr->hist_ok : nullptr, stream);
+                  keep_idx, cu_keep, &hdr->status, hist, hist ? &hdr->hist_ok : nullptr, 0, stream);
   return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "top-k launch");
 }
 
