@@ -39,7 +39,8 @@
 // the threshold among the candidates alone (two 8-bit rounds in shared
 // memory, block barriers only) and knows its output offset. More candidates,
 // or counts that do not add up to the request's tokens, fall back to the
-// radix rounds above (from the second digit, or from the first).
+// radix rounds above (from the second digit, or from the first). Requests of
+// one CTA get no histograms (their rounds need no cluster barrier).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -135,16 +136,11 @@ struct __align__(16) TopkShared {
   // first 16 bits) and per-CTA counts, written by the CTAs that hold them
   uint32_t cand_key[kTopkCand];
   int cand_idx[kTopkCand];
-  // (CTA c's candidates sit in slots [c * cap, c * cap + cnt_of[c]), cap =
-  // kTopkCand / cluster size)
-  int cnt_of[kMaxClusterCtas];    // per CTA: its candidates (all of them, stored or not)
-  int pre_of[kMaxClusterCtas];    // per CTA: candidates of the CTAs before it
   int gt16_of[kMaxClusterCtas];   // per CTA: its keys above the candidates' 16-bit prefix
   int cls_gt[kMaxClusterCtas];    // per CTA: its candidates above the threshold
   int cls_eq[kMaxClusterCtas];    // per CTA: its candidates equal to the threshold
-  int loc_n;                      // this CTA's candidates
-  uint32_t thr_key;               // the threshold key found among the candidates
-  int thr_need;                   // tied keys to keep
+  int cbase[kMaxClusterCtas];     // this CTA's first slot in each CTA's candidate list
+  int cand_n, loc_n;
   __align__(16) int wtot[kTopkWarps];       // digit search: per-warp bin totals
   __align__(16) int gt_w[kTopkWarps];       // last round: per-warp keys above the rounds 0-1 prefix
   __align__(16) int grp_w[kTopkWarps];      // last round: per-warp totals of this CTA's counts
@@ -247,16 +243,14 @@ __global__ void __launch_bounds__(kTopkThreads)
     int4* h = reinterpret_cast<int4*>(&sh.local[0][0]);
     for (int i = tid; i < 6 * kTopkBins / 4; i += kTopkThreads) h[i] = make_int4(0, 0, 0, 0);
     if (tid < kMaxClusterCtas) {
-      sh.cnt_of[tid] = 0;
       sh.gt16_of[tid] = 0;
       sh.cls_gt[tid] = 0;
       sh.cls_eq[tid] = 0;
     }
     if (tid == 0) {
       sh.nan_seen = 0;
+      sh.cand_n = 0;
       sh.loc_n = 0;
-      sh.thr_key = 0;
-      sh.thr_need = 0;
       sh.out_base = 0;
       sh.eq_before = 0;
     }
@@ -293,12 +287,10 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int i = j * kTopkThreads + tid;
     f[j] = i < len ? __ldcg(s + i) : 0.f;
   }
-  // histogram start: this request's first-digit counts (bins 4 tid .. 4 tid +
-  // 3), loaded alongside the flag that says whether they are valid
-  const int32_t* hreq = hist != nullptr ? hist + int64_t(r) * kHistWords : nullptr;
-  const int4 hc = hreq != nullptr ? __ldcg(reinterpret_cast<const int4*>(hreq) + tid)
-                                  : make_int4(0, 0, 0, 0);
+  // histogram start: this request's first-digit counts (bins 4 tid .. 4 tid + 3)
   const bool use_hist = hist != nullptr && *reinterpret_cast<const volatile int32_t*>(hist_ok) != 0;
+  const int32_t* hreq = use_hist ? hist + int64_t(r) * kHistWords : nullptr;
+  const int4 hc = use_hist ? __ldcg(reinterpret_cast<const int4*>(hreq) + tid) : make_int4(0, 0, 0, 0);
 
   // ---- request checks and output offset (every thread, every CTA alike) ----
   long long part = 0;
@@ -423,24 +415,16 @@ __global__ void __launch_bounds__(kTopkThreads)
 
   if (cand_mode) {
     // This CTA's keys above the 16-bit prefix, and its candidates (staged in
-    // the compaction buffer: keys, then indices; the first `cap` are sent).
-    // Slots are taken per warp (one shared atomic per warp and iteration).
-    const int cap = kTopkCand / csize;
+    // the compaction buffer: keys, then indices).
     int gt16 = 0;
-    for (int i0 = 0; i0 < len; i0 += kTopkThreads) {
-      const int i = i0 + tid;
-      const bool in = i < len;
-      const uint32_t kk = in ? (cached ? skeys[i] : order_key(s[i])) : 0u;
+    for (int i = tid; i < len; i += kTopkThreads) {
+      const uint32_t kk = cached ? skeys[i] : order_key(s[i]);
       const uint32_t top = kk >> 16;
-      gt16 += in && top > pfx16;
-      const bool cand = in && top == pfx16;
-      const unsigned m = __ballot_sync(0xffffffffu, cand);
-      if (m != 0u) {
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&sh.loc_n, __popc(m));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const int slot = base + __popc(m & ((1u << lane) - 1u));
-        if (cand && slot < cap) {
+      if (top > pfx16) {
+        ++gt16;
+      } else if (top == pfx16) {
+        const int slot = atomicAdd(&sh.loc_n, 1);
+        if (slot < kTopkCand) {
           sh.stage[slot] = int(kk);
           sh.stage[kTopkCand + slot] = lo + c0 + i;
         }
@@ -449,55 +433,40 @@ __global__ void __launch_bounds__(kTopkThreads)
     gt16 = warp_sum(gt16);
     if (lane == 0) sh.gt_w[warp] = gt16;
     __syncthreads();
-    const int nloc = sh.loc_n, nput = min(nloc, cap);
-    // Every CTA receives every CTA's counts and candidates in that CTA's own
-    // slots: plain stores into distributed shared memory, then one barrier.
+    const int nloc = min(sh.loc_n, kTopkCand);
     if (tid < csize) {
       int gsum = 0;
 #pragma unroll
       for (int w = 0; w < kTopkWarps; ++w) gsum += sh.gt_w[w];
-      TopkShared* dst = solo ? &sh : cluster.map_shared_rank(&sh, tid);
-      dst->cnt_of[crank] = nloc;
-      dst->gt16_of[crank] = gsum;
+      // the full count (a CTA with more candidates than fit stores only the
+      // first kTopkCand; the total then exceeds the list and is rejected below)
+      int* cn = solo ? &sh.cand_n : cluster.map_shared_rank(&sh.cand_n, tid);
+      sh.cbase[tid] = atomicAdd(cn, sh.loc_n);
+      int* g16 = solo ? &sh.gt16_of[crank] : cluster.map_shared_rank(&sh.gt16_of[crank], tid);
+      *g16 = gsum;
     }
-    for (int e = tid; e < csize * nput; e += kTopkThreads) {
-      const int j = e / nput, t = e - j * nput;
-      TopkShared* dst = solo ? &sh : cluster.map_shared_rank(&sh, j);
-      dst->cand_key[crank * cap + t] = uint32_t(sh.stage[t]);
-      dst->cand_idx[crank * cap + t] = sh.stage[kTopkCand + t];
+    __syncthreads();
+    for (int j = 0; j < csize; ++j) {
+      const int base = sh.cbase[j];
+      uint32_t* dk = solo ? sh.cand_key : cluster.map_shared_rank(sh.cand_key, j);
+      int* di = solo ? sh.cand_idx : cluster.map_shared_rank(sh.cand_idx, j);
+      for (int t = tid; t < nloc && base + t < kTopkCand; t += kTopkThreads) {
+        dk[base + t] = uint32_t(sh.stage[t]);
+        di[base + t] = sh.stage[kTopkCand + t];
+      }
     }
     // The one exchange: after it no CTA touches another's shared memory.
     if (!solo) cluster.sync();
     __syncthreads();
     // The threshold lies among the candidates when the keys above their
     // prefix (counted in the slices, not taken from the histograms) number
-    // fewer than B, the candidates make up the rest and every CTA's fitted
-    // its slots; every CTA holds the same counts and takes the same branch.
-    int above16 = 0, total = 0;
-    bool fits = true;
-    for (int c = 0; c < csize; ++c) {
-      above16 += sh.gt16_of[c];
-      total += sh.cnt_of[c];
-      fits = fits && sh.cnt_of[c] <= cap;
-    }
-    if (fits && above16 < B && B <= above16 + total) {
+    // fewer than B and the candidates make up the rest; every CTA holds the
+    // same counts, so every CTA takes the same branch.
+    int above16 = 0;
+    for (int c = 0; c < csize; ++c) above16 += sh.gt16_of[c];
+    if (sh.cand_n <= kTopkCand && above16 < B && B <= above16 + sh.cand_n) {
       remaining = B - above16;
-      cnt16 = total;
-      // one flat list in slice order (the stage buffer is free again)
-      if (tid < csize) {
-        int pre = 0;
-        for (int c = 0; c < tid; ++c) pre += sh.cnt_of[c];
-        sh.pre_of[tid] = pre;
-      }
-      __syncthreads();
-      for (int x = tid; x < csize * cap; x += kTopkThreads) {
-        const int c = x / cap, o = x - c * cap;
-        if (o < sh.cnt_of[c]) {
-          sh.stage[sh.pre_of[c] + o] = int(sh.cand_key[x]);
-          sh.stage[kTopkCand + sh.pre_of[c] + o] = sh.cand_idx[x];
-        }
-      }
-      __syncthreads();
+      cnt16 = sh.cand_n;
     } else {
       // radix rounds from the start
       cand_mode = false;
@@ -516,65 +485,32 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
 
   if (cand_mode) {
-    // The threshold: the candidate of rank remaining - 1 in the order (key
-    // descending, index ascending), and how many keys equal to it to keep.
+    // The threshold among the candidates: two 8-bit rounds over their low
+    // 16 bits (local[0], local[1]: zeroed at entry, unused on this path).
     const int ncand = cnt16;
-    const uint32_t* ck = reinterpret_cast<const uint32_t*>(sh.stage);
-    const int* ci = sh.stage + kTopkCand;
-    if (ncand <= kTopkThreads) {
-      // one candidate per thread, ranked against all of them four at a time
-      if (tid < ncand) {
-        const uint32_t k0 = ck[tid];
-        const int i0 = ci[tid];
-        int gt = 0, eqb = 0;
-        int u = 0;
-        for (; u + 4 <= ncand; u += 4) {
-          const uint4 kv = *reinterpret_cast<const uint4*>(ck + u);
-          const int4 iv = *reinterpret_cast<const int4*>(ci + u);
-          gt += (kv.x > k0) + (kv.y > k0) + (kv.z > k0) + (kv.w > k0);
-          eqb += (kv.x == k0 && iv.x < i0) + (kv.y == k0 && iv.y < i0) +
-                 (kv.z == k0 && iv.z < i0) + (kv.w == k0 && iv.w < i0);
-        }
-        for (; u < ncand; ++u) {
-          gt += ck[u] > k0;
-          eqb += ck[u] == k0 && ci[u] < i0;
-        }
-        if (gt + eqb == remaining - 1) {
-          sh.thr_key = k0;
-          sh.thr_need = remaining - gt;
-        }
-      }
-    } else {
-      // two 8-bit rounds over the candidates' low 16 bits (local[0] and
-      // local[1]: zeroed at entry, unused on this path)
-      int* binsA = sh.local[0];
-      int* binsB = sh.local[1];
-      for (int x = tid; x < ncand; x += kTopkThreads) atomicAdd(&binsA[(ck[x] >> 8) & 255u], 1);
-      __syncthreads();
-      int aboveA;
-      const int dA = find_digit256(binsA, remaining, aboveA);
-      const uint32_t pfx24 = (pfx16 << 8) | uint32_t(dA);
-      for (int x = tid; x < ncand; x += kTopkThreads) {
-        const uint32_t kk = ck[x];
-        if ((kk >> 8) == pfx24) atomicAdd(&binsB[kk & 255u], 1);
-      }
-      __syncthreads();
-      int aboveB;
-      const int dB = find_digit256(binsB, remaining - aboveA, aboveB);
-      if (tid == 0) {
-        sh.thr_key = (pfx24 << 8) | uint32_t(dB);
-        sh.thr_need = remaining - aboveA - aboveB;
-      }
+    int* binsA = sh.local[0];
+    int* binsB = sh.local[1];
+    for (int i = tid; i < ncand; i += kTopkThreads) atomicAdd(&binsA[(sh.cand_key[i] >> 8) & 255u], 1);
+    __syncthreads();
+    int aboveA;
+    const int dA = find_digit256(binsA, remaining, aboveA);
+    remaining -= aboveA;
+    const uint32_t pfx24 = (pfx16 << 8) | uint32_t(dA);
+    for (int i = tid; i < ncand; i += kTopkThreads) {
+      const uint32_t kk = sh.cand_key[i];
+      if ((kk >> 8) == pfx24) atomicAdd(&binsB[kk & 255u], 1);
     }
     __syncthreads();
-    thr = sh.thr_key;
-    need_eq = sh.thr_need;
-    // per CTA (the list is in slice order): its candidates above / equal to
-    // the threshold
-    for (int x = tid; x < ncand; x += kTopkThreads) {
-      const uint32_t kk = ck[x];
+    int aboveB;
+    const int dB = find_digit256(binsB, remaining, aboveB);
+    remaining -= aboveB;
+    thr = (pfx24 << 8) | uint32_t(dB);
+    need_eq = remaining;
+    // per CTA (the slice holding the index): candidates above / equal to thr
+    for (int i = tid; i < ncand; i += kTopkThreads) {
+      const uint32_t kk = sh.cand_key[i];
       if (kk >= thr) {
-        const int src = min(csize - 1, (ci[x] - lo) / chunk);
+        const int src = min(csize - 1, (sh.cand_idx[i] - lo) / chunk);
         atomicAdd(kk > thr ? &sh.cls_gt[src] : &sh.cls_eq[src], 1);
       }
     }
@@ -773,7 +709,6 @@ __global__ void __launch_bounds__(kHistThreads)
     topk_hist_kernel(const float* __restrict__ scores, int total_tokens,
                      const int32_t* __restrict__ req_off, int R, int32_t* hist, int32_t* hist_ok) {
   __shared__ int ok_s;
-  __shared__ int32_t s_off[kHistMaxReq + 1];
   pdl_launch_dependents();
   pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -783,7 +718,6 @@ __global__ void __launch_bounds__(kHistThreads)
       const int o = __ldg(req_off + r);
       const int prev = r > 0 ? __ldg(req_off + r - 1) : 0;
       if (o < prev || o > total_tokens) ok = false;
-      s_off[r] = o;
     }
     ok = __all_sync(0xffffffffu, ok);
     if (lane == 0) {
@@ -798,7 +732,7 @@ __global__ void __launch_bounds__(kHistThreads)
     const int tok = int(w * 32) + lane;
     const bool valid = tok < total_tokens;
     const float sc = valid ? __ldcg(scores + tok) : 0.f;
-    hist_add_warp(hist, s_off, R, tok, sc, valid);
+    hist_add_warp(hist, req_off, R, tok, sc, valid);
   }
 }
 
