@@ -244,8 +244,8 @@ __device__ __forceinline__ void column_sum_chunk(const uint32_t (&r)[32], const 
     const float2 x23 = __ffma2_rn(
         make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), c2,
         make_float2(t.z, t.w));
-    acc[0] = __fadd2_rn(acc[0], make_float2(ex2(x01.x), ex2(x01.y)));
-    acc[1] = __fadd2_rn(acc[1], make_float2(ex2(x23.x), ex2(x23.y)));
+    acc[0] = ex2_add2(acc[0], x01);
+    acc[1] = ex2_add2(acc[1], x23);
   }
 }
 
@@ -296,7 +296,7 @@ __device__ __forceinline__ void cols_exp_sum(const uint32_t (&r)[32], float2 c2,
   for (int j = 0; j < 16; ++j) {
     const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
                                 c2, nm2);
-    a[j & 1] = __fadd2_rn(a[j & 1], make_float2(ex2(x.x), ex2(x.y)));
+    a[j & 1] = ex2_add2(a[j & 1], x);
   }
 }
 

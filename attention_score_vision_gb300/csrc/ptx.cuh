@@ -243,5 +243,22 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// exp2 (as ex2() above) of both halves of x, added to acc with one packed
+// f32x2 add; the two results are formed as one 64-bit pair, so no move is
+// needed to pair them for the add.
+__device__ __forceinline__ float2 ex2_add2(float2 acc, float2 x) {
+  float2 r;
+  asm("{\n\t.reg .f32 e0, e1;\n\t.reg .b64 t, s, d;\n\t"
+      "ex2.approx.ftz.f32 e0, %2;\n\t"
+      "ex2.approx.ftz.f32 e1, %3;\n\t"
+      "mov.b64 t, {e0, e1};\n\t"
+      "mov.b64 s, {%4, %5};\n\t"
+      "add.rn.f32x2 d, s, t;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(x.x), "f"(x.y), "f"(acc.x), "f"(acc.y));
+  return r;
+}
+
 }  // namespace ptx
 }  // namespace tsel
