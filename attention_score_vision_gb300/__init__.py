@@ -25,10 +25,10 @@ __all__ = [
     "tsel_gather_compact_workspace_size", "tsel_gather_compact", "tsel_gather_compact_counted",
     "tsel_dynamic_budget", "TSEL_KEEP_FROM_DEVICE",
     "tsel_keep_count", "tsel_read_device_status", "tsel_clear_device_status",
-    "tsel_importance_redo_pairs", "tsel_select_path_counts",
+    "tsel_importance_redo_pairs", "tsel_select_path_counts", "tsel_importance_one_launch",
     "tsel_status_string", "tsel_last_error", "tsel_probe_ex2",
     "TSEL_DEV_SEQLENS", "TSEL_DEV_REQUESTS", "TSEL_DEV_KEEP_IDX", "TSEL_DEV_TIMEOUT", "TSEL_DEV_NAN",
-    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_SCORE_SUM", "TSEL_IMP_ROWREF_FIXED", "TSEL_IMP_ROWREF_MOVING", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
+    "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_SCORE_SUM", "TSEL_IMP_ROWREF_FIXED", "TSEL_IMP_ROWREF_MOVING", "TSEL_IMP_TWO_PASS", "TSEL_IMP_TEST_STALL", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS1", "TSEL_IMP_STAGE_PASS2",
 ]
 
 TSEL_OK = 0
@@ -51,6 +51,7 @@ TSEL_IMP_FP8_E4M3 = 0x2
 TSEL_IMP_SCORE_SUM = 0x4
 TSEL_IMP_ROWREF_FIXED = 0x8
 TSEL_IMP_ROWREF_MOVING = 0x20
+TSEL_IMP_TWO_PASS = 0x40
 TSEL_IMP_TEST_STALL = 0x10000
 TSEL_IMP_STAGE_PREP = 0x100
 TSEL_IMP_STAGE_PASS1 = 0x200
@@ -76,6 +77,8 @@ _SIGNATURES = {
     "tsel_dynamic_budget": (_c_int, [_p, _c_int, _p, _c_int, _c_int, _c_int, _c_int, _p, _p, _p,
                                      _c_size, _p]),
     "tsel_keep_count": (_c_int, [_c_int, _c_int]),
+    "tsel_importance_one_launch": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                            _c_uint]),
     "tsel_read_device_status": (_c_int, [_p, ctypes.POINTER(ctypes.c_uint32), _p]),
     "tsel_clear_device_status": (_c_int, [_p, _p]),
     "tsel_importance_redo_pairs": (_c_int, [_p, ctypes.POINTER(ctypes.c_int32), _p]),
@@ -493,6 +496,17 @@ def tsel_gather_compact_counted(hidden: torch.Tensor, pos: Optional[torch.Tensor
 # ---------------------------------------------------------------------------
 # Helpers
 # ---------------------------------------------------------------------------
+
+def tsel_importance_one_launch(num_seg: int, total_q: int, total_k: int, max_seqlen_q: int,
+                               max_seqlen_k: int, num_heads: int, head_dim: int,
+                               flags: int = 0) -> int:
+    """1 if tsel_importance takes the one-launch path for these sizes and flags
+    on the current device, 0 if the scheduled two-pass launches, -1 on a CUDA
+    error."""
+    return int(load_library().tsel_importance_one_launch(
+        int(num_seg), int(total_q), int(total_k), int(max_seqlen_q), int(max_seqlen_k),
+        int(num_heads), int(head_dim), int(flags)))
+
 
 def tsel_keep_count(n_tokens: int, keep_permille: int) -> int:
     return int(load_library().tsel_keep_count(int(n_tokens), int(keep_permille)))

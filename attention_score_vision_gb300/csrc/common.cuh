@@ -137,6 +137,23 @@ __host__ __device__ inline int64_t sel_hist_bytes(int R) {
   return (R >= 1 && R <= kHistMaxReq) ? int64_t(R) * kHistWords * 4 : 0;
 }
 
+// One-launch importance of small problems (imp_small.cu): one cluster of H
+// CTAs per segment, both passes per (segment, head) in one CTA.
+struct ImpSmallParams {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int G, Tq, Tk;
+  int max_q, max_k;      // the caller's bounds (<= 256), checked on the device
+  int H, Hkv;
+  float c;               // softmax_scale * log2(e)
+  float* lse_out;        // natural log [H][Tq] (may be null)
+  float* scores;         // [Tk]
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int stall;             // test hook: no loads are issued, every wait runs out
+  int sum_norm;          // 1: total attention received (no division by H*Nq)
+};
+
 struct ImpPassParams {
   const int32_t* cu_q;
   const int32_t* cu_k;

@@ -1,0 +1,434 @@
+// One-launch importance for small problems: every segment has at most 256
+// query rows and 256 keys (a single image of a 256-token ViT, or a handful of
+// them), bf16, at most 16 heads.
+//
+// Same quantity as the two passes of imp_pass.cuh (LiteVLM review, section
+// 3.2; dynamic vision-token compression article, section 3.2: the mean
+// attention each key receives, probabilities recovered from the row LSE and
+// reduced along columns on chip), with the whole 256 x 256 score block of one
+// (segment, head) held in TMEM at once, so one CTA does both passes:
+//
+//   1. S = Q K^T: two 128-row query tiles x two 128-key tiles, four 128x128
+//      tcgen05 accumulators (all 512 TMEM columns). Each epilogue warpgroup
+//      takes one accumulator: per query row a max-referenced exp2 sum over its
+//      128 keys (the reference follows the row max, terms stay below 2^8);
+//      the two warpgroups of a query tile merge into the row's LSE (kept as
+//      -LSE*log2 e in shared memory, written out as the natural-log LSE).
+//   2. S^T = K Q^T into the same columns, keys on the MMA M dimension: each
+//      epilogue thread owns one key and sums exp2(S*c - LSE2) over the query
+//      columns in registers; the two warpgroups of a key tile add up.
+//   3. The CTAs of one segment form a thread-block cluster, one CTA per head;
+//      after a cluster barrier each CTA adds a slice of the keys' per-head sums
+//      over the cluster's distributed shared memory in head order (a fixed
+//      order: the scores are deterministic) and writes the scores.
+//
+// There is no schedule kernel (each CTA checks the cu_seqlens itself), no
+// second launch and no global counter. The launch is programmatically
+// dependent like every kernel of the library; it allocates TMEM before it
+// releases the next kernel, and releases it only after its own grid-dependency
+// wait (so a kernel that launches early may read the caller's inputs).
+//
+// CTA: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer (one thread),
+// warps 2-17 four epilogue warpgroups (warp w reads TMEM lanes 32*(w%4)..).
+// The dynamic shared memory is padded so that a second CTA never shares an SM
+// (each holds all of TMEM while it waits at the cluster barrier).
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+
+#include "imp_pass.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace tsel {
+
+namespace {
+
+constexpr int kSmallThreads = 32 * (2 + kEpiWarps);   // 576
+
+template <int D>
+struct SmallCfg {
+  using C = TileCfg<D, false>;
+  static constexpr int OFF_Q = 0;                        // two query tiles
+  static constexpr int OFF_K = 2 * C::TILE_BYTES;        // two key tiles
+  static constexpr int OFF_NL = 4 * C::TILE_BYTES;       // -LSE2 of the 256 query rows
+  static constexpr int OFF_PS = OFF_NL + kPair * 4;      // per-key sums of this head
+  static constexpr int OFF_CM = OFF_PS + kPair * 4;      // warpgroup exchange [2][128]
+  static constexpr int OFF_CL = OFF_CM + kPair * 4;      // warpgroup exchange [2][128]
+  static constexpr int OFF_BAR = OFF_CL + kPair * 4;     // three mbarriers
+  static constexpr int OFF_MISC = OFF_BAR + 64;
+  static constexpr int USED = OFF_MISC + 64 + 1024;      // + alignment slack
+  static constexpr int MIN_ONE_PER_SM = 120 * 1024;      // two of these exceed an SM
+  static constexpr int SMEM_BYTES = USED > MIN_ONE_PER_SM ? USED : MIN_ONE_PER_SM;
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// Row max/sum of one 128-column accumulator piece (phase 1). `valid` columns
+// lie inside the segment (> 0); m is the row's reference for S*c, l the sum of
+// exp2(S*c - m) before the accumulators acc.
+__device__ __forceinline__ void small_row_lse(uint32_t taddr, int valid, float c, float2 c2,
+                                              float& m, float& l, float2 (&acc)[2]) {
+  uint32_t r0[32], r1[32];
+  tmem_ld32_async(taddr, r0);
+  tmem_ld32_async(taddr + 32, r1);
+  tmem_wait_ld(r0);
+  tmem_wait_ld(r1);
+  mask_cols(r0, valid);
+  mask_cols(r1, valid - 32);
+  move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
+  float2 nm2 = make_float2(-m, -m);
+  cols_exp_sum(r0, c2, nm2, acc);
+  if (valid > 32) cols_exp_sum(r1, c2, nm2, acc);
+  if (valid > 64) {
+    tmem_ld32_async(taddr + 64, r0);
+    tmem_ld32_async(taddr + 96, r1);
+    tmem_wait_ld(r0);
+    tmem_wait_ld(r1);
+    mask_cols(r0, valid - 64);
+    mask_cols(r1, valid - 96);
+    move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
+    nm2 = make_float2(-m, -m);
+    cols_exp_sum(r0, c2, nm2, acc);
+    if (valid > 96) cols_exp_sum(r1, c2, nm2, acc);
+  }
+}
+
+// Per-key sum of exp2(S*c - LSE2) over the 128 query columns of one
+// accumulator (phase 2); nl holds -LSE2 of those columns (-inf past the
+// segment), `vq` of them lie inside the segment (> 0).
+__device__ __forceinline__ void small_col_sum(uint32_t taddr, int vq, const float4* nl, float2 c2,
+                                              float2 (&acc)[2]) {
+  uint32_t r0[32], r1[32];
+  tmem_ld32_async(taddr, r0);
+  tmem_ld32_async(taddr + 32, r1);
+  tmem_wait_ld(r0);
+  tmem_wait_ld(r1);
+  column_sum_chunk(r0, nl, c2, acc);
+  if (vq > 32) column_sum_chunk(r1, nl + 8, c2, acc);
+  if (vq > 64) {
+    tmem_ld32_async(taddr + 64, r0);
+    tmem_ld32_async(taddr + 96, r1);
+    tmem_wait_ld(r0);
+    tmem_wait_ld(r1);
+    column_sum_chunk(r0, nl + 16, c2, acc);
+    if (vq > 96) column_sum_chunk(r1, nl + 24, c2, acc);
+  }
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    imp_small_kernel(const __grid_constant__ CUtensorMap mapQ64,
+                     const __grid_constant__ CUtensorMap mapQ16,
+                     const __grid_constant__ CUtensorMap mapK64,
+                     const __grid_constant__ CUtensorMap mapK16, const ImpSmallParams p) {
+  using C = TileCfg<D, false>;
+  using S = SmallCfg<D>;
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
+  uint8_t* sQ = smem + S::OFF_Q;
+  uint8_t* sK = smem + S::OFF_K;
+  float* sNl = reinterpret_cast<float*>(smem + S::OFF_NL);
+  float* sPs = reinterpret_cast<float*>(smem + S::OFF_PS);
+  float* sCm = reinterpret_cast<float*>(smem + S::OFF_CM);
+  float* sCl = reinterpret_cast<float*>(smem + S::OFF_CL);
+  uint64_t* ld_full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
+  uint64_t* mma1_done = ld_full + 1;
+  uint64_t* mma2_done = ld_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::OFF_MISC + 4);
+  int* s_bad = reinterpret_cast<int*>(smem + S::OFF_MISC + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = int(cluster.num_blocks());   // = the number of heads
+  const int h = int(cluster.block_rank());    // this CTA's head
+  const int g = int(blockIdx.x) / cs;         // this cluster's segment
+  const uint64_t T = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(ld_full, 1);
+    mbar_init(mma1_done, 1);
+    mbar_init(mma2_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&mapQ64);
+    prefetch_tensormap(&mapQ16);
+    prefetch_tensormap(&mapK64);
+    prefetch_tensormap(&mapK16);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();                 // cu_seqlens, Q and K may come from earlier kernels
+  pdl_launch_dependents();    // after the TMEM allocation and the wait (see above)
+
+  // Every CTA checks every segment (the same data gives every CTA the same
+  // outcome, so a bad input sends all of them out before any cluster barrier).
+  if (warp == 0) {
+    bool b = false;
+    for (int i = lane; i < p.G; i += 32) {
+      const int nq = __ldg(p.cu_q + i + 1) - __ldg(p.cu_q + i);
+      const int nk = __ldg(p.cu_k + i + 1) - __ldg(p.cu_k + i);
+      b = b || nq < 0 || nk < 0 || nq > p.max_q || nk > p.max_k;
+    }
+    if (lane == 0)
+      b = b || __ldg(p.cu_q) != 0 || __ldg(p.cu_k) != 0 || __ldg(p.cu_q + p.G) != p.Tq ||
+          __ldg(p.cu_k + p.G) != p.Tk;
+    b = __any_sync(0xffffffffu, b);
+    if (lane == 0) *s_bad = b ? 1 : 0;
+  }
+  __syncthreads();
+  if (*s_bad) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(p.status, TSEL_DEV_SEQLENS);
+    if (warp == 1) tmem_dealloc(tmem, 512);
+    return;
+  }
+  const int q0 = __ldg(p.cu_q + g), nq = __ldg(p.cu_q + g + 1) - q0;
+  const int k0 = __ldg(p.cu_k + g), nk = __ldg(p.cu_k + g + 1) - k0;
+  const int nA = int(ceil_div(nq, kTile)), nB = int(ceil_div(nk, kTile));
+  const bool work = nA > 0 && nB > 0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool issued = false;
+      if (p.stall == 0) {   // the test hook publishes nothing: every wait runs out
+        if (work) {
+          mbar_arrive_expect_tx(ld_full, uint32_t((nA + nB) * C::TILE_BYTES));
+          for (int a = 0; a < nA; ++a)
+            load_tile<D, false>(sQ + a * C::TILE_BYTES, &mapQ64, &mapQ16, ld_full, h,
+                                q0 + a * kTile);
+          const int kvh = h / (p.H / p.Hkv);
+          for (int b = 0; b < nB; ++b)
+            load_tile<D, false>(sK + b * C::TILE_BYTES, &mapK64, &mapK16, ld_full, kvh,
+                                k0 + b * kTile);
+          issued = true;
+        } else {
+          mbar_arrive(ld_full);
+        }
+      }
+      // the copies have landed before the CTA can exit
+      if (issued) wait_drain(ld_full, 0, T);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    uint64_t* pending = nullptr;   // last commit barrier, drained before TMEM is freed
+    if (lane == 0) {
+      if (wait_bounded(ld_full, 0, abort_flag, T)) {
+        tc_fence_after();
+        if (work)
+          for (int a = 0; a < nA; ++a)
+            for (int b = 0; b < nB; ++b)
+              issue_tile_mmas<D, false>(tmem + uint32_t((2 * a + b) * kTile),
+                                        sQ + a * C::TILE_BYTES, sK + b * C::TILE_BYTES);
+        mma_commit(mma1_done);
+        pending = mma1_done;
+      } else {
+        *abort_flag = 1;
+        set_status(p.status, TSEL_DEV_TIMEOUT);
+      }
+    }
+    __syncwarp();
+    // The epilogue has read every phase-1 accumulator: S^T into the same columns.
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * (kEpiWarps + 1)) : "memory");
+    if (lane == 0) {
+      if (pending != nullptr && *abort_flag == 0) {
+        tc_fence_after();
+        if (work)
+          for (int b = 0; b < nB; ++b)
+            for (int a = 0; a < nA; ++a)
+              issue_tile_mmas<D, false>(tmem + uint32_t((2 * b + a) * kTile),
+                                        sK + b * C::TILE_BYTES, sQ + a * C::TILE_BYTES);
+        mma_commit(mma2_done);
+        pending = mma2_done;
+      }
+      if (pending != nullptr) wait_drain(pending, 0, T);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int wg = (warp - kEpiFirstWarp) >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = uint32_t(quad * 32) << 16;
+    const float c = p.c;
+    const float2 c2 = make_float2(c, c);
+    {
+      // Phase 1: warpgroup (a, b) = query tile a x key tile b.
+      const int a = wg >> 1, b = wg & 1;
+      float m = kNegInf, l = 0.f;
+      float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      if (warp_wait(mma1_done, 0, abort_flag, T)) {
+        tc_fence_after();
+        if (work && a < nA && b < nB)
+          small_row_lse(tmem + lane_off + uint32_t((2 * a + b) * kTile), nk - b * kTile, c, c2, m,
+                        l, acc);
+      } else if (lane == 0) {
+        *abort_flag = 1;
+        set_status(p.status, TSEL_DEV_TIMEOUT);
+      }
+      tc_fence_before();
+      const float2 s2 = __fadd2_rn(acc[0], acc[1]);
+      const float L = l + (s2.x + s2.y);
+      if (b == 1) {
+        sCm[a * kTile + row] = m;
+        sCl[a * kTile + row] = L;
+      }
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * (kEpiWarps + 1)) : "memory");
+      if (b == 0) {
+        const float m1 = sCm[a * kTile + row], l1 = sCl[a * kTile + row];
+        const float M = fmaxf(m, m1);
+        float Ls = 0.f;
+        if (M > kNegInf) Ls = __fadd_rn(__fmul_rn(L, ex2(m - M)), __fmul_rn(l1, ex2(m1 - M)));
+        const int qrow = a * kTile + row;
+        const bool valid = qrow < nq;
+        const float lse2 = Ls > 0.f ? M + log2f(Ls) : kNegInf;
+        sNl[qrow] = (valid && Ls > 0.f) ? -lse2 : kNegInf;
+        if (valid && p.lse_out != nullptr && *abort_flag == 0)
+          p.lse_out[int64_t(h) * p.Tq + q0 + qrow] = lse2 * 0.69314718055994531f;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");   // sNl complete
+    }
+    {
+      // Phase 2: warpgroup (b, a) = key tile b x query tile a.
+      const int b = wg >> 1, a = wg & 1;
+      float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      if (warp_wait(mma2_done, 0, abort_flag, T)) {
+        tc_fence_after();
+        if (work && b < nB && a < nA)
+          small_col_sum(tmem + lane_off + uint32_t((2 * b + a) * kTile), nq - a * kTile,
+                        reinterpret_cast<const float4*>(sNl + a * kTile), c2, acc);
+      } else if (lane == 0) {
+        *abort_flag = 1;
+        set_status(p.status, TSEL_DEV_TIMEOUT);
+      }
+      tc_fence_before();
+      const float2 s2 = __fadd2_rn(acc[0], acc[1]);
+      const float part = s2.x + s2.y;
+      if (a == 1) sCm[b * kTile + row] = part;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+      if (a == 0) sPs[b * kTile + row] = part + sCm[b * kTile + row];
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();   // per-key sums complete, every TMEM read done
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+
+  // Head sum over the cluster, in head order; CTA h reduces keys [h*per, (h+1)*per).
+  if (cs > 1) cluster_sync_all();
+  const int per = (kPair + cs - 1) / cs;
+  if (int(threadIdx.x) < per && *abort_flag == 0) {
+    const int key = h * per + int(threadIdx.x);
+    if (key < nk) {
+      float sum = 0.f;
+      for (int r = 0; r < cs; ++r) sum += cs > 1 ? *cluster.map_shared_rank(sPs + key, r) : sPs[key];
+      const float rows = p.sum_norm ? 1.f : float(p.H * nq);
+      p.scores[k0 + key] = nq > 0 ? sum / rows : 0.f;
+    }
+  }
+  __syncwarp();
+  if (cs > 1) cluster_sync_all();   // no CTA leaves while another reads its shared memory
+}
+
+template <int D>
+cudaError_t launch_small_t(const CUtensorMap* maps, const ImpSmallParams& p, cudaStream_t stream) {
+  using S = SmallCfg<D>;
+  auto kern = imp_small_kernel<D>;
+  static bool attr_set[128] = {};   // per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 128) attr_set[dev] = true;
+  }
+  return launch_clusters(kern, p.G, p.H, kSmallThreads, size_t(S::SMEM_BYTES), stream, maps[0],
+                         maps[1], maps[2], maps[3], p);
+}
+
+template <int D>
+int small_active_clusters_t(int H, cudaError_t* err) {
+  using S = SmallCfg<D>;
+  auto kern = imp_small_kernel<D>;
+  *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
+  if (*err != cudaSuccess) return 0;
+  *err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (*err != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(H);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(unsigned(H));
+  cfg.blockDim = dim3(unsigned(kSmallThreads));
+  cfg.dynamicSmemBytes = size_t(S::SMEM_BYTES);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int active = 0;
+  *err = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+  return *err == cudaSuccess ? active : 0;
+}
+
+}  // namespace
+
+cudaError_t launch_imp_small(int head_dim, const CUtensorMap* maps, const ImpSmallParams& p,
+                             cudaStream_t stream) {
+  switch (head_dim) {
+    case 64: return launch_small_t<64>(maps, p, stream);
+    case 80: return launch_small_t<80>(maps, p, stream);
+    case 96: return launch_small_t<96>(maps, p, stream);
+    case 112: return launch_small_t<112>(maps, p, stream);
+    case 128: return launch_small_t<128>(maps, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Whether a cluster of H CTAs of the one-launch kernel fits on the device
+// (cached per device, head_dim and H).
+bool imp_small_fits(int head_dim, int H, cudaError_t* err) {
+  *err = cudaSuccess;
+  if (H < 1 || H > kMaxClusterCtas) return false;
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return false;
+  static signed char cache[128][5][kMaxClusterCtas + 1] = {};   // 0 unknown, 1 no, 2 yes
+  const int di = (head_dim - 64) / 16;
+  if (di < 0 || di > 4 || (head_dim % 16) != 0) return false;
+  const bool cacheable = dev >= 0 && dev < 128;
+  if (cacheable && cache[dev][di][H] != 0) return cache[dev][di][H] == 2;
+  int active = 0;
+  switch (head_dim) {
+    case 64: active = small_active_clusters_t<64>(H, err); break;
+    case 80: active = small_active_clusters_t<80>(H, err); break;
+    case 96: active = small_active_clusters_t<96>(H, err); break;
+    case 112: active = small_active_clusters_t<112>(H, err); break;
+    default: active = small_active_clusters_t<128>(H, err); break;
+  }
+  if (*err != cudaSuccess) {
+    (void)cudaGetLastError();
+    *err = cudaSuccess;   // not a failure of the call: the scheduled path takes the problem
+    active = 0;
+  }
+  if (cacheable) cache[dev][di][H] = active >= 1 ? 2 : 1;
+  return active >= 1;
+}
+
+}  // namespace tsel

@@ -13,6 +13,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "launch_util.cuh"
 
 namespace tsel {
 // Attended-pair bound above which the row-LSE pass fixes its row reference
@@ -25,6 +26,9 @@ cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int
                             cudaStream_t stream);
 cudaError_t launch_imp_pass(int pass, int head_dim, bool fp8, const CUtensorMap* maps,
                             const ImpPassParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_imp_small(int head_dim, const CUtensorMap* maps, const ImpSmallParams& p,
+                             cudaStream_t stream);
+bool imp_small_fits(int head_dim, int H, cudaError_t* err);
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
                               const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
                               int max_qtiles, int H, const uint32_t* status, int32_t* hist,
@@ -199,6 +203,48 @@ size_t tsel_gather_compact_workspace_size(void) { return kWsHeaderBytes; }
 namespace {
 
 // Histograms the column pass builds for the top-B of the fused path.
+// TMA maps of Q and K: bf16 as 64-column boxes (128-byte swizzle) plus, when
+// head_dim is not a multiple of 64, 16-column boxes (32-byte swizzle); E4M3 as
+// one 3-D map each.
+tsel_status make_qk_maps(const void* q, const void* k, int64_t q_row_stride, int64_t k_row_stride,
+                         bool fp8, int head_dim, int64_t hd, int64_t kvd, int num_heads,
+                         int num_kv_heads, int total_q, int total_k, CUtensorMap* qm64,
+                         CUtensorMap* qm16, CUtensorMap* km64, CUtensorMap* km16) {
+  const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw32 = CU_TENSOR_MAP_SWIZZLE_32B;
+  const bool tail = !fp8 && (head_dim % 64) != 0;
+  if (fp8) {
+    if (!make_map_fp8(qm64, q, head_dim, num_heads, total_q, q_row_stride) ||
+        !make_map_fp8(km64, k, head_dim, num_kv_heads, total_k, k_row_stride))
+      return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E4M3 maps)");
+  } else if (!make_map(qm64, q, hd, total_q, q_row_stride * 2, 64, sw128) ||
+             !make_map(km64, k, kvd, total_k, k_row_stride * 2, 64, sw128)) {
+    return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (64-wide box)");
+  }
+  if (tail) {
+    if (!make_map(qm16, q, hd, total_q, q_row_stride * 2, 16, sw32) ||
+        !make_map(km16, k, kvd, total_k, k_row_stride * 2, 16, sw32))
+      return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (16-wide box)");
+  } else {
+    *qm16 = *qm64;
+    *km16 = *km64;
+  }
+  return TSEL_OK;
+}
+
+// The one-launch path's shape rule (tsel_importance's header comment).
+bool one_launch_eligible(unsigned flags, int num_seg, int total_q, int total_k, int max_q,
+                         int max_k, int num_heads, int head_dim, int sms, cudaError_t* err) {
+  *err = cudaSuccess;
+  const unsigned excl = TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2 |
+                        TSEL_SEL_STAGE_TOPK | TSEL_IMP_FP8_E4M3 | TSEL_IMP_LSE_PROVIDED |
+                        TSEL_IMP_ROWREF_FIXED | TSEL_IMP_ROWREF_MOVING | TSEL_IMP_TWO_PASS;
+  if ((flags & excl) != 0 || num_seg < 1 || total_q < 1 || total_k < 1 || max_q > kPairRows ||
+      max_k > kPairRows || num_heads < 1 || num_heads > kMaxClusterCtas ||
+      int64_t(num_seg) * num_heads > sms)
+    return false;
+  return imp_small_fits(head_dim, num_heads, err);
+}
+
 struct SelHist {
   const int32_t* req_off;   // [R+1]
   int R;
@@ -221,7 +267,8 @@ tsel_status importance_impl(const void* q, int64_t q_row_stride, const void* k,
   if (!(head_dim == 64 || head_dim == 80 || head_dim == 96 || head_dim == 112 || head_dim == 128))
     return fail(TSEL_ERR_UNSUPPORTED, "head_dim=%d (supported: 64, 80, 96, 112, 128)", head_dim);
   if ((flags & ~(TSEL_IMP_LSE_PROVIDED | TSEL_IMP_FP8_E4M3 | TSEL_IMP_SCORE_SUM |
-                 TSEL_IMP_ROWREF_FIXED | TSEL_IMP_ROWREF_MOVING | TSEL_IMP_TEST_STALL |
+                 TSEL_IMP_ROWREF_FIXED | TSEL_IMP_ROWREF_MOVING | TSEL_IMP_TWO_PASS |
+                 TSEL_IMP_TEST_STALL |
                  TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2 |
                  (sel.req_off != nullptr ? TSEL_SEL_STAGE_TOPK : 0u))) != 0)
     return fail(TSEL_ERR_UNSUPPORTED, "flags=0x%x", flags);
@@ -263,6 +310,39 @@ tsel_status importance_impl(const void* q, int64_t q_row_stride, const void* k,
   if (sm_count(&sms) != 0) return fail(TSEL_ERR_CUDA, "cannot query the SM count");
   const int hgroups = pass2_head_groups(num_heads, num_seg, total_k, sms);
 
+  // Small problems: both passes in one launch (imp_small.cu), no schedule.
+  if (sel.hist == nullptr) {
+    cudaError_t fe = cudaSuccess;
+    if (one_launch_eligible(flags, num_seg, total_q, total_k, max_seqlen_q, max_seqlen_k,
+                            num_heads, head_dim, sms, &fe)) {
+      CUtensorMap m[4];
+      const tsel_status ms = make_qk_maps(q, k, q_row_stride, k_row_stride, false, head_dim, hd,
+                                          kvd, num_heads, num_kv_heads, total_q, total_k, &m[0],
+                                          &m[1], &m[2], &m[3]);
+      if (ms != TSEL_OK) return ms;
+      ImpSmallParams sp{};
+      sp.cu_q = cu_seqlens_q;
+      sp.cu_k = cu_seqlens_k;
+      sp.G = num_seg;
+      sp.Tq = total_q;
+      sp.Tk = total_k;
+      sp.max_q = max_seqlen_q;
+      sp.max_k = max_seqlen_k;
+      sp.H = num_heads;
+      sp.Hkv = num_kv_heads;
+      const float sc = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(float(head_dim));
+      sp.c = sc * 1.4426950408889634f;
+      sp.lse_out = lse;
+      sp.scores = scores;
+      sp.status = &hdr->status;
+      sp.timeout_ns = (flags & TSEL_IMP_TEST_STALL) ? 50ull * 1000000ull : wait_timeout_ns();
+      sp.stall = (flags & TSEL_IMP_TEST_STALL) ? 1 : 0;
+      sp.sum_norm = (flags & TSEL_IMP_SCORE_SUM) ? 1 : 0;
+      e = launch_imp_small(head_dim, m, sp, stream);
+      return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "one-launch importance");
+    }
+  }
+
   if (stages & TSEL_IMP_STAGE_PREP) {
     e = launch_imp_prep(cu_seqlens_q, cu_seqlens_k, num_seg, total_q, total_k, max_seqlen_q,
                         max_seqlen_k, num_heads, hgroups, ws, L, sel.hist ? sel.req_off : nullptr,
@@ -281,23 +361,11 @@ tsel_status importance_impl(const void* q, int64_t q_row_stride, const void* k,
   if (!(stages & (TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2))) return TSEL_OK;
 
   CUtensorMap qm64, qm16, km64, km16;
-  const CUtensorMapSwizzle sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw32 = CU_TENSOR_MAP_SWIZZLE_32B;
-  const bool tail = !fp8 && (head_dim % 64) != 0;
-  if (fp8) {
-    if (!make_map_fp8(&qm64, q, head_dim, num_heads, total_q, q_row_stride) ||
-        !make_map_fp8(&km64, k, head_dim, num_kv_heads, total_k, k_row_stride))
-      return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (E4M3 maps)");
-  } else if (!make_map(&qm64, q, hd, total_q, q_row_stride * 2, 64, sw128) ||
-             !make_map(&km64, k, kvd, total_k, k_row_stride * 2, 64, sw128)) {
-    return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (64-wide box)");
-  }
-  if (tail) {
-    if (!make_map(&qm16, q, hd, total_q, q_row_stride * 2, 16, sw32) ||
-        !make_map(&km16, k, kvd, total_k, k_row_stride * 2, 16, sw32))
-      return fail(TSEL_ERR_CUDA, "cuTensorMapEncodeTiled failed (16-wide box)");
-  } else {
-    qm16 = qm64;
-    km16 = km64;
+  {
+    const tsel_status ms = make_qk_maps(q, k, q_row_stride, k_row_stride, fp8, head_dim, hd, kvd,
+                                        num_heads, num_kv_heads, total_q, total_k, &qm64, &qm16,
+                                        &km64, &km16);
+    if (ms != TSEL_OK) return ms;
   }
   ImpPassParams p{};
   p.cu_q = cu_seqlens_q;
@@ -421,6 +489,18 @@ tsel_status tsel_importance(const void* q, int64_t q_row_stride, const void* k,
                          total_q, total_k, max_seqlen_q, max_seqlen_k, num_heads, num_kv_heads,
                          head_dim, softmax_scale, flags, lse, scores, workspace, workspace_bytes,
                          need, none, static_cast<cudaStream_t>(stream_));
+}
+
+int tsel_importance_one_launch(int num_seg, int total_q, int total_k, int max_seqlen_q,
+                               int max_seqlen_k, int num_heads, int head_dim, unsigned flags) {
+  if (!(head_dim == 64 || head_dim == 80 || head_dim == 96 || head_dim == 112 || head_dim == 128))
+    return 0;
+  int sms = 0;
+  if (sm_count(&sms) != 0) return -1;
+  cudaError_t e = cudaSuccess;
+  const bool one = one_launch_eligible(flags, num_seg, total_q, total_k, max_seqlen_q, max_seqlen_k,
+                                       num_heads, head_dim, sms, &e);
+  return e != cudaSuccess ? -1 : (one ? 1 : 0);
 }
 
 size_t tsel_score_select_workspace_size(int num_seg, int total_q, int total_k, int num_heads,

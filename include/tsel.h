@@ -92,9 +92,12 @@ typedef enum tsel_status {
 #define TSEL_IMP_ROWREF_MOVING 0x20u /*   or moving reference, one launch; neither = chosen
                                         by size (fixed from 2^28 = H*total_q*max_seqlen_k
                                         attended pairs). Same results up to fp32 rounding. */
+#define TSEL_IMP_TWO_PASS     0x40u  /* always the scheduled two-pass launches, also for the
+                                        small problems the one-launch path would take */
 #define TSEL_IMP_TEST_STALL   0x10000u /* test hook for failure detection: the pass kernels'
                                           scheduler publishes no work, every bounded wait
-                                          runs out after ~50 ms and TSEL_DEV_TIMEOUT is set;
+                                          runs out after ~50 ms and TSEL_DEV_TIMEOUT is set
+                                          (the one-launch path issues no loads instead);
                                           no copy or MMA is in flight, the context stays
                                           usable. Scores are not written. */
 #define TSEL_IMP_STAGE_PREP   0x100u /* run only the listed stages (none listed = all): */
@@ -137,8 +140,8 @@ TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int tot
  * num_heads    H in [1, 256]; num_kv_heads divides it.
  * head_dim     64, 80, 96, 112 or 128 (else TSEL_ERR_UNSUPPORTED).
  * softmax_scale  <= 0 selects 1/sqrt(head_dim).
- * flags        0, TSEL_IMP_LSE_PROVIDED, TSEL_IMP_FP8_E4M3, TSEL_IMP_SCORE_SUM and/or
- *              TSEL_IMP_STAGE_* bits.
+ * flags        0, TSEL_IMP_LSE_PROVIDED, TSEL_IMP_FP8_E4M3, TSEL_IMP_SCORE_SUM,
+ *              TSEL_IMP_TWO_PASS and/or TSEL_IMP_STAGE_* bits.
  *              With TSEL_IMP_FP8_E4M3, q and k are E4M3 [rows, heads, head_dim] (one byte
  *              per element, row strides in bytes, multiples of 16) and softmax_scale is
  *              the full factor applied to the fp8 dot products (scale x q_scale x
@@ -153,7 +156,15 @@ TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int tot
  *
  * Kernels, in order on `stream` (no host synchronisation; capturable): the
  * schedule kernel, the row-LSE pass, its redo launch (large problems only),
- * the column pass. On large problems (or with TSEL_IMP_ROWREF_FIXED) the
+ * the column pass. Small problems take one launch instead: when every
+ * segment has at most 256 query rows and 256 keys (max_seqlen_q and
+ * max_seqlen_k <= 256), bf16 inputs, num_heads <= 16, num_seg * num_heads no
+ * more than the GPU's SMs, no LSE_PROVIDED, ROWREF or STAGE bits, and not
+ * TSEL_IMP_TWO_PASS, one CTA per (segment, head) computes both passes from
+ * TMEM (each row's reference follows its max) and the heads of a segment add
+ * their per-key sums over a thread-block cluster in head order. Both forms
+ * give the same scores up to fp32 rounding, each deterministically.
+ * On large problems (or with TSEL_IMP_ROWREF_FIXED) the
  * row-LSE pass fixes each row's reference max on its first 64 keys; a query
  * pair with a row whose sum then leaves the fp32 range (logits more than ~88
  * above that maximum) is redone by the redo launch with a moving reference,
@@ -169,6 +180,15 @@ TSEL_API tsel_status tsel_importance(const void* q, int64_t q_row_stride,
                             float softmax_scale, unsigned flags,
                             float* lse, float* scores,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Whether tsel_importance with these sizes and flags takes the one-launch path
+ * for small problems (1) or the scheduled two-pass launches (0); -1 on a CUDA
+ * error (queried on the current device). Host-side only: enqueues nothing.
+ */
+TSEL_API int tsel_importance_one_launch(int num_seg, int total_q, int total_k,
+                                        int max_seqlen_q, int max_seqlen_k, int num_heads,
+                                        int head_dim, unsigned flags);
 
 /*
  * Same scores as tsel_importance, for callers that cannot allocate device

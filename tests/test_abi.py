@@ -101,7 +101,7 @@ def test_importance_host_checks_fail_before_any_cuda_call(lib):
     assert _call_importance(lib, ws=128) == 3               # workspace misaligned
     assert _call_importance(lib, wsb=64) == 3               # workspace too small
     assert _call_importance(lib, cuq=0) == 1                # null cu_seqlens
-    assert _call_importance(lib, flags=0x40) == 2           # unknown flag
+    assert _call_importance(lib, flags=0x80) == 2           # unknown flag
     assert _call_importance(lib, flags=0x8 | 0x20) == 1     # fixed and moving reference
     assert _call_importance(lib, flags=0x2) == 1            # E4M3 inputs need softmax_scale
     assert _call_importance(lib, flags=0x2, scale=0.5, qs=4 * 64 + 4) == 1   # E4M3 row stride, 16-byte rule

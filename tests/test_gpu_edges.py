@@ -357,13 +357,16 @@ def test_full_selection_bit_exact_on_mid_size(tsel):
 
 # ---------------------------------------------------------------- device checks
 
-def test_malformed_cu_seqlens_sets_status(tsel):
+@pytest.mark.parametrize("two_pass", [False, True])
+def test_malformed_cu_seqlens_sets_status(tsel, two_pass):
+    # small enough for the one-launch path; TSEL_IMP_TWO_PASS checks the schedule kernel's test
+    flags = tsel.TSEL_IMP_TWO_PASS if two_pass else 0
     q = torch.zeros((10, 2, 64), dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(tsel.tsel_importance_workspace_size(2, 10, 10, 2), dtype=torch.uint8, device="cuda")
     for cu in ([0, 7, 5], [0, 5, 9], [1, 5, 10], [0, 9, 10]):
         tsel.tsel_clear_device_status(ws)
         # [0, 9, 10] violates max_seqlen = 8
-        tsel.tsel_importance(q, q, i32(cu), i32([0, 5, 10]), 8, 8, workspace=ws)
+        tsel.tsel_importance(q, q, i32(cu), i32([0, 5, 10]), 8, 8, flags=flags, workspace=ws)
         assert tsel.tsel_read_device_status(ws) & tsel.TSEL_DEV_SEQLENS, cu
 
 
@@ -436,13 +439,15 @@ def test_bounded_waits_report_timeout_and_context_survives(tsel):
     """The test hook makes the pass kernels' scheduler publish nothing: every
     waiting role gives up after its ~50 ms limit, sets TSEL_DEV_TIMEOUT and
     exits with no copy or MMA in flight. The next call on the same context
-    works and matches the oracle."""
+    works and matches the oracle. (TSEL_IMP_TWO_PASS: the scheduled passes;
+    the one-launch kernel's form of the test is in test_gpu_one_launch.)"""
     w = W.make("six_views_1536")
     q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
     cq, ck = i32(w.cu_seqlens_q), i32(w.cu_seqlens_k)
     ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
                      dtype=torch.uint8, device="cuda")
-    tsel.tsel_importance(q, k, cq, ck, 256, 256, flags=tsel.TSEL_IMP_TEST_STALL, workspace=ws)
+    tsel.tsel_importance(q, k, cq, ck, 256, 256,
+                         flags=tsel.TSEL_IMP_TEST_STALL | tsel.TSEL_IMP_TWO_PASS, workspace=ws)
     bits = tsel.tsel_read_device_status(ws)
     assert bits & tsel.TSEL_DEV_TIMEOUT
     tsel.tsel_clear_device_status(ws)

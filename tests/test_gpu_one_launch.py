@@ -1,0 +1,169 @@
+"""The one-launch importance path for small problems (every segment at most
+256 query rows and 256 keys, bf16, at most 16 heads): parity with the fp64
+oracle and with the scheduled two-pass launches on the same inputs, ragged and
+empty segments, every head_dim and GQA ratio, determinism, the SUM
+normalisation, its bounded waits, and which inputs take it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_util import REL_TOL, bits_to_bf16, i32, max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+# The two paths compute the same fp32 quantities in different orders (row
+# reference per 64 keys vs per segment, the head sum over a cluster vs head
+# groups); both sit ~1e-6 from the oracle, so they agree far inside REL_TOL.
+PATH_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def tsel():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attention_score_vision_gb300 as t
+    t.build()
+    t.load_library()
+    return t
+
+
+def _one(tsel, w, flags=0):
+    return tsel.tsel_importance_one_launch(w.num_seg, w.total_q, w.total_k, max(w.max_seqlen_q, 1),
+                                           max(w.max_seqlen_k, 1), w.num_heads, w.head_dim, flags)
+
+
+def _run(tsel, w, flags=0, fill=None):
+    q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
+                     dtype=torch.uint8, device="cuda")
+    sc = torch.empty(w.total_k, device="cuda")
+    lse = torch.empty((w.num_heads, w.total_q), device="cuda")
+    if fill is not None:
+        sc.fill_(fill)
+        lse.fill_(fill)
+    tsel.tsel_importance(q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), max(w.max_seqlen_q, 1),
+                         max(w.max_seqlen_k, 1), flags=flags, lse=lse, scores=sc, workspace=ws)
+    st = tsel.tsel_read_device_status(ws)
+    return sc.cpu().numpy(), lse.cpu().numpy(), st
+
+
+def _check_both_paths(tsel, w, norm="mean"):
+    extra = tsel.TSEL_IMP_SCORE_SUM if norm == "sum" else 0
+    assert _one(tsel, w, extra) == 1
+    assert _one(tsel, w, extra | tsel.TSEL_IMP_TWO_PASS) == 0
+    s1, l1, st1 = _run(tsel, w, extra)
+    s2, l2, st2 = _run(tsel, w, extra | tsel.TSEL_IMP_TWO_PASS)
+    assert st1 == 0 and st2 == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k, norm=norm)
+    assert max_rel_err(s1, s_ref) <= REL_TOL
+    np.testing.assert_allclose(l1, lse_ref, rtol=1e-5, atol=1e-4)
+    assert max_rel_err(s1, s2.astype(np.float64)) <= PATH_TOL
+    np.testing.assert_allclose(l1, l2, rtol=1e-5, atol=1e-5)
+    return s1
+
+
+@pytest.mark.parametrize("d", [64, 80, 96, 112, 128])
+@pytest.mark.parametrize("H,Hkv", [(1, 1), (4, 4), (4, 2), (3, 1), (12, 4), (16, 16), (16, 8)])
+def test_head_dims_gqa_ragged(tsel, d, H, Hkv):
+    Lq = [1, 127, 128, 129, 256]
+    Lk = [256, 1, 129, 128, 64]
+    w = W.make_segments(Lq, Lk, H, Hkv, d, seed=900 + d + 7 * H + Hkv,
+                        sink_counts=[3, 0, 2, 1, 4], hidden_dim=64)
+    _check_both_paths(tsel, w)
+
+
+def test_empty_segments_and_segments_without_keys(tsel):
+    # no queries -> scores 0; no keys -> nothing scored and LSE -inf
+    w = W.make_segments([0, 5, 256, 0, 3, 40], [4, 0, 256, 7, 0, 1], 8, 4, 80, seed=931,
+                        sink_counts=[0, 0, 3, 1, 0, 0], hidden_dim=64)
+    s = _check_both_paths(tsel, w)
+    assert np.all(s[0:4] == 0.0) and np.all(s[260:267] == 0.0)
+    _, lse, _ = _run(tsel, w)
+    assert np.all(np.isneginf(lse[:, 0:5])) and np.all(np.isneginf(lse[:, 261:264]))
+
+
+def test_sum_normalisation(tsel):
+    w = W.make_segments([200, 31], [256, 97], 16, 4, 128, seed=932, sink_counts=[4, 1], hidden_dim=64)
+    _check_both_paths(tsel, w, norm="sum")
+
+
+@pytest.mark.parametrize("name", ["single_image_256", "six_views_1536"])
+def test_workloads_take_one_launch_and_are_deterministic(tsel, name):
+    w = W.make(name)
+    assert _one(tsel, w) == 1
+    s = _check_both_paths(tsel, w)
+    for _ in range(3):
+        s_again, _, st = _run(tsel, w)
+        assert st == 0
+        assert np.array_equal(s_again.view(np.uint32), s.view(np.uint32))
+
+
+def test_which_inputs_take_one_launch(tsel):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ok = dict(num_seg=6, total_q=1536, total_k=1536, max_seqlen_q=256, max_seqlen_k=256,
+              num_heads=16, head_dim=80)
+    assert tsel.tsel_importance_one_launch(**ok) == 1
+
+    def q(**kw):
+        a = dict(ok)
+        flags = kw.pop("flags", 0)
+        a.update(kw)
+        return tsel.tsel_importance_one_launch(**a, flags=flags)
+
+    assert q(max_seqlen_q=257) == 0
+    assert q(max_seqlen_k=257) == 0
+    assert q(num_heads=17) == 0
+    assert q(num_seg=sms // 16 + 1) == 0          # more CTAs than SMs
+    assert q(head_dim=72) == 0
+    assert q(total_q=0) == 0 and q(total_k=0) == 0
+    for f in ("TSEL_IMP_TWO_PASS", "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_ROWREF_FIXED",
+              "TSEL_IMP_ROWREF_MOVING", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS2"):
+        assert q(flags=getattr(tsel, f)) == 0, f
+    assert q(flags=tsel.TSEL_IMP_SCORE_SUM) == 1
+    assert q(num_heads=1, head_dim=128, num_seg=1) == 1
+
+
+def test_bounded_waits_run_out_in_one_launch(tsel):
+    """With the test hook the one-launch kernel issues no loads: its MMA thread
+    gives up after ~50 ms, sets TSEL_DEV_TIMEOUT, the epilogue warps see the
+    abort and every CTA still passes its barriers and exits with nothing in
+    flight; no score or LSE is written. The next call works."""
+    w = W.make("six_views_1536")
+    assert _one(tsel, w, tsel.TSEL_IMP_TEST_STALL) == 1
+    s, lse, st = _run(tsel, w, tsel.TSEL_IMP_TEST_STALL, fill=7.0)
+    assert st & tsel.TSEL_DEV_TIMEOUT
+    assert np.all(s == 7.0) and np.all(lse == 7.0)
+    s, _, st = _run(tsel, w)
+    assert st == 0
+    _, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+
+
+def test_malformed_cu_seqlens_in_one_launch(tsel):
+    q = torch.zeros((10, 2, 64), dtype=torch.bfloat16, device="cuda")
+    assert tsel.tsel_importance_one_launch(2, 10, 10, 8, 8, 2, 64) == 1
+    ws = torch.zeros(tsel.tsel_importance_workspace_size(2, 10, 10, 2), dtype=torch.uint8, device="cuda")
+    sc = torch.full((10,), 7.0, device="cuda")
+    for cu in ([0, 7, 5], [0, 5, 9], [1, 5, 10], [0, 9, 10]):
+        tsel.tsel_clear_device_status(ws)
+        tsel.tsel_importance(q, q, i32(cu), i32([0, 5, 10]), 8, 8, scores=sc, workspace=ws)
+        assert tsel.tsel_read_device_status(ws) & tsel.TSEL_DEV_SEQLENS, cu
+        assert torch.all(sc == 7.0)   # nothing is computed from malformed metadata
+
+
+def test_large_logit_gaps_follow_the_row_max(tsel):
+    """Keys whose logits stand ~128 nats above the rest of their row (past the
+    first 64 keys): the one-launch kernel's row reference follows the max, so
+    no term leaves the fp32 range and no redo exists to take them."""
+    d = 64
+    w = W.make_far_keys([200, 256, 129], 4, 2, d, seed=951, far_positions=[100, 400],
+                        far_value=128.0 * np.sqrt(d) / 4.0, head_signs=[1, 1, -1, -1], name="far")
+    assert _one(tsel, w) == 1
+    s, lse, st = _run(tsel, w)
+    assert st == 0
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k,
+                                       w.softmax_scale)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=2e-4)
