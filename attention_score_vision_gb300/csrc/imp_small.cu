@@ -9,17 +9,21 @@
 // (segment, head) held in TMEM at once, so one CTA does both passes:
 //
 //   1. S = Q K^T: two 128-row query tiles x two 128-key tiles, four 128x128
-//      tcgen05 accumulators (all 512 TMEM columns). Each epilogue warpgroup
-//      takes one accumulator: per query row a max-referenced exp2 sum over its
-//      128 keys (the reference follows the row max, terms stay below 2^8);
-//      the two warpgroups of a query tile merge into the row's LSE (kept as
-//      -LSE*log2 e in shared memory, written out as the natural-log LSE).
-//   2. S^T = K Q^T into the same columns, keys on the MMA M dimension: each
-//      epilogue thread owns one key and sums exp2(S*c - LSE2) over the query
-//      columns in registers; the two warpgroups of a key tile add up.
-//   3. The CTAs of one segment form a thread-block cluster, one CTA per head;
-//      after a cluster barrier each CTA adds a slice of the keys' per-head sums
-//      over the cluster's distributed shared memory in head order (a fixed
+//      tcgen05 accumulators (all 512 TMEM columns), each issued as soon as its
+//      two tiles have landed. Each epilogue warpgroup takes one accumulator:
+//      per query row a max-referenced exp2 sum over its 128 keys (the
+//      reference follows the row max, terms stay below 2^8), and hands the
+//      accumulator back once its columns are in registers; the two warpgroups
+//      of a query tile merge into the row's LSE (kept as -LSE*log2 e in shared
+//      memory, written out as the natural-log LSE).
+//   2. S^T = K Q^T into the same columns (each as soon as its columns are
+//      handed back), keys on the MMA M dimension: each epilogue thread owns
+//      one key and sums exp2(S*c - LSE2) over the query columns in registers;
+//      the two warpgroups of a key tile add up.
+//   3. The CTAs of one segment form a thread-block cluster, one CTA per head.
+//      Each CTA stores every key's sum for its head into the shared memory of
+//      the CTA that reduces that key (distributed shared memory); after one
+//      cluster barrier each CTA adds its keys' sums in head order (a fixed
 //      order: the scores are deterministic) and writes the scores.
 //
 // There is no schedule kernel (each CTA checks the cu_seqlens itself), no
@@ -31,7 +35,7 @@
 // CTA: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer (one thread),
 // warps 2-17 four epilogue warpgroups (warp w reads TMEM lanes 32*(w%4)..).
 // The dynamic shared memory is padded so that a second CTA never shares an SM
-// (each holds all of TMEM while it waits at the cluster barrier).
+// (each holds all of TMEM until its part of the cluster's work is done).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -51,11 +55,11 @@ struct SmallCfg {
   static constexpr int OFF_Q = 0;                        // two query tiles
   static constexpr int OFF_K = 2 * C::TILE_BYTES;        // two key tiles
   static constexpr int OFF_NL = 4 * C::TILE_BYTES;       // -LSE2 of the 256 query rows
-  static constexpr int OFF_PS = OFF_NL + kPair * 4;      // per-key sums of this head
-  static constexpr int OFF_CM = OFF_PS + kPair * 4;      // warpgroup exchange [2][128]
+  static constexpr int OFF_CM = OFF_NL + kPair * 4;      // warpgroup exchange [2][128]
   static constexpr int OFF_CL = OFF_CM + kPair * 4;      // warpgroup exchange [2][128]
-  static constexpr int OFF_BAR = OFF_CL + kPair * 4;     // three mbarriers
-  static constexpr int OFF_MISC = OFF_BAR + 64;
+  static constexpr int OFF_RECV = OFF_CL + kPair * 4;    // per-head sums of this CTA's keys
+  static constexpr int OFF_BAR = OFF_RECV + 2 * kPair * 4;   // 15 mbarriers
+  static constexpr int OFF_MISC = OFF_BAR + 128;
   static constexpr int USED = OFF_MISC + 64 + 1024;      // + alignment slack
   static constexpr int MIN_ONE_PER_SM = 120 * 1024;      // two of these exceed an SM
   static constexpr int SMEM_BYTES = USED > MIN_ONE_PER_SM ? USED : MIN_ONE_PER_SM;
@@ -65,13 +69,23 @@ struct SmallCfg {
 // Row max/sum of one 128-column accumulator piece (phase 1). `valid` columns
 // lie inside the segment (> 0); m is the row's reference for S*c, l the sum of
 // exp2(S*c - m) before the accumulators acc.
+// The accumulator goes back (`rel`, one arrival per warp) as soon as its last
+// columns are in registers, so S^T can be computed into it meanwhile.
+__device__ __forceinline__ void release_acc(uint64_t* rel, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  mbar_arrive_lane0(rel, lane);
+}
+
 __device__ __forceinline__ void small_row_lse(uint32_t taddr, int valid, float c, float2 c2,
-                                              float& m, float& l, float2 (&acc)[2]) {
+                                              float& m, float& l, float2 (&acc)[2],
+                                              uint64_t* rel, int lane) {
   uint32_t r0[32], r1[32];
   tmem_ld32_async(taddr, r0);
   tmem_ld32_async(taddr + 32, r1);
   tmem_wait_ld(r0);
   tmem_wait_ld(r1);
+  if (valid <= 64) release_acc(rel, lane);
   mask_cols(r0, valid);
   mask_cols(r1, valid - 32);
   move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
@@ -83,6 +97,7 @@ __device__ __forceinline__ void small_row_lse(uint32_t taddr, int valid, float c
     tmem_ld32_async(taddr + 96, r1);
     tmem_wait_ld(r0);
     tmem_wait_ld(r1);
+    release_acc(rel, lane);
     mask_cols(r0, valid - 64);
     mask_cols(r1, valid - 96);
     move_reference(fmaxf(cols_max(r0), cols_max(r1)) * c, m, l, acc);
@@ -132,12 +147,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   uint8_t* sQ = smem + S::OFF_Q;
   uint8_t* sK = smem + S::OFF_K;
   float* sNl = reinterpret_cast<float*>(smem + S::OFF_NL);
-  float* sPs = reinterpret_cast<float*>(smem + S::OFF_PS);
   float* sCm = reinterpret_cast<float*>(smem + S::OFF_CM);
   float* sCl = reinterpret_cast<float*>(smem + S::OFF_CL);
-  uint64_t* ld_full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
-  uint64_t* mma1_done = ld_full + 1;
-  uint64_t* mma2_done = ld_full + 2;
+  float* sRecv = reinterpret_cast<float*>(smem + S::OFF_RECV);
+  uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);   // [2] query tiles
+  uint64_t* k_full = q_full + 2;       // [2] key tiles
+  uint64_t* acc1_full = k_full + 2;    // [4] S accumulators complete
+  uint64_t* acc1_free = acc1_full + 4; // [4] S accumulators read out
+  uint64_t* acc2_full = acc1_free + 4; // [4] S^T accumulators complete
+  uint64_t* mma_done = acc2_full + 4;  // every MMA complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::OFF_MISC + 4);
   int* s_bad = reinterpret_cast<int*>(smem + S::OFF_MISC + 8);
@@ -150,9 +168,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const uint64_t T = p.timeout_ns;
 
   if (threadIdx.x == 0) {
-    mbar_init(ld_full, 1);
-    mbar_init(mma1_done, 1);
-    mbar_init(mma2_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&k_full[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&acc1_full[i], 1);
+      mbar_init(&acc1_free[i], 4);   // the four warps of the reading warpgroup
+      mbar_init(&acc2_full[i], 1);
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -198,94 +223,101 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const int k0 = __ldg(p.cu_k + g), nk = __ldg(p.cu_k + g + 1) - k0;
   const int nA = int(ceil_div(nq, kTile)), nB = int(ceil_div(nk, kTile));
   const bool work = nA > 0 && nB > 0;
+  // Accumulator j holds S tile (query tile j>>1, key tile j&1), then S^T tile
+  // (key tile j>>1, query tile j&1), in TMEM columns [128 j, 128 j + 128).
+  auto exists1 = [&](int j) { return (j >> 1) < nA && (j & 1) < nB; };
+  auto exists2 = [&](int j) { return (j >> 1) < nB && (j & 1) < nA; };
+  // Keys [r * per, (r + 1) * per) are summed over the heads by CTA r.
+  const int per = (kPair + cs - 1) / cs;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      bool issued = false;
-      if (p.stall == 0) {   // the test hook publishes nothing: every wait runs out
-        if (work) {
-          mbar_arrive_expect_tx(ld_full, uint32_t((nA + nB) * C::TILE_BYTES));
-          for (int a = 0; a < nA; ++a)
-            load_tile<D, false>(sQ + a * C::TILE_BYTES, &mapQ64, &mapQ16, ld_full, h,
-                                q0 + a * kTile);
-          const int kvh = h / (p.H / p.Hkv);
-          for (int b = 0; b < nB; ++b)
-            load_tile<D, false>(sK + b * C::TILE_BYTES, &mapK64, &mapK16, ld_full, kvh,
-                                k0 + b * kTile);
-          issued = true;
-        } else {
-          mbar_arrive(ld_full);
-        }
+    if (lane == 0 && work && p.stall == 0) {   // the test hook issues nothing: waits run out
+      const int kvh = h / (p.H / p.Hkv);
+      // in the order the MMAs need them: Q0, K0, K1, Q1
+      mbar_arrive_expect_tx(&q_full[0], uint32_t(C::TILE_BYTES));
+      load_tile<D, false>(sQ, &mapQ64, &mapQ16, &q_full[0], h, q0);
+      mbar_arrive_expect_tx(&k_full[0], uint32_t(C::TILE_BYTES));
+      load_tile<D, false>(sK, &mapK64, &mapK16, &k_full[0], kvh, k0);
+      if (nB > 1) {
+        mbar_arrive_expect_tx(&k_full[1], uint32_t(C::TILE_BYTES));
+        load_tile<D, false>(sK + C::TILE_BYTES, &mapK64, &mapK16, &k_full[1], kvh, k0 + kTile);
+      }
+      if (nA > 1) {
+        mbar_arrive_expect_tx(&q_full[1], uint32_t(C::TILE_BYTES));
+        load_tile<D, false>(sQ + C::TILE_BYTES, &mapQ64, &mapQ16, &q_full[1], h, q0 + kTile);
       }
       // the copies have landed before the CTA can exit
-      if (issued) wait_drain(ld_full, 0, T);
+      wait_drain(&q_full[0], 0, T);
+      wait_drain(&k_full[0], 0, T);
+      if (nB > 1) wait_drain(&k_full[1], 0, T);
+      if (nA > 1) wait_drain(&q_full[1], 0, T);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    uint64_t* pending = nullptr;   // last commit barrier, drained before TMEM is freed
-    if (lane == 0) {
-      if (wait_bounded(ld_full, 0, abort_flag, T)) {
+    if (lane == 0 && work) {
+      bool ok = true;
+      for (int j = 0; j < 4 && ok; ++j) {
+        if (!exists1(j)) continue;
+        if (!wait_bounded(&q_full[j >> 1], 0, abort_flag, T) ||
+            !wait_bounded(&k_full[j & 1], 0, abort_flag, T)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        if (work)
-          for (int a = 0; a < nA; ++a)
-            for (int b = 0; b < nB; ++b)
-              issue_tile_mmas<D, false>(tmem + uint32_t((2 * a + b) * kTile),
-                                        sQ + a * C::TILE_BYTES, sK + b * C::TILE_BYTES);
-        mma_commit(mma1_done);
-        pending = mma1_done;
-      } else {
+        issue_tile_mmas<D, false>(tmem + uint32_t(j * kTile), sQ + (j >> 1) * C::TILE_BYTES,
+                                  sK + (j & 1) * C::TILE_BYTES);
+        mma_commit(&acc1_full[j]);
+      }
+      for (int j = 0; j < 4 && ok; ++j) {
+        if (!exists2(j)) continue;
+        if (exists1(j) && !wait_bounded(&acc1_free[j], 0, abort_flag, T)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_tile_mmas<D, false>(tmem + uint32_t(j * kTile), sK + (j >> 1) * C::TILE_BYTES,
+                                  sQ + (j & 1) * C::TILE_BYTES);
+        mma_commit(&acc2_full[j]);
+      }
+      if (!ok) {
         *abort_flag = 1;
         set_status(p.status, TSEL_DEV_TIMEOUT);
       }
+      // every MMA this thread issued has completed before TMEM is freed
+      mma_commit(mma_done);
+      wait_drain(mma_done, 0, T);
     }
-    __syncwarp();
-    // The epilogue has read every phase-1 accumulator: S^T into the same columns.
-    asm volatile("bar.sync 2, %0;" ::"n"(32 * (kEpiWarps + 1)) : "memory");
-    if (lane == 0) {
-      if (pending != nullptr && *abort_flag == 0) {
-        tc_fence_after();
-        if (work)
-          for (int b = 0; b < nB; ++b)
-            for (int a = 0; a < nA; ++a)
-              issue_tile_mmas<D, false>(tmem + uint32_t((2 * b + a) * kTile),
-                                        sK + b * C::TILE_BYTES, sQ + a * C::TILE_BYTES);
-        mma_commit(mma2_done);
-        pending = mma2_done;
-      }
-      if (pending != nullptr) wait_drain(pending, 0, T);
-    }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wg = (warp - kEpiFirstWarp) >> 2;
+    // Warpgroup j reads accumulator j in both phases.
+    const int j = (warp - kEpiFirstWarp) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const uint32_t lane_off = uint32_t(quad * 32) << 16;
+    const uint32_t taddr = tmem + (uint32_t(quad * 32) << 16) + uint32_t(j * kTile);
     const float c = p.c;
     const float2 c2 = make_float2(c, c);
     {
-      // Phase 1: warpgroup (a, b) = query tile a x key tile b.
-      const int a = wg >> 1, b = wg & 1;
+      // Phase 1: query tile a x key tile b; the two warpgroups of a query tile merge.
+      const int a = j >> 1, b = j & 1;
       float m = kNegInf, l = 0.f;
       float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      if (warp_wait(mma1_done, 0, abort_flag, T)) {
-        tc_fence_after();
-        if (work && a < nA && b < nB)
-          small_row_lse(tmem + lane_off + uint32_t((2 * a + b) * kTile), nk - b * kTile, c, c2, m,
-                        l, acc);
-      } else if (lane == 0) {
-        *abort_flag = 1;
-        set_status(p.status, TSEL_DEV_TIMEOUT);
+      if (exists1(j)) {
+        if (warp_wait(&acc1_full[j], 0, abort_flag, T)) {
+          tc_fence_after();
+          small_row_lse(taddr, nk - b * kTile, c, c2, m, l, acc, &acc1_free[j], lane);
+        } else if (lane == 0) {
+          *abort_flag = 1;
+          set_status(p.status, TSEL_DEV_TIMEOUT);
+        }
       }
-      tc_fence_before();
       const float2 s2 = __fadd2_rn(acc[0], acc[1]);
       const float L = l + (s2.x + s2.y);
       if (b == 1) {
         sCm[a * kTile + row] = m;
         sCl[a * kTile + row] = L;
       }
-      asm volatile("bar.sync 2, %0;" ::"n"(32 * (kEpiWarps + 1)) : "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
       if (b == 0) {
         const float m1 = sCm[a * kTile + row], l1 = sCl[a * kTile + row];
         const float M = fmaxf(m, m1);
@@ -301,24 +333,31 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");   // sNl complete
     }
     {
-      // Phase 2: warpgroup (b, a) = key tile b x query tile a.
-      const int b = wg >> 1, a = wg & 1;
+      // Phase 2: key tile b x query tile a; the two warpgroups of a key tile add up
+      // and send each key's sum for this head to the CTA that reduces it.
+      const int b = j >> 1, a = j & 1;
       float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      if (warp_wait(mma2_done, 0, abort_flag, T)) {
-        tc_fence_after();
-        if (work && b < nB && a < nA)
-          small_col_sum(tmem + lane_off + uint32_t((2 * b + a) * kTile), nq - a * kTile,
-                        reinterpret_cast<const float4*>(sNl + a * kTile), c2, acc);
-      } else if (lane == 0) {
-        *abort_flag = 1;
-        set_status(p.status, TSEL_DEV_TIMEOUT);
+      if (exists2(j)) {
+        if (warp_wait(&acc2_full[j], 0, abort_flag, T)) {
+          tc_fence_after();
+          small_col_sum(taddr, nq - a * kTile, reinterpret_cast<const float4*>(sNl + a * kTile),
+                        c2, acc);
+        } else if (lane == 0) {
+          *abort_flag = 1;
+          set_status(p.status, TSEL_DEV_TIMEOUT);
+        }
       }
-      tc_fence_before();
       const float2 s2 = __fadd2_rn(acc[0], acc[1]);
       const float part = s2.x + s2.y;
       if (a == 1) sCm[b * kTile + row] = part;
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-      if (a == 0) sPs[b * kTile + row] = part + sCm[b * kTile + row];
+      const int key = b * kTile + row;
+      if (a == 0 && key < nk) {
+        const int r = key / per;
+        float* dst = sRecv + h * per + (key - r * per);
+        if (cs > 1) dst = cluster.map_shared_rank(dst, r);
+        *dst = part + sCm[b * kTile + row];
+      }
     }
   }
 
@@ -328,20 +367,19 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
 
-  // Head sum over the cluster, in head order; CTA h reduces keys [h*per, (h+1)*per).
+  // Head sum in head order: every CTA has sent its sums, CTA h adds those of
+  // keys [h * per, (h + 1) * per). No shared memory of another CTA is touched
+  // after this barrier.
   if (cs > 1) cluster_sync_all();
-  const int per = (kPair + cs - 1) / cs;
   if (int(threadIdx.x) < per && *abort_flag == 0) {
     const int key = h * per + int(threadIdx.x);
     if (key < nk) {
       float sum = 0.f;
-      for (int r = 0; r < cs; ++r) sum += cs > 1 ? *cluster.map_shared_rank(sPs + key, r) : sPs[key];
+      for (int r = 0; r < cs; ++r) sum += sRecv[r * per + int(threadIdx.x)];
       const float rows = p.sum_norm ? 1.f : float(p.H * nq);
       p.scores[k0 + key] = nq > 0 ? sum / rows : 0.f;
     }
   }
-  __syncwarp();
-  if (cs > 1) cluster_sync_all();   // no CTA leaves while another reads its shared memory
 }
 
 template <int D>
