@@ -534,8 +534,9 @@ def tsel_importance_redo_pairs(workspace: torch.Tensor, stream=None) -> int:
 def tsel_select_path_counts(workspace: torch.Tensor, stream=None) -> list:
     """Top-B requests per threshold path on `workspace` since it was zeroed:
     [radix rounds, histogram + rounds, histogram + candidates, candidates
-    rejected] (synchronises the stream)."""
-    c = (ctypes.c_int32 * 4)()
+    rejected, ranked in the one-launch importance kernel] (synchronises the
+    stream)."""
+    c = (ctypes.c_int32 * 5)()
     _check(load_library().tsel_select_path_counts(_ptr(workspace), c,
                                                   _stream(stream, workspace.device)))
     return [int(x) for x in c]

@@ -26,8 +26,8 @@ struct WsHeader {
   uint32_t pad4[31];
   int32_t hist_ok;        // 1: the request offsets are valid and the score histograms are built
   uint32_t pad5[31];
-  int32_t sel_paths[4];   // top-B requests per threshold path (tsel_select_path_counts)
-  uint32_t pad6[28];
+  int32_t sel_paths[5];   // top-B requests per threshold path (tsel_select_path_counts)
+  uint32_t pad6[27];
 };
 static_assert(sizeof(WsHeader) <= kWsHeaderBytes, "header too large");
 
@@ -152,6 +152,13 @@ struct ImpSmallParams {
   uint64_t timeout_ns;
   int stall;             // test hook: no loads are issued, every wait runs out
   int sum_norm;          // 1: total attention received (no division by H*Nq)
+  // top-B of a one-segment, one-request problem in the same launch (select = 1)
+  int select;
+  const int32_t* req_off;   // [2] the request's token range
+  const int32_t* keep;      // [1] its budget
+  int total_keep;           // or TSEL_KEEP_FROM_DEVICE
+  int32_t* keep_idx;
+  int32_t* cu_keep;         // [2]
 };
 
 struct ImpPassParams {

@@ -58,7 +58,9 @@ struct SmallCfg {
   static constexpr int OFF_CM = OFF_NL + kPair * 4;      // warpgroup exchange [2][128]
   static constexpr int OFF_CL = OFF_CM + kPair * 4;      // warpgroup exchange [2][128]
   static constexpr int OFF_RECV = OFF_CL + kPair * 4;    // per-head sums of this CTA's keys
-  static constexpr int OFF_BAR = OFF_RECV + 2 * kPair * 4;   // 15 mbarriers
+  static constexpr int OFF_SEL = OFF_RECV + kMaxClusterCtas * kPair * 4;   // top-B scratch [64]
+  static constexpr int OFF_BINS = OFF_SEL + 256;         // top-B histograms [4][256]
+  static constexpr int OFF_BAR = OFF_BINS + 4 * kPair * 4;   // 15 mbarriers
   static constexpr int OFF_MISC = OFF_BAR + 128;
   static constexpr int USED = OFF_MISC + 64 + 1024;      // + alignment slack
   static constexpr int MIN_ONE_PER_SM = 120 * 1024;      // two of these exceed an SM
@@ -126,6 +128,83 @@ __device__ __forceinline__ void small_col_sum(uint32_t taddr, int vq, const floa
     tmem_wait_ld(r1);
     column_sum_chunk(r0, nl + 16, c2, acc);
     if (vq > 96) column_sum_chunk(r1, nl + 24, c2, acc);
+  }
+}
+
+// Top-B of the one request of a one-segment problem, in CTA 0 of its cluster
+// (the pooled global top-B of the dynamic vision-token compression article,
+// section 3.2; one image, so its pool is that image): every key's score from
+// the per-head sums (head order); then each key's rank among the request's
+// keys under the order (score key descending, token index ascending) — the
+// count of larger 64-bit keys (order-preserving score bits, then 255 minus
+// the token index), two threads per key, 128 keys each — and the tokens of
+// rank below B in token order. The request checks, status bits and outputs
+// are those of the top-B kernel (topk.cu) for the same request. sRecv
+// [cs][256] per-head sums; sKey [256]; scratch: 64-bit keys [256] + ranks
+// [2][256]; sW [64] (sW[8..10]: the request's offsets and budget, read at
+// kernel start).
+__device__ __forceinline__ void small_select(const ImpSmallParams& p, int cs, int nq, int nk,
+                                             float rows, const float* sRecv, uint32_t* sKey,
+                                             int* scratch, int* sW) {
+  const int t = int(threadIdx.x);
+  const int lo = sW[8], hi = sW[9], B = sW[10];
+  bool nan_in = false;
+  if (t < nk) {   // one segment: token index = key index
+    float sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxClusterCtas; ++r)
+      if (r < cs) sum += sRecv[r * kPair + t];
+    const float sc = nq > 0 ? sum / rows : 0.f;
+    p.scores[t] = sc;
+    sKey[t] = order_key(sc);
+    nan_in = sc != sc && t >= lo && t < hi;
+  }
+  const int any_nan = __syncthreads_or(nan_in);
+  bool bad = lo < 0 || hi < lo || hi > p.Tk || B < 0 || B > hi - lo;
+  bad = bad || (p.total_keep >= 0 ? B != p.total_keep : B > p.Tk);
+  if (bad) {
+    if (t == 0) set_status(p.status, TSEL_DEV_REQUESTS);
+    return;
+  }
+  if (B > 0) {
+    uint64_t* k64 = reinterpret_cast<uint64_t*>(scratch);   // [256]
+    int* rank = scratch + 2 * kPair;                        // [2][256]
+    // Keys outside [lo, hi) are 0: no key of the request is below it. (hi <= 256)
+    if (t < kPair)
+      k64[t] = (t >= lo && t < hi) ? ((uint64_t(sKey[t]) << 8) | uint64_t(255 - t)) : 0ull;
+    __syncthreads();
+    if (t < 2 * kPair) {
+      const int i = t & (kPair - 1), half = t >> 8;
+      const uint64_t ki = k64[i];
+      const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(k64) + half * 64;
+      int rk = 0;
+#pragma unroll 16
+      for (int q = 0; q < 64; ++q) {
+        const ulonglong2 v = k2[q];
+        rk += int(v.x > ki) + int(v.y > ki);
+      }
+      rank[half * kPair + i] = rk;
+    }
+    __syncthreads();
+    if (t < kPair) {
+      // slot = kept tokens of lower index
+      const int lane = t & 31, w = t >> 5;
+      const bool kept = t >= lo && t < hi && rank[t] + rank[kPair + t] < B;
+      const unsigned mk = __ballot_sync(0xffffffffu, kept);
+      if (lane == 0) sW[w] = __popc(mk);
+      asm volatile("bar.sync 3, %0;" ::"n"(kPair) : "memory");
+      int base = 0;
+      for (int x = 0; x < w; ++x) base += sW[x];
+      if (kept) p.keep_idx[base + __popc(mk & ((1u << lane) - 1u))] = t;
+    }
+  }
+  if (t == 0) {
+    p.cu_keep[0] = 0;
+    p.cu_keep[1] = B;
+    if (B > 0) {
+      atomicAdd(&reinterpret_cast<WsHeader*>(p.status)->sel_paths[4], 1);
+      if (any_nan) set_status(p.status, TSEL_DEV_NAN);
+    }
   }
 }
 
@@ -219,6 +298,12 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, 512);
     return;
   }
+  if (p.select && h == 0 && threadIdx.x == 0) {
+    int* sW = reinterpret_cast<int*>(smem + S::OFF_SEL);
+    sW[8] = __ldg(p.req_off);        // read now: used after the cluster barrier
+    sW[9] = __ldg(p.req_off + 1);
+    sW[10] = __ldg(p.keep);
+  }
   const int q0 = __ldg(p.cu_q + g), nq = __ldg(p.cu_q + g + 1) - q0;
   const int k0 = __ldg(p.cu_k + g), nk = __ldg(p.cu_k + g + 1) - k0;
   const int nA = int(ceil_div(nq, kTile)), nB = int(ceil_div(nk, kTile));
@@ -227,8 +312,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   // (key tile j>>1, query tile j&1), in TMEM columns [128 j, 128 j + 128).
   auto exists1 = [&](int j) { return (j >> 1) < nA && (j & 1) < nB; };
   auto exists2 = [&](int j) { return (j >> 1) < nB && (j & 1) < nA; };
-  // Keys [r * per, (r + 1) * per) are summed over the heads by CTA r.
-  const int per = (kPair + cs - 1) / cs;
+  // Keys [r * per, (r + 1) * per) are summed over the heads by CTA r (all
+  // of them by CTA 0 when it also selects the request's top-B).
+  const int per = p.select ? kPair : (kPair + cs - 1) / cs;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -371,15 +457,22 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   // keys [h * per, (h + 1) * per). No shared memory of another CTA is touched
   // after this barrier.
   if (cs > 1) cluster_sync_all();
-  if (int(threadIdx.x) < per && *abort_flag == 0) {
-    const int key = h * per + int(threadIdx.x);
-    if (key < nk) {
-      float sum = 0.f;
-      for (int r = 0; r < cs; ++r) sum += sRecv[r * per + int(threadIdx.x)];
-      const float rows = p.sum_norm ? 1.f : float(p.H * nq);
-      p.scores[k0 + key] = nq > 0 ? sum / rows : 0.f;
+  if (*abort_flag != 0) return;
+  const float rows = p.sum_norm ? 1.f : float(p.H * nq);
+  if (!p.select) {
+    if (int(threadIdx.x) < per) {
+      const int key = h * per + int(threadIdx.x);
+      if (key < nk) {
+        float sum = 0.f;
+        for (int r = 0; r < cs; ++r) sum += sRecv[r * per + int(threadIdx.x)];
+        p.scores[k0 + key] = nq > 0 ? sum / rows : 0.f;
+      }
     }
+    return;
   }
+  if (h == 0)
+    small_select(p, cs, nq, nk, rows, sRecv, reinterpret_cast<uint32_t*>(sNl),
+                 reinterpret_cast<int*>(smem + S::OFF_BINS), reinterpret_cast<int*>(smem + S::OFF_SEL));
 }
 
 template <int D>

@@ -249,6 +249,13 @@ struct SelHist {
   const int32_t* req_off;   // [R+1]
   int R;
   int32_t* hist;            // R * kHistWords int32 (null: no histograms)
+  // the top-B arguments, for the one-launch kernel to select a one-segment,
+  // one-request problem itself (it then sets *selected)
+  const int32_t* keep = nullptr;
+  int total_keep = 0;
+  int32_t* keep_idx = nullptr;
+  int32_t* cu_keep = nullptr;
+  bool* selected = nullptr;
 };
 
 // Importance: the schedule kernel, the row-LSE pass (or the LSE import) and
@@ -338,6 +345,15 @@ tsel_status importance_impl(const void* q, int64_t q_row_stride, const void* k,
       sp.timeout_ns = (flags & TSEL_IMP_TEST_STALL) ? 50ull * 1000000ull : wait_timeout_ns();
       sp.stall = (flags & TSEL_IMP_TEST_STALL) ? 1 : 0;
       sp.sum_norm = (flags & TSEL_IMP_SCORE_SUM) ? 1 : 0;
+      if (sel.selected != nullptr && sel.R == 1 && num_seg == 1) {
+        sp.select = 1;
+        sp.req_off = sel.req_off;
+        sp.keep = sel.keep;
+        sp.total_keep = sel.total_keep;
+        sp.keep_idx = sel.keep_idx;
+        sp.cu_keep = sel.cu_keep;
+        *sel.selected = true;
+      }
       e = launch_imp_small(head_dim, m, sp, stream);
       return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "one-launch importance");
     }
@@ -528,6 +544,12 @@ tsel_status tsel_score_select(const void* q, int64_t q_row_stride, const void* k
   const ImpWsLayout L = imp_ws_layout(num_seg, total_q, total_k, num_heads);
   const int64_t hbytes = sel_hist_bytes(num_req);
   SelHist sel{req_tok_offsets, num_req, nullptr};
+  bool selected = false;
+  sel.keep = keep_per_req;
+  sel.total_keep = total_keep;
+  sel.keep_idx = keep_idx;
+  sel.cu_keep = cu_keep;
+  sel.selected = &selected;
   // Histograms only for requests the top-B splits over a cluster of CTAs
   // (one CTA per request runs its radix rounds without cluster barriers).
   cudaError_t ce = cudaSuccess;
@@ -541,6 +563,7 @@ tsel_status tsel_score_select(const void* q, int64_t q_row_stride, const void* k
                        head_dim, softmax_scale, flags, lse, scores, workspace, workspace_bytes,
                        need, sel, stream);
   if (st != TSEL_OK) return st;
+  if (selected) return TSEL_OK;   // the one-launch importance kernel also took the top-B
   const unsigned stage_bits = TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2 |
                               TSEL_SEL_STAGE_TOPK;
   if ((flags & stage_bits) && !(flags & TSEL_SEL_STAGE_TOPK)) return TSEL_OK;

@@ -248,7 +248,11 @@ TSEL_API size_t tsel_score_select_workspace_size(int num_seg, int total_q, int t
  * TSEL_SEL_STAGE_TOPK with the TSEL_IMP_STAGE_* bits to run the stages
  * separately (in order, on one workspace). Requests whose offsets are not
  * ordered, more than 64 requests, or scores not all written by this call's
- * column pass make the top-B run its plain radix rounds (same results).
+ * column pass make the top-B run its plain radix rounds (same results). One
+ * segment and one request on tsel_importance's one-launch path (a single
+ * image of at most 256 tokens): the importance launch ranks the request's
+ * keys itself (keys above, then equal keys at lower token indices) and writes
+ * keep_idx and cu_keep; no top-B kernel is launched (same results).
  * workspace: >= tsel_score_select_workspace_size(...) bytes, 256-byte aligned;
  * its status word collects the device checks of both steps.
  */
@@ -427,11 +431,14 @@ TSEL_API tsel_status tsel_read_device_status(const void* workspace, uint32_t* bi
 TSEL_API tsel_status tsel_importance_redo_pairs(const void* workspace, int32_t* pairs, void* stream);
 
 /* Reads, after synchronising `stream`, how many requests the top-B calls on
- * `workspace` resolved by each threshold path since the workspace was zeroed:
- * counts[0] radix rounds over the scores (no histograms), counts[1] first
- * digit from the histograms then radix rounds, counts[2] histograms and one
- * candidate exchange, counts[3] candidate exchange rejected (its counts did not
- * bracket the budget), radix rounds from the start. A diagnostic. */
+ * `workspace` resolved by each threshold path since the workspace was zeroed,
+ * into counts[5]: counts[0] radix rounds over the scores (no histograms),
+ * counts[1] first digit from the histograms then radix rounds, counts[2]
+ * histograms and one candidate exchange, counts[3] candidate exchange rejected
+ * (its counts did not bracket the budget), radix rounds from the start,
+ * counts[4] ranked inside the one-launch importance kernel (tsel_score_select
+ * of one segment and one request on the one-launch path). Requests with B = 0
+ * are not counted. A diagnostic. */
 TSEL_API tsel_status tsel_select_path_counts(const void* workspace, int32_t* counts, void* stream);
 
 /* Enqueues a reset of the device status word to zero. */

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_util import REL_TOL, bits_to_bf16, i32, max_rel_err
+from gpu_util import REL_TOL, bits_to_bf16, i32, max_rel_err, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -167,3 +167,71 @@ def test_large_logit_gaps_follow_the_row_max(tsel):
                                        w.softmax_scale)
     assert max_rel_err(s, s_ref) <= REL_TOL
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-5, atol=2e-4)
+
+
+# ------------------------------------------------ top-B in the same launch
+
+def _score_select(tsel, w, req_off, keep, total_keep=None):
+    dev = to_device(w)
+    ws = torch.zeros(tsel.tsel_score_select_workspace_size(w.num_seg, w.total_q, w.total_k,
+                                                           w.num_heads, len(keep)),
+                     dtype=torch.uint8, device="cuda")
+    tk = int(sum(keep)) if total_keep is None else total_keep
+    s, _, kidx, cu = tsel.tsel_score_select(dev["q"], dev["k"], dev["cu_q"], dev["cu_k"],
+                                            max(w.max_seqlen_q, 1), max(w.max_seqlen_k, 1),
+                                            i32(req_off), i32(keep), tk, workspace=ws)
+    st = tsel.tsel_read_device_status(ws)
+    return (s.cpu().numpy(), kidx.cpu().numpy(), cu.cpu().numpy(), st,
+            tsel.tsel_select_path_counts(ws))
+
+
+@pytest.mark.parametrize("n,H,Hkv,d", [(256, 16, 16, 80), (200, 8, 2, 64), (1, 4, 4, 128),
+                                       (129, 1, 1, 96), (37, 16, 8, 112)])
+@pytest.mark.parametrize("frac", [0.0, 0.01, 0.6, 1.0])
+def test_single_image_selected_in_the_importance_launch(tsel, n, H, Hkv, d, frac):
+    """One image and one request: the one-launch kernel ranks the keys itself;
+    keep_idx and cu_keep equal oracle.select_topk on the same fp32 scores, and
+    the scores equal tsel_importance's bit for bit."""
+    w = W.make_segments([n], [n], H, Hkv, d, seed=960 + n + H + d, sink_counts=[min(n, 3)],
+                        hidden_dim=64)
+    B = int(frac * n)
+    s, kidx, cu, st, paths = _score_select(tsel, w, [0, n], [B])
+    assert st == 0
+    assert paths == [0, 0, 0, 0, 1 if B > 0 else 0], paths
+    k_ref, cu_ref = oracle.select_topk(s, [0, n], [B])
+    assert np.array_equal(kidx[:B], k_ref) and np.array_equal(cu, cu_ref)
+    s_imp, _, _ = _run(tsel, w)
+    assert np.array_equal(s.view(np.uint32), s_imp.view(np.uint32))
+    _, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s, s_ref) <= REL_TOL
+
+
+@pytest.mark.parametrize("lo,hi,B", [(17, 200, 50), (0, 128, 128), (255, 256, 1), (100, 100, 0)])
+def test_selection_of_a_token_range(tsel, lo, hi, B):
+    w = W.make_segments([256], [256], 8, 8, 80, seed=971, sink_counts=[4], hidden_dim=64)
+    s, kidx, cu, st, paths = _score_select(tsel, w, [lo, hi], [B])
+    assert st == 0
+    k_ref, cu_ref = oracle.select_topk(s, [lo, hi], [B])
+    assert np.array_equal(kidx[:B], k_ref) and np.array_equal(cu, cu_ref)
+
+
+def test_selection_ties_keep_the_lowest_indices(tsel):
+    # Q = 0: every probability of a row is equal, so every key's score is too
+    w = W.make_segments([256], [256], 4, 4, 64, seed=972, hidden_dim=64)
+    w.q_bits[:] = 0
+    s, kidx, cu, st, _ = _score_select(tsel, w, [10, 250], [77])
+    assert st == 0
+    assert np.all(s == s[0])
+    assert np.array_equal(kidx, np.arange(10, 87, dtype=np.int32))
+    assert np.array_equal(cu, [0, 77])
+
+
+@pytest.mark.parametrize("req_off,keep,total_keep", [([0, 257], [5], 5), ([0, 100], [101], 101),
+                                                     ([50, 40], [1], 1), ([0, 256], [5], 6)])
+def test_selection_bad_requests_set_status(tsel, req_off, keep, total_keep):
+    w = W.make_segments([256], [256], 4, 4, 64, seed=973, hidden_dim=64)
+    s, _, _, st, paths = _score_select(tsel, w, req_off, keep, total_keep)
+    assert st & tsel.TSEL_DEV_REQUESTS
+    assert paths == [0, 0, 0, 0, 0]
+    _, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    assert max_rel_err(s, s_ref) <= REL_TOL   # the scores are still written

@@ -18,7 +18,7 @@ from gpu_util import REL_TOL, check_selection_exact, i32, max_rel_err, to_device
 
 pytestmark = pytest.mark.gpu
 
-PLAIN, HIST_ROUNDS, CANDIDATES, REJECTED = range(4)
+PLAIN, HIST_ROUNDS, CANDIDATES, REJECTED, IN_IMPORTANCE = range(5)
 
 
 @pytest.fixture(scope="module")
@@ -75,13 +75,16 @@ def test_fused_equals_separate_calls_and_oracle(tsel, name):
     assert np.array_equal(a[2].cpu().numpy(), k_ref)
     assert np.array_equal(a[3].cpu().numpy(), cu_ref)
     R = w.keep_per_req.size
-    assert b[5] == [R, 0, 0, 0]                             # separate calls: no histograms
+    assert b[5] == [R, 0, 0, 0, 0]                          # separate calls: no histograms
     if name in ("thirty_images", "batch_8x16x1024"):
         # requests split over clusters of CTAs start from the histograms
-        assert a[5] == [0, 0, R, 0], a[5]
+        assert a[5] == [0, 0, R, 0, 0], a[5]
+    elif name == "single_image_256":
+        # one image of 256 tokens: ranked inside the one-launch importance kernel
+        assert a[5] == [0, 0, 0, 0, R], a[5]
     else:
         # one CTA per request: no histograms, plain radix rounds
-        assert a[5] == [R, 0, 0, 0], a[5]
+        assert a[5] == [R, 0, 0, 0, 0], a[5]
 
 
 def test_fused_lse_provided_and_fp8(tsel):
@@ -282,7 +285,7 @@ def test_hist_start_many_requests(tsel):
         if R == 64:
             assert paths[PLAIN] == 0 and sum(paths) == served
         else:
-            assert paths == [served, 0, 0, 0]
+            assert paths == [served, 0, 0, 0, 0]
 
 
 def test_hist_start_device_budgets(tsel):
