@@ -391,6 +391,16 @@ def workload_throughput(tsel, w, dev, flush, stream, ex2_peak, bf16_peak, steps:
         tsel.tsel_gather_compact(hidden, pos, ck, keep_idx, out_hidden=oh, out_pos=op, out_img_id=oi,
                                  out_cu_seqlens=oc, workspace=ws, stream=stream)
 
+    one_launch = tsel.tsel_importance_one_launch(G, Tq, Tk, w.max_seqlen_q, w.max_seqlen_k, H,
+                                                 w.head_dim) == 1
+
+    def importance_alone():
+        if one_launch:   # the one-launch kernel (the stage bits would select the two-pass form)
+            tsel.tsel_importance(q, k, cq, ck, w.max_seqlen_q, w.max_seqlen_k, lse=lse,
+                                 scores=scores, workspace=ws, stream=stream)
+        else:
+            score_select(IMP)
+
     whole, stage = [], []
     for i in range(warmup + steps):       # the path as it runs: one fused call + compaction
         flush.fill_(i & 0xFF)
@@ -405,7 +415,7 @@ def workload_throughput(tsel, w, dev, flush, stream, ex2_peak, bf16_peak, steps:
         flush.fill_(i & 0xFF)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         ev[0].record(stream)
-        score_select(IMP)
+        importance_alone()
         ev[1].record(stream)
         score_select(tsel.TSEL_SEL_STAGE_TOPK)
         gather()
@@ -421,8 +431,10 @@ def workload_throughput(tsel, w, dev, flush, stream, ex2_peak, bf16_peak, steps:
     return {"tokens": Tk, "ms_per_step": t_step, "tokens_per_s": Tk / (t_step * 1e-3),
             "importance_ms": t_imp, "importance_roofline_frac": roof / (t_imp * 1e-3),
             "topk_paths": tsel.tsel_select_path_counts(ws),
+            "importance_launches": "one" if one_launch else "schedule + two passes",
             "note": f"{steps} steps of the fused score + select call and the compaction; "
-                    "importance timed apart (its three stages, then an event)"}
+                    "importance timed apart (the one-launch kernel, or the schedule and the "
+                    "two passes, then an event)"}
 
 
 def small_request_latency(tsel, w, dev, flush, stream, reps: int = 20) -> dict:
@@ -931,8 +943,8 @@ def gpu_arm(args) -> None:
         # the fused call's top-B, started from the column pass's histograms
         "topk": {"ms": mean["topk"], "GB/s": topk_bytes / (mean["topk"] * 1e-3) / 1e9,
                  "hbm_frac": topk_bytes / (mean["topk"] * 1e-3) / hbm_peak,
-                 "paths": dict(zip(["radix", "hist_rounds", "hist_candidates", "rejected"],
-                                   topk_paths))},
+                 "paths": dict(zip(["radix", "hist_rounds", "hist_candidates", "rejected",
+                                    "in_importance_launch"], topk_paths))},
         "topk_plain": {"ms": mean["topk_plain"],
                        "GB/s": topk_bytes / (mean["topk_plain"] * 1e-3) / 1e9,
                        "note": "tsel_select_topk on the same scores (three radix rounds)"},
