@@ -147,6 +147,7 @@ struct ImpSmallParams {
   int H, Hkv;
   float c;               // softmax_scale * log2(e)
   float* lse_out;        // natural log [H][Tq] (may be null)
+  const float* lse_in;   // the caller's natural-log LSE [H][Tq]: no row-LSE phase (or null)
   float* scores;         // [Tk]
   uint32_t* status;
   uint64_t timeout_ns;

@@ -49,9 +49,9 @@ namespace {
 
 constexpr int kSmallThreads = 32 * (2 + kEpiWarps);   // 576
 
-template <int D>
+template <int D, bool FP8>
 struct SmallCfg {
-  using C = TileCfg<D, false>;
+  using C = TileCfg<D, FP8>;
   static constexpr int OFF_Q = 0;                        // two query tiles
   static constexpr int OFF_K = 2 * C::TILE_BYTES;        // two key tiles
   static constexpr int OFF_NL = 4 * C::TILE_BYTES;       // -LSE2 of the 256 query rows
@@ -213,14 +213,14 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kSmallThreads, 1)
     imp_small_kernel(const __grid_constant__ CUtensorMap mapQ64,
                      const __grid_constant__ CUtensorMap mapQ16,
                      const __grid_constant__ CUtensorMap mapK64,
                      const __grid_constant__ CUtensorMap mapK16, const ImpSmallParams p) {
-  using C = TileCfg<D, false>;
-  using S = SmallCfg<D>;
+  using C = TileCfg<D, FP8>;
+  using S = SmallCfg<D, FP8>;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = smem_dyn + ((1024u - (smem_u32(smem_dyn) & 1023u)) & 1023u);
   uint8_t* sQ = smem + S::OFF_Q;
@@ -310,7 +310,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const bool work = nA > 0 && nB > 0;
   // Accumulator j holds S tile (query tile j>>1, key tile j&1), then S^T tile
   // (key tile j>>1, query tile j&1), in TMEM columns [128 j, 128 j + 128).
-  auto exists1 = [&](int j) { return (j >> 1) < nA && (j & 1) < nB; };
+  // With the caller's LSE there is no S phase.
+  const bool lse_given = p.lse_in != nullptr;
+  auto exists1 = [&](int j) { return !lse_given && (j >> 1) < nA && (j & 1) < nB; };
   auto exists2 = [&](int j) { return (j >> 1) < nB && (j & 1) < nA; };
   // Keys [r * per, (r + 1) * per) are summed over the heads by CTA r (all
   // of them by CTA 0 when it also selects the request's top-B).
@@ -322,16 +324,16 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       const int kvh = h / (p.H / p.Hkv);
       // in the order the MMAs need them: Q0, K0, K1, Q1
       mbar_arrive_expect_tx(&q_full[0], uint32_t(C::TILE_BYTES));
-      load_tile<D, false>(sQ, &mapQ64, &mapQ16, &q_full[0], h, q0);
+      load_tile<D, FP8>(sQ, &mapQ64, &mapQ16, &q_full[0], h, q0);
       mbar_arrive_expect_tx(&k_full[0], uint32_t(C::TILE_BYTES));
-      load_tile<D, false>(sK, &mapK64, &mapK16, &k_full[0], kvh, k0);
+      load_tile<D, FP8>(sK, &mapK64, &mapK16, &k_full[0], kvh, k0);
       if (nB > 1) {
         mbar_arrive_expect_tx(&k_full[1], uint32_t(C::TILE_BYTES));
-        load_tile<D, false>(sK + C::TILE_BYTES, &mapK64, &mapK16, &k_full[1], kvh, k0 + kTile);
+        load_tile<D, FP8>(sK + C::TILE_BYTES, &mapK64, &mapK16, &k_full[1], kvh, k0 + kTile);
       }
       if (nA > 1) {
         mbar_arrive_expect_tx(&q_full[1], uint32_t(C::TILE_BYTES));
-        load_tile<D, false>(sQ + C::TILE_BYTES, &mapQ64, &mapQ16, &q_full[1], h, q0 + kTile);
+        load_tile<D, FP8>(sQ + C::TILE_BYTES, &mapQ64, &mapQ16, &q_full[1], h, q0 + kTile);
       }
       // the copies have landed before the CTA can exit
       wait_drain(&q_full[0], 0, T);
@@ -351,19 +353,24 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           break;
         }
         tc_fence_after();
-        issue_tile_mmas<D, false>(tmem + uint32_t(j * kTile), sQ + (j >> 1) * C::TILE_BYTES,
-                                  sK + (j & 1) * C::TILE_BYTES);
+        issue_tile_mmas<D, FP8>(tmem + uint32_t(j * kTile), sQ + (j >> 1) * C::TILE_BYTES,
+                                sK + (j & 1) * C::TILE_BYTES);
         mma_commit(&acc1_full[j]);
       }
       for (int j = 0; j < 4 && ok; ++j) {
         if (!exists2(j)) continue;
+        if (lse_given && (!wait_bounded(&q_full[j & 1], 0, abort_flag, T) ||
+                          !wait_bounded(&k_full[j >> 1], 0, abort_flag, T))) {
+          ok = false;
+          break;
+        }
         if (exists1(j) && !wait_bounded(&acc1_free[j], 0, abort_flag, T)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        issue_tile_mmas<D, false>(tmem + uint32_t(j * kTile), sK + (j >> 1) * C::TILE_BYTES,
-                                  sQ + (j & 1) * C::TILE_BYTES);
+        issue_tile_mmas<D, FP8>(tmem + uint32_t(j * kTile), sK + (j >> 1) * C::TILE_BYTES,
+                                sQ + (j & 1) * C::TILE_BYTES);
         mma_commit(&acc2_full[j]);
       }
       if (!ok) {
@@ -404,7 +411,19 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         sCl[a * kTile + row] = L;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-      if (b == 0) {
+      if (lse_given) {
+        // the caller's natural-log LSE as -LSE2; a row without keys (-inf) or a
+        // NaN adds nothing, as in the two-pass path's LSE import
+        const int qrow = (warp - kEpiFirstWarp) * 32 + lane;   // 0..511
+        if (qrow < kPair) {
+          float v = kNegInf;
+          if (qrow < nq) {
+            v = -__ldg(p.lse_in + int64_t(h) * p.Tq + q0 + qrow) * 1.4426950408889634f;
+            if (!(v < __builtin_huge_valf() && v > kNegInf)) v = kNegInf;
+          }
+          sNl[qrow] = v;
+        }
+      } else if (b == 0) {
         const float m1 = sCm[a * kTile + row], l1 = sCl[a * kTile + row];
         const float M = fmaxf(m, m1);
         float Ls = 0.f;
@@ -475,10 +494,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                  reinterpret_cast<int*>(smem + S::OFF_BINS), reinterpret_cast<int*>(smem + S::OFF_SEL));
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_small_t(const CUtensorMap* maps, const ImpSmallParams& p, cudaStream_t stream) {
-  using S = SmallCfg<D>;
-  auto kern = imp_small_kernel<D>;
+  using S = SmallCfg<D, FP8>;
+  auto kern = imp_small_kernel<D, FP8>;
   static bool attr_set[128] = {};   // per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -494,10 +513,10 @@ cudaError_t launch_small_t(const CUtensorMap* maps, const ImpSmallParams& p, cud
                          maps[1], maps[2], maps[3], p);
 }
 
-template <int D>
+template <int D, bool FP8>
 int small_active_clusters_t(int H, cudaError_t* err) {
-  using S = SmallCfg<D>;
-  auto kern = imp_small_kernel<D>;
+  using S = SmallCfg<D, FP8>;
+  auto kern = imp_small_kernel<D, FP8>;
   *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
   if (*err != cudaSuccess) return 0;
   *err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -520,45 +539,58 @@ int small_active_clusters_t(int H, cudaError_t* err) {
 
 }  // namespace
 
-cudaError_t launch_imp_small(int head_dim, const CUtensorMap* maps, const ImpSmallParams& p,
-                             cudaStream_t stream) {
+cudaError_t launch_imp_small(int head_dim, bool fp8, const CUtensorMap* maps,
+                             const ImpSmallParams& p, cudaStream_t stream) {
+#define TSEL_SMALL_CASE(DD)                                                               \
+  case DD:                                                                                \
+    return fp8 ? launch_small_t<DD, true>(maps, p, stream) : launch_small_t<DD, false>(maps, p, stream);
   switch (head_dim) {
-    case 64: return launch_small_t<64>(maps, p, stream);
-    case 80: return launch_small_t<80>(maps, p, stream);
-    case 96: return launch_small_t<96>(maps, p, stream);
-    case 112: return launch_small_t<112>(maps, p, stream);
-    case 128: return launch_small_t<128>(maps, p, stream);
-    default: return cudaErrorInvalidValue;
+    TSEL_SMALL_CASE(64)
+    TSEL_SMALL_CASE(80)
+    TSEL_SMALL_CASE(96)
+    TSEL_SMALL_CASE(112)
+    TSEL_SMALL_CASE(128)
+    default:
+      return cudaErrorInvalidValue;
   }
+#undef TSEL_SMALL_CASE
 }
 
 // Whether a cluster of H CTAs of the one-launch kernel fits on the device
-// (cached per device, head_dim and H).
-bool imp_small_fits(int head_dim, int H, cudaError_t* err) {
+// (cached per device, input type, head_dim and H).
+bool imp_small_fits(int head_dim, bool fp8, int H, cudaError_t* err) {
   *err = cudaSuccess;
   if (H < 1 || H > kMaxClusterCtas) return false;
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return false;
-  static signed char cache[128][5][kMaxClusterCtas + 1] = {};   // 0 unknown, 1 no, 2 yes
+  static signed char cache[128][2][5][kMaxClusterCtas + 1] = {};   // 0 unknown, 1 no, 2 yes
   const int di = (head_dim - 64) / 16;
   if (di < 0 || di > 4 || (head_dim % 16) != 0) return false;
   const bool cacheable = dev >= 0 && dev < 128;
-  if (cacheable && cache[dev][di][H] != 0) return cache[dev][di][H] == 2;
+  const int fi = fp8 ? 1 : 0;
+  if (cacheable && cache[dev][fi][di][H] != 0) return cache[dev][fi][di][H] == 2;
   int active = 0;
+#define TSEL_SMALL_OCC(DD)                                                                   \
+  case DD:                                                                                   \
+    active = fp8 ? small_active_clusters_t<DD, true>(H, err) : small_active_clusters_t<DD, false>(H, err); \
+    break;
   switch (head_dim) {
-    case 64: active = small_active_clusters_t<64>(H, err); break;
-    case 80: active = small_active_clusters_t<80>(H, err); break;
-    case 96: active = small_active_clusters_t<96>(H, err); break;
-    case 112: active = small_active_clusters_t<112>(H, err); break;
-    default: active = small_active_clusters_t<128>(H, err); break;
+    TSEL_SMALL_OCC(64)
+    TSEL_SMALL_OCC(80)
+    TSEL_SMALL_OCC(96)
+    TSEL_SMALL_OCC(112)
+    default:
+      active = fp8 ? small_active_clusters_t<128, true>(H, err) : small_active_clusters_t<128, false>(H, err);
+      break;
   }
+#undef TSEL_SMALL_OCC
   if (*err != cudaSuccess) {
     (void)cudaGetLastError();
     *err = cudaSuccess;   // not a failure of the call: the scheduled path takes the problem
     active = 0;
   }
-  if (cacheable) cache[dev][di][H] = active >= 1 ? 2 : 1;
+  if (cacheable) cache[dev][fi][di][H] = active >= 1 ? 2 : 1;
   return active >= 1;
 }
 

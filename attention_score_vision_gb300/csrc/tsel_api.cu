@@ -26,9 +26,9 @@ cudaError_t launch_imp_prep(const int32_t* cu_q, const int32_t* cu_k, int G, int
                             cudaStream_t stream);
 cudaError_t launch_imp_pass(int pass, int head_dim, bool fp8, const CUtensorMap* maps,
                             const ImpPassParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_imp_small(int head_dim, const CUtensorMap* maps, const ImpSmallParams& p,
-                             cudaStream_t stream);
-bool imp_small_fits(int head_dim, int H, cudaError_t* err);
+cudaError_t launch_imp_small(int head_dim, bool fp8, const CUtensorMap* maps,
+                             const ImpSmallParams& p, cudaStream_t stream);
+bool imp_small_fits(int head_dim, bool fp8, int H, cudaError_t* err);
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
                               const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
                               int max_qtiles, int H, const uint32_t* status, int32_t* hist,
@@ -236,13 +236,13 @@ bool one_launch_eligible(unsigned flags, int num_seg, int total_q, int total_k, 
                          int max_k, int num_heads, int head_dim, int sms, cudaError_t* err) {
   *err = cudaSuccess;
   const unsigned excl = TSEL_IMP_STAGE_PREP | TSEL_IMP_STAGE_PASS1 | TSEL_IMP_STAGE_PASS2 |
-                        TSEL_SEL_STAGE_TOPK | TSEL_IMP_FP8_E4M3 | TSEL_IMP_LSE_PROVIDED |
-                        TSEL_IMP_ROWREF_FIXED | TSEL_IMP_ROWREF_MOVING | TSEL_IMP_TWO_PASS;
+                        TSEL_SEL_STAGE_TOPK | TSEL_IMP_ROWREF_FIXED | TSEL_IMP_ROWREF_MOVING |
+                        TSEL_IMP_TWO_PASS;
   if ((flags & excl) != 0 || num_seg < 1 || total_q < 1 || total_k < 1 || max_q > kPairRows ||
       max_k > kPairRows || num_heads < 1 || num_heads > kMaxClusterCtas ||
       int64_t(num_seg) * num_heads > sms)
     return false;
-  return imp_small_fits(head_dim, num_heads, err);
+  return imp_small_fits(head_dim, (flags & TSEL_IMP_FP8_E4M3) != 0, num_heads, err);
 }
 
 struct SelHist {
@@ -323,7 +323,7 @@ tsel_status importance_impl(const void* q, int64_t q_row_stride, const void* k,
     if (one_launch_eligible(flags, num_seg, total_q, total_k, max_seqlen_q, max_seqlen_k,
                             num_heads, head_dim, sms, &fe)) {
       CUtensorMap m[4];
-      const tsel_status ms = make_qk_maps(q, k, q_row_stride, k_row_stride, false, head_dim, hd,
+      const tsel_status ms = make_qk_maps(q, k, q_row_stride, k_row_stride, fp8, head_dim, hd,
                                           kvd, num_heads, num_kv_heads, total_q, total_k, &m[0],
                                           &m[1], &m[2], &m[3]);
       if (ms != TSEL_OK) return ms;
@@ -339,7 +339,8 @@ tsel_status importance_impl(const void* q, int64_t q_row_stride, const void* k,
       sp.Hkv = num_kv_heads;
       const float sc = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(float(head_dim));
       sp.c = sc * 1.4426950408889634f;
-      sp.lse_out = lse;
+      sp.lse_out = lse_provided ? nullptr : lse;
+      sp.lse_in = lse_provided ? lse : nullptr;
       sp.scores = scores;
       sp.status = &hdr->status;
       sp.timeout_ns = (flags & TSEL_IMP_TEST_STALL) ? 50ull * 1000000ull : wait_timeout_ns();
@@ -354,7 +355,7 @@ tsel_status importance_impl(const void* q, int64_t q_row_stride, const void* k,
         sp.cu_keep = sel.cu_keep;
         *sel.selected = true;
       }
-      e = launch_imp_small(head_dim, m, sp, stream);
+      e = launch_imp_small(head_dim, fp8, m, sp, stream);
       return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "one-launch importance");
     }
   }

@@ -118,10 +118,11 @@ def test_which_inputs_take_one_launch(tsel):
     assert q(num_seg=sms // 16 + 1) == 0          # more CTAs than SMs
     assert q(head_dim=72) == 0
     assert q(total_q=0) == 0 and q(total_k=0) == 0
-    for f in ("TSEL_IMP_TWO_PASS", "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3", "TSEL_IMP_ROWREF_FIXED",
-              "TSEL_IMP_ROWREF_MOVING", "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS2"):
+    for f in ("TSEL_IMP_TWO_PASS", "TSEL_IMP_ROWREF_FIXED", "TSEL_IMP_ROWREF_MOVING",
+              "TSEL_IMP_STAGE_PREP", "TSEL_IMP_STAGE_PASS2"):
         assert q(flags=getattr(tsel, f)) == 0, f
-    assert q(flags=tsel.TSEL_IMP_SCORE_SUM) == 1
+    for f in ("TSEL_IMP_SCORE_SUM", "TSEL_IMP_LSE_PROVIDED", "TSEL_IMP_FP8_E4M3"):
+        assert q(flags=getattr(tsel, f)) == 1, f
     assert q(num_heads=1, head_dim=128, num_seg=1) == 1
 
 
@@ -235,3 +236,63 @@ def test_selection_bad_requests_set_status(tsel, req_off, keep, total_keep):
     assert paths == [0, 0, 0, 0, 0]
     _, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
     assert max_rel_err(s, s_ref) <= REL_TOL   # the scores are still written
+
+
+# ---------------------------------------------- the caller's LSE, one launch
+
+@pytest.mark.parametrize("Lq,Lk,H,Hkv,d", [([256], [256], 16, 16, 80), ([1, 127, 200], [256, 3, 129], 8, 2, 64),
+                                           ([0, 50, 9], [40, 0, 256], 4, 4, 128)])
+def test_lse_provided_in_one_launch(tsel, Lq, Lk, H, Hkv, d):
+    """TSEL_IMP_LSE_PROVIDED on the one-launch path: no row-LSE phase, the
+    column sums from the caller's LSE (here the oracle's, rounded to fp32),
+    against the oracle and against the two-pass form with the same LSE."""
+    w = W.make_segments(Lq, Lk, H, Hkv, d, seed=1000 + H + d, sink_counts=[min(n, 2) for n in Lk],
+                        hidden_dim=64)
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k)
+    F = tsel.TSEL_IMP_LSE_PROVIDED
+    assert _one(tsel, w, F) == 1 and _one(tsel, w, F | tsel.TSEL_IMP_TWO_PASS) == 0
+    out = []
+    for flags in (F, F | tsel.TSEL_IMP_TWO_PASS):
+        q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
+        ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
+                         dtype=torch.uint8, device="cuda")
+        lse = torch.from_numpy(lse_ref.astype(np.float32)).cuda()
+        s, _ = tsel.tsel_importance(q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k),
+                                    max(w.max_seqlen_q, 1), max(w.max_seqlen_k, 1), flags=flags,
+                                    lse=lse, workspace=ws)
+        assert tsel.tsel_read_device_status(ws) == 0
+        out.append(s.cpu().numpy())
+    assert max_rel_err(out[0], s_ref) <= REL_TOL
+    assert max_rel_err(out[0], out[1].astype(np.float64)) <= PATH_TOL
+
+
+# ------------------------------------------------------- E4M3, one launch
+
+@pytest.mark.parametrize("d", [64, 80, 96, 112, 128])
+@pytest.mark.parametrize("lse_given", [False, True])
+def test_fp8_in_one_launch(tsel, d, lse_given):
+    """E4M3 Q/K (kind::f8f6f4 MMAs) on the one-launch path against the
+    E4M3-decoding oracle and against the two-pass form on the same bytes."""
+    L = [1, 127, 128, 129, 256]
+    w = W.to_e4m3(W.make_segments(L, L, 8, 4, d, seed=1100 + d, sink_counts=[0, 1, 2, 3, 6],
+                                  hidden_dim=16))
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k,
+                                       w.softmax_scale, fmt="e4m3")
+    F = tsel.TSEL_IMP_FP8_E4M3 | (tsel.TSEL_IMP_LSE_PROVIDED if lse_given else 0)
+    assert _one(tsel, w, F) == 1
+    out = []
+    for flags in (0, tsel.TSEL_IMP_TWO_PASS):
+        q = torch.from_numpy(w.q_bits).cuda()
+        k = torch.from_numpy(w.k_bits).cuda()
+        ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, w.num_heads),
+                         dtype=torch.uint8, device="cuda")
+        lse = torch.from_numpy(lse_ref.astype(np.float32)).cuda() if lse_given else None
+        kw = {"flags": flags | (tsel.TSEL_IMP_LSE_PROVIDED if lse_given else 0)}
+        s, lse_out = tsel.tsel_importance(q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), 256, 256,
+                                          softmax_scale=w.softmax_scale, lse=lse, workspace=ws, **kw)
+        assert tsel.tsel_read_device_status(ws) == 0
+        out.append((s.cpu().numpy(), lse_out.cpu().numpy()))
+    assert max_rel_err(out[0][0], s_ref) <= REL_TOL
+    assert max_rel_err(out[0][0], out[1][0].astype(np.float64)) <= PATH_TOL
+    if not lse_given:
+        np.testing.assert_allclose(out[0][1], lse_ref, rtol=1e-5, atol=1e-4)
