@@ -172,7 +172,7 @@ def test_large_logit_gaps_follow_the_row_max(tsel):
 
 # ------------------------------------------------ top-B in the same launch
 
-def _score_select(tsel, w, req_off, keep, total_keep=None):
+def _score_select(tsel, w, req_off, keep, total_keep=None, scale=0.0):
     dev = to_device(w)
     ws = torch.zeros(tsel.tsel_score_select_workspace_size(w.num_seg, w.total_q, w.total_k,
                                                            w.num_heads, len(keep)),
@@ -180,7 +180,8 @@ def _score_select(tsel, w, req_off, keep, total_keep=None):
     tk = int(sum(keep)) if total_keep is None else total_keep
     s, _, kidx, cu = tsel.tsel_score_select(dev["q"], dev["k"], dev["cu_q"], dev["cu_k"],
                                             max(w.max_seqlen_q, 1), max(w.max_seqlen_k, 1),
-                                            i32(req_off), i32(keep), tk, workspace=ws)
+                                            i32(req_off), i32(keep), tk, softmax_scale=scale,
+                                            workspace=ws)
     st = tsel.tsel_read_device_status(ws)
     return (s.cpu().numpy(), kidx.cpu().numpy(), cu.cpu().numpy(), st,
             tsel.tsel_select_path_counts(ws))
@@ -296,3 +297,58 @@ def test_fp8_in_one_launch(tsel, d, lse_given):
     assert max_rel_err(out[0][0], out[1][0].astype(np.float64)) <= PATH_TOL
     if not lse_given:
         np.testing.assert_allclose(out[0][1], lse_ref, rtol=1e-5, atol=1e-4)
+
+
+# ------------------------------------------------------ seeded random sweep
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_small_problems(tsel, seed):
+    """Random problems that all take the one-launch path (segments of 0..256
+    queries and keys, 1..9 segments, 1..16 heads with GQA, every head_dim,
+    explicit scales): scores and LSE against the oracle and the two-pass form;
+    a single image also gets a random budget selected in the same launch."""
+    rng = np.random.default_rng(1200 + seed)
+    G = int(rng.integers(1, 10))
+    H = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16]))
+    while G * H > 144:
+        G -= 1
+    Hkv = int(rng.choice([x for x in range(1, H + 1) if H % x == 0]))
+    d = int(rng.choice([64, 80, 96, 112, 128]))
+    lens = [0, 1, 2, 31, 64, 127, 128, 129, 200, 255, 256]
+    lk = rng.choice(lens, size=G)
+    lq = lk.copy() if rng.random() < 0.5 else rng.choice(lens, size=G)
+    if lq.sum() == 0:
+        lq[0] = 5
+    if lk.sum() == 0:
+        lk[0] = 7
+    scale = float(rng.choice([0.0, 0.05, 0.3]))
+    w = W.make_segments(lq, lk, H, Hkv, d, seed=1300 + seed, q_std=float(rng.choice([0.2, 1.0, 2.0])),
+                        sink_counts=rng.integers(0, 3, size=G), hidden_dim=64,
+                        softmax_scale=scale if scale > 0 else None)
+    assert _one(tsel, w) == 1
+    lse_ref, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k,
+                                       softmax_scale=scale if scale > 0 else None)
+    outs = []
+    for flags in (0, tsel.TSEL_IMP_TWO_PASS):
+        q, k = bits_to_bf16(w.q_bits), bits_to_bf16(w.k_bits)
+        ws = torch.zeros(tsel.tsel_importance_workspace_size(w.num_seg, w.total_q, w.total_k, H),
+                         dtype=torch.uint8, device="cuda")
+        s, lse = tsel.tsel_importance(q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k),
+                                      max(w.max_seqlen_q, 1), max(w.max_seqlen_k, 1), flags=flags,
+                                      softmax_scale=scale, workspace=ws)
+        assert tsel.tsel_read_device_status(ws) == 0
+        outs.append((s.cpu().numpy(), lse.cpu().numpy()))
+    s1, l1 = outs[0]
+    assert max_rel_err(s1, s_ref) <= REL_TOL
+    assert max_rel_err(s1, outs[1][0].astype(np.float64)) <= PATH_TOL
+    fin = np.isfinite(lse_ref)
+    assert np.all(np.isneginf(l1[~fin]))
+    np.testing.assert_allclose(l1[fin], lse_ref[fin], rtol=1e-5, atol=2e-4)
+    if G == 1 and w.total_k > 0:
+        n = w.total_k
+        B = int(rng.integers(0, n + 1))
+        s_sel, kidx, cu, st, paths = _score_select(tsel, w, [0, n], [B], scale=scale)
+        assert st == 0 and paths == [0, 0, 0, 0, 1 if B > 0 else 0]
+        assert np.array_equal(s_sel.view(np.uint32), s1.view(np.uint32))
+        k_ref, cu_ref = oracle.select_topk(s_sel, [0, n], [B])
+        assert np.array_equal(kidx[:B], k_ref) and np.array_equal(cu, cu_ref)
