@@ -556,20 +556,20 @@ cudaError_t launch_imp_small(int head_dim, bool fp8, const CUtensorMap* maps,
 #undef TSEL_SMALL_CASE
 }
 
-// Whether a cluster of H CTAs of the one-launch kernel fits on the device
-// (cached per device, input type, head_dim and H).
-bool imp_small_fits(int head_dim, bool fp8, int H, cudaError_t* err) {
+// How many clusters of H CTAs of the one-launch kernel the device holds at
+// once (cached per device, input type, head_dim and H; 0 when none fits).
+int imp_small_clusters(int head_dim, bool fp8, int H, cudaError_t* err) {
   *err = cudaSuccess;
-  if (H < 1 || H > kMaxClusterCtas) return false;
+  if (H < 1 || H > kMaxClusterCtas) return 0;
   int dev = 0;
   *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return false;
-  static signed char cache[128][2][5][kMaxClusterCtas + 1] = {};   // 0 unknown, 1 no, 2 yes
+  if (*err != cudaSuccess) return 0;
+  static int cache[128][2][5][kMaxClusterCtas + 1] = {};   // 1 + resident clusters (0 unknown)
   const int di = (head_dim - 64) / 16;
-  if (di < 0 || di > 4 || (head_dim % 16) != 0) return false;
+  if (di < 0 || di > 4 || (head_dim % 16) != 0) return 0;
   const bool cacheable = dev >= 0 && dev < 128;
   const int fi = fp8 ? 1 : 0;
-  if (cacheable && cache[dev][fi][di][H] != 0) return cache[dev][fi][di][H] == 2;
+  if (cacheable && cache[dev][fi][di][H] != 0) return cache[dev][fi][di][H] - 1;
   int active = 0;
 #define TSEL_SMALL_OCC(DD)                                                                   \
   case DD:                                                                                   \
@@ -590,8 +590,8 @@ bool imp_small_fits(int head_dim, bool fp8, int H, cudaError_t* err) {
     *err = cudaSuccess;   // not a failure of the call: the scheduled path takes the problem
     active = 0;
   }
-  if (cacheable) cache[dev][fi][di][H] = active >= 1 ? 2 : 1;
-  return active >= 1;
+  if (cacheable) cache[dev][fi][di][H] = active + 1;
+  return active;
 }
 
 }  // namespace tsel

@@ -28,7 +28,7 @@ cudaError_t launch_imp_pass(int pass, int head_dim, bool fp8, const CUtensorMap*
                             const ImpPassParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_imp_small(int head_dim, bool fp8, const CUtensorMap* maps,
                              const ImpSmallParams& p, cudaStream_t stream);
-bool imp_small_fits(int head_dim, bool fp8, int H, cudaError_t* err);
+int imp_small_clusters(int head_dim, bool fp8, int H, cudaError_t* err);
 cudaError_t launch_lse_import(const float* lse_in, int Tq, const int32_t* cu_q, int G,
                               const int32_t* qtile_off, float* nlse2, int64_t lse_stride,
                               int max_qtiles, int H, const uint32_t* status, int32_t* hist,
@@ -242,7 +242,9 @@ bool one_launch_eligible(unsigned flags, int num_seg, int total_q, int total_k, 
       max_k > kPairRows || num_heads < 1 || num_heads > kMaxClusterCtas ||
       int64_t(num_seg) * num_heads > sms)
     return false;
-  return imp_small_fits(head_dim, (flags & TSEL_IMP_FP8_E4M3) != 0, num_heads, err);
+  // every segment's cluster resident at once (a cluster that waits for
+  // another would double the latency this path is for)
+  return imp_small_clusters(head_dim, (flags & TSEL_IMP_FP8_E4M3) != 0, num_heads, err) >= num_seg;
 }
 
 struct SelHist {

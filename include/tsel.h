@@ -158,13 +158,14 @@ TSEL_API size_t tsel_importance_workspace_size(int num_seg, int total_q, int tot
  * schedule kernel, the row-LSE pass, its redo launch (large problems only),
  * the column pass. Small problems take one launch instead: when every
  * segment has at most 256 query rows and 256 keys (max_seqlen_q and
- * max_seqlen_k <= 256), bf16 inputs, num_heads <= 16, num_seg * num_heads no
- * more than the GPU's SMs, no FP8, ROWREF or STAGE bits, and not
- * TSEL_IMP_TWO_PASS, one CTA per (segment, head) computes both passes from
- * TMEM (each row's reference follows its max; with TSEL_IMP_LSE_PROVIDED only
- * the column sums, from the caller's LSE) and the heads of a segment add
- * their per-key sums over a thread-block cluster in head order. Both forms
- * give the same scores up to fp32 rounding, each deterministically.
+ * max_seqlen_k <= 256), num_heads <= 16, num_seg * num_heads no more than the
+ * GPU's SMs with every segment's cluster of CTAs resident at once, no ROWREF or
+ * STAGE bits and not TSEL_IMP_TWO_PASS (bf16 or E4M3 inputs), one CTA per
+ * (segment, head) computes both passes from TMEM (each row's reference follows
+ * its max; with TSEL_IMP_LSE_PROVIDED only the column sums, from the caller's
+ * LSE) and the heads of a segment add their per-key sums over a thread-block
+ * cluster in head order. Both forms give the same scores up to fp32 rounding,
+ * each deterministically (tsel_importance_one_launch tells which a call takes).
  * On large problems (or with TSEL_IMP_ROWREF_FIXED) the
  * row-LSE pass fixes each row's reference max on its first 64 keys; a query
  * pair with a row whose sum then leaves the fp32 range (logits more than ~88

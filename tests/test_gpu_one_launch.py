@@ -314,6 +314,9 @@ def test_random_small_problems(tsel, seed):
         G -= 1
     Hkv = int(rng.choice([x for x in range(1, H + 1) if H % x == 0]))
     d = int(rng.choice([64, 80, 96, 112, 128]))
+    # as many segments as have their clusters resident at once
+    while G > 1 and tsel.tsel_importance_one_launch(G, 256 * G, 256 * G, 256, 256, H, d) != 1:
+        G -= 1
     lens = [0, 1, 2, 31, 64, 127, 128, 129, 200, 255, 256]
     lk = rng.choice(lens, size=G)
     lq = lk.copy() if rng.random() < 0.5 else rng.choice(lens, size=G)
