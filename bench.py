@@ -57,6 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-fp8", action="store_true")
     ap.add_argument("--cpu-child", nargs=3, metavar=("WORKLOAD", "PAIRS", "IMAGES"),
                     help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-small", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -150,6 +151,38 @@ def cpu_child(workload: str, pair_budget: float, images: int = 0) -> dict:
         res = oracle_step(w, chosen, pool)
     res["cores"] = workers
     return res
+
+
+SMALL_REQUESTS = ("single_image_256", "six_views_1536", "text_query_3072")
+
+
+def cpu_small_child() -> dict:
+    """The oracle on each small request in one process with one BLAS thread:
+    importance, pooled top-B and compaction; input generation not timed."""
+    import oracle
+    import workloads as W
+    out = {}
+    for name in SMALL_REQUESTS:
+        w = W.make(name)
+        t0 = time.perf_counter()
+        _, s = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k,
+                                 w.softmax_scale)
+        keep_idx, _ = oracle.select_topk(s, w.req_tok_offsets, w.keep_per_req)
+        oracle.gather_compact(w.hidden_bits, w.pos, w.cu_seqlens_k, keep_idx)
+        dt = time.perf_counter() - t0
+        out[name] = {"seconds": dt, "tokens_per_s": w.total_k / dt, "cores": 1}
+    return out
+
+
+def run_cpu_small_child() -> dict:
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = "1"
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-small"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def host_cores() -> int:
@@ -516,6 +549,12 @@ def gpu_arm(args) -> None:
             cpu = run_cpu_child(args.workload, float("inf"), args.images)
         except Exception as exc:  # reported, never fatal
             cpu = {"error": str(exc)[-300:]}
+    cpu_small = {}
+    if rank == 0 and not args.no_cpu_baseline and not args.no_small:
+        try:
+            cpu_small = run_cpu_small_child()
+        except Exception as exc:  # reported, never fatal
+            cpu_small = {"error": str(exc)[-300:]}
 
     torch.cuda.set_device(local)
     if world > 1:
@@ -882,8 +921,10 @@ def gpu_arm(args) -> None:
     # --- small requests: whole path replayed from one CUDA graph -------------
     small = {}
     if not args.no_small:
-        for name in ("single_image_256", "six_views_1536", "text_query_3072"):
+        for name in SMALL_REQUESTS:
             small[name] = small_request_latency(tsel, W.make(name), dev, flush, stream)
+            if name in cpu_small:   # the oracle on one host core, same request
+                small[name]["cpu_oracle_1core"] = cpu_small[name]
 
     # --- the other seeded workloads: throughput and importance roofline -------
     sweep = {}
@@ -1031,6 +1072,10 @@ def main():
     if args.cpu_child:
         print(json.dumps(cpu_child(args.cpu_child[0], float(args.cpu_child[1]),
                                    int(args.cpu_child[2]))))
+        return
+    if args.cpu_small:
+        _single_thread_blas()
+        print(json.dumps(cpu_small_child()))
         return
     if args.impl == "reference":
         reference_arm(args)
