@@ -355,3 +355,23 @@ def test_random_small_problems(tsel, seed):
         assert np.array_equal(s_sel.view(np.uint32), s1.view(np.uint32))
         k_ref, cu_ref = oracle.select_topk(s_sel, [0, n], [B])
         assert np.array_equal(kidx[:B], k_ref) and np.array_equal(cu, cu_ref)
+
+
+def test_fp8_single_image_selected_in_the_launch(tsel):
+    """E4M3 inputs take the same single-launch selection: keep_idx equals the
+    oracle's selection on the same fp32 scores."""
+    w = W.to_e4m3(W.make_segments([256], [256], 8, 4, 128, seed=1400, sink_counts=[3], hidden_dim=16))
+    q, k = torch.from_numpy(w.q_bits).cuda(), torch.from_numpy(w.k_bits).cuda()
+    ws = torch.zeros(tsel.tsel_score_select_workspace_size(1, 256, 256, 8, 1), dtype=torch.uint8,
+                     device="cuda")
+    s, _, kidx, cu = tsel.tsel_score_select(q, k, i32(w.cu_seqlens_q), i32(w.cu_seqlens_k), 256, 256,
+                                            i32([0, 256]), i32([100]), 100,
+                                            softmax_scale=w.softmax_scale, workspace=ws)
+    assert tsel.tsel_read_device_status(ws) == 0
+    assert tsel.tsel_select_path_counts(ws) == [0, 0, 0, 0, 1]
+    s = s.cpu().numpy()
+    k_ref, cu_ref = oracle.select_topk(s, [0, 256], [100])
+    assert np.array_equal(kidx.cpu().numpy(), k_ref) and np.array_equal(cu.cpu().numpy(), cu_ref)
+    _, s_ref = oracle.importance(w.q_bits, w.k_bits, w.cu_seqlens_q, w.cu_seqlens_k, w.softmax_scale,
+                                 fmt="e4m3")
+    assert max_rel_err(s, s_ref) <= REL_TOL
