@@ -1,6 +1,7 @@
 // One-launch importance for small problems: every segment has at most 256
 // query rows and 256 keys (a single image of a 256-token ViT, or a handful of
-// them), bf16, at most 16 heads.
+// them), bf16 or E4M3, at most 16 heads; with the caller's LSE, the column
+// sums alone.
 //
 // Same quantity as the two passes of imp_pass.cuh (LiteVLM review, section
 // 3.2; dynamic vision-token compression article, section 3.2: the mean
@@ -59,19 +60,17 @@ struct SmallCfg {
   static constexpr int OFF_CL = OFF_CM + kPair * 4;      // warpgroup exchange [2][128]
   static constexpr int OFF_RECV = OFF_CL + kPair * 4;    // per-head sums of this CTA's keys
   static constexpr int OFF_SEL = OFF_RECV + kMaxClusterCtas * kPair * 4;   // top-B scratch [64]
-  static constexpr int OFF_BINS = OFF_SEL + 256;         // top-B histograms [4][256]
-  static constexpr int OFF_BAR = OFF_BINS + 4 * kPair * 4;   // 15 mbarriers
-  static constexpr int OFF_MISC = OFF_BAR + 128;
+  static constexpr int OFF_RANK = OFF_SEL + 256;         // top-B: 64-bit keys [256], ranks [2][256]
+  static constexpr int NUM_BARS = 2 + 2 + 4 + 4 + 4 + 1;   // tiles, S, S freed, S^T, MMAs done
+  static constexpr int OFF_BAR = OFF_RANK + 4 * kPair * 4;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NUM_BARS;   // TMEM address, abort flag, check
   static constexpr int USED = OFF_MISC + 64 + 1024;      // + alignment slack
   static constexpr int MIN_ONE_PER_SM = 120 * 1024;      // two of these exceed an SM
   static constexpr int SMEM_BYTES = USED > MIN_ONE_PER_SM ? USED : MIN_ONE_PER_SM;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// Row max/sum of one 128-column accumulator piece (phase 1). `valid` columns
-// lie inside the segment (> 0); m is the row's reference for S*c, l the sum of
-// exp2(S*c - m) before the accumulators acc.
-// The accumulator goes back (`rel`, one arrival per warp) as soon as its last
+// Hands an accumulator back (`rel`, one arrival per warp) once its last
 // columns are in registers, so S^T can be computed into it meanwhile.
 __device__ __forceinline__ void release_acc(uint64_t* rel, int lane) {
   tc_fence_before();
@@ -79,6 +78,9 @@ __device__ __forceinline__ void release_acc(uint64_t* rel, int lane) {
   mbar_arrive_lane0(rel, lane);
 }
 
+// Row max/sum of one 128-column accumulator piece (phase 1). `valid` columns
+// lie inside the segment (> 0); m is the row's reference for S*c, l the sum of
+// exp2(S*c - m) before the accumulators acc.
 __device__ __forceinline__ void small_row_lse(uint32_t taddr, int valid, float c, float2 c2,
                                               float& m, float& l, float2 (&acc)[2],
                                               uint64_t* rel, int lane) {
@@ -235,6 +237,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   uint64_t* acc1_free = acc1_full + 4; // [4] S accumulators read out
   uint64_t* acc2_full = acc1_free + 4; // [4] S^T accumulators complete
   uint64_t* mma_done = acc2_full + 4;  // every MMA complete
+  static_assert(2 + 2 + 4 + 4 + 4 + 1 == S::NUM_BARS, "barrier region");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::OFF_MISC + 4);
   int* s_bad = reinterpret_cast<int*>(smem + S::OFF_MISC + 8);
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   }
   if (h == 0)
     small_select(p, cs, nq, nk, rows, sRecv, reinterpret_cast<uint32_t*>(sNl),
-                 reinterpret_cast<int*>(smem + S::OFF_BINS), reinterpret_cast<int*>(smem + S::OFF_SEL));
+                 reinterpret_cast<int*>(smem + S::OFF_RANK), reinterpret_cast<int*>(smem + S::OFF_SEL));
 }
 
 template <int D, bool FP8>
