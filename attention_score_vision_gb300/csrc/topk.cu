@@ -23,24 +23,26 @@
 //      rounds' prefix and in higher groups. After the barrier one warp of
 //      each CTA reads every CTA's counts at the chosen digit, so the output
 //      offset needs no further exchange;
-//   3. each CTA writes its kept indices in index order: per pass of 4096
-//      tokens one block-wide prefix sum gives every thread's slots (tokens
-//      above the key, and the lowest-index tokens equal to it), the indices
-//      are staged in shared memory and stored with coalesced writes.
+//   3. each CTA writes its kept indices in index order: each warp counts its
+//      run of the slice's keys above and equal to the threshold, one block
+//      barrier and a warp scan of those counts give every warp its output
+//      slots and tie ranks, and each warp stores one coalesced word of
+//      indices per 32 tokens.
 // The output is deterministic and independent of the cluster size.
 //
 // Histogram-seeded start (fused score + select path): the column pass that
 // wrote the scores also counted them per request by their first 11 and first
-// 16 key bits. The top-B then reads the 2048 first-digit counts with its
-// slice (no first round), and the 32 counts under the chosen digit give the
-// threshold's first 16 bits. When at most kTopkCand keys share them, every
-// CTA sends those candidates (key, index) and its count of keys above them to
-// every CTA of the cluster: one cluster barrier, after which each CTA finds
-// the threshold among the candidates alone (two 8-bit rounds in shared
-// memory, block barriers only) and knows its output offset. More candidates,
-// or counts that do not add up to the request's tokens, fall back to the
-// radix rounds above (from the second digit, or from the first). Requests of
-// one CTA get no histograms (their rounds need no cluster barrier).
+// 16 key bits. Every CTA reads the 2048 first-digit counts beside its slice,
+// and the 32 counts under the chosen digit give the threshold's first 16
+// bits, before any cluster barrier. When at most kTopkCand keys share them,
+// each CTA lists its own candidates (key, index) and counts its keys above
+// them in one pass over its slice; after one cluster barrier every CTA reads
+// the other CTAs' counts and lists (distributed shared memory loads) and finds
+// the threshold among the candidates alone: by ranking them (up to kTopkRank)
+// or in two 8-bit rounds. More candidates, or counts that do not add up to
+// the request's tokens, fall back to the radix rounds above (from the second
+// digit, or from the first). Requests of one CTA get no histograms (their
+// rounds need no cluster barrier).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -56,12 +58,11 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkBins = 2048;                    // 11-bit digits (the last round uses 1024)
 constexpr int kTopkGroups = kTopkBins / 4;         // one group of four bins per thread
 static_assert(kTopkGroups == kTopkThreads, "one bin group per thread");
-constexpr int kTopkItems = 8;                      // consecutive tokens per thread when compacting
-constexpr int kTopkPass = kTopkThreads * kTopkItems;   // tokens per compaction pass (<= 65535)
 constexpr int kTopkCacheKeys = 16384;              // keys cached in shared memory per CTA
 constexpr int kTopkLoad = 8;                       // score loads in flight per thread
 constexpr int kTopkCand = 2048;                    // histogram start: candidates exchanged in the cluster
-static_assert(2 * kTopkCand <= kTopkPass, "candidates are staged in the compaction stage buffer");
+constexpr int kTopkLoc = 1024;                     // histogram start: candidates listed per CTA
+constexpr int kTopkRank = 256;                     // up to this many: threshold by ranking the candidates
 
 // Digit of round `round` (0, 1, 2): bits 31..21, 20..10, 9..0.
 __device__ __forceinline__ int topk_shift(int round) { return round == 0 ? 21 : (round == 1 ? 10 : 0); }
@@ -94,57 +95,33 @@ __device__ __forceinline__ int warp_sum(int x) {
   return x;
 }
 
-// Exclusive scan of one value per thread over the block; `total` gets the
-// sum. One block barrier: every warp adds the totals of the warps below it.
-// The caller separates two calls by a barrier (warp_sums is rewritten).
-__device__ __forceinline__ int topk_block_scan(int v, int* warp_sums, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int x = warp_incl_scan(v);
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  int below = 0, all = 0;
-#pragma unroll
-  for (int i = 0; i < kTopkWarps; i += 4) {
-    const int4 w = *reinterpret_cast<const int4*>(warp_sums + i);
-    below += (i < warp ? w.x : 0) + (i + 1 < warp ? w.y : 0) + (i + 2 < warp ? w.z : 0) +
-             (i + 3 < warp ? w.w : 0);
-    all += w.x + w.y + w.z + w.w;
-  }
-  total = all;
-  return x - v + below;
-}
-
-// Sum of w[i] over the warps i > warp (16 per-warp values).
-__device__ __forceinline__ int sum_warps_above(const int* w, int warp) {
-  int s = 0;
-#pragma unroll
-  for (int i = 0; i < kTopkWarps; i += 4) {
-    const int4 v = *reinterpret_cast<const int4*>(w + i);
-    s += (i > warp ? v.x : 0) + (i + 1 > warp ? v.y : 0) + (i + 2 > warp ? v.z : 0) +
-         (i + 3 > warp ? v.w : 0);
-  }
-  return s;
-}
-
 struct __align__(16) TopkShared {
   int local[3][kTopkBins];    // this CTA's digit counts per round
   int merged[3][kTopkBins];   // cluster-wide counts; bin group g lives in CTA g % cluster size
   int bins[kTopkBins];        // this round's cluster-wide counts, gathered for the digit search
   int grp_sfx[kTopkGroups];   // last round: this CTA's keys in the groups above g of g's warp
-  int stage[kTopkPass];       // kept indices of one compaction pass
-  // histogram start: every CTA's candidates (keys sharing the threshold's
-  // first 16 bits) and per-CTA counts, written by the CTAs that hold them
-  uint32_t cand_key[kTopkCand];
+  // histogram start: this CTA's candidates (keys sharing the threshold's
+  // first 16 bits) and counts, read by every CTA of the cluster ...
+  uint32_t loc_key[kTopkLoc];
+  int loc_idx[kTopkLoc];
+  int pub_gt;                     // this CTA's keys above the 16-bit prefix
+  int pub_n;                      // this CTA's candidates (all, even past kTopkLoc)
+  // ... and every CTA's, merged in CTA order
+  __align__(16) uint32_t cand_key[kTopkCand];
   int cand_idx[kTopkCand];
+  int n_of[kMaxClusterCtas];      // per CTA: its candidates
   int gt16_of[kMaxClusterCtas];   // per CTA: its keys above the candidates' 16-bit prefix
   int cls_gt[kMaxClusterCtas];    // per CTA: its candidates above the threshold
   int cls_eq[kMaxClusterCtas];    // per CTA: its candidates equal to the threshold
-  int cbase[kMaxClusterCtas];     // this CTA's first slot in each CTA's candidate list
-  int cand_n, loc_n;
+  int cbase[kMaxClusterCtas];     // per CTA: its first entry in the merged list
+  uint32_t thr_s;                 // threshold key found by ranking
+  int need_s;                     // ... and its ties still to keep
+  int loc_n;
   __align__(16) int wtot[kTopkWarps];       // digit search: per-warp bin totals
   __align__(16) int gt_w[kTopkWarps];       // last round: per-warp keys above the rounds 0-1 prefix
   __align__(16) int grp_w[kTopkWarps];      // last round: per-warp totals of this CTA's counts
-  __align__(16) int warp_sums[kTopkWarps];  // compaction scan
+  int cw_gt[kTopkWarps];                    // compaction: per-warp keys above the threshold
+  int cw_eq[kTopkWarps];                    // ... and equal to it
   __align__(16) long long pre_w[kTopkWarps];  // budgets of earlier requests, per warp
   int neg_w[kTopkWarps];
   int out_base, eq_before;
@@ -152,6 +129,31 @@ struct __align__(16) TopkShared {
   int pad_[1];
 };
 static_assert(sizeof(TopkShared) % 16 == 0, "key cache follows at a 16-byte boundary");
+
+// Threshold among ncand candidate keys (ncand <= kTopkThreads, keys 16-byte
+// aligned): the key with fewer than `remaining` keys above it and at least
+// `remaining` at or above it; its ties all write the same values to thr_s
+// and need_s (the ties still to keep). The caller separates this from the
+// reads of thr_s / need_s by a block barrier.
+__device__ __forceinline__ void rank_threshold(const uint32_t* keys, int ncand, int remaining,
+                                               uint32_t* thr_s, int* need_s) {
+  const int tid = threadIdx.x;
+  if (tid >= ncand) return;
+  const uint32_t ki = keys[tid];
+  const uint4* ck = reinterpret_cast<const uint4*>(keys);
+  int gt = 0, ge = 0;
+#pragma unroll 4
+  for (int j = 0; j < ncand; j += 4) {
+    const uint4 v = ck[j >> 2];
+    const int m = ncand - j;   // keys of this load inside the list (>= 1)
+    gt += (v.x > ki) + (m > 1 && v.y > ki) + (m > 2 && v.z > ki) + (m > 3 && v.w > ki);
+    ge += (v.x >= ki) + (m > 1 && v.y >= ki) + (m > 2 && v.z >= ki) + (m > 3 && v.w >= ki);
+  }
+  if (gt < remaining && remaining <= ge) {
+    *thr_s = ki;
+    *need_s = remaining - gt;
+  }
+}
 
 // Finds the bin holding the `remaining`-th largest key, bins descending, in
 // every warp at once (no further block barrier): the warp totals give the
@@ -249,7 +251,6 @@ __global__ void __launch_bounds__(kTopkThreads)
     }
     if (tid == 0) {
       sh.nan_seen = 0;
-      sh.cand_n = 0;
       sh.loc_n = 0;
       sh.out_base = 0;
       sh.eq_before = 0;
@@ -287,10 +288,12 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int i = j * kTopkThreads + tid;
     f[j] = i < len ? __ldcg(s + i) : 0.f;
   }
-  // histogram start: this request's first-digit counts (bins 4 tid .. 4 tid + 3)
+  // histogram start: this request's first-digit counts (bins 4 tid .. 4 tid + 3),
+  // loaded beside the flag that says whether they were built (not after it)
+  const int32_t* hreq = hist != nullptr ? hist + int64_t(r) * kHistWords : nullptr;
+  const int4 hc = hreq != nullptr ? __ldcg(reinterpret_cast<const int4*>(hreq) + tid)
+                                  : make_int4(0, 0, 0, 0);
   const bool use_hist = hist != nullptr && *reinterpret_cast<const volatile int32_t*>(hist_ok) != 0;
-  const int32_t* hreq = use_hist ? hist + int64_t(r) * kHistWords : nullptr;
-  const int4 hc = use_hist ? __ldcg(reinterpret_cast<const int4*>(hreq) + tid) : make_int4(0, 0, 0, 0);
 
   // ---- request checks and output offset (every thread, every CTA alike) ----
   long long part = 0;
@@ -335,30 +338,9 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
   if (B == 0) return;
 
-  // Zeroed histograms are released to the cluster now; the wait comes after
-  // the slice is loaded.
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  int nan_local = 0;
-  for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkLoad) {
-    if (i0 > 0) {
-#pragma unroll
-      for (int j = 0; j < kTopkLoad; ++j) {
-        const int i = i0 + j * kTopkThreads + tid;
-        f[j] = i < len ? __ldcg(s + i) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kTopkLoad; ++j) {
-      const int i = i0 + j * kTopkThreads + tid;
-      nan_local |= (f[j] != f[j]);
-      if (cached && i < len) skeys[i] = order_key(f[j]);
-    }
-  }
-  if (nan_local) atomicOr(&sh.nan_seen, 1);
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-  __syncthreads();
-
-  // ---- threshold -----------------------------------------------------------
+  // ---- histogram start: the threshold's first 16 bits from the column
+  // pass's counts. Every CTA of the cluster reads the same counts, so all
+  // take the same branch, before any cluster barrier. -----------------------
   uint32_t prefix = 0, mask = 0;
   int remaining = B;   // how many still to take among keys matching `prefix`
   int gt_part = 0;     // this thread's share: this CTA's keys above the prefix
@@ -367,6 +349,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   bool cand_mode = false;
   uint32_t pfx16 = 0;  // candidates: keys whose first 16 bits are pfx16
   int cnt16 = 0;
+  int d0 = 0;
   uint32_t thr = 0;
   int need_eq = 0;     // tokens equal to the threshold to keep (request-wide)
   int path = 0;        // 0 radix rounds, 1 histogram + rounds, 2 candidates, 3 candidates rejected
@@ -382,11 +365,10 @@ __global__ void __launch_bounds__(kTopkThreads)
       counted += v.x + v.y + v.z + v.w;
     }
     // Every token of the request counted (else the scores did not all come
-    // from the column pass that built the histogram): the same outcome in
-    // every CTA of the cluster, which all read the same counts.
+    // from the column pass that built the histogram).
     if (counted == n) {
       int above0;
-      const int d0 = find_digit(sh.bins, sh.wtot, remaining, above0);
+      d0 = find_digit(sh.bins, sh.wtot, remaining, above0);
       const int rem0 = remaining - above0;
       // the 32 first-16-bit bins under d0, bins descending = lanes descending
       const int fb = __ldcg(hreq + kHistCoarse + d0 * 32 + lane);
@@ -399,74 +381,119 @@ __global__ void __launch_bounds__(kTopkThreads)
         path = 2;
         pfx16 = (uint32_t(d0) << 5) | uint32_t(d1);
       } else {
-        path = 1;
         // too many candidates: radix rounds from the second digit on
+        path = 1;
         round0 = 1;
         prefix = uint32_t(d0) << 21;
         mask = 0x7FFu << 21;
         remaining = rem0;
-        for (int i = tid; i < len; i += kTopkThreads) {
-          const uint32_t kk = cached ? skeys[i] : order_key(s[i]);
-          gt_part += (kk >> 21) > uint32_t(d0);
-        }
       }
     }
   }
 
+  int nan_local = 0;
   if (cand_mode) {
-    // This CTA's keys above the 16-bit prefix, and its candidates (staged in
-    // the compaction buffer: keys, then indices).
+    // One pass over the slice: keys cached, keys above the 16-bit prefix
+    // counted, candidates (keys sharing it) listed in this CTA's own list.
     int gt16 = 0;
-    for (int i = tid; i < len; i += kTopkThreads) {
-      const uint32_t kk = cached ? skeys[i] : order_key(s[i]);
-      const uint32_t top = kk >> 16;
-      if (top > pfx16) {
-        ++gt16;
-      } else if (top == pfx16) {
-        const int slot = atomicAdd(&sh.loc_n, 1);
-        if (slot < kTopkCand) {
-          sh.stage[slot] = int(kk);
-          sh.stage[kTopkCand + slot] = lo + c0 + i;
+    for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkLoad) {
+      if (i0 > 0) {
+#pragma unroll
+        for (int j = 0; j < kTopkLoad; ++j) {
+          const int i = i0 + j * kTopkThreads + tid;
+          f[j] = i < len ? __ldcg(s + i) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kTopkLoad; ++j) {
+        const int i = i0 + j * kTopkThreads + tid;
+        if (i < len) {
+          const uint32_t kk = order_key(f[j]);
+          nan_local |= (f[j] != f[j]);
+          if (cached) skeys[i] = kk;
+          const uint32_t top = kk >> 16;
+          if (top > pfx16) {
+            ++gt16;
+          } else if (top == pfx16) {
+            const int slot = atomicAdd(&sh.loc_n, 1);
+            if (slot < kTopkLoc) {
+              sh.loc_key[slot] = kk;
+              sh.loc_idx[slot] = lo + c0 + i;
+            }
+          }
         }
       }
     }
+    if (nan_local) atomicOr(&sh.nan_seen, 1);
     gt16 = warp_sum(gt16);
     if (lane == 0) sh.gt_w[warp] = gt16;
     __syncthreads();
-    const int nloc = min(sh.loc_n, kTopkCand);
-    if (tid < csize) {
-      int gsum = 0;
+    if (tid == 0) {
+      int g = 0;
 #pragma unroll
-      for (int w = 0; w < kTopkWarps; ++w) gsum += sh.gt_w[w];
-      // the full count (a CTA with more candidates than fit stores only the
-      // first kTopkCand; the total then exceeds the list and is rejected below)
-      int* cn = solo ? &sh.cand_n : cluster.map_shared_rank(&sh.cand_n, tid);
-      sh.cbase[tid] = atomicAdd(cn, sh.loc_n);
-      int* g16 = solo ? &sh.gt16_of[crank] : cluster.map_shared_rank(&sh.gt16_of[crank], tid);
-      *g16 = gsum;
+      for (int w = 0; w < kTopkWarps; ++w) g += sh.gt_w[w];
+      sh.pub_gt = g;
+      sh.pub_n = sh.loc_n;   // the full count (a list that overflowed is rejected below)
     }
-    __syncthreads();
-    for (int j = 0; j < csize; ++j) {
-      const int base = sh.cbase[j];
-      uint32_t* dk = solo ? sh.cand_key : cluster.map_shared_rank(sh.cand_key, j);
-      int* di = solo ? sh.cand_idx : cluster.map_shared_rank(sh.cand_idx, j);
-      for (int t = tid; t < nloc && base + t < kTopkCand; t += kTopkThreads) {
-        dk[base + t] = uint32_t(sh.stage[t]);
-        di[base + t] = sh.stage[kTopkCand + t];
+    // The one exchange: every CTA publishes its counts and list, then reads
+    // the others' (warp c reads CTA c: counts and first 32 entries in one
+    // round trip, further entries after).
+    if (!solo) {
+      asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+      asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    } else {
+      __syncthreads();
+    }
+    const TopkShared* src = nullptr;
+    int n_c = 0;
+    uint32_t k_e = 0;
+    int i_e = 0;
+    if (warp < csize) {
+      src = solo ? &sh : cluster.map_shared_rank(&sh, warp);
+      n_c = src->pub_n;
+      const int g_c = src->pub_gt;
+      k_e = src->loc_key[lane];   // read whatever the count; kept only below it
+      i_e = src->loc_idx[lane];
+      if (lane == 0) {
+        sh.n_of[warp] = n_c;
+        sh.gt16_of[warp] = g_c;
       }
     }
-    // The one exchange: after it no CTA touches another's shared memory.
-    if (!solo) cluster.sync();
+    __syncthreads();
+    int above16 = 0, c_all = 0, base = 0;
+    bool fit = true;
+    for (int c = 0; c < csize; ++c) {
+      const int nc = sh.n_of[c];
+      base += c < warp ? nc : 0;
+      c_all += nc;
+      above16 += sh.gt16_of[c];
+      fit &= nc <= kTopkLoc;
+    }
+    fit &= c_all <= kTopkCand;
+    if (fit && warp < csize) {
+      if (lane < n_c) {
+        sh.cand_key[base + lane] = k_e;
+        sh.cand_idx[base + lane] = i_e;
+      }
+      for (int x = 32 + lane; x < n_c; x += 32) {
+        sh.cand_key[base + x] = src->loc_key[x];
+        sh.cand_idx[base + x] = src->loc_idx[x];
+      }
+      if (lane == 0) sh.cbase[warp] = base;
+    }
     __syncthreads();
     // The threshold lies among the candidates when the keys above their
     // prefix (counted in the slices, not taken from the histograms) number
     // fewer than B and the candidates make up the rest; every CTA holds the
     // same counts, so every CTA takes the same branch.
-    int above16 = 0;
-    for (int c = 0; c < csize; ++c) above16 += sh.gt16_of[c];
-    if (sh.cand_n <= kTopkCand && above16 < B && B <= above16 + sh.cand_n) {
+    if (fit && above16 < B && B <= above16 + c_all) {
       remaining = B - above16;
-      cnt16 = sh.cand_n;
+      cnt16 = c_all;
+      // This CTA reads no other CTA's shared memory after this point (every
+      // value read is in its own shared memory, behind the block barrier
+      // above, so the arrival orders nothing else); no CTA leaves before
+      // every CTA has arrived here (wait at the end).
+      if (!solo) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     } else {
       // radix rounds from the start
       cand_mode = false;
@@ -475,7 +502,35 @@ __global__ void __launch_bounds__(kTopkThreads)
       prefix = 0;
       mask = 0;
       remaining = B;
-      gt_part = 0;
+    }
+  }
+  if (!cand_mode) {
+    // Zeroed histograms are released to the cluster now; the wait comes
+    // after the slice is loaded.
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkLoad) {
+      if (i0 > 0 || path == 3) {
+#pragma unroll
+        for (int j = 0; j < kTopkLoad; ++j) {
+          const int i = i0 + j * kTopkThreads + tid;
+          f[j] = i < len ? __ldcg(s + i) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kTopkLoad; ++j) {
+        const int i = i0 + j * kTopkThreads + tid;
+        nan_local |= (f[j] != f[j]);
+        if (cached && i < len) skeys[i] = order_key(f[j]);
+      }
+    }
+    if (nan_local) atomicOr(&sh.nan_seen, 1);
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    __syncthreads();
+    if (path == 1) {
+      for (int i = tid; i < len; i += kTopkThreads) {
+        const uint32_t kk = cached ? skeys[i] : order_key(s[i]);
+        gt_part += (kk >> 21) > uint32_t(d0);
+      }
     }
   }
 
@@ -485,45 +540,64 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
 
   if (cand_mode) {
-    // The threshold among the candidates: two 8-bit rounds over their low
-    // 16 bits (local[0], local[1]: zeroed at entry, unused on this path).
     const int ncand = cnt16;
-    int* binsA = sh.local[0];
-    int* binsB = sh.local[1];
-    for (int i = tid; i < ncand; i += kTopkThreads) atomicAdd(&binsA[(sh.cand_key[i] >> 8) & 255u], 1);
-    __syncthreads();
-    int aboveA;
-    const int dA = find_digit256(binsA, remaining, aboveA);
-    remaining -= aboveA;
-    const uint32_t pfx24 = (pfx16 << 8) | uint32_t(dA);
-    for (int i = tid; i < ncand; i += kTopkThreads) {
-      const uint32_t kk = sh.cand_key[i];
-      if ((kk >> 8) == pfx24) atomicAdd(&binsB[kk & 255u], 1);
+    if (ncand <= kTopkRank) {
+      rank_threshold(sh.cand_key, ncand, remaining, &sh.thr_s, &sh.need_s);
+      __syncthreads();
+      thr = sh.thr_s;
+      need_eq = sh.need_s;
+    } else {
+      // Two 8-bit rounds over the candidates' low 16 bits (local[0],
+      // local[1]: zeroed at entry, unused on this path).
+      int* binsA = sh.local[0];
+      int* binsB = sh.local[1];
+      for (int i = tid; i < ncand; i += kTopkThreads) atomicAdd(&binsA[(sh.cand_key[i] >> 8) & 255u], 1);
+      __syncthreads();
+      int aboveA;
+      const int dA = find_digit256(binsA, remaining, aboveA);
+      remaining -= aboveA;
+      const uint32_t pfx24 = (pfx16 << 8) | uint32_t(dA);
+      for (int i = tid; i < ncand; i += kTopkThreads) {
+        const uint32_t kk = sh.cand_key[i];
+        if ((kk >> 8) == pfx24) atomicAdd(&binsB[kk & 255u], 1);
+      }
+      __syncthreads();
+      int aboveB;
+      const int dB = find_digit256(binsB, remaining, aboveB);
+      remaining -= aboveB;
+      thr = (pfx24 << 8) | uint32_t(dB);
+      need_eq = remaining;
     }
-    __syncthreads();
-    int aboveB;
-    const int dB = find_digit256(binsB, remaining, aboveB);
-    remaining -= aboveB;
-    thr = (pfx24 << 8) | uint32_t(dB);
-    need_eq = remaining;
-    // per CTA (the slice holding the index): candidates above / equal to thr
-    for (int i = tid; i < ncand; i += kTopkThreads) {
-      const uint32_t kk = sh.cand_key[i];
-      if (kk >= thr) {
-        const int src = min(csize - 1, (sh.cand_idx[i] - lo) / chunk);
-        atomicAdd(kk > thr ? &sh.cls_gt[src] : &sh.cls_eq[src], 1);
+    // Per CTA (warp c: CTA c's entries of the merged list): its candidates
+    // above and equal to the threshold.
+    if (warp < csize) {
+      const int nc = sh.n_of[warp], bc = sh.cbase[warp];
+      int g = 0, q = 0;
+      for (int x = lane; x < nc; x += 32) {
+        const uint32_t kk = sh.cand_key[bc + x];
+        g += kk > thr;
+        q += kk == thr;
+      }
+      g = warp_sum(g);
+      q = warp_sum(q);
+      if (lane == 0) {
+        sh.cls_gt[warp] = g;
+        sh.cls_eq[warp] = q;
       }
     }
     __syncthreads();
-    if (tid == 0) {
-      int base = 0, eqb = 0;
-      for (int c = 0; c < crank; ++c) {
-        const int take = max(0, min(sh.cls_eq[c], need_eq - eqb));
-        base += sh.gt16_of[c] + sh.cls_gt[c] + take;
-        eqb += sh.cls_eq[c];
+    if (warp == 0) {
+      // lane c: CTA c's counts; exclusive prefixes give this CTA's output slot
+      const int gt = lane < csize ? sh.gt16_of[lane] + sh.cls_gt[lane] : 0;
+      const int eq = lane < csize ? sh.cls_eq[lane] : 0;
+      const int e_incl = warp_incl_scan(eq);
+      const int e_before = e_incl - eq;
+      const int take = max(0, min(eq, need_eq - e_before));
+      const int t_incl = warp_incl_scan(gt + take);
+      if (lane == crank) {
+        sh.out_base = t_incl - (gt + take);   // read after the compaction's first block barrier
+        sh.eq_before = e_before;
       }
-      sh.out_base = base;     // read after the compaction's first block barrier
-      sh.eq_before = eqb;
     }
     if (tid == 0 && sh.nan_seen) set_status(status, TSEL_DEV_NAN);   // this CTA's slice
     pdl_launch_dependents();
@@ -634,69 +708,54 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
 
   // ---- compaction in index order --------------------------------------------
-  // kTopkItems consecutive tokens per thread; one block scan per pass gives
-  // both the tied tokens (for their rank) and the tokens above the threshold
-  // in front of each thread (16-bit halves: a pass has <= 4096 tokens). The
-  // output offset written by warp 0 above is read after the first scan's
-  // barrier.
-  int32_t* out = keep_idx + before;
-  int written = 0, eq_seen = 0, room = B;
-  for (int i0 = 0; i0 < len; i0 += kTopkPass) {
-    const int ib = i0 + tid * kTopkItems;
-    uint32_t k[kTopkItems];
-    if (cached && ib + kTopkItems <= len) {
-#pragma unroll
-      for (int j = 0; j < kTopkItems; j += 4) {
-        const uint4 v = *reinterpret_cast<const uint4*>(skeys + ib + j);
-        k[j] = v.x;
-        k[j + 1] = v.y;
-        k[j + 2] = v.z;
-        k[j + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < kTopkItems; ++j) {
-        const int i = ib + j;
-        k[j] = i < len ? (cached ? skeys[i] : order_key(s[i])) : 0u;
-      }
-    }
-    int n_eq = 0, n_gt = 0;
-#pragma unroll
-    for (int j = 0; j < kTopkItems; ++j) {
-      const bool valid = ib + j < len;
-      n_eq += valid && k[j] == thr;
-      n_gt += valid && k[j] > thr;
-    }
-    int tot;
-    const int pre = topk_block_scan((n_eq << 16) | n_gt, sh.warp_sums, tot);
-    if (i0 == 0) {   // (0 for one CTA on the radix-round path)
-      out += sh.out_base;
-      room = B - sh.out_base;
-      eq_seen = sh.eq_before;
-    }
-    int eq_rank = eq_seen + (pre >> 16);
-    int pos = (pre & 0xFFFF) + max(0, min(pre >> 16, need_eq - eq_seen));
-#pragma unroll
-    for (int j = 0; j < kTopkItems; ++j) {
-      const bool valid = ib + j < len;
-      bool t = valid && k[j] > thr;
-      if (valid && k[j] == thr) {
-        t = eq_rank < need_eq;
-        ++eq_rank;
-      }
-      if (t) sh.stage[pos++] = lo + c0 + ib + j;
-    }
-    const int tot_eq = tot >> 16, tot_gt = tot & 0xFFFF;
-    const int cnt = tot_gt + max(0, min(tot_eq, need_eq - eq_seen));
-    __syncthreads();
-    // (every thread has read warp_sums and the stage is read here before the
-    // next pass's first barrier, so the next pass may rewrite both)
-    // (stores stay inside the request's B slots whatever the counts said)
-    for (int i = tid; i < cnt && written + i < room; i += kTopkThreads) out[written + i] = sh.stage[i];
-    written += cnt;
-    eq_seen += tot_eq;
+  // Warp w takes a run of whole 32-token words of the slice. One pass counts
+  // the warp's keys above and equal to the threshold (ballots); after one
+  // block barrier every warp scans the warps' counts itself (its output slot,
+  // the ties in front of it) and a second pass writes its kept indices, one
+  // coalesced store per word. The CTA's output offset and the ties in the
+  // CTAs before it, written above, are read after that barrier.
+  const int span = ((len + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
+  const int w0 = min(len, warp * span), w1 = min(len, w0 + span);
+  const unsigned lt = (1u << lane) - 1u;
+  int c_gt = 0, c_eq = 0;
+#pragma unroll 4
+  for (int b = w0; b < w1; b += 32) {
+    const int i = b + lane;
+    const bool valid = i < w1;
+    const uint32_t kk = valid ? (cached ? skeys[i] : order_key(s[i])) : 0u;
+    c_gt += __popc(__ballot_sync(0xffffffffu, valid && kk > thr));
+    c_eq += __popc(__ballot_sync(0xffffffffu, valid && kk == thr));
   }
-  if (!solo && !cand_mode) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (lane == 0) {
+    sh.cw_gt[warp] = c_gt;
+    sh.cw_eq[warp] = c_eq;
+  }
+  __syncthreads();
+  const int gv = lane < kTopkWarps ? sh.cw_gt[lane] : 0;
+  const int ev = lane < kTopkWarps ? sh.cw_eq[lane] : 0;
+  const int e_incl = warp_incl_scan(ev);
+  const int e_before = sh.eq_before + e_incl - ev;   // ties before warp `lane`'s run
+  const int take = max(0, min(ev, need_eq - e_before));
+  const int k_incl = warp_incl_scan(gv + take);
+  int pos = sh.out_base + __shfl_sync(0xffffffffu, k_incl - (gv + take), warp);
+  int eqb = __shfl_sync(0xffffffffu, e_before, warp);
+  int32_t* out = keep_idx + before;
+#pragma unroll 2
+  for (int b = w0; b < w1; b += 32) {
+    const int i = b + lane;
+    const bool valid = i < w1;
+    const uint32_t kk = valid ? (cached ? skeys[i] : order_key(s[i])) : 0u;
+    const bool eq = valid && kk == thr;
+    const unsigned em = __ballot_sync(0xffffffffu, eq);
+    const bool kept = (valid && kk > thr) || (eq && eqb + __popc(em & lt) < need_eq);
+    const unsigned km = __ballot_sync(0xffffffffu, kept);
+    const int p = pos + __popc(km & lt);
+    // (stores stay inside the request's B slots whatever the counts said)
+    if (kept && p < B) out[p] = lo + c0 + i;
+    pos += __popc(km);
+    eqb += __popc(em);
+  }
+  if (!solo) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // Per-request histograms of given scores (tsel_select_topk_hist), into a

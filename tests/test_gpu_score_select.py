@@ -243,6 +243,35 @@ def test_hist_start_ties_across_slices(tsel):
         assert paths[CANDIDATES] == 1
 
 
+def _shared_prefix_count(s, B):
+    """Keys sharing the first 16 bits of the B-th largest key (-0 as +0): the
+    candidates the histogram start resolves the threshold among."""
+    u = np.where(s == 0, np.float32(0), s).astype(np.float32).view(np.uint32)
+    key = np.where(u & 0x80000000, ~u, u | 0x80000000).astype(np.uint32)
+    thr = np.sort(key)[::-1][B - 1]
+    return int(np.sum((key >> 16) == (thr >> 16)))
+
+
+@pytest.mark.parametrize("ties, ranked", [(90, True), (1500, False)])
+def test_hist_start_threshold_by_rank_or_rounds(tsel, ties, ranked):
+    # log-uniform scores (about 25 keys per 16-bit bin near 0.5) plus `ties`
+    # copies of 0.5 spread over every slice: at most 256 candidates are
+    # ranked directly, more take the two 8-bit rounds; both must keep the
+    # lowest indices of the tied keys across the cluster's CTAs
+    rng = np.random.default_rng(11 + ties)
+    n = 60000
+    s = np.exp2(rng.uniform(-20, 0, n)).astype(np.float32)
+    tie = np.sort(rng.choice(n, ties, replace=False))
+    s[tie] = np.float32(0.5)
+    above = int(np.sum(s > 0.5))
+    for B in (above + 1, above + ties // 2, above + ties):
+        assert (_shared_prefix_count(s, B) <= 256) == ranked
+        got, cu, st, paths = _topk_hist(tsel, s, [0, n], [B])
+        assert st == 0
+        _check(got, cu, s, [0, n], [B])
+        assert paths[CANDIDATES] == 1
+
+
 def test_hist_start_too_many_candidates_uses_rounds(tsel):
     # few distinct values: the threshold's 16-bit bin holds far more than the
     # candidate list, so the top-B runs its rounds from the second digit
