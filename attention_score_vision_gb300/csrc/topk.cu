@@ -310,6 +310,12 @@ __global__ void __launch_bounds__(kTopkThreads)
     sh.pre_w[warp] = part;
     sh.neg_w[warp] = neg;
   }
+  // the histogram start's first-digit counts are staged under the same barrier
+  if (hreq != nullptr) {
+    reinterpret_cast<int4*>(sh.bins)[tid] = hc;
+    const int t = warp_sum(hc.x + hc.y + hc.z + hc.w);
+    if (lane == 0) sh.wtot[warp] = t;
+  }
   __syncthreads();
   long long before64 = 0;
   bool bad = false;
@@ -354,10 +360,6 @@ __global__ void __launch_bounds__(kTopkThreads)
   int need_eq = 0;     // tokens equal to the threshold to keep (request-wide)
   int path = 0;        // 0 radix rounds, 1 histogram + rounds, 2 candidates, 3 candidates rejected
   if (use_hist) {
-    reinterpret_cast<int4*>(sh.bins)[tid] = hc;
-    const int t = warp_sum(hc.x + hc.y + hc.z + hc.w);
-    if (lane == 0) sh.wtot[warp] = t;
-    __syncthreads();
     int counted = 0;
 #pragma unroll
     for (int w = 0; w < kTopkWarps; w += 4) {
@@ -444,33 +446,36 @@ __global__ void __launch_bounds__(kTopkThreads)
     } else {
       __syncthreads();
     }
+    // Lane l of every warp reads CTA l's counts; warp c also reads CTA c's
+    // first 32 list entries (whatever the count; kept only below it). All in
+    // one round trip, so each warp finds the totals and its CTA's place in
+    // the merged list without a block barrier.
+    int nl = 0, gl = 0;
+    if (lane < csize) {
+      const TopkShared* o = solo ? &sh : cluster.map_shared_rank(&sh, lane);
+      nl = o->pub_n;
+      gl = o->pub_gt;
+    }
     const TopkShared* src = nullptr;
-    int n_c = 0;
     uint32_t k_e = 0;
     int i_e = 0;
     if (warp < csize) {
       src = solo ? &sh : cluster.map_shared_rank(&sh, warp);
-      n_c = src->pub_n;
-      const int g_c = src->pub_gt;
-      k_e = src->loc_key[lane];   // read whatever the count; kept only below it
+      k_e = src->loc_key[lane];
       i_e = src->loc_idx[lane];
-      if (lane == 0) {
-        sh.n_of[warp] = n_c;
-        sh.gt16_of[warp] = g_c;
-      }
     }
-    __syncthreads();
-    int above16 = 0, c_all = 0, base = 0;
-    bool fit = true;
-    for (int c = 0; c < csize; ++c) {
-      const int nc = sh.n_of[c];
-      base += c < warp ? nc : 0;
-      c_all += nc;
-      above16 += sh.gt16_of[c];
-      fit &= nc <= kTopkLoc;
+    const int c_all = warp_sum(nl);
+    const int above16 = warp_sum(gl);
+    const bool fit = __all_sync(0xffffffffu, nl <= kTopkLoc) && c_all <= kTopkCand;
+    const int n_incl = warp_incl_scan(nl);
+    if (warp == 0 && lane < kMaxClusterCtas) {
+      sh.n_of[lane] = nl;
+      sh.gt16_of[lane] = gl;
+      sh.cbase[lane] = n_incl - nl;
     }
-    fit &= c_all <= kTopkCand;
     if (fit && warp < csize) {
+      const int n_c = __shfl_sync(0xffffffffu, nl, warp);
+      const int base = __shfl_sync(0xffffffffu, n_incl - nl, warp);
       if (lane < n_c) {
         sh.cand_key[base + lane] = k_e;
         sh.cand_idx[base + lane] = i_e;
@@ -479,7 +484,6 @@ __global__ void __launch_bounds__(kTopkThreads)
         sh.cand_key[base + x] = src->loc_key[x];
         sh.cand_idx[base + x] = src->loc_idx[x];
       }
-      if (lane == 0) sh.cbase[warp] = base;
     }
     __syncthreads();
     // The threshold lies among the candidates when the keys above their
@@ -569,7 +573,7 @@ __global__ void __launch_bounds__(kTopkThreads)
       need_eq = remaining;
     }
     // Per CTA (warp c: CTA c's entries of the merged list): its candidates
-    // above and equal to the threshold.
+    // above and equal to the threshold, read after the compaction's barrier.
     if (warp < csize) {
       const int nc = sh.n_of[warp], bc = sh.cbase[warp];
       int g = 0, q = 0;
@@ -583,20 +587,6 @@ __global__ void __launch_bounds__(kTopkThreads)
       if (lane == 0) {
         sh.cls_gt[warp] = g;
         sh.cls_eq[warp] = q;
-      }
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane c: CTA c's counts; exclusive prefixes give this CTA's output slot
-      const int gt = lane < csize ? sh.gt16_of[lane] + sh.cls_gt[lane] : 0;
-      const int eq = lane < csize ? sh.cls_eq[lane] : 0;
-      const int e_incl = warp_incl_scan(eq);
-      const int e_before = e_incl - eq;
-      const int take = max(0, min(eq, need_eq - e_before));
-      const int t_incl = warp_incl_scan(gt + take);
-      if (lane == crank) {
-        sh.out_base = t_incl - (gt + take);   // read after the compaction's first block barrier
-        sh.eq_before = e_before;
       }
     }
     if (tid == 0 && sh.nan_seen) set_status(status, TSEL_DEV_NAN);   // this CTA's slice
@@ -713,7 +703,7 @@ __global__ void __launch_bounds__(kTopkThreads)
   // block barrier every warp scans the warps' counts itself (its output slot,
   // the ties in front of it) and a second pass writes its kept indices, one
   // coalesced store per word. The CTA's output offset and the ties in the
-  // CTAs before it, written above, are read after that barrier.
+  // CTAs before it are found after that barrier too.
   const int span = ((len + kTopkWarps - 1) / kTopkWarps + 31) & ~31;
   const int w0 = min(len, warp * span), w1 = min(len, w0 + span);
   const unsigned lt = (1u << lane) - 1u;
@@ -731,13 +721,26 @@ __global__ void __launch_bounds__(kTopkThreads)
     sh.cw_eq[warp] = c_eq;
   }
   __syncthreads();
+  // This CTA's output slot and the ties in the CTAs before it: from warp 0's
+  // exchange on the radix path, else from every CTA's candidate counts (lane
+  // c: CTA c), scanned by each warp.
+  int cta_base = sh.out_base, cta_eq = sh.eq_before;
+  if (cand_mode) {
+    const int gc = lane < csize ? sh.gt16_of[lane] + sh.cls_gt[lane] : 0;
+    const int ec = lane < csize ? sh.cls_eq[lane] : 0;
+    const int ec_incl = warp_incl_scan(ec);
+    const int tc = max(0, min(ec, need_eq - (ec_incl - ec)));
+    const int kc_incl = warp_incl_scan(gc + tc);
+    cta_base = __shfl_sync(0xffffffffu, kc_incl - (gc + tc), crank);
+    cta_eq = __shfl_sync(0xffffffffu, ec_incl - ec, crank);
+  }
   const int gv = lane < kTopkWarps ? sh.cw_gt[lane] : 0;
   const int ev = lane < kTopkWarps ? sh.cw_eq[lane] : 0;
   const int e_incl = warp_incl_scan(ev);
-  const int e_before = sh.eq_before + e_incl - ev;   // ties before warp `lane`'s run
+  const int e_before = cta_eq + e_incl - ev;   // ties before warp `lane`'s run
   const int take = max(0, min(ev, need_eq - e_before));
   const int k_incl = warp_incl_scan(gv + take);
-  int pos = sh.out_base + __shfl_sync(0xffffffffu, k_incl - (gv + take), warp);
+  int pos = cta_base + __shfl_sync(0xffffffffu, k_incl - (gv + take), warp);
   int eqb = __shfl_sync(0xffffffffu, e_before, warp);
   int32_t* out = keep_idx + before;
 #pragma unroll 2
