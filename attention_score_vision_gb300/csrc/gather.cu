@@ -8,10 +8,13 @@
 // old ones in keep_idx.
 //
 // Rows are copied with 16-byte streaming loads/stores. Each warp takes two
-// consecutive kept rows at a time and issues every load of both rows before
-// its stores (rows of up to 4 KB stay in registers), so each lane keeps up to
-// 16 loads in flight (HBM-bound: the algorithmic bytes are the kept rows read
-// once and written once).
+// consecutive kept rows at a time and issues every load of both rows (and
+// their positions) before its stores (rows of up to 4 KB stay in registers),
+// so each lane keeps up to 16 loads in flight (HBM-bound: the algorithmic
+// bytes are the kept rows read once and written once). A few warps at the end
+// of the grid find the new image boundaries meanwhile, by 32-ary searches of
+// keep_idx (a handful of dependent loads each, which for small requests would
+// otherwise be the kernel's longest chain).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -33,20 +36,33 @@ __device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int v) {
   return lo;
 }
 
-__device__ __forceinline__ int lower_bound_i32(const int32_t* a, int n, int v) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(a + mid) < v) lo = mid + 1;
-    else hi = mid;
+// First index i in [0, n) with a[i] >= v (n if none) for ascending a: a
+// 32-ary search by one warp, so that a search over the kept tokens takes two
+// or three dependent loads (n up to 64K) instead of log2(n). Every lane
+// returns the index. For input that is not ascending it still returns an
+// index in [0, n].
+__device__ __forceinline__ int warp_lower_bound(const int32_t* a, int n, int v) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = n;   // the index lies in [lo, hi]
+  while (hi - lo > 64) {
+    const int step = (hi - lo + 31) >> 5;
+    const int idx = lo + (lane + 1) * step - 1;   // last element of sub-range `lane`
+    const bool below = idx < hi && __ldg(a + idx) < v;
+    lo += step * __popc(__ballot_sync(0xffffffffu, below));   // sub-ranges wholly below v
+    hi = min(hi, lo + step);
   }
-  return lo;
+  const int i0 = lo + lane, i1 = lo + 32 + lane;
+  const bool b0 = i0 < hi && __ldg(a + i0) < v;
+  const bool b1 = i1 < hi && __ldg(a + i1) < v;
+  return lo + __popc(__ballot_sync(0xffffffffu, b0)) + __popc(__ballot_sync(0xffffffffu, b1));
 }
 
 // VPL = 16-byte vectors per lane per row (rows of up to 32 * VPL vectors in
 // registers); VPL = 0 copies rows of any length in a loop.
+// Register caps keep the blocks per SM the copy's loads in flight need: 4
+// (32 warps) for rows of up to 5 vectors per lane, 3 for 6 or 7.
 template <int VPL>
-__global__ void __launch_bounds__(kGatherThreads)
+__global__ void __launch_bounds__(kGatherThreads, (VPL >= 1 && VPL <= 5) ? 4 : ((VPL == 6 || VPL == 7) ? 3 : 1))
     gather_kernel(const uint8_t* __restrict__ hidden, int64_t row_stride_bytes, int row_vecs,
                   const int32_t* __restrict__ pos, int pos_dim,
                   const int32_t* __restrict__ cu_k, int G, int Tk,
@@ -67,19 +83,27 @@ __global__ void __launch_bounds__(kGatherThreads)
   }
   const int gwarp = (blockIdx.x * kGatherThreads + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * kGatherThreads) >> 5;
-  const int gtid = blockIdx.x * kGatherThreads + threadIdx.x;
-
-  // New per-image boundaries: kept tokens below each old boundary.
-  for (int g = gtid; g <= G; g += gridDim.x * kGatherThreads)
-    out_cu[g] = lower_bound_i32(keep_idx, K, __ldg(cu_k + g));
+  // The last nb warps find the new per-image boundaries (kept tokens below
+  // each old boundary), one boundary per warp at a time, while the others
+  // copy rows.
+  const int nb = min(G + 1, nwarps / 16 + 1);
+  const int row_warps = nwarps - nb;
+  if (gwarp >= row_warps) {
+    for (int g = gwarp - row_warps; g <= G; g += nb) {
+      const int b = warp_lower_bound(keep_idx, K, __ldg(cu_k + g));
+      if (lane == 0) out_cu[g] = b;
+    }
+    return;
+  }
 
   // Image of a token: boundaries <= t, minus one (a ballot when they fit a warp).
   const bool few_images = G < 32;
   const int cu_lane = few_images && lane <= G ? __ldg(cu_k + lane) : 0x7FFFFFFF;
 
-  for (int k0 = kGatherRows * gwarp; k0 < K; k0 += kGatherRows * nwarps) {
+  for (int k0 = kGatherRows * gwarp; k0 < K; k0 += kGatherRows * row_warps) {
     int t[kGatherRows];
     bool ok[kGatherRows];
+    int pv[kGatherRows];   // position component `lane` of each row, loaded with the row
 #pragma unroll
     for (int r = 0; r < kGatherRows; ++r) {
       const int k = k0 + r;
@@ -87,6 +111,7 @@ __global__ void __launch_bounds__(kGatherThreads)
       const int prev = k > 0 && k < K ? __ldg(keep_idx + k - 1) : -1;
       ok[r] = k < K && t[r] >= 0 && t[r] < Tk && prev < t[r];
       if (k < K && !ok[r] && lane == 0) set_status(status, TSEL_DEV_KEEP_IDX);
+      pv[r] = ok[r] && lane < pos_dim ? __ldg(pos + int64_t(t[r]) * pos_dim + lane) : 0;
     }
     if (VPL > 0) {
       uint4 x[kGatherRows][VPL > 0 ? VPL : 1];
@@ -129,8 +154,7 @@ __global__ void __launch_bounds__(kGatherThreads)
     for (int r = 0; r < kGatherRows; ++r) {
       if (!ok[r]) continue;
       const int k = k0 + r;
-      if (lane < pos_dim)
-        out_pos[int64_t(k) * pos_dim + lane] = __ldg(pos + int64_t(t[r]) * pos_dim + lane);
+      if (lane < pos_dim) out_pos[int64_t(k) * pos_dim + lane] = pv[r];
       if (few_images) {
         const int img = __popc(__ballot_sync(0xffffffffu, cu_lane <= t[r])) - 1;
         if (lane == 0) out_img[k] = img;
@@ -174,8 +198,9 @@ cudaError_t launch_gather(const void* hidden, int64_t row_stride_bytes, int row_
                           void* out_hidden, int32_t* out_pos, int32_t* out_img, int32_t* out_cu,
                           uint32_t* status, int num_sms, cudaStream_t stream) {
   const int row_vecs = row_bytes / 16;
+  // row warps plus the boundary warps (the kernel keeps min(G + 1, warps / 16 + 1))
   const int64_t row_warps = (int64_t(K) + kGatherRows - 1) / kGatherRows;
-  const int64_t warps_needed = row_warps > G + 1 ? row_warps : G + 1;
+  const int64_t warps_needed = row_warps + (G + 1 < 32 ? G + 1 : 32);
   const int vpl = (row_vecs + 31) / 32;
   const auto* h = static_cast<const uint8_t*>(hidden);
   auto* oh = static_cast<uint8_t*>(out_hidden);
