@@ -909,14 +909,29 @@ def gpu_arm(args) -> None:
         b.record(stream)
         torch.cuda.synchronize()
         e2e_ms = reduce_max_over_ranks(a.elapsed_time(b) / n_e2e, dev)
+        # the host link alone: the same input bytes copied in, nothing else
+        link = []
+        for i in range(4):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(copy_stream)
+            with torch.cuda.stream(copy_stream):
+                for k2, v in pin.items():
+                    dbufs[0][k2].copy_(v, non_blocking=True)
+            c1.record(copy_stream)
+            link.append((c0, c1))
+        torch.cuda.synchronize()
+        copy_ms = min(x.elapsed_time(y) for x, y in link[1:])
         e2e = {"value": replica_throughput(Tk, world, e2e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms,
+               "h2d_copy_ms": copy_ms, "h2d_GB/s": h2d / (copy_ms * 1e-3) / 1e9,
                "note": "every step copies its request's inputs in from pinned host memory "
                        "(Q, K and metadata, then hidden rows and positions during the importance "
                        "passes; two input sets, so the next request's copy overlaps this one's "
                        "kernels), runs importance+top-B+compaction and copies the selection "
-                       "metadata out; compacted hidden rows stay on the device"}
+                       "metadata out; compacted hidden rows stay on the device. h2d_copy_ms: "
+                       "the same input bytes copied in alone (the step's floor when the "
+                       "host link is slower than the kernels)"}
 
     # --- small requests: whole path replayed from one CUDA graph -------------
     small = {}
