@@ -134,6 +134,13 @@ def test_random_selection_layouts(tsel, seed):
     ref, cref = oracle.select_topk(s, off, keep)
     assert tsel.tsel_read_device_status(ws) == 0
     assert np.array_equal(ki.cpu().numpy(), ref) and np.array_equal(cu.cpu().numpy(), cref)
+    # the histogram-started top-B (candidate exchange, ranking or 8-bit rounds,
+    # or its fallbacks, whichever the layout calls for) on the same layout
+    wsh = torch.zeros(tsel.tsel_select_topk_hist_workspace_size(len(keep)), dtype=torch.uint8,
+                      device="cuda")
+    kh, ch = tsel.tsel_select_topk_hist(sd, i32(off), i32(keep), int(sum(keep)), workspace=wsh)
+    assert tsel.tsel_read_device_status(wsh) == 0
+    assert np.array_equal(kh.cpu().numpy(), ref) and np.array_equal(ch.cpu().numpy(), cref)
     # the dynamic budget on the same layout, and the device-count selection it feeds
     rng = np.random.default_rng(seed)
     tau, lo = int(rng.choice([1, 300, 900, 1000])), int(rng.choice([0, 100]))
