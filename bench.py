@@ -736,6 +736,31 @@ def gpu_arm(args) -> None:
     if tsel.tsel_read_device_status(ws) != 0:
         raise RuntimeError("device status set in the selection loop")
 
+    # --- what top-B + compaction add to the step: the whole step against the
+    # same importance chain alone (schedule and both passes in one call), each
+    # with events only around it and interleaved, so the top-B's launch
+    # overlaps the column pass's drain as it does in the step ----------------
+    chain_evs, whole_evs = [], []
+    for i in range(n_stage):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        score_select(S1 | S2 | S3)
+        b.record(stream)
+        chain_evs.append((a, b))
+        flush.fill_((i + 1) & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        score_select(0)
+        gather()
+        b.record(stream)
+        whole_evs.append((a, b))
+    torch.cuda.synchronize()
+    chain_ms = sum(a.elapsed_time(b) for a, b in chain_evs) / len(chain_evs)
+    whole_ms = sum(a.elapsed_time(b) for a, b in whole_evs) / len(whole_evs)
+    if tsel.tsel_read_device_status(ws) != 0:
+        raise RuntimeError("device status set in the step-difference loop")
+
     # --- the same path as three separate calls (importance, plain top-B,
     # compaction), for comparison with the fused call ------------------------
     sep = []
@@ -1015,7 +1040,16 @@ def gpu_arm(args) -> None:
                       "hbm_frac": (topk_bytes + gather_bytes) / (sel_mean * 1e-3) / hbm_peak,
                       "ms_isolated_sum": mean["topk"] + mean["gather"],
                       "hbm_frac_isolated_sum": (topk_bytes + gather_bytes)
-                                               / ((mean["topk"] + mean["gather"]) * 1e-3) / hbm_peak},
+                                               / ((mean["topk"] + mean["gather"]) * 1e-3) / hbm_peak,
+                      "in_step_ms": whole_ms - chain_ms,
+                      "in_step_GB/s": (topk_bytes + gather_bytes) / ((whole_ms - chain_ms) * 1e-3) / 1e9,
+                      "in_step_hbm_frac": (topk_bytes + gather_bytes)
+                                          / ((whole_ms - chain_ms) * 1e-3) / hbm_peak,
+                      "in_step_note": f"whole step {whole_ms:.4f} ms minus the importance chain "
+                                      f"alone {chain_ms:.4f} ms (interleaved runs, events only "
+                                      "around each): the time top-B and compaction add to the "
+                                      "step. `ms` has an event between the column pass and the "
+                                      "top-B, which keeps the top-B's launch off the pass's drain"},
     }
 
     if fp8 is not None:
