@@ -740,23 +740,24 @@ def gpu_arm(args) -> None:
     # same importance chain alone (schedule and both passes in one call), each
     # with events only around it and interleaved, so the top-B's launch
     # overlaps the column pass's drain as it does in the step ----------------
-    chain_evs, whole_evs = [], []
+    chain_evs, fused_evs, whole_evs = [], [], []
     for i in range(n_stage):
-        flush.fill_(i & 0xFF)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        score_select(S1 | S2 | S3)
-        b.record(stream)
-        chain_evs.append((a, b))
-        flush.fill_((i + 1) & 0xFF)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        score_select(0)
-        gather()
-        b.record(stream)
-        whole_evs.append((a, b))
+        for j, evl in enumerate((chain_evs, fused_evs, whole_evs)):
+            flush.fill_((i + j) & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            if j == 0:
+                score_select(S1 | S2 | S3)   # schedule and both passes
+            elif j == 1:
+                score_select(0)              # ... and the top-B
+            else:
+                score_select(0)              # ... and the compaction
+                gather()
+            b.record(stream)
+            evl.append((a, b))
     torch.cuda.synchronize()
     chain_ms = sum(a.elapsed_time(b) for a, b in chain_evs) / len(chain_evs)
+    fused_ms = sum(a.elapsed_time(b) for a, b in fused_evs) / len(fused_evs)
     whole_ms = sum(a.elapsed_time(b) for a, b in whole_evs) / len(whole_evs)
     if tsel.tsel_read_device_status(ws) != 0:
         raise RuntimeError("device status set in the step-difference loop")
@@ -1024,6 +1025,11 @@ def gpu_arm(args) -> None:
         # the fused call's top-B, started from the column pass's histograms
         "topk": {"ms": mean["topk"], "GB/s": topk_bytes / (mean["topk"] * 1e-3) / 1e9,
                  "hbm_frac": topk_bytes / (mean["topk"] * 1e-3) / hbm_peak,
+                 "in_step_ms": fused_ms - chain_ms,
+                 "in_step_note": f"the fused call {fused_ms:.4f} ms minus the importance chain "
+                                 f"alone {chain_ms:.4f} ms (interleaved runs, events only around "
+                                 "each): what the top-B adds to the call, its launch overlapping "
+                                 "the column pass's drain; `ms` times it alone between events",
                  "paths": dict(zip(["radix", "hist_rounds", "hist_candidates", "rejected",
                                     "in_importance_launch"], topk_paths))},
         "topk_plain": {"ms": mean["topk_plain"],
