@@ -438,8 +438,7 @@ __global__ void __launch_bounds__(kTopkThreads)
       sh.pub_n = sh.loc_n;   // the full count (a list that overflowed is rejected below)
     }
     // The one exchange: every CTA publishes its counts and list, then reads
-    // the others' (warp c reads CTA c: counts and first 32 entries in one
-    // round trip, further entries after).
+    // the others' (below).
     if (!solo) {
       asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
       asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
