@@ -555,9 +555,11 @@ def tsel_last_error() -> str:
 
 
 def tsel_probe_ex2(blocks: int, iters: int, sink: torch.Tensor, stream=None) -> None:
-    """Enqueues the MUFU exp2 throughput probe (blocks*512*iters*8 exp2)."""
+    """Enqueues the MUFU exp2 throughput probe (blocks*512*iters*8 exp2).
+    sink[blocks*512:] receives block 0's SM cycles and nanoseconds (two
+    int64 words), whose ratio is the SM clock during the probe."""
     _need(sink, torch.float32, "sink")
-    if sink.numel() < blocks * 512:
-        raise ValueError("sink needs blocks*512 floats")
+    if sink.numel() < blocks * 512 + 4:
+        raise ValueError("sink needs blocks*512 + 4 floats")
     _check(load_library().tsel_probe_ex2(int(blocks), int(iters), _ptr(sink),
                                          _stream(stream, sink.device)))

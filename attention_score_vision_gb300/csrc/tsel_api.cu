@@ -786,6 +786,8 @@ tsel_status tsel_clear_device_status(void* workspace, void* stream_) {
 
 tsel_status tsel_probe_ex2(int blocks, int iters, float* sink, void* stream_) {
   if (blocks < 1 || iters < 1 || sink == nullptr) return fail(TSEL_ERR_INVALID_VALUE, "bad probe args");
+  if ((reinterpret_cast<uintptr_t>(sink) & 7u) != 0)
+    return fail(TSEL_ERR_INVALID_VALUE, "probe sink must be 8-byte aligned");
   cudaError_t e = launch_probe_ex2(blocks, iters, sink, static_cast<cudaStream_t>(stream_));
   return e == cudaSuccess ? TSEL_OK : cuda_fail(e, "probe launch");
 }

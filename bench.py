@@ -632,7 +632,7 @@ def gpu_arm(args) -> None:
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
     pblocks, piters = sms * 4, 2048
-    sink = torch.empty(pblocks * 512, dtype=torch.float32, device=dev)
+    sink = torch.empty(pblocks * 512 + 4, dtype=torch.float32, device=dev)
     tsel.tsel_probe_ex2(pblocks, piters, sink)
     best = None
     for _ in range(3):
@@ -644,6 +644,9 @@ def gpu_arm(args) -> None:
         t = a.elapsed_time(b) * 1e-3
         best = t if best is None else min(best, t)
     ex2_peak = pblocks * 512 * piters * 8 / best        # exp2 / s
+    # the SM clock during the last probe launch: block 0's cycles over its ns
+    p_cyc, p_ns = (int(x) for x in sink[pblocks * 512:].view(torch.int64).cpu().tolist())
+    probe_mhz = p_cyc / p_ns * 1e3 if p_ns > 0 else None
 
     # --- warm-up -----------------------------------------------------------
     for _ in range(args.warmup):
@@ -1104,6 +1107,9 @@ def gpu_arm(args) -> None:
         "peaks": {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
                   "ex2_per_s": ex2_peak, "ex2_per_clk_per_sm_at_max":
                       ex2_peak / sms / (clocks["sm_max_mhz"] * 1e6) if clocks.get("sm_max_mhz") else None,
+                  "ex2_probe_sm_mhz": probe_mhz,
+                  "ex2_per_clk_per_sm_at_probe_clock":
+                      ex2_peak / sms / (probe_mhz * 1e6) if probe_mhz else None,
                   "source": peak_src},
         "wall_s_timed": wall,
     }

@@ -454,7 +454,10 @@ TSEL_API const char* tsel_last_error(void);
 /* Measurement probe: enqueues a kernel of `blocks` x 512 threads, each thread
  * issuing `iters` x 8 dependent-chain ex2.approx.f32 operations (a MUFU
  * throughput probe; the count of exp2 per launch is blocks*512*iters*8).
- * `sink` receives one float per thread so nothing is optimised away. */
+ * `sink` (device, 8-byte aligned, blocks*512 + 4 floats) receives one float
+ * per thread so nothing is optimised away, then two uint64 words: the SM
+ * clock cycles and the nanoseconds (%globaltimer) that block 0's first thread
+ * took, so the SM clock during the probe is cycles / ns. */
 TSEL_API tsel_status tsel_probe_ex2(int blocks, int iters, float* sink, void* stream);
 
 #ifdef __cplusplus
