@@ -509,8 +509,8 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
   if (!cand_mode) {
     // Zeroed histograms are released to the cluster now; the wait comes
-    // after the slice is loaded.
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    // after the slice is loaded (one CTA: the block barrier below suffices).
+    if (!solo) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     for (int i0 = 0; i0 < len; i0 += kTopkThreads * kTopkLoad) {
       if (i0 > 0 || path == 3) {
 #pragma unroll
@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kTopkThreads)
       }
     }
     if (nan_local) atomicOr(&sh.nan_seen, 1);
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (!solo) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     __syncthreads();
     if (path == 1) {
       for (int i = tid; i < len; i += kTopkThreads) {
