@@ -762,6 +762,10 @@ def gpu_arm(args) -> None:
     chain_ms = sum(a.elapsed_time(b) for a, b in chain_evs) / len(chain_evs)
     fused_ms = sum(a.elapsed_time(b) for a, b in fused_evs) / len(fused_evs)
     whole_ms = sum(a.elapsed_time(b) for a, b in whole_evs) / len(whole_evs)
+    # the differences mean what they say only when the fused call scores with
+    # the same launches as the chain (not the one-launch kernel of small problems)
+    same_chain = tsel.tsel_importance_one_launch(G, Tq, Tk, w.max_seqlen_q, w.max_seqlen_k, H,
+                                                 hd) == 0
     if tsel.tsel_read_device_status(ws) != 0:
         raise RuntimeError("device status set in the step-difference loop")
 
@@ -1028,7 +1032,7 @@ def gpu_arm(args) -> None:
         # the fused call's top-B, started from the column pass's histograms
         "topk": {"ms": mean["topk"], "GB/s": topk_bytes / (mean["topk"] * 1e-3) / 1e9,
                  "hbm_frac": topk_bytes / (mean["topk"] * 1e-3) / hbm_peak,
-                 "in_step_ms": fused_ms - chain_ms,
+                 "in_step_ms": fused_ms - chain_ms if same_chain else None,
                  "in_step_note": f"the fused call {fused_ms:.4f} ms minus the importance chain "
                                  f"alone {chain_ms:.4f} ms (interleaved runs, events only around "
                                  "each): what the top-B adds to the call, its launch overlapping "
@@ -1050,10 +1054,12 @@ def gpu_arm(args) -> None:
                       "ms_isolated_sum": mean["topk"] + mean["gather"],
                       "hbm_frac_isolated_sum": (topk_bytes + gather_bytes)
                                                / ((mean["topk"] + mean["gather"]) * 1e-3) / hbm_peak,
-                      "in_step_ms": whole_ms - chain_ms,
-                      "in_step_GB/s": (topk_bytes + gather_bytes) / ((whole_ms - chain_ms) * 1e-3) / 1e9,
+                      "in_step_ms": whole_ms - chain_ms if same_chain else None,
+                      "in_step_GB/s": (topk_bytes + gather_bytes) / ((whole_ms - chain_ms) * 1e-3)
+                                      / 1e9 if same_chain else None,
                       "in_step_hbm_frac": (topk_bytes + gather_bytes)
-                                          / ((whole_ms - chain_ms) * 1e-3) / hbm_peak,
+                                          / ((whole_ms - chain_ms) * 1e-3) / hbm_peak
+                                          if same_chain else None,
                       "in_step_note": f"whole step {whole_ms:.4f} ms minus the importance chain "
                                       f"alone {chain_ms:.4f} ms (interleaved runs, events only "
                                       "around each): the time top-B and compaction add to the "
